@@ -1,0 +1,152 @@
+"""Reference oracle for weighted isotonic regression (fp64, CPU).
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA library
+never links, loads or calls it, and it never calls the CUDA library.
+
+The arithmetic lives in ``iso_oracle.c`` (plain C, compiled with gcc by
+:func:`build`); this module only marshals numpy arrays.  Citations are to
+"Merge Hulls Without Copying Vertices: GPU Isotonic Regression" (the paper):
+
+* :func:`pava` -- weighted pool adjacent violators in fp64, Section 2.1, eq. (1).
+* :func:`hull_fit` -- lower hull of the cumulative-sum diagram, Section 2.1,
+  eqs. (2)-(3); an independent route used only to cross-check :func:`pava`.
+* :func:`points` -- the cumulative-sum diagram itself, eq. (2).
+* :func:`backward` / :func:`backward_w` -- block averaging, Section 6, "Gradient".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "iso_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libiso_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+BAD_Y = 1
+BAD_W = 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (portable flags: it runs on x86_64 and aarch64)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    # -ffp-contract=off: no fused multiply-adds, so every operation rounds as written.
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                           "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+            for name in ("oracle_pava_rows", "oracle_hull_rows"):
+                f = getattr(lib, name)
+                f.argtypes = [i64, i64, vp, vp, ci, vp, vp, vp]
+                f.restype = None
+            lib.oracle_points.argtypes = [i64, vp, vp, ci, vp, vp]
+            lib.oracle_points.restype = None
+            lib.oracle_backward_rows.argtypes = [i64, i64, vp, vp, vp, vp]
+            lib.oracle_backward_rows.restype = None
+            lib.oracle_backward_w.argtypes = [i64, vp, vp, vp, vp, vp, vp]
+            lib.oracle_backward_w.restype = None
+            _lib = lib
+    return _lib
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _as2d(y, w):
+    y = _f32(y)
+    squeeze = y.ndim == 1
+    y2 = y.reshape(1, -1) if squeeze else y
+    w2 = None
+    if w is not None:
+        w2 = _f32(w).reshape(y2.shape)
+    return y2, w2, squeeze
+
+
+def _rows(fn_name, y, w, increasing):
+    y2, w2, squeeze = _as2d(y, w)
+    rows, n = y2.shape
+    z = np.empty((rows, n), dtype=np.float64)
+    blocks = np.empty((rows, n), dtype=np.uint8)
+    status = np.empty(rows, dtype=np.uint32)
+    getattr(_load(), fn_name)(rows, n, _ptr(y2), _ptr(w2), int(bool(increasing)),
+                              _ptr(z), _ptr(blocks), _ptr(status))
+    if squeeze:
+        return z[0], blocks[0], status[0]
+    return z, blocks, status
+
+
+def pava(y, w=None, increasing=True):
+    """Fit by weighted PAVA in fp64.  Returns ``(z, blocks, status)``.
+
+    ``y``: float32 ``[n]`` or ``[rows, n]``; ``w``: same shape or None (unit
+    weights).  ``z`` is float64, ``blocks[i] == 1`` where element i starts a
+    block, ``status`` is 0 or a mask of :data:`BAD_Y` / :data:`BAD_W` per row
+    (that row's z is NaN)."""
+    return _rows("oracle_pava_rows", y, w, increasing)
+
+
+def hull_fit(y, w=None, increasing=True):
+    """Fit by the lower hull of the cumulative-sum diagram (fp64 monotone chain)."""
+    return _rows("oracle_hull_rows", y, w, increasing)
+
+
+def points(y, w=None, increasing=True):
+    """Cumulative-sum diagram of one row: arrays ``W, S`` of n+1 entries, eq. (2)."""
+    y = _f32(y).ravel()
+    n = y.size
+    w1 = None if w is None else _f32(w).ravel()
+    W = np.empty(n + 1, dtype=np.float64)
+    S = np.empty(n + 1, dtype=np.float64)
+    _load().oracle_points(n, _ptr(y), _ptr(w1), int(bool(increasing)), _ptr(W), _ptr(S))
+    return W, S
+
+
+def backward(grad, blocks, w=None):
+    """Block averaging: ``out_i = w_i * G_B / W_B`` over the blocks that
+    ``blocks`` marks (uint8 block starts).  fp64 result."""
+    g2 = _f32(grad)
+    squeeze = g2.ndim == 1
+    if squeeze:
+        g2 = g2.reshape(1, -1)
+    b2 = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(g2.shape)
+    w2 = None if w is None else _f32(w).reshape(g2.shape)
+    out = np.empty(g2.shape, dtype=np.float64)
+    _load().oracle_backward_rows(g2.shape[0], g2.shape[1], _ptr(g2), _ptr(b2), _ptr(w2),
+                                 _ptr(out))
+    return out[0] if squeeze else out
+
+
+def backward_w(grad, blocks, w, y, z):
+    """Weight gradient of one row: ``(y_i - z_i) * G_B / W_B``."""
+    g = _f32(grad).ravel()
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).ravel()
+    w1 = None if w is None else _f32(w).ravel()
+    y1 = _f32(y).ravel()
+    z1 = np.ascontiguousarray(z, dtype=np.float64).ravel()
+    out = np.empty(g.size, dtype=np.float64)
+    _load().oracle_backward_w(g.size, _ptr(g), _ptr(b), _ptr(w1), _ptr(y1), _ptr(z1),
+                              _ptr(out))
+    return out

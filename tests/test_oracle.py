@@ -1,0 +1,339 @@
+"""Pins of the fp64 oracle against facts fixed by the pages and by the mathematics,
+not against itself (CPU only).
+
+Citations are to "Merge Hulls Without Copying Vertices: GPU Isotonic Regression"
+(the paper), the "groupant" page on the Rust PAVA (mod.rs) and the blog post
+"Isotonic Regression on GPU".
+"""
+from fractions import Fraction
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from convex_hull_pava_gb300 import workloads as wl
+from golden_io import load as load_golden
+
+
+# ---------------------------------------------------------------------------
+# independent exact helpers (rational arithmetic, tiny n)
+# ---------------------------------------------------------------------------
+def _frac(a):
+    return [Fraction(float(v)) for v in a]
+
+
+def brute_force(y, w):
+    """Minimum of eq. (1) over every contiguous partition whose block means are
+    non-decreasing, in exact rational arithmetic ("groupant" page, kkt_prefix:
+    enumerated contiguous partitions independently select the minimum squared
+    loss).  Returns (objective, fit, starts)."""
+    n = len(y)
+    yf, wf = _frac(y), _frac(w)
+    best = None
+    for cuts in itertools.product((0, 1), repeat=n - 1):
+        starts = [0] + [i + 1 for i, c in enumerate(cuts) if c]
+        ends = starts[1:] + [n]
+        means = []
+        for a, b in zip(starts, ends):
+            sw = sum(wf[a:b])
+            means.append(sum(wf[i] * yf[i] for i in range(a, b)) / sw)
+        if any(means[k + 1] < means[k] for k in range(len(means) - 1)):
+            continue
+        z = []
+        for m, a, b in zip(means, starts, ends):
+            z += [m] * (b - a)
+        obj = sum(wf[i] * (z[i] - yf[i]) ** 2 for i in range(n))
+        if best is None or obj < best[0]:
+            best = (obj, z, starts)
+    return best
+
+
+def minmax_formula(y, w):
+    """z_i = max_{s<=i} min_{t>=i} Av_w(s..t): the textbook min-max formula of
+    isotonic regression (not printed on the pages), O(n^3) in floats."""
+    y = np.asarray(y, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    n = y.size
+    cw = np.concatenate([[0.0], np.cumsum(w)])
+    cs = np.concatenate([[0.0], np.cumsum(w * y)])
+    z = np.empty(n)
+    for i in range(n):
+        best = -np.inf
+        for s in range(i + 1):
+            t = np.arange(i, n)
+            av = (cs[t + 1] - cs[s]) / (cw[t + 1] - cw[s])
+            best = max(best, av.min())
+        z[i] = best
+    return z
+
+
+def kkt_residuals(y, w, z):
+    """Prefix residuals r_k = sum_{j<=k} w_j (y_j - z_j) in fp64 (paper Section 7.6;
+    groupant page, Invariant)."""
+    w = np.ones_like(y, dtype=np.float64) if w is None else np.asarray(w, np.float64)
+    return np.cumsum(w * (np.asarray(y, np.float64) - z))
+
+
+# ---------------------------------------------------------------------------
+# worked examples printed on the pages (tests/golden/worked_examples.txt)
+# ---------------------------------------------------------------------------
+GOLDEN = load_golden()
+
+
+@pytest.mark.parametrize("case", [c for c in GOLDEN if "z" in c], ids=lambda c: c["name"])
+@pytest.mark.parametrize("route", ["pava", "hull"])
+def test_golden_fit(case, route):
+    y = np.array([float(v) for v in case["y"]], dtype=np.float32)
+    w = None if "w" not in case else np.array([float(v) for v in case["w"]], np.float32)
+    fn = oracle.pava if route == "pava" else oracle.hull_fit
+    z, starts, st = fn(y, w, bool(case.get("inc", 1)))
+    assert st == 0
+    np.testing.assert_allclose(z, [float(v) for v in case["z"]], rtol=0, atol=1e-15)
+    if "starts" in case:
+        assert list(starts) == [int(v) for v in case["starts"]]
+
+
+def test_golden_running_totals():
+    case = [c for c in GOLDEN if c["name"] == "running_totals"][0]
+    W, S = oracle.points(np.array([float(v) for v in case["y"]], np.float32))
+    assert list(W) == [float(v) for v in case["W"]]
+    assert list(S) == [float(v) for v in case["S"]]
+
+
+def test_golden_gradient():
+    case = [c for c in GOLDEN if c["name"] == "grad_four"][0]
+    y = np.array([float(v) for v in case["y"]], np.float32)
+    _, starts, _ = oracle.pava(y)
+    dy = oracle.backward(np.array([float(v) for v in case["g"]], np.float32), starts)
+    np.testing.assert_allclose(dy, [float(v) for v in case["dy"]], atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# brute force over contiguous partitions, n <= 10
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(12))
+def test_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 11))
+    if seed % 3 == 0:
+        y = rng.integers(-3, 4, size=n).astype(np.float32)      # many ties
+    else:
+        y = rng.standard_normal(n).astype(np.float32)
+    w = None if seed % 2 == 0 else rng.uniform(0.1, 3.0, n).astype(np.float32)
+    obj, zb, _ = brute_force(y, np.ones(n, np.float32) if w is None else w)
+    for fn in (oracle.pava, oracle.hull_fit):
+        z, starts, st = fn(y, w)
+        assert st == 0
+        np.testing.assert_allclose(z, [float(v) for v in zb], rtol=0, atol=1e-12)
+    # the oracle's objective equals the brute-force minimum
+    z, _, _ = oracle.pava(y, w)
+    ww = np.ones(n) if w is None else w.astype(np.float64)
+    assert abs(float(np.sum(ww * (z - y) ** 2)) - float(obj)) <= 1e-10 * (1 + float(obj))
+
+
+def test_brute_force_catches_wrong_fits():
+    """The brute-force pin itself rejects plausible mistakes: a fit that pools on
+    a strict rise, or a plain (unweighted) mean used with weights."""
+    y = np.array([1, 3, 2, 4], np.float32)
+    w = np.array([1, 2, 1, 1], np.float32)
+    obj, zb, _ = brute_force(y, w)
+    assert [float(v) for v in zb] == [1.0, 8 / 3, 8 / 3, 4.0]   # weighted mean of (3,2) with w (2,1)
+    assert float(obj) > 0
+
+
+# ---------------------------------------------------------------------------
+# min-max formula (textbook identity), n <= 40
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(6))
+def test_minmax_formula(seed):
+    rng = np.random.default_rng(100 + seed)
+    n = 40
+    y = wl.family(wl.FAMILIES[seed % len(wl.FAMILIES)], 1, n, seed)[0]
+    w = rng.uniform(0.2, 2.0, n).astype(np.float32)
+    z, _, _ = oracle.pava(y, w)
+    scale = 1.0 + np.abs(y).max()
+    np.testing.assert_allclose(z, minmax_formula(y, w), rtol=0, atol=1e-12 * scale)
+
+
+# ---------------------------------------------------------------------------
+# KKT conditions (paper Section 7.6; groupant page Invariant / kkt_prefix)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fam", wl.FAMILIES)
+@pytest.mark.parametrize("weighting", wl.WEIGHTINGS)
+def test_kkt(fam, weighting):
+    n = 3000
+    y = wl.family(fam, 1, n, 3)[0]
+    w = wl.weights(weighting, 1, n, 3)
+    w = None if w is None else w[0]
+    z, starts, st = oracle.pava(y, w)
+    assert st == 0
+    ww = np.ones(n) if w is None else w.astype(np.float64)
+    tau = 1e-12 * float(np.sum(ww * np.abs(y.astype(np.float64)))) + 1e-300
+    r = kkt_residuals(y, w, z)
+    assert r.min() >= -tau                      # every prefix residual >= 0
+    assert abs(r[-1]) <= tau                    # total residual zero
+    rises = np.nonzero(z[1:] > z[:-1])[0]       # strict rise between k and k+1
+    assert np.all(np.abs(r[rises]) <= tau)      # prefix residual zero at every strict rise
+    assert np.all(np.diff(z) >= 0)              # feasible
+    # blocks partition the row and the fit is constant on each block (block conservation)
+    assert starts[0] == 1
+    b = np.cumsum(starts) - 1
+    for k in range(b[-1] + 1):
+        sel = b == k
+        zz = z[sel]
+        assert np.all(zz == zz[0])
+        mean = np.sum(ww[sel] * y[sel]) / np.sum(ww[sel])
+        mag = np.sum(ww[sel] * np.abs(y[sel])) / np.sum(ww[sel])   # cancellation scale
+        assert abs(mean - zz[0]) <= 1e-12 * (1 + mag)
+
+
+# ---------------------------------------------------------------------------
+# idempotence, invariances, closed forms
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", range(4))
+def test_idempotent_on_monotone(seed):
+    """Already non-decreasing vectors, ties included, are fixed points (groupant
+    page, ties_and_idempotence)."""
+    rng = np.random.default_rng(seed)
+    y = np.sort(rng.integers(0, 20, 500)).astype(np.float32)
+    z, _, _ = oracle.pava(y)
+    assert np.array_equal(z, y.astype(np.float64))
+    z2, _, _ = oracle.pava(z.astype(np.float32))
+    assert np.array_equal(z2, z)
+
+
+def test_shift_and_weight_scale():
+    rng = np.random.default_rng(5)
+    y = rng.integers(-50, 50, 400).astype(np.float32) / 8        # exact in fp32 under +3
+    w = rng.uniform(0.5, 2, 400).astype(np.float32)
+    z, _, _ = oracle.pava(y, w)
+    zs, _, _ = oracle.pava(y + np.float32(3.0), w)
+    np.testing.assert_allclose(zs, z + 3.0, atol=1e-12)
+    zw, _, _ = oracle.pava(y, w * np.float32(4.0))                # power of two: exact
+    np.testing.assert_allclose(zw, z, atol=1e-13)
+
+
+def test_decreasing_is_increasing_of_negated():
+    """The decreasing problem is the increasing one for -y (paper Section 2.1)."""
+    y = wl.family("gaussian", 1, 777, 9)[0]
+    w = wl.weights("uniform", 1, 777, 9)[0]
+    zd, bd, _ = oracle.pava(y, w, increasing=False)
+    zi, bi, _ = oracle.pava(-y, w, increasing=True)
+    np.testing.assert_array_equal(zd, -zi)
+    np.testing.assert_array_equal(bd, bi)
+    assert np.all(np.diff(zd) <= 0)
+
+
+def test_closed_forms():
+    # constant row: one block, identity
+    y = np.full(100, 2.5, np.float32)
+    z, s, _ = oracle.pava(y)
+    assert np.all(z == 2.5) and s.sum() == 1
+    # strictly decreasing row with weights: one block equal to the weighted mean
+    y = np.arange(50, 0, -1).astype(np.float32)
+    w = np.linspace(0.5, 2.0, 50).astype(np.float32)
+    z, s, _ = oracle.pava(y, w)
+    mean = np.sum(w.astype(np.float64) * y) / np.sum(w.astype(np.float64))
+    np.testing.assert_allclose(z, mean, atol=1e-12)
+    assert s.sum() == 1
+    # soft rank at eps = 1 pools every row into one block (paper Section 7.9)
+    ys = wl.soft_rank_rows(8, 512, 1.0, 0)
+    z, s, _ = oracle.pava(ys, None, increasing=False)
+    assert np.all(s.sum(axis=1) == 1)
+    np.testing.assert_allclose(z, np.broadcast_to(ys.astype(np.float64).mean(1, keepdims=True),
+                                                  ys.shape), atol=1e-9)
+    # n = 1: identity
+    z, s, _ = oracle.pava(np.array([-7.25], np.float32))
+    assert z[0] == -7.25 and s[0] == 1
+
+
+def test_every_point_a_vertex_on_increasing_data():
+    """Strictly increasing data: the fit is the data and every element starts a
+    block (paper Section 7.1, "in strictly increasing data all points are vertices")."""
+    y = np.cumsum(np.full(300, 0.25, np.float32)).astype(np.float32)
+    z, s, _ = oracle.pava(y)
+    assert np.array_equal(z, y.astype(np.float64)) and s.all()
+
+
+# ---------------------------------------------------------------------------
+# cross-checks: two routes of the oracle, and scipy / scikit-learn where installed
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("fam", wl.FAMILIES)
+def test_pava_matches_hull(fam):
+    y = wl.family(fam, 3, 2500, 11)
+    w = wl.weights("uniform", 3, 2500, 11)
+    for inc in (True, False):
+        zp, _, _ = oracle.pava(y, w, inc)
+        zh, _, _ = oracle.hull_fit(y, w, inc)
+        scale = 1.0 + np.abs(y).max()
+        np.testing.assert_allclose(zp, zh, rtol=0, atol=1e-9 * scale)
+
+
+def test_against_scipy():
+    so = pytest.importorskip("scipy.optimize")
+    if not hasattr(so, "isotonic_regression"):
+        pytest.skip("scipy without isotonic_regression")
+    y = wl.noisy_ramp(1, 20000, 4)[0]
+    w = wl.weights("uniform", 1, 20000, 4)[0]
+    ref = so.isotonic_regression(y.astype(np.float64), weights=w.astype(np.float64)).x
+    z, _, _ = oracle.pava(y, w)
+    np.testing.assert_allclose(z, ref, rtol=0, atol=1e-10)
+
+
+def test_against_sklearn():
+    iso = pytest.importorskip("sklearn.isotonic")
+    y = wl.noisy_ramp(1, 5000, 6)[0]
+    ref = iso.isotonic_regression(y.astype(np.float64), increasing=False)
+    z, _, _ = oracle.pava(y, None, increasing=False)
+    np.testing.assert_allclose(z, ref, rtol=0, atol=1e-10)
+
+
+# ---------------------------------------------------------------------------
+# gradients: finite differences in fp64 on data without near-ties (paper App. C)
+# ---------------------------------------------------------------------------
+def test_backward_finite_differences():
+    rng = np.random.default_rng(21)
+    n = 60
+    y = (rng.integers(-64, 64, n) / 16).astype(np.float32)
+    y = y + (np.arange(n) % 7) * np.float32(1 / 256)             # break exact ties
+    w = rng.uniform(0.5, 2.0, n).astype(np.float32)
+    g = rng.standard_normal(n).astype(np.float32)
+    z0, starts, _ = oracle.pava(y, w)
+    dy = oracle.backward(g, starts, w)
+    dw = oracle.backward_w(g, starts, w, y, z0)
+    h = np.float32(2.0 ** -12)
+    for j in range(n):
+        yp = y.copy(); yp[j] += h
+        zp, sp, _ = oracle.pava(yp, w)
+        fd = float(np.dot(g.astype(np.float64), (zp - z0))) / float(h)
+        if np.array_equal(sp, starts):
+            assert abs(fd - dy[j]) <= 1e-6 * (1 + abs(dy[j])), j
+        wp = w.copy(); wp[j] += h
+        zq, sq, _ = oracle.pava(y, wp)
+        fdw = float(np.dot(g.astype(np.float64), (zq - z0))) / float(np.float32(wp[j]) - w[j])
+        if np.array_equal(sq, starts):
+            assert abs(fdw - dw[j]) <= 1e-3 * (1 + abs(dw[j])), j
+
+
+def test_backward_row_mean_closed_form():
+    """One block per row: the gradient is the row mean of g, broadcast."""
+    ys = wl.soft_rank_rows(4, 256, 1.0, 2)
+    _, s, _ = oracle.pava(ys, None, increasing=False)
+    g = wl.normal((4, 256), 3)
+    out = oracle.backward(g, s)
+    np.testing.assert_allclose(out, np.broadcast_to(g.astype(np.float64).mean(1, keepdims=True),
+                                                    g.shape), atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# error convention
+# ---------------------------------------------------------------------------
+def test_bad_rows_flagged():
+    y = wl.noisy_ramp(3, 50, 1)
+    y[1, 7] = np.nan
+    w = np.ones_like(y)
+    w[2, 3] = 0.0
+    z, _, st = oracle.pava(y, w)
+    assert list(st) == [0, oracle.BAD_Y, oracle.BAD_W]
+    assert np.isnan(z[1]).all() and np.isnan(z[2]).all() and np.isfinite(z[0]).all()
