@@ -1,0 +1,216 @@
+"""GB300 (sm_103a) batched and long-row weighted isotonic regression.
+
+Thin Python binding over the C ABI of ``libiso.so`` (declared in
+``include/iso.h``): argument marshalling only.  Every step of the fit and of its
+backward runs in the library's CUDA kernels; PyTorch supplies device memory
+and the current stream.  There is no CPU fallback: without the compiled
+library or a CUDA device the calls raise.
+
+Entry points (same names as the C ABI):
+
+* :func:`iso_fit` -- forward fit of ``[rows, n]`` float32 CUDA tensors.
+* :func:`iso_backward` -- block-averaging backward.
+* :func:`iso_fit_workspace_bytes`, :func:`iso_backward_workspace_bytes`.
+* :func:`isotonic` -- differentiable convenience op (autograd), which also
+  accepts host tensors (copied to the GPU and back).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libiso.so")
+
+ISO_OK = 0
+ISO_ERR_INVALID_ARG = -1
+ISO_ERR_WORKSPACE = -2
+ISO_ERR_CUDA = -3
+ISO_ERR_TIMEOUT = -4
+ISO_ROW_BAD_Y = 1
+ISO_ROW_BAD_W = 2
+
+EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
+           "iso_backward_workspace_bytes", "iso_backward")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class IsoError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load_library(path: str | None = None):
+    """Load libiso.so (building it first if it is missing and nvcc is present)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            from . import _build
+            _build.build()
+        lib = ctypes.CDLL(p)
+        i64, vp, ci, sz = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.iso_version.argtypes = []
+        lib.iso_version.restype = ci
+        lib.iso_status_string.argtypes = [ci]
+        lib.iso_status_string.restype = ctypes.c_char_p
+        lib.iso_fit_workspace_bytes.argtypes = [i64, i64, ci]
+        lib.iso_fit_workspace_bytes.restype = sz
+        lib.iso_backward_workspace_bytes.argtypes = [i64, i64, ci]
+        lib.iso_backward_workspace_bytes.restype = sz
+        lib.iso_fit.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp, sz, vp, vp]
+        lib.iso_fit.restype = ci
+        lib.iso_backward.argtypes = [vp, vp, vp, i64, i64, vp, vp, sz, vp]
+        lib.iso_backward.restype = ci
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().iso_status_string(int(status)).decode()
+
+
+def iso_fit_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
+    return int(load_library().iso_fit_workspace_bytes(int(rows), int(n), int(bool(weighted))))
+
+
+def iso_backward_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
+    return int(load_library().iso_backward_workspace_bytes(int(rows), int(n), int(bool(weighted))))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check_dev(t, name, dtype):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _shape2(t):
+    if t.dim() == 1:
+        return 1, t.shape[0]
+    if t.dim() == 2:
+        return t.shape[0], t.shape[1]
+    raise ValueError("expected a [n] or [rows, n] tensor")
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, workspace, device):
+    torch = _torch()
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def iso_fit(y, w=None, increasing: bool = True, *, out=None, blocks=None, want_blocks: bool = True,
+            row_status=None, workspace=None, stream=None):
+    """Fit every row of ``y`` (float32 CUDA, ``[n]`` or ``[rows, n]``).
+
+    Returns ``(out, blocks, row_status)``; ``blocks`` is None when
+    ``want_blocks`` is False and none was given.  ``workspace`` may be a uint8
+    CUDA tensor of at least :func:`iso_fit_workspace_bytes` bytes (allocated
+    here otherwise)."""
+    torch = _torch()
+    _check_dev(y, "y", torch.float32)
+    rows, n = _shape2(y)
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+        if w.shape != y.shape:
+            raise ValueError("w must have the shape of y")
+    if out is None:
+        out = torch.empty_like(y)
+    if blocks is None and want_blocks:
+        blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+    if row_status is None:
+        row_status = torch.empty(rows, dtype=torch.int32, device=y.device)
+    nbytes = iso_fit_workspace_bytes(rows, n, w is not None)
+    ws, ws_bytes = _workspace(nbytes, workspace, y.device)
+    st = load_library().iso_fit(
+        y.data_ptr(), None if w is None else w.data_ptr(), rows, n, int(bool(increasing)),
+        out.data_ptr(), None if blocks is None else blocks.data_ptr(),
+        None if ws is None else ws.data_ptr(), ws_bytes, row_status.data_ptr(), _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_fit")
+    return out, blocks, row_status
+
+
+def iso_backward(grad, blocks, w=None, *, out=None, workspace=None, stream=None):
+    """Block-averaging backward: ``out_i = w_i * G / W`` over the blocks of ``blocks``."""
+    torch = _torch()
+    _check_dev(grad, "grad", torch.float32)
+    _check_dev(blocks, "blocks", torch.uint8)
+    rows, n = _shape2(grad)
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+    if out is None:
+        out = torch.empty_like(grad)
+    nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
+    ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
+    st = load_library().iso_backward(
+        grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), rows, n,
+        out.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_backward")
+    return out
+
+
+def _make_function():
+    torch = _torch()
+
+    class _Isotonic(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, y, w, increasing):
+            out, blocks, _ = iso_fit(y.contiguous(), None if w is None else w.contiguous(),
+                                     increasing)
+            ctx.save_for_backward(blocks, w)
+            return out
+
+        @staticmethod
+        def backward(ctx, g):
+            blocks, w = ctx.saved_tensors
+            gy = iso_backward(g.contiguous(), blocks, w)
+            return gy, None, None
+
+    return _Isotonic
+
+
+_Fn = None
+
+
+def isotonic(y, w=None, increasing: bool = True):
+    """Differentiable isotonic regression of each row of ``y`` (gradient with
+    respect to ``y``).  Host tensors are copied to the current CUDA device and
+    the result is copied back."""
+    global _Fn
+    torch = _torch()
+    if _Fn is None:
+        _Fn = _make_function()
+    host = not y.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        y = y.to(dev, non_blocking=True)
+        w = None if w is None else w.to(dev, non_blocking=True)
+    z = _Fn.apply(y, w, bool(increasing))
+    if host:
+        z = z.to("cpu")
+    return z

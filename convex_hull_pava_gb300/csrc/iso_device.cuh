@@ -1,0 +1,333 @@
+// Device building blocks of the isotonic fit: fixed-point coordinates, the turn
+// predicate, lane hulls in a register bit mask, and walking merges of neighbouring
+// hulls inside a tile of lanes.
+//
+// References are to "Merge Hulls Without Copying Vertices: GPU Isotonic
+// Regression" (the paper).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace isodev {
+
+constexpr int kPts = 32;        // elements (points) per lane, Section 3.1
+constexpr int kRow = 33;        // lane-relative cumulative sums per lane: points 0..32
+constexpr unsigned kFull = 0xffffffffu;
+
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// ---------------------------------------------------------------------------
+// Fixed point.  A tile (a short row, or one chunk of a long row) rounds its
+// values to integer multiples of a power of two chosen from the largest
+// exponent in the tile, so that every value is below 2^50 in magnitude: the
+// grid is 2^-50 of the tile's largest value, as fine as an fp64 sum of that
+// tile.  Sums of these integers (below 2^63 for 8,192 values) are exact and
+// independent of order, and every turn test on them is exact.  The fp32 input
+// carries 24 significant bits, so values within 2^26 of the tile's largest
+// exponent are represented without any rounding.
+// ---------------------------------------------------------------------------
+
+// Biased float32 exponent, with zero and subnormals mapped to 1.
+__device__ __forceinline__ int bexp(float v) {
+    int e = (__float_as_uint(v) >> 23) & 0xff;
+    return e == 0 ? 1 : e;
+}
+
+// round(v / 2^(emax - 176)): |result| < 2^50 when bexp(v) <= emax.
+// Rounds half away from zero; a non-finite v gives an arbitrary finite value
+// (the row is flagged and its output discarded).
+__device__ __forceinline__ int64_t quant(float v, int emax) {
+    const uint32_t b = __float_as_uint(v);
+    int e = (b >> 23) & 0xff;
+    uint32_t m = b & 0x7fffffu;
+    if (e) m |= 0x800000u; else e = 1;
+    const int s = e - emax + 26;
+    uint64_t mag;
+    if (s >= 0) {
+        mag = (uint64_t)m << min(s, 26);
+    } else {
+        const int r = -s;
+        mag = r >= 32 ? 0ull : (uint64_t)((m + ((1u << r) >> 1)) >> r);
+    }
+    const int64_t v64 = (int64_t)mag;
+    return (b >> 31) ? -v64 : v64;
+}
+
+// round(w*y / 2^(pemax - 302)) from the exact 48-bit product of the mantissas:
+// |result| < 2^50 when bexp(w) + bexp(y) <= pemax.
+__device__ __forceinline__ int64_t quant_prod(float w, float y, int pemax) {
+    const uint32_t bw = __float_as_uint(w), by = __float_as_uint(y);
+    int ew = (bw >> 23) & 0xff, ey = (by >> 23) & 0xff;
+    uint32_t mw = bw & 0x7fffffu, my = by & 0x7fffffu;
+    if (ew) mw |= 0x800000u; else ew = 1;
+    if (ey) my |= 0x800000u; else ey = 1;
+    const uint64_t prod = (uint64_t)mw * (uint64_t)my;
+    const int t = pemax - (ew + ey) - 2;
+    uint64_t mag;
+    if (t <= 0) {
+        mag = prod << min(-t, 2);
+    } else {
+        mag = t >= 64 ? 0ull : ((prod >> (t - 1)) + 1ull) >> 1;   // round half up
+    }
+    const int64_t v64 = (int64_t)mag;
+    return ((bw ^ by) >> 31) ? -v64 : v64;
+}
+
+// Quantum exponents: value = integer * 2^q.
+__device__ __forceinline__ int qexp_unit(int emax) { return emax - 176; }
+__device__ __forceinline__ int qexp_prod(int pemax) { return pemax - 302; }
+
+// ---------------------------------------------------------------------------
+// Turn predicate.  For points O, A, B with A - O = (w1, s1), B - O = (w2, s2),
+// the turn O -> A -> B is strictly left (A strictly below the segment O-B on a
+// lower hull scanned by increasing W) iff w1*s2 - s1*w2 > 0.  WIDE selects
+// 128-bit products: needed everywhere except inside one lane of a unit-weight
+// tile, where |w| <= 32 and |s| < 2^56.
+// ---------------------------------------------------------------------------
+template <bool WIDE>
+__device__ __forceinline__ bool left_turn(int64_t w1, int64_t s1, int64_t w2, int64_t s2) {
+    if constexpr (WIDE) {
+        __int128 a = (__int128)w1 * (__int128)s2;
+        __int128 b = (__int128)s1 * (__int128)w2;
+        return a > b;
+    } else {
+        return w1 * s2 > s1 * w2;
+    }
+}
+
+// Exact sign of a*b - c*d for signed 128-bit operands (products up to 256 bits),
+// used by the merge levels, whose row coordinates exceed 64 bits.
+struct U256 { uint64_t w[4]; };
+
+__device__ __forceinline__ U256 mul_u128(unsigned __int128 a, unsigned __int128 b) {
+    const uint64_t a0 = (uint64_t)a, a1 = (uint64_t)(a >> 64);
+    const uint64_t b0 = (uint64_t)b, b1 = (uint64_t)(b >> 64);
+    const unsigned __int128 p00 = (unsigned __int128)a0 * b0;
+    const unsigned __int128 p01 = (unsigned __int128)a0 * b1;
+    const unsigned __int128 p10 = (unsigned __int128)a1 * b0;
+    const unsigned __int128 p11 = (unsigned __int128)a1 * b1;
+    U256 r;
+    r.w[0] = (uint64_t)p00;
+    unsigned __int128 mid = (p00 >> 64) + (uint64_t)p01 + (uint64_t)p10;
+    r.w[1] = (uint64_t)mid;
+    unsigned __int128 hi = (mid >> 64) + (p01 >> 64) + (p10 >> 64) + (uint64_t)p11;
+    r.w[2] = (uint64_t)hi;
+    r.w[3] = (uint64_t)(hi >> 64) + (uint64_t)(p11 >> 64);
+    return r;
+}
+
+__device__ __forceinline__ int cmp_u256(const U256& x, const U256& y) {
+    for (int i = 3; i >= 0; --i) {
+        if (x.w[i] != y.w[i]) return x.w[i] > y.w[i] ? 1 : -1;
+    }
+    return 0;
+}
+
+// sign(a*b - c*d)
+__device__ __forceinline__ int sign_det128(__int128 a, __int128 b, __int128 c, __int128 d) {
+    const int sab = ((a > 0) - (a < 0)) * ((b > 0) - (b < 0));
+    const int scd = ((c > 0) - (c < 0)) * ((d > 0) - (d < 0));
+    if (sab != scd) return sab > scd ? 1 : -1;        // also covers zero products
+    if (sab == 0) return 0;
+    auto uabs = [](__int128 x) -> unsigned __int128 {
+        return x < 0 ? (unsigned __int128)(-(x + 1)) + 1u : (unsigned __int128)x;
+    };
+    const int c3 = cmp_u256(mul_u128(uabs(a), uabs(b)), mul_u128(uabs(c), uabs(d)));
+    return sab > 0 ? c3 : -c3;
+}
+
+// ---------------------------------------------------------------------------
+// Lane hull (Section 3.1).  One lane runs the monotone chain over its points
+// 0..e (e <= 32 elements), keeping the stack as a bit mask: bit k set while
+// point k is on the stack; the top and the entry below it are kept in
+// registers and the next entry below is found by count-leading-zeros.  A turn
+// of zero pops, so collinear middle points are dropped (Section 4).
+//
+// Only points that are locally convex can be vertices of any hull that
+// contains them (Lemma 4.1); `cand` holds those among 1..e-1, and the chain
+// visits only them.  Point e (the lane's end) is always pushed last and is
+// not part of the returned mask.
+// ---------------------------------------------------------------------------
+template <bool WEIGHTED>
+__device__ __forceinline__ uint32_t lane_hull(const int64_t* Sx, const int64_t* Wx, uint32_t cand,
+                                              int e) {
+    uint32_t mask = 1u;
+    int t = 0, b = -1;
+    int64_t St = 0, Wt = 0, Sb = 0, Wb = 0;
+    uint32_t rem = cand & ~1u;
+    int k = rem ? (__ffs(rem) - 1) : e;
+    rem &= rem - 1u;
+    int64_t Sk = Sx[k];
+    int64_t Wk = WEIGHTED ? Wx[k] : (int64_t)k;
+    bool done = (e <= 0);
+    // each point is pushed once and popped at most once
+    for (int it = 0; it < 2 * kPts + 2 && !done; ++it) {
+        bool push = (b < 0) || left_turn<WEIGHTED>(Wt - Wb, St - Sb, Wk - Wb, Sk - Sb);
+        if (push) {
+            if (k >= e) {
+                done = true;
+            } else {
+                mask |= 1u << k;
+                b = t; Sb = St; Wb = Wt;
+                t = k; St = Sk; Wt = Wk;
+                k = rem ? (__ffs(rem) - 1) : e;
+                rem &= rem - 1u;
+                Sk = Sx[k];
+                Wk = WEIGHTED ? Wx[k] : (int64_t)k;
+            }
+        } else {
+            mask &= ~(1u << t);
+            t = b; St = Sb; Wt = Wb;
+            uint32_t below = mask & ((1u << t) - 1u);
+            b = below ? (31 - __clz(below)) : -1;
+            if (b >= 0) {
+                Sb = Sx[b];
+                Wb = WEIGHTED ? Wx[b] : (int64_t)b;
+            }
+        }
+    }
+    return mask;
+}
+
+// ---------------------------------------------------------------------------
+// A tile: L consecutive lanes (a power of two) holding one row, or one chunk of
+// a row, with nt elements (points 0..nt).  Vertex flags for points 0..nt-1 are
+// the lanes' mask bits (point p: lane p/32, bit p%32); point nt, the tile's
+// end, is always a vertex.  Coordinates are tile-relative: the lane's start
+// plus the lane-relative cumulative sum.
+// ---------------------------------------------------------------------------
+struct Tile {
+    const int64_t* Sx;   // [L][kRow] lane-relative S (row of the tile's lane 0 first)
+    const int64_t* Wx;   // [L][kRow] lane-relative W, weighted tiles only
+    const int64_t* LS;   // [L+1] lane starts of S, LS[L] = tile total
+    const int64_t* LW;   // [L+1] lane starts of W (weighted)
+    uint32_t* mask;      // [L] vertex masks
+    uint32_t* summ;      // non-empty-lane bits; bit (sbase + lane) for lane of this tile
+    int sbase;           // bit offset of the tile's lane 0 in summ
+    int L;               // lanes
+    int nt;              // elements
+};
+
+template <bool WEIGHTED>
+__device__ __forceinline__ int64_t tile_S(const Tile& T, int p) {
+    int l = p >> 5, k = p & 31;
+    return T.LS[l] + (k ? T.Sx[l * kRow + k] : 0);
+}
+template <bool WEIGHTED>
+__device__ __forceinline__ int64_t tile_W(const Tile& T, int p) {
+    if constexpr (WEIGHTED) {
+        int l = p >> 5, k = p & 31;
+        return T.LW[l] + (k ? T.Wx[l * kRow + k] : 0);
+    } else {
+        return (int64_t)p;
+    }
+}
+
+__device__ __forceinline__ bool summ_bit(const Tile& T, int lane) {
+    int b = T.sbase + lane;
+    return (T.summ[b >> 5] >> (b & 31)) & 1u;
+}
+
+// Highest non-empty lane in [lo, hi), or -1.
+__device__ __forceinline__ int prev_nonempty(const Tile& T, int lo, int hi) {
+    int b = T.sbase + hi - 1, bl = T.sbase + lo;
+    while (b >= bl) {
+        int wi = b >> 5;
+        uint32_t word = T.summ[wi] & (0xffffffffu >> (31 - (b & 31)));
+        int wlo = wi << 5;
+        if (wlo < bl) word &= ~((1u << (bl - wlo)) - 1u);
+        if (word) return wlo + 31 - __clz(word) - T.sbase;
+        b = wlo - 1;
+    }
+    return -1;
+}
+
+// Lowest non-empty lane in [lo, hi), or -1.
+__device__ __forceinline__ int next_nonempty(const Tile& T, int lo, int hi) {
+    int b = T.sbase + lo, bh = T.sbase + hi;
+    while (b < bh) {
+        int wi = b >> 5;
+        int wlo = wi << 5;
+        uint32_t word = T.summ[wi] & (0xffffffffu << (b & 31));
+        if (bh - wlo < 32) word &= (1u << (bh - wlo)) - 1u;
+        if (word) return wlo + __ffs(word) - 1 - T.sbase;
+        b = wlo + 32;
+    }
+    return -1;
+}
+
+// Highest vertex < p among lanes [lo_lane, ...); -1 if none.
+__device__ __forceinline__ int tile_pred(const Tile& T, int p, int lo_lane) {
+    int l = p >> 5, k = p & 31;
+    if (l < T.L) {
+        uint32_t m = T.mask[l] & ((1u << k) - 1u);
+        if (m) return (l << 5) + 31 - __clz(m);
+    }
+    int q = prev_nonempty(T, lo_lane, min(l, T.L));
+    if (q < 0) return -1;
+    return (q << 5) + 31 - __clz(T.mask[q]);
+}
+
+// Lowest vertex > p among lanes [.., hi_lane); `endp` if none.
+__device__ __forceinline__ int tile_succ(const Tile& T, int p, int hi_lane, int endp) {
+    int l = p >> 5, k = p & 31;
+    uint32_t m = T.mask[l] & ~((2u << k) - 1u);
+    if (k == 31) m = 0;
+    if (m) return (l << 5) + __ffs(m) - 1;
+    int q = next_nonempty(T, l + 1, hi_lane);
+    if (q < 0) return endp;
+    return (q << 5) + __ffs(T.mask[q]) - 1;
+}
+
+// Turn test on three tile points.
+template <bool WEIGHTED>
+__device__ __forceinline__ bool tile_left(const Tile& T, int o, int a, int b) {
+    int64_t So = tile_S<WEIGHTED>(T, o), Wo = tile_W<WEIGHTED>(T, o);
+    int64_t Sa = tile_S<WEIGHTED>(T, a), Wa = tile_W<WEIGHTED>(T, a);
+    int64_t Sb = tile_S<WEIGHTED>(T, b), Wb = tile_W<WEIGHTED>(T, b);
+    return left_turn<true>(Wa - Wo, Sa - So, Wb - Wo, Sb - So);
+}
+
+// Bridge of the merge of lane groups A = [A0, B0) and B = [B0, Bend) (Section
+// 3.2, Lemma 4.2): s = 32*B0 is the last vertex of H(A) and the first of H(B).
+// If the chain is convex at s, returns (s, s).  Otherwise walks from s's
+// neighbours, the left end left and the right end right, until the line
+// between them supports both hulls.  Each step removes a vertex (Lemma 5.1).
+template <bool WEIGHTED>
+__device__ void tile_bridge(const Tile& T, int A0, int B0, int Bend, int& ra, int& rb) {
+    const int s = B0 << 5;
+    const int endB = min(Bend << 5, T.nt);
+    const int startA = A0 << 5;
+    int a = tile_pred(T, s, A0);
+    int b = tile_succ(T, s, Bend, endB);
+    if (tile_left<WEIGHTED>(T, a, s, b)) { ra = s; rb = s; return; }
+    for (;;) {
+        bool moved = false;
+        while (a > startA) {
+            int p = tile_pred(T, a, A0);
+            if (tile_left<WEIGHTED>(T, p, a, b)) break;
+            a = p; moved = true;
+        }
+        while (b < endB) {
+            int q = tile_succ(T, b, Bend, endB);
+            if (tile_left<WEIGHTED>(T, a, b, q)) break;
+            b = q; moved = true;
+        }
+        if (!moved) break;
+    }
+    ra = a; rb = b;
+}
+
+// Clear this lane's vertex bits strictly between a and b.
+__device__ __forceinline__ uint32_t clear_between(uint32_t m, int lane, int a, int b) {
+    int lo = max(a + 1 - (lane << 5), 0);
+    int hi = min(b - (lane << 5), 32);
+    if (lo < hi) {
+        uint32_t span = (hi - lo == 32) ? 0xffffffffu : (((1u << (hi - lo)) - 1u) << lo);
+        m &= ~span;
+    }
+    return m;
+}
+
+}  // namespace isodev

@@ -1,0 +1,29 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace isodev {
+
+// Longest row handled by the whole-row kernels (one CTA of 256 lanes x 32).
+constexpr int kRowMax = 8192;
+
+cudaError_t rows_fit(const float* y, const float* w, int64_t rows, int n, int increasing,
+                     float* out, uint8_t* blocks, uint32_t* row_status, cudaStream_t stream);
+
+cudaError_t rows_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
+                          int n, float* out, cudaStream_t stream);
+
+// Long rows (n > kRowMax): chunk hulls, segment-list merge tree, expansion.
+size_t long_fit_workspace(int64_t rows, int64_t n, bool weighted);
+cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, int increasing,
+                     float* out, uint8_t* blocks, void* ws, size_t ws_bytes, uint32_t* row_status,
+                     cudaStream_t stream);
+
+size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted);
+cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
+                          int64_t n, float* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+}  // namespace isodev

@@ -1,0 +1,127 @@
+/*
+ * iso.h -- C ABI of the GB300 (sm_103a) isotonic-regression library libiso.so.
+ *
+ * The operation ("Merge Hulls Without Copying Vertices: GPU Isotonic Regression",
+ * Section 2.1, eq. (1)): for every row y_1..y_n with weights w_i > 0, the unique
+ * z with z_1 <= z_2 <= ... <= z_n that minimises sum_i w_i (z_i - y_i)^2.  The
+ * decreasing problem is the increasing one for -y (same section).  z is taken,
+ * as in eq. (3), as the slopes of the lower convex hull of the cumulative-sum
+ * diagram P_k = (W_k, S_k), W_k = sum_{i<=k} w_i, S_k = sum_{i<=k} w_i y_i
+ * (eq. (2)); the hull's vertices are the starts of the fit's blocks.
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: row-major, contiguous [rows, n] float32 arrays (row r starts at
+ *    element r*n), on the device.  Any 4-byte alignment is accepted.
+ *  - Ownership: the caller owns every buffer, the workspace and the stream.
+ *    The library allocates no memory, keeps no state between calls, and never
+ *    synchronises the stream: every call only enqueues kernels on `stream`
+ *    (a cudaStream_t; NULL = the legacy default stream) and returns.
+ *  - Errors the host can see (NULL pointers, non-positive or oversized shapes,
+ *    a workspace that is too small or misaligned) return a negative status and
+ *    enqueue nothing.  A failed kernel launch returns ISO_ERR_CUDA.
+ *  - Errors in the data (a non-finite y, a weight that is not finite and
+ *    positive) never fail the call: that row's outputs are NaN, its block
+ *    flags are 0, and its bit in `row_status` is set (the paper's per-row NaN
+ *    flags, Section 6 "Blocks and memory", without its host synchronisation).
+ *  - Limits: 1 <= n <= 2^31 - 1, 1 <= rows, rows * n <= 2^40.
+ */
+#ifndef ISO_H
+#define ISO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ISO_OK = 0,
+    ISO_ERR_INVALID_ARG = -1, /* NULL pointer, bad shape or flag                 */
+    ISO_ERR_WORKSPACE = -2,   /* workspace NULL / too small / not 256-B aligned */
+    ISO_ERR_CUDA = -3,        /* a CUDA call or kernel launch failed            */
+    ISO_ERR_TIMEOUT = -4      /* reserved: a bounded device-side wait gave up   */
+} iso_status;
+
+/* Bits of a row's status word. */
+#define ISO_ROW_BAD_Y 1u /* the row holds a NaN or infinite y                   */
+#define ISO_ROW_BAD_W 2u /* the row holds a weight that is not finite and > 0   */
+
+/* Version of this ABI (major * 10000 + minor * 100 + patch). */
+int iso_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char *iso_status_string(int status);
+
+/*
+ * Bytes of device workspace that iso_fit needs for `rows` rows of `n` elements
+ * (`weighted` != 0 when w is given).  0 means no workspace is needed.  Returns
+ * 0 as well for invalid shapes (iso_fit then reports the error).
+ */
+size_t iso_fit_workspace_bytes(int64_t rows, int64_t n, int weighted);
+
+/*
+ * iso_fit -- forward fit.
+ *
+ * Defined by eq. (1)-(3) of the paper (Section 2.1); the method is the paper's
+ * Section 3: lane hulls kept in register bit masks, lane and chunk merges by
+ * walking to the bridge, and, for rows longer than one chunk, a merge tree
+ * whose nodes are lists of segments of the chunk hulls (Section 3.3), followed
+ * by reconstruction (Section 3.4).
+ *
+ *  y          [rows, n] float32, device, read only.
+ *  w          [rows, n] float32, device, read only, or NULL for unit weights.
+ *  rows, n    shape.
+ *  increasing 1: non-decreasing fit; 0: non-increasing fit (fit of -y, negated).
+ *  out        [rows, n] float32, device, written: the fit.  Every value is
+ *             rounded to float32 once from the slope of its hull edge; the
+ *             output is not forced to be monotone (no cumulative maximum),
+ *             as in the paper's Section 6 "Output".
+ *  blocks     [rows, n] uint8, device, written, or NULL: blocks[i] = 1 where
+ *             element i starts a block (its left point is a hull vertex; the
+ *             paper's block-start byte of Section 6 "Gradient"), else 0.
+ *             blocks[0] of a valid row is always 1.  Needed by iso_backward.
+ *  workspace  device scratch of at least iso_fit_workspace_bytes(rows, n, w != NULL)
+ *             bytes, 256-byte aligned; may be NULL when that size is 0.  Its
+ *             contents on entry do not matter.  Calls that share one workspace
+ *             must not overlap in time (use one stream).
+ *  row_status [rows] uint32, device, written, or NULL: 0 or ISO_ROW_BAD_* bits.
+ *  stream     cudaStream_t to enqueue on.
+ *
+ * Accuracy: cumulative sums are exact integer sums of values rounded to a
+ * fixed-point grid of 2^-31 of the largest |w*y| (and |w|) of each chunk; the
+ * fit deviates from the exact one by about that amount plus one float32
+ * rounding of each slope.
+ */
+iso_status iso_fit(const float *y, const float *w, int64_t rows, int64_t n, int increasing,
+                   float *out, uint8_t *blocks, void *workspace, size_t workspace_bytes,
+                   uint32_t *row_status, void *stream);
+
+/* Bytes of device workspace that iso_backward needs (0 = none). */
+size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted);
+
+/*
+ * iso_backward -- vector-Jacobian product of the fit with respect to y.
+ *
+ * The paper's Section 6 "Gradient": the fit is constant on blocks and equals
+ * the block's weighted mean, so with G and W the sums of grad and of w over
+ * element i's block, d/dy_i = w_i * G / W (G / |block| for unit weights).
+ * The blocks are those that iso_fit wrote into `blocks`.
+ *
+ *  grad       [rows, n] float32, device: gradient with respect to the fit.
+ *  blocks     [rows, n] uint8, device: block starts as written by iso_fit
+ *             (element 0 of a row is treated as a start whatever its value).
+ *  w          [rows, n] float32 or NULL, the weights given to iso_fit.
+ *  out        [rows, n] float32, device, written.
+ *  workspace  as for iso_fit, of iso_backward_workspace_bytes(rows, n, w != NULL) bytes.
+ *  stream     cudaStream_t.
+ */
+iso_status iso_backward(const float *grad, const uint8_t *blocks, const float *w, int64_t rows,
+                        int64_t n, float *out, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ISO_H */

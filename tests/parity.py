@@ -1,0 +1,59 @@
+"""Parity criteria between the CUDA path and the fp64 oracle.
+
+* Fit: max_i |out_i - z*_i| <= 1e-5 * (1 + max_i |y_i|) per row, with z* the
+  oracle's fp64 value (not rounded to fp32).
+* Blocks: every oracle block boundary whose adjacent block means differ by more
+  than 1e-6 relative (|m_k - m_{k-1}| > 1e-6 * max(|m_k|, |m_{k-1}|)) must be a
+  boundary of the CUDA path; a CUDA boundary that the oracle does not have must
+  split a tie (|out_i - out_{i-1}| within the fit tolerance); inside one CUDA
+  block the output is constant; element 0 starts a block.
+"""
+import numpy as np
+
+FIT_TOL = 1e-5
+GAP_REL = 1e-6
+
+
+def fit_tol(y):
+    y = np.asarray(y, dtype=np.float64)
+    return FIT_TOL * (1.0 + np.abs(y).max(axis=-1))
+
+
+def check_row(y, out, blocks, z, zb, label=""):
+    """y: float32 [n]; out: float32 [n] (CUDA); blocks: uint8 [n] (CUDA);
+    z: float64 [n] (oracle); zb: uint8 [n] (oracle block starts)."""
+    y = np.asarray(y, np.float64)
+    out = np.asarray(out, np.float64)
+    tol = FIT_TOL * (1.0 + np.abs(y).max())
+    err = np.abs(out - z)
+    imax = int(err.argmax())
+    assert err[imax] <= tol, f"{label}: fit error {err[imax]:.3e} > {tol:.3e} at {imax} (out {out[imax]!r}, oracle {z[imax]!r})"
+    if blocks is None:
+        return
+    blocks = np.asarray(blocks).astype(bool)
+    zb = np.asarray(zb).astype(bool)
+    assert blocks[0], f"{label}: element 0 does not start a block"
+    n = y.size
+    if n > 1:
+        inner = ~blocks[1:]
+        bad = np.nonzero(inner & (out[1:] != out[:-1]))[0]
+        assert bad.size == 0, f"{label}: output not constant inside a block at {bad[:5] + 1}"
+        gap = np.abs(z[1:] - z[:-1])
+        scale = np.maximum(np.abs(z[1:]), np.abs(z[:-1]))
+        required = zb[1:] & (gap > GAP_REL * scale)
+        missing = np.nonzero(required & ~blocks[1:])[0]
+        assert missing.size == 0, f"{label}: oracle boundaries missing at {missing[:5] + 1} (gaps {gap[missing[:5]]})"
+        extra = np.nonzero(blocks[1:] & ~zb[1:])[0]
+        if extra.size:
+            d = np.abs(out[1:] - out[:-1])[extra]
+            assert d.max() <= tol, f"{label}: extra boundaries that are not ties at {extra[:5] + 1}"
+
+
+def check_rows(y, out, blocks, z, zb, label=""):
+    y = np.atleast_2d(y)
+    out = np.atleast_2d(out)
+    z = np.atleast_2d(z)
+    zb = np.atleast_2d(zb)
+    blocks = None if blocks is None else np.atleast_2d(blocks)
+    for r in range(y.shape[0]):
+        check_row(y[r], out[r], None if blocks is None else blocks[r], z[r], zb[r], f"{label} row {r}")

@@ -1,0 +1,74 @@
+"""The C ABI library builds, loads and exports every symbol include/iso.h
+declares; host-side argument checks work without a GPU (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import convex_hull_pava_gb300 as chp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "iso.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(iso_[a-z_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_names_match_binding():
+    assert set(declared_functions()) == set(chp.EXPORTS)
+
+
+def test_library_loads_and_exports():
+    lib = chp.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.iso_version() >= 100
+
+
+def test_workspace_queries_host_only():
+    assert chp.iso_fit_workspace_bytes(4096, 1024, False) == 0
+    assert chp.iso_fit_workspace_bytes(1, 10_000_000, False) > 0
+    assert chp.iso_fit_workspace_bytes(16, 4_194_304, True) > chp.iso_fit_workspace_bytes(16, 4_194_304, False)
+    assert chp.iso_backward_workspace_bytes(1024, 8192, False) == 0
+    assert chp.iso_backward_workspace_bytes(1, 10_000_000, False) > 0
+    # invalid shapes report 0
+    assert chp.iso_fit_workspace_bytes(0, 10, False) == 0
+    assert chp.iso_fit_workspace_bytes(1, 0, False) == 0
+    assert chp.iso_fit_workspace_bytes(1, 1 << 31, False) == 0
+
+
+def test_invalid_arguments_rejected_on_host():
+    lib = chp.load_library()
+    fake = ctypes.c_void_p(0x1000)
+    # NULL y / out, bad shapes, bad flag: rejected before any CUDA call
+    assert lib.iso_fit(None, None, 1, 10, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, 1, 10, 1, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, 0, 10, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, 1, -3, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, 1, 10, 2, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, 1 << 30, 1 << 30, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    # long rows need a workspace: missing / too small / misaligned
+    need = lib.iso_fit_workspace_bytes(1, 100000, 0)
+    assert lib.iso_fit(fake, None, 1, 100000, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_WORKSPACE
+    assert lib.iso_fit(fake, None, 1, 100000, 1, fake, None, ctypes.c_void_p(0x100000), need - 1, None, None) == chp.ISO_ERR_WORKSPACE
+    assert lib.iso_fit(fake, None, 1, 100000, 1, fake, None, ctypes.c_void_p(0x100010), need, None, None) == chp.ISO_ERR_WORKSPACE
+    assert lib.iso_backward(None, fake, None, 1, 10, fake, None, 0, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_backward(fake, None, None, 1, 10, fake, None, 0, None) == chp.ISO_ERR_INVALID_ARG
+    nb = lib.iso_backward_workspace_bytes(1, 100000, 0)
+    assert lib.iso_backward(fake, fake, None, 1, 100000, fake, None, 0, None) == chp.ISO_ERR_WORKSPACE
+    assert nb > 0
+
+
+def test_status_strings():
+    assert chp.status_string(0) == "ok"
+    assert "workspace" in chp.status_string(chp.ISO_ERR_WORKSPACE)
+
+
+def test_binding_rejects_host_tensors_without_fallback():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        chp.iso_fit(torch.zeros(10))
