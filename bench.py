@@ -1,0 +1,385 @@
+"""Benchmark of the isotonic fit on one GB300 (or N replicas under torchrun).
+
+Default workload: one row of 10,000,000 float32 values, y = linspace(0, 3, n)
++ N(0, 1) (seed 0), unit weights, non-decreasing fit.  One step is one call of
+iso_fit over that row (chunk hulls, segment-list merge tree, expansion).  The
+input (40 MB) and the fit (40 MB) fit in L2, so L2 is flushed (a 256 MB write)
+before every timed step, outside the timed interval; each step is timed with
+CUDA events on the launching stream.
+
+Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead
+(the reference arm of this build), on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "isotonic fit elements/s (1x10^7 row; batched rows) and HBM GB/s vs GB300 peak"
+UNIT = "elements/s"
+WORKLOAD = "row1e7"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_desc(W):
+    return {
+        "workload": "1 row x 10,000,000 fp32, y = linspace(0,3,n) + N(0,1) (seed 0), unit weights, "
+                    "non-decreasing fit",
+        "name": W.name, "rows": W.rows, "n": W.n, "weighted": W.weighted,
+        "increasing": W.increasing,
+        "l2": "flushed before every timed step (256 MB write outside the timed interval)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() in ("active", "1", "0x1"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# traffic figure from the committed ncu summary, valid only for the current source
+# ---------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "convex_hull_pava_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# reference arm / CPU baseline: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+def time_oracle(W, budget_s=10.0, max_reps=200):
+    import oracle
+    import numpy as np
+    oracle.build()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.pava(W.y, W.w, W.increasing)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= max_reps:
+            break
+    per = el / reps
+    return {"value": W.elements / per, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full passes of the fp64 PAVA oracle over the {W.rows}x{W.n} "
+                      f"workload, one thread, {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from convex_hull_pava_gb300 import workloads as wl
+    W = wl.make(WORKLOAD)
+    import oracle
+    oracle.build()
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.pava(W.y, W.w, W.increasing)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per = sum(times) / len(times)
+    val = W.elements / per
+    cb = {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle",
+          "sample": f"{len(times)} timed full passes over the {W.rows}x{W.n} workload, one thread"}
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_desc(W), "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import convex_hull_pava_gb300 as chp
+    from convex_hull_pava_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, peak_kind = peaks()
+
+    W = wl.make(WORKLOAD)
+    y = torch.from_numpy(W.y).to(dev)
+    w = None if W.w is None else torch.from_numpy(W.w).to(dev)
+    out = torch.empty_like(y)
+    blocks = torch.empty(y.shape, dtype=torch.uint8, device=dev)
+    status = torch.empty(W.rows, dtype=torch.int32, device=dev)
+    ws = torch.empty(max(chp.iso_fit_workspace_bytes(W.rows, W.n, w is not None), 1),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(want_blocks=False):
+        chp.iso_fit(y, w, W.increasing, out=out, blocks=blocks if want_blocks else None,
+                    want_blocks=want_blocks, row_status=status, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, L2 flushed before each, per-kernel events ----
+    chp.profile_enable(True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms, kern = [], {}
+    launches = 0
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        b.synchronize()
+        step_ms.append(a.elapsed_time(b))
+        for name, ms in chp.profile_read():
+            kern.setdefault(name, []).append(ms)
+            launches += 1
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    chp.profile_enable(False)
+
+    ms_step = float(np.mean(step_ms))
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * W.elements / (ms_step * 1e-3)
+
+    # dominant kernel and its roofline: algorithmic bytes of that kernel per launch
+    kavg = {k: float(np.mean(v)) for k, v in kern.items()}
+    dom = max(kavg, key=kavg.get)
+    alg_bytes = {
+        # read y (and w); the chunk hull reads the input once
+        "chunk_hull": W.elements * (8 if W.weighted else 4),
+        # write the fit
+        "expand": W.elements * 4,
+        # descriptor lists only; no per-element traffic
+        "merge": 0,
+    }
+    ab = alg_bytes.get(dom, W.elements * (12 if W.weighted else 8))
+    achieved = ab / (kavg[dom] * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "traffic": committed_traffic(dom),
+            "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab,
+            "kernel_ms": kavg}
+    fit_bytes = W.elements * (12 if W.weighted else 8)
+    whole = fit_bytes / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers ----
+    yh = torch.from_numpy(W.y).pin_memory()
+    oh = torch.empty(W.y.shape, dtype=torch.float32).pin_memory()
+    e2e_ms = []
+    for i in range(max(3, args.steps // 4) + 2):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        yd = yh.to(dev, non_blocking=True)
+        z, _, _ = chp.iso_fit(yd, None, W.increasing, want_blocks=False, workspace=ws,
+                              stream=stream)
+        oh.copy_(z, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = world * W.elements / (float(np.mean(e2e_ms)) * 1e-3)
+
+    # ---- the other named workloads (parity-test configurations), for context ----
+    also = {}
+    if not args.quick:
+        for name in ("batch4096x1024", "dense16x4m", "softrank1024x8192", "row65k"):
+            V = wl.make(name)
+            yv = torch.from_numpy(V.y).to(dev)
+            wv = None if V.w is None else torch.from_numpy(V.w).to(dev)
+            ov = torch.empty_like(yv)
+            bv = torch.empty(yv.shape, dtype=torch.uint8, device=dev)
+            wsv = torch.empty(max(chp.iso_fit_workspace_bytes(V.rows, V.n, wv is not None), 1),
+                              dtype=torch.uint8, device=dev)
+            def fv():
+                chp.iso_fit(yv, wv, V.increasing, out=ov, blocks=bv, workspace=wsv, stream=stream)
+            ts = []
+            for i in range(13):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+                a.record(stream); fv(); b.record(stream); b.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(b))
+            t = float(np.median(ts)) * 1e-3
+            by = V.elements * (12 if V.weighted else 8)
+            rec = {"elements_per_s": V.elements / t, "ms": t * 1e3, "gbs": by / t / 1e9,
+                   "frac": by / t / 1e9 / hbm_peak, "bytes": by}
+            if V.grad is not None:
+                gv = torch.from_numpy(V.grad).to(dev)
+                dv = torch.empty_like(gv)
+                wsb = torch.empty(max(chp.iso_backward_workspace_bytes(V.rows, V.n, wv is not None), 1),
+                                  dtype=torch.uint8, device=dev)
+                ts = []
+                for i in range(13):
+                    flush.zero_()
+                    a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    chp.iso_backward(gv, bv, wv, out=dv, workspace=wsb, stream=stream)
+                    b.record(stream); b.synchronize()
+                    if i >= 3:
+                        ts.append(a.elapsed_time(b))
+                tb = float(np.median(ts)) * 1e-3
+                bb = V.elements * (9 if wv is None else 13)
+                rec["backward"] = {"elements_per_s": V.elements / tb, "ms": tb * 1e3,
+                                   "gbs": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak}
+            also[name] = rec
+            del yv, wv, ov, bv, wsv
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = time_oracle(W, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "config": workload_desc(W),
+            "hbm_gbs_whole_call": whole, "hbm_frac_whole_call": whole / hbm_peak,
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": W.elements * 4,
+                    "d2h_bytes_per_step": W.elements * 4},
+            "gpu_launches": launches, "clocks": clocks, "also": also,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--quick", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -32,7 +32,7 @@ ISO_ROW_BAD_Y = 1
 ISO_ROW_BAD_W = 2
 
 EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
-           "iso_backward_workspace_bytes", "iso_backward")
+           "iso_backward_workspace_bytes", "iso_backward", "iso_profile_enable", "iso_profile_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -68,6 +68,11 @@ def load_library(path: str | None = None):
         lib.iso_fit.restype = ci
         lib.iso_backward.argtypes = [vp, vp, vp, i64, i64, vp, vp, sz, vp]
         lib.iso_backward.restype = ci
+        lib.iso_profile_enable.argtypes = [ci]
+        lib.iso_profile_enable.restype = ci
+        lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_char_p), ci]
+        lib.iso_profile_read.restype = ci
         _lib = lib
         return lib
 
@@ -82,6 +87,23 @@ def iso_fit_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
 
 def iso_backward_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
     return int(load_library().iso_backward_workspace_bytes(int(rows), int(n), int(bool(weighted))))
+
+
+def profile_enable(on: bool = True) -> None:
+    """Record CUDA events around every kernel of later calls (benchmarks only)."""
+    st = load_library().iso_profile_enable(int(bool(on)))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_profile_enable")
+
+
+def profile_read(max_kernels: int = 16):
+    """Per-kernel durations (ms) of the most recent call: list of (name, ms)."""
+    ms = (ctypes.c_float * max_kernels)()
+    names = (ctypes.c_char_p * max_kernels)()
+    k = load_library().iso_profile_read(ms, names, max_kernels)
+    if k < 0:
+        raise IsoError(k, "iso_profile_read")
+    return [(names[i].decode(), float(ms[i])) for i in range(k)]
 
 
 def _torch():

@@ -3,6 +3,34 @@
 #include "../../include/iso.h"
 #include "iso_internal.h"
 
+namespace isodev {
+
+namespace {
+constexpr int kProfMax = 16;
+struct Profile {
+    bool on = false;
+    bool created = false;
+    cudaEvent_t ev[kProfMax + 1];
+    const char* name[kProfMax];
+    int count = 0;      // kernels marked in the current call
+    bool started = false;
+} g_prof;
+}  // namespace
+
+void prof_start(cudaStream_t stream) {
+    if (!g_prof.on) return;
+    g_prof.count = 0;
+    g_prof.started = cudaEventRecord(g_prof.ev[0], stream) == cudaSuccess;
+}
+
+void prof_mark(cudaStream_t stream, const char* name) {
+    if (!g_prof.on || !g_prof.started || g_prof.count >= kProfMax) return;
+    if (cudaEventRecord(g_prof.ev[g_prof.count + 1], stream) == cudaSuccess)
+        g_prof.name[g_prof.count++] = name;
+}
+
+}  // namespace isodev
+
 namespace {
 
 constexpr int64_t kMaxN = 2147483647LL;
@@ -43,6 +71,7 @@ iso_status iso_fit(const float* y, const float* w, int64_t rows, int64_t n, int 
     if (!y || !out || !shape_ok(rows, n) || (increasing != 0 && increasing != 1))
         return ISO_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
     if (n <= isodev::kRowMax)
         return from_cuda(isodev::rows_fit(y, w, rows, (int)n, increasing, out, blocks,
                                           row_status, st));
@@ -65,6 +94,7 @@ iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w
                         void* stream) {
     if (!grad || !blocks || !out || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
     if (n <= isodev::kRowMax)
         return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out, st));
     const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
@@ -73,6 +103,33 @@ iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w
         return ISO_ERR_WORKSPACE;
     return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out, workspace,
                                            workspace_bytes, st));
+}
+
+int iso_profile_enable(int on) {
+    auto& P = isodev::g_prof;
+    if (on && !P.created) {
+        for (int i = 0; i <= isodev::kProfMax; ++i)
+            if (cudaEventCreate(&P.ev[i]) != cudaSuccess) return ISO_ERR_CUDA;
+        P.created = true;
+    }
+    P.on = on != 0;
+    P.count = 0;
+    P.started = false;
+    return ISO_OK;
+}
+
+int iso_profile_read(float* ms, const char** names, int max_kernels) {
+    auto& P = isodev::g_prof;
+    if (!P.created || !P.started) return ISO_ERR_INVALID_ARG;
+    const int k = P.count < max_kernels ? P.count : max_kernels;
+    if (k > 0 && cudaEventSynchronize(P.ev[P.count]) != cudaSuccess) return ISO_ERR_CUDA;
+    for (int i = 0; i < k; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, P.ev[i], P.ev[i + 1]) != cudaSuccess) return ISO_ERR_CUDA;
+        if (ms) ms[i] = t;
+        if (names) names[i] = P.name[i];
+    }
+    return k;
 }
 
 }  // extern "C"

@@ -373,6 +373,7 @@ cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const floa
     const int R = NT / L;
     const int64_t grid = (rows + R - 1) / R;
     kern<<<(unsigned)grid, NT, SM::kBytes, stream>>>(grad, blocks, w, rows, n, L, out);
+    prof_mark(stream, "rows_backward");
     return cudaGetLastError();
 }
 
@@ -390,9 +391,12 @@ cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w,
     if (err != cudaSuccess) return err;
     k1<<<(unsigned)M, kBNT, SM::kBytes, stream>>>(grad, blocks, w, n, m, out, rec);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "bwd_tiles");
     long_bwd_totals_kernel<<<(unsigned)((rows + 63) / 64), 64, 0, stream>>>(rows, m, rec, tot);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "bwd_totals");
     long_bwd_fill_kernel<WEIGHTED><<<(unsigned)M, kBNT, 0, stream>>>(w, n, m, rec, tot, out);
+    prof_mark(stream, "bwd_fill");
     return cudaGetLastError();
 }
 

@@ -7,6 +7,11 @@
 
 namespace isodev {
 
+// Optional per-kernel timing (see iso_profile_enable): marks the start of an
+// API call, and the end of each kernel it launches.
+void prof_start(cudaStream_t stream);
+void prof_mark(cudaStream_t stream, const char* name);
+
 // Longest row handled by the whole-row kernels (one CTA of 256 lanes x 32).
 constexpr int kRowMax = 8192;
 

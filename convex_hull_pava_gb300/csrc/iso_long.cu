@@ -583,13 +583,16 @@ static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int6
     if (err != cudaSuccess) return err;
     chunk_hull_kernel<WEIGHTED><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, n, m, increasing, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "chunk_hull");
     merge_kernel<WEIGHTED><<<(unsigned)rows, 1024, 0, stream>>>(m, ws, row_status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "merge");
     err = cudaFuncSetAttribute(expand_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                ExpandSmem<WEIGHTED>::kBytes);
     if (err != cudaSuccess) return err;
     expand_kernel<WEIGHTED><<<(unsigned)M, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
         n, m, increasing, ws, out, blocks);
+    prof_mark(stream, "expand");
     return cudaGetLastError();
 }
 

@@ -93,6 +93,7 @@ static cudaError_t launch_rows_fit(const float* y, const float* w, int64_t rows,
     const int64_t grid = (rows + R - 1) / R;
     kern<<<(unsigned)grid, NT, SM::kBytes, stream>>>(y, w, rows, n, L, increasing, out, blocks,
                                                     row_status);
+    prof_mark(stream, "rows_fit");
     return cudaGetLastError();
 }
 

@@ -120,6 +120,21 @@ iso_status iso_backward(const float *grad, const uint8_t *blocks, const float *w
                         int64_t n, float *out, void *workspace, size_t workspace_bytes,
                         void *stream);
 
+/*
+ * Optional per-kernel timing for benchmarks (not part of the fit).
+ * iso_profile_enable(1) makes the library create a few CUDA events (once, on
+ * first use; the only state the library keeps) and record one before the first
+ * kernel of every later iso_fit / iso_backward call and one after each of its
+ * kernels, on the call's stream.  iso_profile_enable(0) stops the recording.
+ * iso_profile_read waits for the events of the most recent call and writes the
+ * duration of each of its kernels in launch order (milliseconds, into ms[0..])
+ * and a static name for each (names may be NULL); it returns the number of
+ * kernels, or a negative iso_status.  Calls must not run concurrently from
+ * several host threads while profiling is enabled.
+ */
+int iso_profile_enable(int on);
+int iso_profile_read(float *ms, const char **names, int max_kernels);
+
 #ifdef __cplusplus
 }
 #endif

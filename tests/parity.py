@@ -3,8 +3,10 @@
 * Fit: max_i |out_i - z*_i| <= 1e-5 * (1 + max_i |y_i|) per row, with z* the
   oracle's fp64 value (not rounded to fp32).
 * Blocks: every oracle block boundary whose adjacent block means differ by more
-  than 1e-6 relative (|m_k - m_{k-1}| > 1e-6 * max(|m_k|, |m_{k-1}|)) must be a
-  boundary of the CUDA path; a CUDA boundary that the oracle does not have must
+  than 1e-6 relative (|m_k - m_{k-1}| > 1e-6 * max(|m_k|, |m_{k-1}|)) and by
+  more than 2^-44 * max|y| (the data's scale: below it neither the oracle's
+  fp64 sums nor the 2^-50 fixed-point grid of the CUDA path decide the order,
+  so such a pair is a tie) must be a boundary of the CUDA path; a CUDA boundary that the oracle does not have must
   split a tie (|out_i - out_{i-1}| within the fit tolerance); inside one CUDA
   block the output is constant; element 0 starts a block.
 """
@@ -12,6 +14,7 @@ import numpy as np
 
 FIT_TOL = 1e-5
 GAP_REL = 1e-6
+GAP_FLOOR = 2.0 ** -44
 
 
 def fit_tol(y):
@@ -40,7 +43,7 @@ def check_row(y, out, blocks, z, zb, label=""):
         assert bad.size == 0, f"{label}: output not constant inside a block at {bad[:5] + 1}"
         gap = np.abs(z[1:] - z[:-1])
         scale = np.maximum(np.abs(z[1:]), np.abs(z[:-1]))
-        required = zb[1:] & (gap > GAP_REL * scale)
+        required = zb[1:] & (gap > GAP_REL * scale) & (gap > GAP_FLOOR * np.abs(y).max())
         missing = np.nonzero(required & ~blocks[1:])[0]
         assert missing.size == 0, f"{label}: oracle boundaries missing at {missing[:5] + 1} (gaps {gap[missing[:5]]})"
         extra = np.nonzero(blocks[1:] & ~zb[1:])[0]
