@@ -16,6 +16,24 @@ namespace isodev {
 
 namespace {
 
+// Shared memory of a backward tile of NT lanes: grad and w staging, the
+// block-prefix sums of both, masks of block starts and scan scratch.
+template <int NT>
+struct BwdSmem {
+    static constexpr int oStage = 0;                              // grad (later the output)
+    static constexpr int oStageW = oStage + NT * 128;             // w
+    static constexpr int oSx = oStageW + NT * 128;                // block prefix of grad
+    static constexpr int oWx = oSx + NT * kRow * 8;               // block prefix of w
+    static constexpr int oMask = oWx + NT * kRow * 8;
+    static constexpr int oSumm = oMask + NT * 4;
+    static constexpr int oInfo = oSumm + ((NT + 63) / 64) * 8;
+    static constexpr int oScan = oInfo + NT * 16;
+    static constexpr int oLS = oScan + (NT / 16 + 2) * 8;         // per-lane inclusive carries
+    static constexpr int oLW = oLS + NT * 8;
+    static constexpr int oBridge = oLW + NT * 8;                  // scan flags
+    static constexpr int kBytes = ((oBridge + NT * 4 + 127) / 128) * 128;
+};
+
 // Block sums of one tile: on return, stage holds, for every element whose
 // block both starts and ends inside the tile, its output value; `Px`/`Qx` hold
 // the block-prefix sums (fixed point) of grad and w, restarting at each block
@@ -34,7 +52,7 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
                                                const float* __restrict__ wr, int nt, bool live,
                                                bool first_is_start, int L, unsigned char* smem,
                                                BwdTile& B) {
-    using SM = TileSmem<NT, true>;
+    using SM = BwdSmem<NT>;
     float* stage = reinterpret_cast<float*>(smem + SM::oStage);
     int64_t* Px = reinterpret_cast<int64_t*>(smem + SM::oSx);
     int64_t* Qx = reinterpret_cast<int64_t*>(smem + SM::oWx);
@@ -217,7 +235,7 @@ rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__
                      const float* __restrict__ w, int64_t rows, int n, int L,
                      float* __restrict__ out) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = TileSmem<NT, true>;
+    using SM = BwdSmem<NT>;
     const int R = NT / L;
     const int tile = threadIdx.x / L;
     const int lane = threadIdx.x - tile * L;
@@ -257,7 +275,7 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
                       const float* __restrict__ w, int64_t n, int64_t m, float* __restrict__ out,
                       BwdRec* __restrict__ rec) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = TileSmem<kBNT, true>;
+    using SM = BwdSmem<kBNT>;
     const int64_t c = blockIdx.x;
     const int64_t row = c / m;
     const int64_t j = c - row * m;
@@ -365,7 +383,7 @@ __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(25
 template <int NT, bool WEIGHTED>
 cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const float* w,
                             int64_t rows, int n, int L, float* out, cudaStream_t stream) {
-    using SM = TileSmem<NT, true>;
+    using SM = BwdSmem<NT>;
     auto kern = rows_backward_kernel<NT, WEIGHTED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
@@ -380,7 +398,7 @@ cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const floa
 template <bool WEIGHTED>
 cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
                        int64_t n, float* out, void* ws, cudaStream_t stream) {
-    using SM = TileSmem<kBNT, true>;
+    using SM = BwdSmem<kBNT>;
     const int64_t m = (n + kBT - 1) / kBT;
     const int64_t M = rows * m;
     BwdRec* rec = static_cast<BwdRec*>(ws);

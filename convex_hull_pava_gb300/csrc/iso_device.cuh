@@ -152,39 +152,38 @@ __device__ __forceinline__ int sign_det128(__int128 a, __int128 b, __int128 c, _
 template <bool WEIGHTED>
 __device__ __forceinline__ uint32_t lane_hull(const int64_t* Sx, const int64_t* Wx, uint32_t cand,
                                               int e) {
-    uint32_t mask = 1u;
-    int t = 0, b = -1;
+    if (e <= 0) return 0u;
+    uint32_t mask = 1u;          // stack membership
+    int t = 0, b = -1;           // top and the entry below it
     int64_t St = 0, Wt = 0, Sb = 0, Wb = 0;
-    uint32_t rem = cand & ~1u;
+    uint32_t rem = cand & ~1u & (e >= 32 ? 0xffffffffu : ((1u << e) - 1u));
     int k = rem ? (__ffs(rem) - 1) : e;
     rem &= rem - 1u;
     int64_t Sk = Sx[k];
     int64_t Wk = WEIGHTED ? Wx[k] : (int64_t)k;
-    bool done = (e <= 0);
-    // each point is pushed once and popped at most once
-    for (int it = 0; it < 2 * kPts + 2 && !done; ++it) {
-        bool push = (b < 0) || left_turn<WEIGHTED>(Wt - Wb, St - Sb, Wk - Wb, Sk - Sb);
+    // Every iteration pushes or pops; both loads it may need next are issued
+    // before the turn is known, so a lane never waits on a dependent load.
+    for (int it = 0; it < 2 * kPts + 2; ++it) {
+        const int k2 = rem ? (__ffs(rem) - 1) : e;                 // next point after a push
+        const uint32_t below = b > 0 ? (mask & ((1u << b) - 1u)) : 0u;
+        const int b2 = below ? (31 - __clz(below)) : -1;           // new below-top after a pop
+        const int bl = b2 < 0 ? 0 : b2;
+        const int64_t Sk2 = Sx[k2];
+        const int64_t Wk2 = WEIGHTED ? Wx[k2] : (int64_t)k2;
+        const int64_t Sb2 = Sx[bl];
+        const int64_t Wb2 = WEIGHTED ? Wx[bl] : (int64_t)bl;
+        const bool push = (b < 0) || left_turn<WEIGHTED>(Wt - Wb, St - Sb, Wk - Wb, Sk - Sb);
         if (push) {
-            if (k >= e) {
-                done = true;
-            } else {
-                mask |= 1u << k;
-                b = t; Sb = St; Wb = Wt;
-                t = k; St = Sk; Wt = Wk;
-                k = rem ? (__ffs(rem) - 1) : e;
-                rem &= rem - 1u;
-                Sk = Sx[k];
-                Wk = WEIGHTED ? Wx[k] : (int64_t)k;
-            }
+            if (k >= e) break;
+            mask |= 1u << k;
+            b = t; Sb = St; Wb = Wt;
+            t = k; St = Sk; Wt = Wk;
+            k = k2; Sk = Sk2; Wk = Wk2;
+            rem &= rem - 1u;
         } else {
             mask &= ~(1u << t);
             t = b; St = Sb; Wt = Wb;
-            uint32_t below = mask & ((1u << t) - 1u);
-            b = below ? (31 - __clz(below)) : -1;
-            if (b >= 0) {
-                Sb = Sx[b];
-                Wb = WEIGHTED ? Wx[b] : (int64_t)b;
-            }
+            b = b2; Sb = Sb2; Wb = Wb2;
         }
     }
     return mask;
@@ -280,20 +279,13 @@ __device__ __forceinline__ int tile_succ(const Tile& T, int p, int hi_lane, int 
     return (q << 5) + __ffs(T.mask[q]) - 1;
 }
 
-// Turn test on three tile points.
-template <bool WEIGHTED>
-__device__ __forceinline__ bool tile_left(const Tile& T, int o, int a, int b) {
-    int64_t So = tile_S<WEIGHTED>(T, o), Wo = tile_W<WEIGHTED>(T, o);
-    int64_t Sa = tile_S<WEIGHTED>(T, a), Wa = tile_W<WEIGHTED>(T, a);
-    int64_t Sb = tile_S<WEIGHTED>(T, b), Wb = tile_W<WEIGHTED>(T, b);
-    return left_turn<true>(Wa - Wo, Sa - So, Wb - Wo, Sb - So);
-}
-
 // Bridge of the merge of lane groups A = [A0, B0) and B = [B0, Bend) (Section
 // 3.2, Lemma 4.2): s = 32*B0 is the last vertex of H(A) and the first of H(B).
 // If the chain is convex at s, returns (s, s).  Otherwise walks from s's
 // neighbours, the left end left and the right end right, until the line
 // between them supports both hulls.  Each step removes a vertex (Lemma 5.1).
+// The coordinates of the two current ends stay in registers; a step loads one
+// new point.
 template <bool WEIGHTED>
 __device__ void tile_bridge(const Tile& T, int A0, int B0, int Bend, int& ra, int& rb) {
     const int s = B0 << 5;
@@ -301,18 +293,25 @@ __device__ void tile_bridge(const Tile& T, int A0, int B0, int Bend, int& ra, in
     const int startA = A0 << 5;
     int a = tile_pred(T, s, A0);
     int b = tile_succ(T, s, Bend, endB);
-    if (tile_left<WEIGHTED>(T, a, s, b)) { ra = s; rb = s; return; }
+    int64_t Wa = tile_W<WEIGHTED>(T, a), Sa = tile_S<WEIGHTED>(T, a);
+    int64_t Wb = tile_W<WEIGHTED>(T, b), Sb = tile_S<WEIGHTED>(T, b);
+    {
+        const int64_t Ws = tile_W<WEIGHTED>(T, s), Ss = tile_S<WEIGHTED>(T, s);
+        if (left_turn<true>(Ws - Wa, Ss - Sa, Wb - Wa, Sb - Sa)) { ra = s; rb = s; return; }
+    }
     for (;;) {
         bool moved = false;
         while (a > startA) {
-            int p = tile_pred(T, a, A0);
-            if (tile_left<WEIGHTED>(T, p, a, b)) break;
-            a = p; moved = true;
+            const int p = tile_pred(T, a, A0);
+            const int64_t Wp = tile_W<WEIGHTED>(T, p), Sp = tile_S<WEIGHTED>(T, p);
+            if (left_turn<true>(Wa - Wp, Sa - Sp, Wb - Wp, Sb - Sp)) break;   // p -> a -> b convex
+            a = p; Wa = Wp; Sa = Sp; moved = true;
         }
         while (b < endB) {
-            int q = tile_succ(T, b, Bend, endB);
-            if (tile_left<WEIGHTED>(T, a, b, q)) break;
-            b = q; moved = true;
+            const int q = tile_succ(T, b, Bend, endB);
+            const int64_t Wq = tile_W<WEIGHTED>(T, q), Sq = tile_S<WEIGHTED>(T, q);
+            if (left_turn<true>(Wb - Wa, Sb - Sa, Wq - Wa, Sq - Sa)) break;   // a -> b -> q convex
+            b = q; Wb = Wq; Sb = Sq; moved = true;
         }
         if (!moved) break;
     }

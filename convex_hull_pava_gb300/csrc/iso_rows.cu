@@ -15,7 +15,7 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
                 int L, int increasing, float* __restrict__ out, uint8_t* __restrict__ blocks,
                 uint32_t* __restrict__ row_status) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = TileSmem<NT, WEIGHTED>;
+    using SM = TileSmem<NT, WEIGHTED, true>;
     const int R = NT / L;
     const int tile = threadIdx.x / L;
     const int64_t row = (int64_t)blockIdx.x * R + tile;
@@ -25,58 +25,89 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
     const bool neg = !increasing;
 
     TileHull H;
-    tile_hull_phase<NT, WEIGHTED>(yr, wr, n, live, neg, L, smem, H);
+    tile_hull_phase<NT, WEIGHTED, true>(yr, wr, n, live, neg, L, smem, H);
 
-    float* stage = reinterpret_cast<float*>(smem + SM::oStage);
-    uint8_t* bst = smem + SM::oBst;
+    float* slope = reinterpret_cast<float*>(smem + SM::oY);   // y until it becomes slopes
     const Tile& T = H.T;
     const int lane = H.lane, gl = H.gl, e = H.e;
     const bool work = live && H.bad == 0;
+    const uint32_t mask = work ? T.mask[lane] : 0u;
 
-    // ---- emit the fit: each element gets the slope of the hull edge above it
-    // (eq. (3)); an element whose point is a vertex starts a block. ----
-    if (work && e > 0) {
-        const int p0 = lane << 5;
-        const uint32_t mask = T.mask[lane];
-        int a = (mask & 1u) ? p0 : tile_pred(T, p0, 0);
-        int k = 0;
-        while (k < e) {
-            const int b = tile_succ(T, p0 + k, L, n);
-            const int kend = min(b - p0, e);
-            float slope;
-            if (b == a + 1) {
-                slope = stage[spos(gl, k)];            // one-element block: its own value
-            } else {
-                slope = tile_slope<WEIGHTED>(T, a, b, H.qs, H.qw);
-            }
-            if (neg) slope = -slope;
-            for (int j = k; j < kend; ++j) {
-                stage[spos(gl, j)] = slope;
-                bst[(gl << 5) + j] = (uint8_t)(p0 + j == a);
-            }
-            k = kend;
-            a = b;
+    // ---- 1. every vertex: the slope of the hull edge leaving it (eq. (3)).  A
+    // one-element block is fitted by its own value. ----
+    {
+        uint32_t m = mask;
+        while (m) {
+            const int k = __ffs(m) - 1;
+            m &= m - 1u;
+            const int v = (lane << 5) + k;
+            const int b = m ? (lane << 5) + __ffs(m) - 1 : tile_succ(T, v, L, n);
+            if (b != v + 1) slope[spos(gl, k)] = tile_slope<WEIGHTED>(T, v, b, H.qs, H.qw);
         }
     }
     __syncthreads();
+    // ---- 2. every element: the slope of the edge leaving the last vertex at or
+    // before it ----
+    float o[32];
+    {
+        float carry = 0.f;
+        if (work && e > 0 && !(mask & 1u)) {
+            const int cv = tile_pred(T, lane << 5, 0);
+            carry = slope[spos(H.tile * L + (cv >> 5), cv & 31)];
+        }
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const uint32_t upto = k == 31 ? mask : (mask & ((2u << k) - 1u));
+            const float v = upto ? slope[spos(gl, 31 - __clz(upto))] : carry;
+            o[k] = neg ? -v : v;
+        }
+    }
+    __syncthreads();   // Sx and the slopes are dead: stage the output in Sx
+    float4* ost4 = reinterpret_cast<float4*>(smem + SM::oSx);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        ost4[sunit(gl, q)] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    __syncthreads();
 
-    // ---- coalesced write-out ----
+    // ---- coalesced write-out of the fit and of the block-start bytes ----
     if (live) {
-        const int lane_in = threadIdx.x - H.tile * L;
         float* orow = out + row * (int64_t)n;
-        uint8_t* brow = blocks ? blocks + row * (int64_t)n : nullptr;
+        const float* ost = reinterpret_cast<const float*>(ost4);
         const float qnan = __int_as_float(0x7fffffff);
-        for (int i = lane_in; i < n; i += L) {
-            const int g = H.tile * L + (i >> 5);
-            if (work) {
-                orow[i] = stage[spos(g, i & 31)];
-                if (brow) brow[i] = bst[(g << 5) + (i & 31)];
+        const int g0 = H.tile * L;
+        if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
+            const int n4 = n >> 2;
+            for (int i = lane; i < n4; i += L) {
+                const int e4 = i << 2;
+                float4 v = ost4[sunit(g0 + (e4 >> 5), (e4 & 31) >> 2)];
+                if (!work) v = make_float4(qnan, qnan, qnan, qnan);
+                reinterpret_cast<float4*>(orow)[i] = v;
+            }
+            for (int i = (n4 << 2) + lane; i < n; i += L)
+                orow[i] = work ? ost[spos(g0 + (i >> 5), i & 31)] : qnan;
+        } else {
+            for (int i = lane; i < n; i += L) orow[i] = work ? ost[spos(g0 + (i >> 5), i & 31)] : qnan;
+        }
+        if (blocks) {
+            uint8_t* brow = blocks + row * (int64_t)n;
+            const uint32_t* ma = T.mask;
+            if ((reinterpret_cast<uintptr_t>(brow) & 3u) == 0) {
+                const int n4 = n >> 2;
+                for (int i = lane; i < n4; i += L) {
+                    const int e4 = i << 2;
+                    const uint32_t bits = work ? (ma[e4 >> 5] >> (e4 & 31)) & 0xfu : 0u;
+                    const uint32_t word = (bits & 1u) | ((bits & 2u) << 7) | ((bits & 4u) << 14) |
+                                          ((bits & 8u) << 21);
+                    reinterpret_cast<uint32_t*>(brow)[i] = word;
+                }
+                for (int i = (n4 << 2) + lane; i < n; i += L)
+                    brow[i] = work ? (uint8_t)((ma[i >> 5] >> (i & 31)) & 1u) : 0;
             } else {
-                orow[i] = qnan;
-                if (brow) brow[i] = 0;
+                for (int i = lane; i < n; i += L)
+                    brow[i] = work ? (uint8_t)((ma[i >> 5] >> (i & 31)) & 1u) : 0;
             }
         }
-        if (row_status && lane_in == 0) row_status[row] = H.bad;
+        if (row_status && lane == 0) row_status[row] = H.bad;
     }
 }
 
@@ -84,7 +115,7 @@ template <int NT, bool WEIGHTED>
 static cudaError_t launch_rows_fit(const float* y, const float* w, int64_t rows, int n, int L,
                                    int increasing, float* out, uint8_t* blocks,
                                    uint32_t* row_status, cudaStream_t stream) {
-    using SM = TileSmem<NT, WEIGHTED>;
+    using SM = TileSmem<NT, WEIGHTED, true>;
     auto kern = rows_fit_kernel<NT, WEIGHTED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
@@ -103,27 +134,16 @@ cudaError_t rows_fit(const float* y, const float* w, int64_t rows, int n, int in
     int L = 1;
     while (32 * L < n) L <<= 1;
     const bool weighted = w != nullptr;
-    if (L <= 32) {
-        // several rows per CTA of 128 threads
-        return weighted ? launch_rows_fit<128, true>(y, w, rows, n, L, increasing, out, blocks,
-                                                     row_status, stream)
-                        : launch_rows_fit<128, false>(y, w, rows, n, L, increasing, out, blocks,
-                                                      row_status, stream);
-    }
-    if (L <= 64)
-        return weighted ? launch_rows_fit<64, true>(y, w, rows, n, L, increasing, out, blocks,
-                                                    row_status, stream)
-                        : launch_rows_fit<64, false>(y, w, rows, n, L, increasing, out, blocks,
-                                                     row_status, stream);
-    if (L <= 128)
-        return weighted ? launch_rows_fit<128, true>(y, w, rows, n, L, increasing, out, blocks,
-                                                     row_status, stream)
-                        : launch_rows_fit<128, false>(y, w, rows, n, L, increasing, out, blocks,
-                                                      row_status, stream);
-    return weighted ? launch_rows_fit<256, true>(y, w, rows, n, L, increasing, out, blocks,
-                                                 row_status, stream)
-                    : launch_rows_fit<256, false>(y, w, rows, n, L, increasing, out, blocks,
-                                                  row_status, stream);
+#define ISO_ROWS_LAUNCH(NT_)                                                                    \
+    return weighted ? launch_rows_fit<NT_, true>(y, w, rows, n, L, increasing, out, blocks,    \
+                                                 row_status, stream)                           \
+                    : launch_rows_fit<NT_, false>(y, w, rows, n, L, increasing, out, blocks,   \
+                                                  row_status, stream)
+    if (L <= 32) { ISO_ROWS_LAUNCH(128); }   // several rows per CTA of 128 threads
+    if (L <= 64) { ISO_ROWS_LAUNCH(64); }
+    if (L <= 128) { ISO_ROWS_LAUNCH(128); }
+    ISO_ROWS_LAUNCH(256);
+#undef ISO_ROWS_LAUNCH
 }
 
 }  // namespace isodev

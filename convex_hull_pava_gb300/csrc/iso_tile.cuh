@@ -15,46 +15,47 @@ namespace isodev {
 __device__ __forceinline__ int spos(int gl, int k) {
     return (gl << 5) | ((((k >> 2) ^ gl) & 7) << 2) | (k & 3);
 }
+__device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ gl) & 7); }
 
 // Layout of the dynamic shared memory of a CTA of NT threads holding R = NT/L
-// tiles of L lanes.  The w staging is separate from the coordinate arrays (it
-// is read while they are written); the block-start byte staging of the
-// whole-row kernels reuses it (weighted) once the hull is built.
-template <int NT, bool WEIGHTED>
+// tiles of L lanes.  The input staging lives inside the lane-relative sums
+// array Sx (2 x 128 B per lane fit in its 264 B per lane): it is read into
+// registers before Sx is written.  Kernels that write the fit (EMIT) keep y in
+// a separate area, which later holds each vertex's edge slope.
+template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 struct TileSmem {
-    static constexpr int kStageB = NT * 32 * 4;                 // y (or output) staging
-    static constexpr int kStageWB = WEIGHTED ? NT * 32 * 4 : 0; // w staging
-    static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S
+    static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
-    static constexpr int kLSB = (NT + NT) * 8;                  // lane starts, L+1 per tile <= 2*NT
+    static constexpr int kYB = EMIT ? NT * 32 * 4 : 0;          // kept y / slope per vertex
+    static constexpr int kLSB = (NT + RMAX) * 8;                // lane starts, L+1 per tile
     static constexpr int kLWB = WEIGHTED ? kLSB : 0;
     static constexpr int kMaskB = NT * 4;
     static constexpr int kSummB = ((NT + 63) / 64) * 8;
     static constexpr int kBridgeB = (NT / 2 > 0 ? NT / 2 : 1) * 8;
-    static constexpr int kInfoB = NT * 4 * 4;                   // 4 ints per tile (R <= NT)
-    static constexpr int kBstB = WEIGHTED ? 0 : NT * 32;        // block-start byte staging
+    static constexpr int kInfoB = RMAX * 4 * 4;                 // 4 ints per tile
     static constexpr int kScanB = (NT / 16 + 2) * 8;            // cross-warp scan partials
-    static constexpr int oStage = 0;
-    static constexpr int oStageW = oStage + kStageB;
-    static constexpr int oSx = oStageW + kStageWB;
+    static constexpr int oSx = 0;
     static constexpr int oWx = oSx + kSxB;
-    static constexpr int oLS = oWx + kWxB;
+    static constexpr int oY = oWx + kWxB;
+    static constexpr int oLS = oY + kYB;
     static constexpr int oLW = oLS + kLSB;
     static constexpr int oMask = oLW + kLWB;
     static constexpr int oSumm = oMask + kMaskB;
     static constexpr int oBridge = oSumm + kSummB;
     static constexpr int oInfo = oBridge + kBridgeB;
     static constexpr int oScan = oInfo + kInfoB;
-    static constexpr int oBstOwn = oScan + kScanB;
-    static constexpr int oBst = WEIGHTED ? oStageW : oBstOwn;
-    static constexpr int kBytes = ((oBstOwn + kBstB + 127) / 128) * 128;
+    static constexpr int kBytes = ((oScan + kScanB + 127) / 128) * 128;
+    // staging: y at the start of Sx (or in the Y area when EMIT), w after it
+    static constexpr int oStageY = EMIT ? oY : oSx;
+    static constexpr int oStageW = oSx + NT * 128;
 };
 
 // Per-tile reduction slots in the info area.
 enum { kInfoEmax = 0, kInfoPemax = 1, kInfoEwmax = 2, kInfoBad = 3 };
 
 // Inclusive prefix sum of an int64 over the L lanes of each tile of a CTA of NT
-// threads (L a power of two).  `tmp` holds NT/32 int64 entries.
+// threads (L a power of two).  `tmp` holds NT/32 int64 entries.  Every thread of
+// the CTA must call it.
 template <int NT>
 __device__ __forceinline__ int64_t tile_scan_incl(int64_t v, int lane, int L, int64_t* tmp) {
     const int wl = threadIdx.x & 31;
@@ -69,20 +70,96 @@ __device__ __forceinline__ int64_t tile_scan_incl(int64_t v, int lane, int L, in
         const int warp = threadIdx.x >> 5;
         if (wl == 31) tmp[warp] = v;
         __syncthreads();
-        const int wpt = L >> 5;                 // warps per tile
         const int w0 = warp - (lane >> 5);      // first warp of this tile
         int64_t add = 0;
         for (int q = w0; q < warp; ++q) add += tmp[q];
         __syncthreads();
         v += add;
-        (void)wpt;
     }
     return v;
 }
 
-}  // namespace isodev
+// Maximum / bitwise or of v over the lanes of a tile that share this warp
+// (L < 32: the tile's L lanes; else the whole warp).
+__device__ __forceinline__ int tile_warp_max(int v, int L) {
+    const int seg = L < 32 ? L : 32;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+        if (d < seg) v = max(v, __shfl_xor_sync(kFull, v, d));
+    return v;
+}
+__device__ __forceinline__ int tile_warp_or(int v, int L) {
+    const int seg = L < 32 ? L : 32;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+        if (d < seg) v |= __shfl_xor_sync(kFull, v, d);
+    return v;
+}
 
-namespace isodev {
+// Coalesced load of a tile's nt floats from `src` into the swizzled staging
+// rows of lanes [gl0, gl0 + L), by the tile's L threads.  All loads of a
+// thread are issued before any store.  Tracks the largest biased exponent and
+// flags non-finite values (and, for weights, values that are not > 0).
+template <bool IS_W>
+__device__ __forceinline__ void stage_tile(const float* __restrict__ src, int nt, int lane, int L,
+                                           int gl0, bool neg, float* stage, int& emax,
+                                           uint32_t& bad) {
+    auto note = [&](float v) {
+        const int e = (__float_as_uint(v) >> 23) & 0xff;
+        if (IS_W) {
+            if (!(v > 0.0f) || e == 0xff) bad |= 2u;
+            else emax = max(emax, e == 0 ? 1 : e);
+        } else {
+            if (e == 0xff) bad |= 1u;
+            else emax = max(emax, e == 0 ? 1 : e);
+        }
+    };
+    const bool aligned = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
+    if (aligned) {
+        const int n4 = nt >> 2;
+        const float4* s4 = reinterpret_cast<const float4*>(src);
+        float4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = lane + j * L;
+            v[j] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4* st4 = reinterpret_cast<float4*>(stage);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int i = lane + j * L;
+            if (i < n4) {
+                float4 x = v[j];
+                if (neg) { x.x = -x.x; x.y = -x.y; x.z = -x.z; x.w = -x.w; }
+                note(x.x); note(x.y); note(x.z); note(x.w);
+                const int e = i << 2;
+                st4[sunit(gl0 + (e >> 5), (e & 31) >> 2)] = x;
+            }
+        }
+        for (int e = (n4 << 2) + lane; e < nt; e += L) {
+            float x = __ldg(src + e);
+            if (neg) x = -x;
+            note(x);
+            stage[spos(gl0 + (e >> 5), e & 31)] = x;
+        }
+    } else {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int e = lane + j * L;
+            v[j] = e < nt ? __ldg(src + e) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int e = lane + j * L;
+            if (e < nt) {
+                const float x = neg ? -v[j] : v[j];
+                note(x);
+                stage[spos(gl0 + (e >> 5), e & 31)] = x;
+            }
+        }
+    }
+}
 
 // Result of the common hull phase, per thread (one lane of one tile).
 struct TileHull {
@@ -103,15 +180,15 @@ struct TileHull {
 // 3.2), up to the hull of the whole tile.  `yr`/`wr` point at the tile's first
 // element; `neg` negates y on load (the decreasing fit, Section 2.1).
 // All threads of the CTA must call it (it synchronises the CTA).
-template <int NT, bool WEIGHTED>
+template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                                                 const float* __restrict__ wr, int nt, bool live,
                                                 bool neg, int L, unsigned char* smem,
                                                 TileHull& H) {
-    using SM = TileSmem<NT, WEIGHTED>;
-    float* stage = reinterpret_cast<float*>(smem + SM::oStage);
+    using SM = TileSmem<NT, WEIGHTED, EMIT, RMAX>;
     int64_t* Sx = reinterpret_cast<int64_t*>(smem + SM::oSx);
     int64_t* Wx = reinterpret_cast<int64_t*>(smem + SM::oWx);
+    float* stagey = reinterpret_cast<float*>(smem + SM::oStageY);
     float* stagew = reinterpret_cast<float*>(smem + SM::oStageW);
     int64_t* LSa = reinterpret_cast<int64_t*>(smem + SM::oLS);
     int64_t* LWa = reinterpret_cast<int64_t*>(smem + SM::oLW);
@@ -125,116 +202,116 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     const int tile = tid / L;
     const int lane = tid - tile * L;
     const int gl = tid;
+    const int seg = L < 32 ? L : 32;
+    const bool seg_first = ((tid & 31) & (seg - 1)) == 0;
     H.tile = tile; H.lane = lane; H.gl = gl; H.live = live;
 
     for (int i = lane; i < 4; i += L) info[tile * 4 + i] = 0;
     __syncthreads();
 
-    // ---- load (coalesced) into the swizzled staging rows, with validation ----
-    int emax = 0, pemax = 0, ewmax = 0;
+    // ---- load (coalesced, vectorised) into the swizzled staging rows ----
+    int emax = 0, ewmax = 0;
     uint32_t bad = 0;
     if (live) {
-        for (int e = lane; e < nt; e += L) {
-            float v = __ldg(yr + e);
-            if (neg) v = -v;
-            const int pos = spos(tile * L + (e >> 5), e & 31);
-            stage[pos] = v;
-            int ey = (__float_as_uint(v) >> 23) & 0xff;
-            if (ey == 0xff) bad |= 1u;
-            else emax = max(emax, ey == 0 ? 1 : ey);
-            if constexpr (WEIGHTED) {
-                float wv = __ldg(wr + e);
-                stagew[pos] = wv;
-                int ew = (__float_as_uint(wv) >> 23) & 0xff;
-                if (!(wv > 0.0f) || ew == 0xff) bad |= 2u;
-                else {
-                    int eww = ew == 0 ? 1 : ew;
-                    ewmax = max(ewmax, eww);
-                    if (ey != 0xff) pemax = max(pemax, eww + (ey == 0 ? 1 : ey));
-                }
-            }
-        }
-        if (emax) atomicMax(&info[tile * 4 + kInfoEmax], emax);
-        if (WEIGHTED && pemax) atomicMax(&info[tile * 4 + kInfoPemax], pemax);
-        if (WEIGHTED && ewmax) atomicMax(&info[tile * 4 + kInfoEwmax], ewmax);
-        if (bad) atomicOr(&info[tile * 4 + kInfoBad], (int)bad);
+        stage_tile<false>(yr, nt, lane, L, tile * L, neg, stagey, emax, bad);
+        if constexpr (WEIGHTED) stage_tile<true>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
+    }
+    emax = tile_warp_max(emax, L);
+    const int bad_or = tile_warp_or((int)bad, L);
+    if (WEIGHTED) ewmax = tile_warp_max(ewmax, L);
+    if (live && seg_first) {
+        atomicMax(&info[tile * 4 + kInfoEmax], emax);
+        if (WEIGHTED) atomicMax(&info[tile * 4 + kInfoEwmax], ewmax);
+        if (bad_or) atomicOr(&info[tile * 4 + kInfoBad], bad_or);
     }
     __syncthreads();
+    H.bad = live ? (uint32_t)info[tile * 4 + kInfoBad] : 0u;
+    const bool work = live && H.bad == 0;
+    const int e = work ? min(max(nt - (lane << 5), 0), 32) : 0;
+    H.e = e;
+
+    // ---- the lane's values into registers ----
+    float yv[32], wv[WEIGHTED ? 32 : 1];
+    {
+        const float4* sy4 = reinterpret_cast<const float4*>(stagey);
+        const float4* sw4 = reinterpret_cast<const float4*>(stagew);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 v = sy4[sunit(gl, q)];
+            yv[4 * q] = v.x; yv[4 * q + 1] = v.y; yv[4 * q + 2] = v.z; yv[4 * q + 3] = v.w;
+            if constexpr (WEIGHTED) {
+                const float4 x = sw4[sunit(gl, q)];
+                wv[4 * q] = x.x; wv[4 * q + 1] = x.y; wv[4 * q + 2] = x.z; wv[4 * q + 3] = x.w;
+            }
+        }
+    }
+    int pemax = 0;
+    if constexpr (WEIGHTED) {
+        // the S grid comes from the largest exponent of the products w*y
+        int pe = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < e) pe = max(pe, bexp(wv[k]) + bexp(yv[k]));
+        pe = tile_warp_max(pe, L);
+        if (live && seg_first) atomicMax(&info[tile * 4 + kInfoPemax], pe);
+    }
+    __syncthreads();   // staging read: Sx may now be written
     emax = max(info[tile * 4 + kInfoEmax], 1);
     pemax = max(info[tile * 4 + kInfoPemax], 2);
     ewmax = max(info[tile * 4 + kInfoEwmax], 1);
-    H.bad = live ? (uint32_t)info[tile * 4 + kInfoBad] : 0u;
     H.qs = WEIGHTED ? qexp_prod(pemax) : qexp_unit(emax);
     H.qw = WEIGHTED ? qexp_unit(ewmax) : 0;
-    const bool work = live && H.bad == 0;
 
-    // ---- lane values, candidates and lane-relative cumulative sums, in one
-    // pass over the lane's 32 staged values ----
-    const int e = work ? min(max(nt - (lane << 5), 0), 32) : 0;
-    H.e = e;
+    // ---- candidates and lane-relative cumulative sums ----
     int64_t* myS = Sx + gl * kRow;
     int64_t* myW = Wx + gl * kRow;
     int64_t s = 0, wsum = 0;
     uint32_t cand = 0;
     {
-        const float4* st4 = reinterpret_cast<const float4*>(stage);
-        const float4* sw4 = reinterpret_cast<const float4*>(stagew);
         int64_t up = 0, op = 1;   // previous element's value and weight
         myS[0] = 0;
         if constexpr (WEIGHTED) myW[0] = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int unit = (gl << 3) | ((q ^ gl) & 7);
-            const float4 v = st4[unit];
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-            float ww[4] = {1.f, 1.f, 1.f, 1.f};
+        for (int k = 0; k < 32; ++k) {
+            const bool in = k < e;
+            int64_t uk, ok;
             if constexpr (WEIGHTED) {
-                const float4 wq = sw4[unit];
-                ww[0] = wq.x; ww[1] = wq.y; ww[2] = wq.z; ww[3] = wq.w;
+                uk = in ? quant_prod(wv[k], yv[k], pemax) : 0;
+                ok = in ? max(quant(wv[k], ewmax), (int64_t)1) : 0;
+                // point k is locally convex: mean of element k-1 < mean of element k
+                if (k > 0 && in && (__int128)up * ok < (__int128)uk * op) cand |= 1u << k;
+            } else {
+                uk = in ? quant(yv[k], emax) : 0;
+                ok = in ? 1 : 0;
+                if (k > 0 && in && up < uk) cand |= 1u << k;
             }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int k = 4 * q + j;
-                const bool in = k < e;
-                int64_t uk, ok;
-                if constexpr (WEIGHTED) {
-                    uk = in ? quant_prod(ww[j], vv[j], pemax) : 0;
-                    ok = in ? max(quant(ww[j], ewmax), (int64_t)1) : 0;
-                    // point k is locally convex: mean of element k-1 < mean of element k
-                    if (k > 0 && in && (__int128)up * ok < (__int128)uk * op) cand |= 1u << k;
-                } else {
-                    uk = in ? quant(vv[j], emax) : 0;
-                    ok = in ? 1 : 0;
-                    if (k > 0 && in && up < uk) cand |= 1u << k;
-                }
-                up = uk;
-                op = ok > 0 ? ok : 1;
-                s += uk;
-                myS[k + 1] = s;
-                if constexpr (WEIGHTED) {
-                    wsum += ok;
-                    myW[k + 1] = wsum;
-                }
+            up = uk;
+            op = ok > 0 ? ok : 1;
+            s += uk;
+            myS[k + 1] = s;
+            if constexpr (WEIGHTED) {
+                wsum += ok;
+                myW[k + 1] = wsum;
             }
         }
     }
     // lane starts: exclusive scan of lane totals over the tile
     {
-        int64_t inc = tile_scan_incl<NT>(s, lane, L, scan);
+        const int64_t inc = tile_scan_incl<NT>(s, lane, L, scan);
         LSa[tile * (L + 1) + lane] = inc - s;
         if (lane == L - 1) LSa[tile * (L + 1) + L] = inc;
         if constexpr (WEIGHTED) {
-            int64_t incw = tile_scan_incl<NT>(wsum, lane, L, scan);
+            const int64_t incw = tile_scan_incl<NT>(wsum, lane, L, scan);
             LWa[tile * (L + 1) + lane] = incw - wsum;
             if (lane == L - 1) LWa[tile * (L + 1) + L] = incw;
         }
     }
 
     // ---- lane hulls in bit masks ----
-    uint32_t mask = e > 0 ? lane_hull<WEIGHTED>(myS, myW, cand, e) : 0u;
+    uint32_t mask = lane_hull<WEIGHTED>(myS, myW, cand, e);
     maska[gl] = mask;
     {
-        uint32_t bal = __ballot_sync(kFull, mask != 0u);
+        const uint32_t bal = __ballot_sync(kFull, mask != 0u);
         if ((tid & 31) == 0) summ[tid >> 5] = bal;
     }
     __syncthreads();
@@ -250,39 +327,44 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     T.L = L;
     T.nt = nt;
 
-    // ---- merge rounds: pairs of 2^r lanes, up to the whole tile ----
+    // ---- merge rounds: pairs of 2^r lanes, up to the whole tile.  Rounds whose
+    // groups lie inside one warp synchronise the warp only. ----
     for (int r = 0; (1 << r) < L; ++r) {
         const int grp = lane >> (r + 1);
         const int A0 = grp << (r + 1);
         const int B0 = A0 + (1 << r);
         const int Bend = A0 + (2 << r);
         const bool active = work && ((B0 << 5) < nt);
+        // one slot per group; rounds inside a warp use slots of their own warp
+        // only, since warps are not synchronised with each other there
+        const int slot = r < 5 ? ((tid >> 5) << 4) + ((tid & 31) >> (r + 1)) : (tid >> (r + 1));
         if (active && lane == A0) {
             int a, b;
             tile_bridge<WEIGHTED>(T, A0, B0, Bend, a, b);
-            bridge[tid >> (r + 1)] = make_int2(a, b);
+            bridge[slot] = make_int2(a, b);
         }
-        __syncthreads();
+        if (r < 5) __syncwarp(); else __syncthreads();
         if (active) {
-            int2 ab = bridge[tid >> (r + 1)];
+            const int2 ab = bridge[slot];
             if (ab.x != ab.y) {
                 mask = clear_between(mask, lane, ab.x, ab.y);
                 maska[gl] = mask;
             }
         }
-        uint32_t bal = __ballot_sync(kFull, mask != 0u);
+        const uint32_t bal = __ballot_sync(kFull, mask != 0u);
         if ((tid & 31) == 0) summ[tid >> 5] = bal;
-        __syncthreads();
+        if (r + 1 < 5) __syncwarp(); else __syncthreads();
     }
+    __syncthreads();
 }
 
-// Slope of the edge between tile points a < b, rounded to float32 once from
-// the exact integer differences (up to the rounding of the two conversions).
+// Slope of the edge between tile points a < b, rounded to float32 from the
+// exact integer differences (up to the rounding of the two conversions).
 template <bool WEIGHTED>
 __device__ __forceinline__ float tile_slope(const Tile& T, int a, int b, int qs, int qw) {
-    int64_t dS = tile_S<WEIGHTED>(T, b) - tile_S<WEIGHTED>(T, a);
-    int64_t dW = tile_W<WEIGHTED>(T, b) - tile_W<WEIGHTED>(T, a);
-    float f = __ll2float_rn(dS) / __ll2float_rn(dW);
+    const int64_t dS = tile_S<WEIGHTED>(T, b) - tile_S<WEIGHTED>(T, a);
+    const int64_t dW = tile_W<WEIGHTED>(T, b) - tile_W<WEIGHTED>(T, a);
+    const float f = __ll2float_rn(dS) / __ll2float_rn(dW);
     return ldexpf(f, qs - qw);
 }
 
