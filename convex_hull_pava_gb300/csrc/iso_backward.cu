@@ -70,29 +70,46 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     const int lane = tid - tile * L;
     const int gl = tid;
 
-    maska[gl] = 0u;
     for (int i = lane; i < 4; i += L) info[tile * 4 + i] = 0;
     __syncthreads();
-    int gmax = 0, ewmax = 0, nonfinite = 0;
+    int gmax = 0, ewmax = 0;
+    uint32_t bad = 0;
+    uint32_t starts = 0;
+    const int e = live ? min(max(nt - (lane << 5), 0), 32) : 0;
     if (live) {
-        for (int e = lane; e < nt; e += L) {
-            const float g = __ldg(gr + e);
-            const int pos = spos(tile * L + (e >> 5), e & 31);
-            stage[pos] = g;
-            if (((__float_as_uint(g) >> 23) & 0xff) == 0xff) nonfinite = 1;
-            else gmax = max(gmax, bexp(g));
-            if ((e == 0 && first_is_start) || br[e])
-                atomicOr(&maska[tile * L + (e >> 5)], 1u << (e & 31));
-            if constexpr (WEIGHTED) {
-                const float wv = __ldg(wr + e);
-                stagew[pos] = wv;
-                if (!(wv > 0.0f) || ((__float_as_uint(wv) >> 23) & 0xff) == 0xff) nonfinite = 1;
-                else ewmax = max(ewmax, bexp(wv));
+        stage_tile<false>(gr, nt, lane, L, tile * L, false, stage, gmax, bad);
+        if constexpr (WEIGHTED) stage_tile<true>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
+        // the lane's 32 block-start bytes, as a bit mask
+        const uint8_t* bl = br + (lane << 5);
+        if (e == 32 && (reinterpret_cast<uintptr_t>(bl) & 15u) == 0) {
+            const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(bl));
+            const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(bl) + 1);
+            const uint32_t wd[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                // high bit of each byte set iff the byte is non-zero
+                const uint32_t h = ((wd[q] & 0x7f7f7f7fu) + 0x7f7f7f7fu) | wd[q];
+                const uint32_t b4 = (((h >> 7) & 0x01010101u) * 0x01020408u) >> 24;
+                starts |= (b4 & 0xfu) << (4 * q);
             }
+        } else {
+            uint8_t v[32];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = k < e ? __ldg(bl + k) : (uint8_t)0;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) starts |= (v[k] != 0 ? 1u : 0u) << k;
         }
+        if (lane == 0 && first_is_start) starts |= 1u;
+    }
+    maska[gl] = starts;
+    gmax = tile_warp_max(gmax, L);
+    if (WEIGHTED) ewmax = tile_warp_max(ewmax, L);
+    const int bad_or = tile_warp_or((int)bad, L);
+    const int seg = L < 32 ? L : 32;
+    if (live && ((tid & 31) & (seg - 1)) == 0) {
         atomicMax(&info[tile * 4 + 0], gmax);
         if (WEIGHTED) atomicMax(&info[tile * 4 + 1], ewmax);
-        if (nonfinite) atomicOr(&info[tile * 4 + 2], 1);
+        if (bad_or) atomicOr(&info[tile * 4 + 2], 1);
     }
     __syncthreads();
     gmax = max(info[tile * 4 + 0], 1);
@@ -100,10 +117,8 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     B.nan = info[tile * 4 + 2] != 0;
     B.qg = qexp_unit(gmax);
     B.qw = WEIGHTED ? qexp_unit(ewmax) : 0;
-    const int e = live ? min(max(nt - (lane << 5), 0), 32) : 0;
-    const uint32_t starts = maska[gl];
     {
-        uint32_t bal = __ballot_sync(kFull, starts != 0u);
+        const uint32_t bal = __ballot_sync(kFull, starts != 0u);
         if ((tid & 31) == 0) summ[tid >> 5] = bal;
     }
 

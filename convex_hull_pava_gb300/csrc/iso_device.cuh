@@ -208,19 +208,39 @@ struct Tile {
     int nt;              // elements
 };
 
+// Tile-relative coordinates of point p (0..nt).  After the lane hulls are
+// built, row l of Sx (Wx) holds the tile-relative cumulative sums at points
+// 32l .. 32l+32; the end point of a tile of exactly 32 L elements is LS[L].
 template <bool WEIGHTED>
 __device__ __forceinline__ int64_t tile_S(const Tile& T, int p) {
-    int l = p >> 5, k = p & 31;
-    return T.LS[l] + (k ? T.Sx[l * kRow + k] : 0);
+    const int l = p >> 5, k = p & 31;
+    return l < T.L ? T.Sx[l * kRow + k] : T.LS[T.L];
 }
 template <bool WEIGHTED>
 __device__ __forceinline__ int64_t tile_W(const Tile& T, int p) {
     if constexpr (WEIGHTED) {
-        int l = p >> 5, k = p & 31;
-        return T.LW[l] + (k ? T.Wx[l * kRow + k] : 0);
+        const int l = p >> 5, k = p & 31;
+        return l < T.L ? T.Wx[l * kRow + k] : T.LW[T.L];
     } else {
         return (int64_t)p;
     }
+}
+
+// Exact sign test w1*s2 - w2*s1 > 0 for |w| < 2^30 (point counts of a tile):
+// 32 x 64-bit products split in two halves, without 128-bit arithmetic.
+__device__ __forceinline__ bool left_turn_w32(int w1, int64_t s1, int w2, int64_t s2) {
+    const int64_t h = (int64_t)w1 * (int32_t)(s2 >> 32) - (int64_t)w2 * (int32_t)(s1 >> 32);
+    const int64_t l = (int64_t)w1 * (int64_t)(uint32_t)s2 - (int64_t)w2 * (int64_t)(uint32_t)s1;
+    const int64_t H = h + (l >> 32);
+    return H > 0 || (H == 0 && (uint32_t)l != 0u);
+}
+
+// Turn test on tile points, with the differences taken from o.
+template <bool WEIGHTED>
+__device__ __forceinline__ bool tile_turn(int64_t Wo, int64_t So, int64_t Wa, int64_t Sa,
+                                          int64_t Wb, int64_t Sb) {
+    if constexpr (WEIGHTED) return left_turn<true>(Wa - Wo, Sa - So, Wb - Wo, Sb - So);
+    else return left_turn_w32((int)(Wa - Wo), Sa - So, (int)(Wb - Wo), Sb - So);
 }
 
 __device__ __forceinline__ bool summ_bit(const Tile& T, int lane) {
@@ -279,38 +299,70 @@ __device__ __forceinline__ int tile_succ(const Tile& T, int p, int hi_lane, int 
     return (q << 5) + __ffs(T.mask[q]) - 1;
 }
 
+// Predecessor / successor vertex for merge groups that lie inside one warp:
+// `word` is the warp's non-empty-lane word, so no loop over lanes is needed
+// and the leaders of all groups of a warp run the same instructions.
+__device__ __forceinline__ int wpred(const Tile& T, uint32_t word, int p, int lo_lane) {
+    const int l = p >> 5, k = p & 31;
+    const int bl = (T.sbase + l) & 31, blo = (T.sbase + lo_lane) & 31;
+    const uint32_t m0 = T.mask[l] & ((1u << k) - 1u);
+    const uint32_t below = word & ((1u << bl) - 1u) & ~((1u << blo) - 1u);
+    const int q = m0 ? l : max(lo_lane, l - bl + 31 - __clz(below));
+    const uint32_t mq = m0 ? m0 : T.mask[q];
+    return (q << 5) + 31 - __clz(mq);
+}
+__device__ __forceinline__ int wsucc(const Tile& T, uint32_t word, int p, int hi_lane, int endp) {
+    const int l = p >> 5, k = p & 31;
+    const int bl = (T.sbase + l) & 31;
+    const int bhi = bl + (hi_lane - l);                  // one past the group's last bit
+    const uint32_t m0 = k == 31 ? 0u : (T.mask[l] & ~((2u << k) - 1u));
+    uint32_t above = bl == 31 ? 0u : (word & ~((2u << bl) - 1u));
+    if (bhi < 32) above &= (1u << bhi) - 1u;
+    const int q = m0 ? l : (above ? l - bl + __ffs(above) - 1 : l);
+    const uint32_t mq = m0 ? m0 : T.mask[q];
+    const int r = (q << 5) + __ffs(mq) - 1;
+    return (m0 | above) ? r : endp;
+}
+
 // Bridge of the merge of lane groups A = [A0, B0) and B = [B0, Bend) (Section
 // 3.2, Lemma 4.2): s = 32*B0 is the last vertex of H(A) and the first of H(B).
 // If the chain is convex at s, returns (s, s).  Otherwise walks from s's
 // neighbours, the left end left and the right end right, until the line
 // between them supports both hulls.  Each step removes a vertex (Lemma 5.1).
 // The coordinates of the two current ends stay in registers; a step loads one
-// new point.
-template <bool WEIGHTED>
-__device__ void tile_bridge(const Tile& T, int A0, int B0, int Bend, int& ra, int& rb) {
+// new point.  IN_WARP selects the warp-local lookups.
+template <bool WEIGHTED, bool IN_WARP>
+__device__ __forceinline__ void tile_bridge(const Tile& T, int A0, int B0, int Bend, int& ra,
+                                            int& rb) {
     const int s = B0 << 5;
     const int endB = min(Bend << 5, T.nt);
     const int startA = A0 << 5;
-    int a = tile_pred(T, s, A0);
-    int b = tile_succ(T, s, Bend, endB);
+    uint32_t word = 0;
+    if constexpr (IN_WARP) word = T.summ[(T.sbase + A0) >> 5];
+    auto pred = [&](int p) { return IN_WARP ? wpred(T, word, p, A0) : tile_pred(T, p, A0); };
+    auto succ = [&](int p) {
+        return IN_WARP ? wsucc(T, word, p, Bend, endB) : tile_succ(T, p, Bend, endB);
+    };
+    int a = pred(s);
+    int b = succ(s);
     int64_t Wa = tile_W<WEIGHTED>(T, a), Sa = tile_S<WEIGHTED>(T, a);
     int64_t Wb = tile_W<WEIGHTED>(T, b), Sb = tile_S<WEIGHTED>(T, b);
     {
         const int64_t Ws = tile_W<WEIGHTED>(T, s), Ss = tile_S<WEIGHTED>(T, s);
-        if (left_turn<true>(Ws - Wa, Ss - Sa, Wb - Wa, Sb - Sa)) { ra = s; rb = s; return; }
+        if (tile_turn<WEIGHTED>(Wa, Sa, Ws, Ss, Wb, Sb)) { ra = s; rb = s; return; }
     }
     for (;;) {
         bool moved = false;
         while (a > startA) {
-            const int p = tile_pred(T, a, A0);
+            const int p = pred(a);
             const int64_t Wp = tile_W<WEIGHTED>(T, p), Sp = tile_S<WEIGHTED>(T, p);
-            if (left_turn<true>(Wa - Wp, Sa - Sp, Wb - Wp, Sb - Sp)) break;   // p -> a -> b convex
+            if (tile_turn<WEIGHTED>(Wp, Sp, Wa, Sa, Wb, Sb)) break;   // p -> a -> b convex
             a = p; Wa = Wp; Sa = Sp; moved = true;
         }
         while (b < endB) {
-            const int q = tile_succ(T, b, Bend, endB);
+            const int q = succ(b);
             const int64_t Wq = tile_W<WEIGHTED>(T, q), Sq = tile_S<WEIGHTED>(T, q);
-            if (left_turn<true>(Wb - Wa, Sb - Sa, Wq - Wa, Sq - Sa)) break;   // a -> b -> q convex
+            if (tile_turn<WEIGHTED>(Wa, Sa, Wb, Sb, Wq, Sq)) break;   // a -> b -> q convex
             b = q; Wb = Wq; Sb = Sq; moved = true;
         }
         if (!moved) break;

@@ -24,7 +24,7 @@ namespace isodev {
 namespace {
 
 constexpr int kWalkCap = 64;              // steps of a walk before the bisection (Section 6)
-constexpr int kMergeThreads = 1024;
+constexpr int kMergeThreads = 512;
 constexpr int kMergeSmem = 210 * 1024;    // shared memory of the merge kernel
 
 template <bool WEIGHTED> struct LongCfg;
@@ -215,16 +215,31 @@ struct MStore {
     __device__ __forceinline__ void at(Pos p, i128& Wv, i128& Sv) const {
         vertex(seg[p.k].x, p.r, Wv, Sv);
     }
-    // the turn o -> a -> b is strictly left (exact, 256-bit products)
+    // the turn o -> a -> b is strictly left.  Exact: 128-bit products when the
+    // differences fit in 64 bits, 256-bit ones otherwise.
+    static __device__ __forceinline__ bool turn(i128 Wo, i128 So, i128 Wa, i128 Sa, i128 Wb,
+                                                i128 Sb) {
+        const i128 w1 = Wa - Wo, s1 = Sa - So, w2 = Wb - Wo, s2 = Sb - So;
+        auto fits = [](i128 x) { return (i128)(int64_t)x == x; };
+        if (fits(w1) && fits(s1) && fits(w2) && fits(s2))
+            return left_turn<true>((int64_t)w1, (int64_t)s1, (int64_t)w2, (int64_t)s2);
+        return sign_det128(w1, s2, s1, w2) > 0;
+    }
     __device__ __forceinline__ bool left(Pos o, Pos a, Pos b) const {
         i128 Wo, So, Wa, Sa, Wb, Sb;
         at(o, Wo, So); at(a, Wa, Sa); at(b, Wb, Sb);
-        return sign_det128(Wa - Wo, Sb - So, Sa - So, Wb - Wo) > 0;
+        return turn(Wo, So, Wa, Sa, Wb, Sb);
     }
 };
 
+// A merge's descriptor move: seg[dst + t] = seg[src + t] for t < len (dst < src).
+struct Move { int dst, src, len; };
+
+// Merge of the lists of the neighbouring nodes starting at j0 and j1
+// (Algorithm 1): finds the bridge, cuts the two segments it lands in, sets the
+// merged list's length, and returns the move of the right list's tail.
 template <bool WEIGHTED>
-__device__ void merge_pair(const MStore<WEIGHTED>& V, int j0, int j1) {
+__device__ __forceinline__ Move merge_plan(const MStore<WEIGHTED> V, int j0, int j1) {
     int4* seg = V.seg;
     const int nL = V.cnt[j0], nR = V.cnt[j1];
     const int kLl = j0 + nL - 1, kR0 = j1, kRl = j1 + nR - 1;
@@ -246,27 +261,35 @@ __device__ void merge_pair(const MStore<WEIGHTED>& V, int j0, int j1) {
         const int lo = seg[kR0].y + 1;
         if (lo > seg[kR0].z) first = kR0 + 1;
         else seg[kR0].y = lo;
-        int dst = j0 + nL;
-        for (int k = first; k <= kRl; ++k) seg[dst++] = seg[k];
-        V.cnt[j0] = dst - j0;
-        return;
+        const int len = kRl - first + 1;
+        V.cnt[j0] = nL + len;
+        return Move{j0 + nL, first, len};
     }
+    // walk from s's neighbours; the two current ends keep their coordinates in
+    // registers, so a step reads one new vertex
     Pos a = pa, b = sb;
+    i128 Wa, Sa, Wb, Sb;
+    V.at(a, Wa, Sa);
+    V.at(b, Wb, Sb);
     int steps = 0;
     bool gave_up = false;
     for (;;) {
         bool moved = false;
         while (hasPrev(a)) {
-            Pos p = prev(a);
-            if (V.left(p, a, b)) break;
-            a = p; moved = true;
+            const Pos p = prev(a);
+            i128 Wp, Sp;
+            V.at(p, Wp, Sp);
+            if (V.turn(Wp, Sp, Wa, Sa, Wb, Sb)) break;
+            a = p; Wa = Wp; Sa = Sp; moved = true;
             if (++steps > kWalkCap) { gave_up = true; break; }
         }
         if (gave_up) break;
         while (hasNext(b)) {
-            Pos q = next(b);
-            if (V.left(a, b, q)) break;
-            b = q; moved = true;
+            const Pos q = next(b);
+            i128 Wq, Sq;
+            V.at(q, Wq, Sq);
+            if (V.turn(Wa, Sa, Wb, Sb, Wq, Sq)) break;
+            b = q; Wb = Wq; Sb = Sq; moved = true;
             if (++steps > kWalkCap) { gave_up = true; break; }
         }
         if (gave_up || !moved) break;
@@ -307,12 +330,12 @@ __device__ void merge_pair(const MStore<WEIGHTED>& V, int j0, int j1) {
         a = flatL(lo);
         b = flatR(tangent(a));
     }
-    // cut L at a, R at b, and move R's tail down
+    // cut L at a and R at b; R's tail moves down behind L's kept part
     seg[a.k].z = a.r;
     seg[b.k].y = b.r;
-    int dst = a.k + 1;
-    for (int k = b.k; k <= kRl; ++k) seg[dst++] = seg[k];
-    V.cnt[j0] = dst - j0;
+    const int len = kRl - b.k + 1;
+    V.cnt[j0] = (a.k - j0 + 1) + len;
+    return Move{a.k + 1, b.k, len};
 }
 
 // Exclusive block-wide scan of one 128-bit value per thread (blockDim.x <= 1024).
@@ -363,10 +386,19 @@ merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
             const ChunkMeta mt = ws.meta[c0 + j];
             qs = max(qs, mt.qs); qw = max(qw, mt.qw); bad |= mt.bad; hsum += (unsigned)mt.h;
         }
-        atomicMax(&s_qs, qs);
-        atomicMax(&s_qw, qw);
-        if (bad) atomicOr(&s_bad, bad);
-        atomicAdd(&s_H, hsum);
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            qs = max(qs, __shfl_xor_sync(kFull, qs, d));
+            qw = max(qw, __shfl_xor_sync(kFull, qw, d));
+            bad |= __shfl_xor_sync(kFull, bad, d);
+            hsum += __shfl_xor_sync(kFull, hsum, d);
+        }
+        if ((tid & 31) == 0) {
+            atomicMax(&s_qs, qs);
+            atomicMax(&s_qw, qw);
+            if (bad) atomicOr(&s_bad, bad);
+            atomicAdd(&s_H, hsum);
+        }
     }
     __syncthreads();
     const int qs = s_qs, qw = s_qw, bad = s_bad;
@@ -453,18 +485,26 @@ merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
     }
     __syncthreads();
     if (in_smem) {
-        // read every chunk hull of the row once into shared memory: each warp
-        // copies whole chunks, its lanes striding over the chunk's vertices
+        // read every chunk hull of the row once into shared memory; each thread
+        // copies a contiguous range of vertices
         const size_t cap = (size_t)C + 1;
-        const int warp = tid >> 5, wl = tid & 31, nw = nth >> 5;
-        for (int64_t j = warp; j < m; j += nw) {
-            const int h = ws.meta[c0 + j].h;
-            const int base = vb[j];
-            const size_t g = (size_t)(c0 + j) * cap;
-            for (int r = wl; r < h; r += 32) {
-                P[base + r] = ws.slot_p[g + r];
-                S[base + r] = ws.slot_S[g + r];
-                if (WEIGHTED) W[base + r] = ws.slot_W[g + r];
+        const int64_t pv = (Htot + nth - 1) / nth;
+        const int64_t i0 = imin64(Htot, tid * pv), i1 = imin64(Htot, i0 + pv);
+        if (i0 < i1) {
+            int lo = 0, hi = (int)m - 1;        // chunk holding vertex i0
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (vb[mid] <= i0) lo = mid; else hi = mid - 1;
+            }
+            int jc = lo;
+            int nextb = jc + 1 < m ? vb[jc + 1] : (int)Htot;
+#pragma unroll 4
+            for (int64_t i = i0; i < i1; ++i) {
+                while (i >= nextb) { ++jc; nextb = jc + 1 < m ? vb[jc + 1] : (int)Htot; }
+                const size_t g = (size_t)(c0 + jc) * cap + (size_t)(i - vb[jc]);
+                P[i] = ws.slot_p[g];
+                S[i] = ws.slot_S[g];
+                if (WEIGHTED) W[i] = ws.slot_W[g];
             }
         }
     }
@@ -475,12 +515,40 @@ merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
     V.offS = offS; V.offW = offW; V.dS = dS; V.dW = dW;
     V.seg = seg; V.cnt = cnt; V.pre = pre;
     V.c0 = c0; V.C = C;
+    // Levels with many merges run one thread per merge; the others one warp per
+    // merge, whose lanes move the descriptors in coalesced rounds of 32
+    // (Section 6, "Merge levels").
+    const int warp = tid >> 5, wl = tid & 31, nw = nth >> 5;
     for (int r = 0; ((int64_t)1 << r) < m; ++r) {
         const int64_t span = (int64_t)2 << r;
         const int64_t merges = (m + span - 1) / span;
-        for (int64_t g = tid; g < merges; g += nth) {
-            const int64_t j0 = g * span, j1 = j0 + (span >> 1);
-            if (j1 < m) merge_pair<WEIGHTED>(V, (int)j0, (int)j1);
+        if (merges >= nw) {
+            for (int64_t g = tid; g < merges; g += nth) {
+                const int64_t j0 = g * span, j1 = j0 + (span >> 1);
+                if (j1 < m) {
+                    const Move mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
+                    for (int t = 0; t < mv.len; ++t) seg[mv.dst + t] = seg[mv.src + t];
+                }
+            }
+        } else {
+            for (int64_t g = warp; g < merges; g += nw) {
+                const int64_t j0 = g * span, j1 = j0 + (span >> 1);
+                if (j1 >= m) continue;
+                Move mv{0, 0, 0};
+                if (wl == 0) mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
+                mv.dst = __shfl_sync(kFull, mv.dst, 0);
+                mv.src = __shfl_sync(kFull, mv.src, 0);
+                mv.len = __shfl_sync(kFull, mv.len, 0);
+                __syncwarp();
+                for (int t0 = 0; t0 < mv.len; t0 += 32) {
+                    const int t = t0 + wl;
+                    int4 d = make_int4(0, 0, 0, 0);
+                    if (t < mv.len) d = seg[mv.src + t];
+                    __syncwarp();
+                    if (t < mv.len) seg[mv.dst + t] = d;
+                    __syncwarp();
+                }
+            }
         }
         __syncthreads();
     }

@@ -307,8 +307,19 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         }
     }
 
-    // ---- lane hulls in bit masks ----
+    // ---- lane hulls in bit masks, on lane-relative sums; then the lane's row
+    // becomes tile-relative for the merges ----
     uint32_t mask = lane_hull<WEIGHTED>(myS, myW, cand, e);
+    {
+        const int64_t ls = LSa[tile * (L + 1) + lane];
+#pragma unroll
+        for (int k = 0; k <= 32; ++k) myS[k] += ls;
+        if constexpr (WEIGHTED) {
+            const int64_t lw = LWa[tile * (L + 1) + lane];
+#pragma unroll
+            for (int k = 0; k <= 32; ++k) myW[k] += lw;
+        }
+    }
     maska[gl] = mask;
     {
         const uint32_t bal = __ballot_sync(kFull, mask != 0u);
@@ -340,7 +351,8 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         const int slot = r < 5 ? ((tid >> 5) << 4) + ((tid & 31) >> (r + 1)) : (tid >> (r + 1));
         if (active && lane == A0) {
             int a, b;
-            tile_bridge<WEIGHTED>(T, A0, B0, Bend, a, b);
+            if (r < 5) tile_bridge<WEIGHTED, true>(T, A0, B0, Bend, a, b);
+            else tile_bridge<WEIGHTED, false>(T, A0, B0, Bend, a, b);
             bridge[slot] = make_int2(a, b);
         }
         if (r < 5) __syncwarp(); else __syncthreads();
