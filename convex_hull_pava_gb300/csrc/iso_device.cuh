@@ -299,6 +299,43 @@ __device__ __forceinline__ int tile_succ(const Tile& T, int p, int hi_lane, int 
     return (q << 5) + __ffs(T.mask[q]) - 1;
 }
 
+// Monotone chain over entries 0..e (e <= 32) of a list of points with
+// explicit coordinates, every entry a candidate.  Same stack discipline as
+// lane_hull; returns the mask of kept entries among 0..e-1 (entry e, the end,
+// is always kept).  Unit-weight lists carry point indices as W (|dW| < 2^14).
+template <bool WEIGHTED>
+__device__ __forceinline__ uint32_t list_chain(const int64_t* S, const int64_t* W, int e) {
+    if (e <= 0) return 0u;
+    auto turn = [](int64_t Wo, int64_t So, int64_t Wa, int64_t Sa, int64_t Wb, int64_t Sb) {
+        if constexpr (WEIGHTED) return left_turn<true>(Wa - Wo, Sa - So, Wb - Wo, Sb - So);
+        else return left_turn_w32((int)(Wa - Wo), Sa - So, (int)(Wb - Wo), Sb - So);
+    };
+    uint32_t mask = 1u;
+    int t = 0, b = -1, k = 1;
+    int64_t St = S[0], Wt = W[0], Sb = 0, Wb = 0;
+    int64_t Sk = S[1], Wk = W[1];
+    for (int it = 0; it < 2 * kPts + 2; ++it) {
+        const int k2 = k < e ? k + 1 : e;
+        const uint32_t below = b > 0 ? (mask & ((1u << b) - 1u)) : 0u;
+        const int b2 = below ? (31 - __clz(below)) : -1;
+        const int bl = b2 < 0 ? 0 : b2;
+        const int64_t Sk2 = S[k2], Wk2 = W[k2], Sb2 = S[bl], Wb2 = W[bl];
+        const bool push = (b < 0) || turn(Wb, Sb, Wt, St, Wk, Sk);
+        if (push) {
+            if (k >= e) break;
+            mask |= 1u << k;
+            b = t; Sb = St; Wb = Wt;
+            t = k; St = Sk; Wt = Wk;
+            k = k2; Sk = Sk2; Wk = Wk2;
+        } else {
+            mask &= ~(1u << t);
+            t = b; St = Sb; Wt = Wb;
+            b = b2; Sb = Sb2; Wb = Wb2;
+        }
+    }
+    return mask;
+}
+
 // Predecessor / successor vertex for merge groups that lie inside one warp:
 // `word` is the warp's non-empty-lane word, so no loop over lanes is needed
 // and the leaders of all groups of a warp run the same instructions.

@@ -27,14 +27,14 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, true>(yr, wr, n, live, neg, L, smem, H);
 
-    float* slope = reinterpret_cast<float*>(smem + SM::oY);   // y until it becomes slopes
+    float* slope = reinterpret_cast<float*>(smem + SM::oY);   // slope of each vertex's edge
     const Tile& T = H.T;
     const int lane = H.lane, gl = H.gl, e = H.e;
     const bool work = live && H.bad == 0;
     const uint32_t mask = work ? T.mask[lane] : 0u;
 
     // ---- 1. every vertex: the slope of the hull edge leaving it (eq. (3)).  A
-    // one-element block is fitted by its own value. ----
+    // one-element block is fitted by its own value, read again from y. ----
     {
         uint32_t m = mask;
         while (m) {
@@ -42,7 +42,14 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
             m &= m - 1u;
             const int v = (lane << 5) + k;
             const int b = m ? (lane << 5) + __ffs(m) - 1 : tile_succ(T, v, L, n);
-            if (b != v + 1) slope[spos(gl, k)] = tile_slope<WEIGHTED>(T, v, b, H.qs, H.qw);
+            float sl;
+            if (b == v + 1) {
+                const float yv = __ldg(yr + v);            // a one-element block keeps its value
+                sl = neg ? -yv : yv;
+            } else {
+                sl = tile_slope<WEIGHTED>(T, v, b, H.qs, H.qw);
+            }
+            slope[spos(gl, k)] = sl;
         }
     }
     __syncthreads();

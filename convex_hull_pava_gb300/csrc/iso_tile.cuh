@@ -24,9 +24,16 @@ __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ g
 // a separate area, which later holds each vertex's edge slope.
 template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 struct TileSmem {
+    // lists of the multi-level chains: capacities (entries) for the whole CTA
+    static constexpr int kCapA = (WEIGHTED ? 4 : 5) * NT;
+    static constexpr int kCapB = kCapA / 2;
+    static constexpr int kEntB = WEIGHTED ? 20 : 16;            // S, W (and the point index)
+    static constexpr int kListBytes = (kCapA + kCapB) * kEntB;
     static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
-    static constexpr int kYB = EMIT ? NT * 32 * 4 : 0;          // kept y / slope per vertex
+    // EMIT: slope per vertex at emission; before that, the lists
+    static constexpr int kYB = EMIT ? (NT * 128 > kListBytes ? NT * 128 : kListBytes) : 0;
+    static constexpr int kOwnListB = EMIT ? 0 : kListBytes;
     static constexpr int kLSB = (NT + RMAX) * 8;                // lane starts, L+1 per tile
     static constexpr int kLWB = WEIGHTED ? kLSB : 0;
     static constexpr int kMaskB = NT * 4;
@@ -37,7 +44,8 @@ struct TileSmem {
     static constexpr int oSx = 0;
     static constexpr int oWx = oSx + kSxB;
     static constexpr int oY = oWx + kWxB;
-    static constexpr int oLS = oY + kYB;
+    static constexpr int oOwnList = oY + kYB;
+    static constexpr int oLS = oOwnList + kOwnListB;
     static constexpr int oLW = oLS + kLSB;
     static constexpr int oMask = oLW + kLWB;
     static constexpr int oSumm = oMask + kMaskB;
@@ -45,9 +53,10 @@ struct TileSmem {
     static constexpr int oInfo = oBridge + kBridgeB;
     static constexpr int oScan = oInfo + kInfoB;
     static constexpr int kBytes = ((oScan + kScanB + 127) / 128) * 128;
-    // staging: y at the start of Sx (or in the Y area when EMIT), w after it
-    static constexpr int oStageY = EMIT ? oY : oSx;
+    // staging: y at the start of Sx, w after it (2 x 128 B per lane < 264 B)
+    static constexpr int oStageY = oSx;
     static constexpr int oStageW = oSx + NT * 128;
+    static constexpr int oList = EMIT ? oY : oOwnList;
 };
 
 // Per-tile reduction slots in the info area.
@@ -338,9 +347,120 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     T.L = L;
     T.nt = nt;
 
+    // ---- the tile hull from the lane hulls.  When the lane hulls are small
+    // (few vertices survive, as on noisy data), their vertices are listed and
+    // hulled again by lane chains over groups of 32 entries, level after level,
+    // until one chain finishes the tile: every level discards only points that
+    // are not vertices of a subset's hull (Lemma 4.1).  Otherwise, or when a
+    // level does not halve the list, the lane hulls are merged in rounds by
+    // walking to the bridges (Section 3.2). ----
+    bool fast = false;
+    {
+        const int R = NT / L;
+        const int capA = SM::kCapA / R, capB = SM::kCapB / R;
+        int64_t* SA = reinterpret_cast<int64_t*>(smem + SM::oList);
+        int64_t* WA = SA + SM::kCapA;
+        int64_t* SB = WA + SM::kCapA;
+        int64_t* WB = SB + SM::kCapB;
+        int32_t* PA = reinterpret_cast<int32_t*>(WB + SM::kCapB);
+        int32_t* PB = PA + SM::kCapA;
+        int64_t* cS[2] = {SA + tile * capA, SB + tile * capB};
+        int64_t* cW[2] = {WA + tile * capA, WB + tile * capB};
+        int32_t* cP[2] = {PA + tile * capA, PB + tile * capB};
+        const int cap[2] = {capA, capB};
+
+        const int cnt = __popc(mask);
+        const int64_t ci = tile_scan_incl<NT>((int64_t)cnt, lane, L, scan);
+        if (lane == L - 1) info[tile * 4 + 0] = (int)ci;
+        __syncthreads();
+        const int V1 = info[tile * 4 + 0];
+        const bool ok = !work || (V1 + 1 <= capA);
+        fast = __syncthreads_and(ok) != 0;
+        int n = work ? V1 + 1 : 0;
+        int cur = 0;
+        if (fast) {
+            if (work) {
+                uint32_t mm = mask;
+                int i = (int)(ci - cnt);
+                while (mm) {
+                    const int k = __ffs(mm) - 1;
+                    mm &= mm - 1u;
+                    cS[0][i] = myS[k];
+                    cW[0][i] = WEIGHTED ? myW[k] : (int64_t)((lane << 5) + k);
+                    if (WEIGHTED) cP[0][i] = (lane << 5) + k;
+                    ++i;
+                }
+                if (lane == L - 1) {
+                    cS[0][V1] = LSa[tile * (L + 1) + L];
+                    cW[0][V1] = WEIGHTED ? LWa[tile * (L + 1) + L] : (int64_t)nt;
+                    if (WEIGHTED) cP[0][V1] = nt;
+                }
+            }
+            for (int level = 0; level < 12; ++level) {
+                const bool more = work && n > 33;
+                if (!__syncthreads_or(more)) break;
+                const int G = more ? (n - 1 + 31) >> 5 : 0;
+                uint32_t gm = 0;
+                if (lane < G) {
+                    const int e = min(32, n - 1 - (lane << 5));
+                    gm = list_chain<WEIGHTED>(cS[cur] + (lane << 5), cW[cur] + (lane << 5), e);
+                }
+                const int gc = __popc(gm);
+                const int64_t gi = tile_scan_incl<NT>((int64_t)gc, lane, L, scan);
+                if (lane == L - 1) info[tile * 4 + 1] = (int)gi;
+                __syncthreads();
+                const int n2 = more ? info[tile * 4 + 1] + 1 : n;
+                const bool fits = !more || (n2 <= cap[cur ^ 1] && 2 * n2 <= n + 2);
+                if (!__syncthreads_and(fits)) { fast = false; break; }
+                if (more) {
+                    const int nx = cur ^ 1;
+                    int i = (int)(gi - gc);
+                    uint32_t mm = gm;
+                    while (mm) {
+                        const int k = __ffs(mm) - 1;
+                        mm &= mm - 1u;
+                        const int src = (lane << 5) + k;
+                        cS[nx][i] = cS[cur][src];
+                        cW[nx][i] = cW[cur][src];
+                        if (WEIGHTED) cP[nx][i] = cP[cur][src];
+                        ++i;
+                    }
+                    if (lane == 0) {
+                        cS[nx][n2 - 1] = cS[cur][n - 1];
+                        cW[nx][n2 - 1] = cW[cur][n - 1];
+                        if (WEIGHTED) cP[nx][n2 - 1] = cP[cur][n - 1];
+                    }
+                    n = n2;
+                    cur = nx;
+                }
+            }
+        }
+        if (fast) {
+            // one chain over the last list; its kept entries are the tile hull
+            __syncthreads();
+            uint32_t fm = 0;
+            if (work && lane == 0) fm = list_chain<WEIGHTED>(cS[cur], cW[cur], n - 1);
+            mask = 0u;
+            maska[gl] = 0u;
+            __syncthreads();
+            if (work && lane == 0) {
+                while (fm) {
+                    const int k = __ffs(fm) - 1;
+                    fm &= fm - 1u;
+                    const int p = WEIGHTED ? cP[cur][k] : (int)cW[cur][k];
+                    if (p < nt) T.mask[p >> 5] |= 1u << (p & 31);
+                }
+            }
+            __syncthreads();
+            mask = maska[gl];
+            const uint32_t bal = __ballot_sync(kFull, mask != 0u);
+            if ((tid & 31) == 0) summ[tid >> 5] = bal;
+        }
+    }
+
     // ---- merge rounds: pairs of 2^r lanes, up to the whole tile.  Rounds whose
     // groups lie inside one warp synchronise the warp only. ----
-    for (int r = 0; (1 << r) < L; ++r) {
+    for (int r = 0; !fast && (1 << r) < L; ++r) {
         const int grp = lane >> (r + 1);
         const int A0 = grp << (r + 1);
         const int B0 = A0 + (1 << r);
