@@ -32,7 +32,8 @@ ISO_ROW_BAD_Y = 1
 ISO_ROW_BAD_W = 2
 
 EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
-           "iso_backward_workspace_bytes", "iso_backward", "iso_profile_enable", "iso_profile_read")
+           "iso_backward_workspace_bytes", "iso_backward", "iso_backward_noalloc",
+           "iso_profile_enable", "iso_profile_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -68,6 +69,8 @@ def load_library(path: str | None = None):
         lib.iso_fit.restype = ci
         lib.iso_backward.argtypes = [vp, vp, vp, i64, i64, vp, vp, sz, vp]
         lib.iso_backward.restype = ci
+        lib.iso_backward_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp]
+        lib.iso_backward_noalloc.restype = ci
         lib.iso_profile_enable.argtypes = [ci]
         lib.iso_profile_enable.restype = ci
         lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
@@ -193,6 +196,27 @@ def iso_backward(grad, blocks, w=None, *, out=None, workspace=None, stream=None)
         out.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))
     if st != ISO_OK:
         raise IsoError(st, "iso_backward")
+    return out
+
+
+def iso_backward_noalloc(grad, blocks, w=None, *, out=None, stream=None):
+    """Backward without a workspace, for callers that cannot allocate device
+    memory: long rows use a fixed scratch array inside the library (limit:
+    rows * ceil(n / 8192) <= 21,845), and calls that may overlap on the GPU
+    must be serialised by the caller."""
+    torch = _torch()
+    _check_dev(grad, "grad", torch.float32)
+    _check_dev(blocks, "blocks", torch.uint8)
+    rows, n = _shape2(grad)
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+    if out is None:
+        out = torch.empty_like(grad)
+    st = load_library().iso_backward_noalloc(
+        grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), rows, n,
+        out.data_ptr(), _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_backward_noalloc")
     return out
 
 

@@ -121,6 +121,29 @@ iso_status iso_backward(const float *grad, const uint8_t *blocks, const float *w
                         void *stream);
 
 /*
+ * iso_backward_noalloc -- iso_backward for callers that cannot allocate device
+ * memory (no counterpart in the paper: it is an interface addition).
+ *
+ * Same arguments, results and errors as iso_backward, without the workspace:
+ * the per-tile records that rows longer than 8,192 elements need live in a
+ * fixed 2 MiB array inside the library (device memory that every GPU which
+ * loads the library holds until the process exits), which limits such calls to
+ * rows * ceil(n / 8192) <= 21,845 tiles; larger calls return ISO_ERR_WORKSPACE
+ * and enqueue nothing.  Rows of at most 8,192 elements need no scratch and have
+ * no such limit.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, on the calling thread's current device); make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array: calls whose work may overlap on the GPU
+ *    (different streams, several host threads) race on it and must be
+ *    serialised by the caller.  Each call writes every record it reads, so
+ *    nothing needs clearing between calls.
+ *  - It calls no allocating function (no cudaMalloc, no cudaFree).
+ */
+iso_status iso_backward_noalloc(const float *grad, const uint8_t *blocks, const float *w,
+                                int64_t rows, int64_t n, float *out, void *stream);
+
+/*
  * Optional per-kernel timing for benchmarks (not part of the fit).
  * iso_profile_enable(1) makes the library create a few CUDA events (once, on
  * first use; the only state the library keeps) and record one before the first
