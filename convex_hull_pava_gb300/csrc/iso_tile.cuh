@@ -25,6 +25,8 @@ __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ g
 template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 struct TileSmem {
     // lists of the multi-level chains: capacities (entries) for the whole CTA
+    // (entry j of a list lives at j + j/32: groups of 32 entries start 33 apart,
+    // so the lanes of a level read different banks)
     static constexpr int kCapA = (WEIGHTED ? 4 : 5) * NT;
     static constexpr int kCapB = kCapA / 2;
     static constexpr int kEntB = WEIGHTED ? 20 : 16;            // S, W (and the point index)
@@ -369,12 +371,25 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         int32_t* cP[2] = {PA + tile * capA, PB + tile * capB};
         const int cap[2] = {capA, capB};
 
+        // entry j of a list lives at j + j/32, and an entry that starts a group of
+        // 32 (j = 32g, g > 0) is also copied just before it, where the previous
+        // group reads its shared end: every group is 33 contiguous entries
+        auto lpos = [](int j) { return j + (j >> 5); };
+        auto put = [&](int b, int j, int64_t sv, int64_t wv, int32_t pv) {
+            const int x = lpos(j);
+            cS[b][x] = sv; cW[b][x] = wv;
+            if (WEIGHTED) cP[b][x] = pv;
+            if (j > 0 && (j & 31) == 0) {
+                cS[b][x - 1] = sv; cW[b][x - 1] = wv;
+                if (WEIGHTED) cP[b][x - 1] = pv;
+            }
+        };
         const int cnt = __popc(mask);
         const int64_t ci = tile_scan_incl<NT>((int64_t)cnt, lane, L, scan);
         if (lane == L - 1) info[tile * 4 + 0] = (int)ci;
         __syncthreads();
         const int V1 = info[tile * 4 + 0];
-        const bool ok = !work || (V1 + 1 <= capA);
+        const bool ok = !work || (lpos(V1) + 1 <= capA);
         fast = __syncthreads_and(ok) != 0;
         int n = work ? V1 + 1 : 0;
         int cur = 0;
@@ -385,16 +400,11 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                 while (mm) {
                     const int k = __ffs(mm) - 1;
                     mm &= mm - 1u;
-                    cS[0][i] = myS[k];
-                    cW[0][i] = WEIGHTED ? myW[k] : (int64_t)((lane << 5) + k);
-                    if (WEIGHTED) cP[0][i] = (lane << 5) + k;
+                    put(0, i, myS[k], WEIGHTED ? myW[k] : (int64_t)((lane << 5) + k), (lane << 5) + k);
                     ++i;
                 }
-                if (lane == L - 1) {
-                    cS[0][V1] = LSa[tile * (L + 1) + L];
-                    cW[0][V1] = WEIGHTED ? LWa[tile * (L + 1) + L] : (int64_t)nt;
-                    if (WEIGHTED) cP[0][V1] = nt;
-                }
+                if (lane == L - 1)
+                    put(0, V1, LSa[tile * (L + 1) + L], WEIGHTED ? LWa[tile * (L + 1) + L] : (int64_t)nt, nt);
             }
             for (int level = 0; level < 12; ++level) {
                 const bool more = work && n > 33;
@@ -403,14 +413,14 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                 uint32_t gm = 0;
                 if (lane < G) {
                     const int e = min(32, n - 1 - (lane << 5));
-                    gm = list_chain<WEIGHTED>(cS[cur] + (lane << 5), cW[cur] + (lane << 5), e);
+                    gm = list_chain<WEIGHTED>(cS[cur] + 33 * lane, cW[cur] + 33 * lane, e);
                 }
                 const int gc = __popc(gm);
                 const int64_t gi = tile_scan_incl<NT>((int64_t)gc, lane, L, scan);
                 if (lane == L - 1) info[tile * 4 + 1] = (int)gi;
                 __syncthreads();
                 const int n2 = more ? info[tile * 4 + 1] + 1 : n;
-                const bool fits = !more || (n2 <= cap[cur ^ 1] && 2 * n2 <= n + 2);
+                const bool fits = !more || (lpos(n2 - 1) + 1 <= cap[cur ^ 1] && (n2 <= 33 || 2 * n2 <= n + 2));
                 if (!__syncthreads_and(fits)) { fast = false; break; }
                 if (more) {
                     const int nx = cur ^ 1;
@@ -419,16 +429,13 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                     while (mm) {
                         const int k = __ffs(mm) - 1;
                         mm &= mm - 1u;
-                        const int src = (lane << 5) + k;
-                        cS[nx][i] = cS[cur][src];
-                        cW[nx][i] = cW[cur][src];
-                        if (WEIGHTED) cP[nx][i] = cP[cur][src];
+                        const int src = 33 * lane + k;
+                        put(nx, i, cS[cur][src], cW[cur][src], WEIGHTED ? cP[cur][src] : 0);
                         ++i;
                     }
                     if (lane == 0) {
-                        cS[nx][n2 - 1] = cS[cur][n - 1];
-                        cW[nx][n2 - 1] = cW[cur][n - 1];
-                        if (WEIGHTED) cP[nx][n2 - 1] = cP[cur][n - 1];
+                        const int src = lpos(n - 1);
+                        put(nx, n2 - 1, cS[cur][src], cW[cur][src], WEIGHTED ? cP[cur][src] : 0);
                     }
                     n = n2;
                     cur = nx;
@@ -445,7 +452,7 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
             __syncthreads();
             if (work && lane == 0) {
                 while (fm) {
-                    const int k = __ffs(fm) - 1;
+                    const int k = __ffs(fm) - 1;      // entries 0..31: stored at k
                     fm &= fm - 1u;
                     const int p = WEIGHTED ? cP[cur][k] : (int)cW[cur][k];
                     if (p < nt) T.mask[p >> 5] |= 1u << (p & 31);
