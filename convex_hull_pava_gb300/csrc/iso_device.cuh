@@ -34,25 +34,26 @@ __device__ __forceinline__ int bexp(float v) {
     return e == 0 ? 1 : e;
 }
 
-// round(v / 2^(emax - 176)): |result| < 2^50 when bexp(v) <= emax.
-// Rounds half away from zero; a non-finite v gives an arbitrary finite value
+// round(v / 2^(emax - 176)): |result| < 2^50 when bexp(v) <= emax.  The
+// scaling by a power of two is exact in float32 wherever the result is at
+// least 1/2 (it only moves the exponent), so one conversion rounds it to the
+// nearest integer (ties to even).  Scales above 2^127 (tiles whose values are
+// all below 2^-78) take two factors.  A non-finite v gives an arbitrary value
 // (the row is flagged and its output discarded).
-__device__ __forceinline__ int64_t quant(float v, int emax) {
-    const uint32_t b = __float_as_uint(v);
-    int e = (b >> 23) & 0xff;
-    uint32_t m = b & 0x7fffffu;
-    if (e) m |= 0x800000u; else e = 1;
-    const int s = e - emax + 26;
-    uint64_t mag;
-    if (s >= 0) {
-        mag = (uint64_t)m << min(s, 26);
-    } else {
-        const int r = -s;
-        mag = r >= 32 ? 0ull : (uint64_t)((m + ((1u << r) >> 1)) >> r);
+struct Quant {
+    float s1, s2;
+    __device__ __forceinline__ explicit Quant(int emax) {
+        const int sh = 176 - emax;                 // -78 .. 175
+        const int a = sh < 127 ? sh : 127;
+        s1 = __int_as_float((a + 127) << 23);
+        s2 = __int_as_float((sh - a + 127) << 23);  // 1 unless sh > 127
     }
-    const int64_t v64 = (int64_t)mag;
-    return (b >> 31) ? -v64 : v64;
-}
+    __device__ __forceinline__ int64_t operator()(float v) const {
+        return __float2ll_rn((v * s1) * s2);
+    }
+};
+
+__device__ __forceinline__ int64_t quant(float v, int emax) { return Quant(emax)(v); }
 
 // round(w*y / 2^(pemax - 302)) from the exact 48-bit product of the mantissas:
 // |result| < 2^50 when bexp(w) + bexp(y) <= pemax.

@@ -5,9 +5,10 @@
 //     chunk's slot, with coordinates relative to the chunk (Section 3.3).
 //  2. merge_kernel: one CTA per row merges the chunk hulls in a tree.  A node
 //     is a list of segments (chunk, first vertex, last vertex), at most one per
-//     chunk (Definition 4.3, Theorem 4.4); a merge finds the bridge by a capped
-//     walk, or by a nested bisection when the walk gives up (Section 5.2),
-//     cuts two segments and moves the right list's descriptors down.  No
+//     chunk (Definition 4.3, Theorem 4.4); a merge finds the bridge by moving
+//     its two ends to their tangent points in turn, a few steps by walking and
+//     then by bisection over the list, cuts two segments and moves the right
+//     list's descriptors down.  No
 //     vertex is ever copied between levels.  When a row's chunk hulls fit in
 //     shared memory (noisy rows keep few vertices) they are read once into it
 //     and the whole tree runs there; otherwise the tree reads them from the
@@ -23,7 +24,6 @@ namespace isodev {
 
 namespace {
 
-constexpr int kWalkCap = 64;              // steps of a walk before the bisection (Section 6)
 constexpr int kMergeThreads = 512;
 constexpr int kMergeSmem = 210 * 1024;    // shared memory of the merge kernel
 
@@ -55,7 +55,6 @@ struct LongWs {
     int64_t* slot_W;   // [M][C+1] (weighted)
     int4* seg;         // [M] segment lists (global-memory trees)
     int32_t* cnt;      // [M]
-    int32_t* pre;      // [M]
     int32_t* segOf;    // [M]
     int32_t* nextSeg;  // [M]
     int32_t* prevSeg;  // [M]
@@ -89,7 +88,6 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t n, Lon
     w.slot_W = WEIGHTED ? (int64_t*)take(sizeof(int64_t) * cap * M) : nullptr;
     w.seg = (int4*)take(sizeof(int4) * M);
     w.cnt = (int32_t*)take(sizeof(int32_t) * M);
-    w.pre = (int32_t*)take(sizeof(int32_t) * M);
     w.segOf = (int32_t*)take(sizeof(int32_t) * M);
     w.nextSeg = (int32_t*)take(sizeof(int32_t) * M);
     w.prevSeg = (int32_t*)take(sizeof(int32_t) * M);
@@ -103,11 +101,15 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t n, Lon
     return off;
 }
 
-// Nearest double of a 128-bit integer (two roundings at most).
+__device__ __forceinline__ bool fits64(i128 x) { return (i128)(int64_t)x == x; }
+
+// A double within 3 ulp of a 128-bit integer (exact below 2^53).
 __device__ __forceinline__ double i128_to_double(i128 x) {
-    const int64_t hi = (int64_t)(x >> 64);
-    const uint64_t lo = (uint64_t)x;
-    return ldexp((double)hi, 64) + (double)lo;
+    if (fits64(x)) return (double)(int64_t)x;
+    const bool neg = x < 0;
+    const unsigned __int128 u = neg ? (unsigned __int128)0 - (unsigned __int128)x : (unsigned __int128)x;
+    const double d = ldexp((double)(uint64_t)(u >> 64), 64) + (double)(uint64_t)u;
+    return neg ? -d : d;
 }
 
 // Round x / 2^d to nearest (half up); d >= 0.
@@ -183,79 +185,122 @@ chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int6
 // ---------------------------------------------------------------------------
 // 2. merge tree over segment lists (one CTA per row)
 // ---------------------------------------------------------------------------
-struct Pos { int k, r; };   // segment index in the row's list array, rank in its chunk
-
-// Where the merge tree finds a row's chunk hulls and keeps its lists: shared
-// memory (compact copies) or the workspace slots in global memory.
-template <bool WEIGHTED>
-struct MStore {
-    const int32_t* vb;       // first vertex of each chunk in P/S/W; nullptr: slot layout
-    const uint16_t* P;
-    const int64_t* S;
-    const int64_t* W;
-    const i128* offS;
-    const i128* offW;
-    const int32_t* dS;
-    const int32_t* dW;
-    int4* seg;               // (chunk in row, lo, hi, 0)
-    int32_t* cnt;
-    int32_t* pre;
-    int64_t c0;              // global index of the row's chunk 0 (slot layout)
-    int C;
-
-    __device__ __forceinline__ size_t vidx(int jc, int r) const {
-        return vb ? (size_t)vb[jc] + r : (size_t)(c0 + jc) * ((size_t)C + 1) + r;
-    }
-    __device__ __forceinline__ void vertex(int jc, int r, i128& Wv, i128& Sv) const {
-        const size_t i = vidx(jc, r);
-        Sv = offS[jc] + conv(S[i], dS[jc]);
-        if constexpr (WEIGHTED) Wv = offW[jc] + conv(W[i], dW[jc]);
-        else Wv = (i128)((int64_t)jc * C + P[i]);
-    }
-    __device__ __forceinline__ void at(Pos p, i128& Wv, i128& Sv) const {
-        vertex(seg[p.k].x, p.r, Wv, Sv);
-    }
-    // the turn o -> a -> b is strictly left.  Exact: 128-bit products when the
-    // differences fit in 64 bits, 256-bit ones otherwise.
-    static __device__ __forceinline__ bool turn(i128 Wo, i128 So, i128 Wa, i128 Sa, i128 Wb,
-                                                i128 Sb) {
-        const i128 w1 = Wa - Wo, s1 = Sa - So, w2 = Wb - Wo, s2 = Sb - So;
-        auto fits = [](i128 x) { return (i128)(int64_t)x == x; };
-        if (fits(w1) && fits(s1) && fits(w2) && fits(s2))
-            return left_turn<true>((int64_t)w1, (int64_t)s1, (int64_t)w2, (int64_t)s2);
-        return sign_det128(w1, s2, s1, w2) > 0;
-    }
-    __device__ __forceinline__ bool left(Pos o, Pos a, Pos b) const {
-        i128 Wo, So, Wa, Sa, Wb, Sb;
-        at(o, Wo, So); at(a, Wa, Sa); at(b, Wb, Sb);
-        return turn(Wo, So, Wa, Sa, Wb, Sb);
-    }
-};
+extern __shared__ __align__(16) unsigned char merge_smem[];
 
 // A merge's descriptor move: seg[dst + t] = seg[src + t] for t < len (dst < src).
 struct Move { int dst, src, len; };
 
-// Merge of the lists of the neighbouring nodes starting at j0 and j1
-// (Algorithm 1): finds the bridge, cuts the two segments it lands in, sets the
-// merged list's length, and returns the move of the right list's tail.
+// One segment of a list: a chunk's vertex range, with what its vertices need.
+struct Seg {
+    int jc, lo, hi;   // chunk (in the row), first and last vertex rank
+    int vb;           // first vertex of the chunk in the compact arrays (shared memory)
+    int dS, dW;       // chunk-to-row quantum shifts (global memory)
+    i128 oS, oW;      // chunk start in row coordinates
+};
+
+// Where the merge tree reads a row's chunk hulls and keeps its lists.  SMEM:
+// compact copies in shared memory, S and W already on the row's grid; else the
+// workspace slots in global memory, converted at every read.
+template <bool WEIGHTED, bool SMEM>
+struct MView {
+    int4* seg;               // (chunk in row, lo, hi, 0)
+    int32_t* cnt;
+    const i128* offS;
+    const i128* offW;
+    const int32_t* dS;       // global memory only
+    const int32_t* dW;
+    const int32_t* vb;       // shared memory only
+    const int64_t* S;
+    const int64_t* W;
+    const uint16_t* P;
+    int64_t c0;              // global index of the row's chunk 0
+    int C;
+
+    __device__ __forceinline__ Seg load(int k) const {
+        const int4 s = seg[k];
+        Seg g;
+        g.jc = s.x; g.lo = s.y; g.hi = s.z;
+        g.oS = offS[s.x];
+        g.oW = WEIGHTED ? offW[s.x] : (i128)0;
+        if constexpr (SMEM) { g.vb = vb[s.x]; g.dS = 0; g.dW = 0; }
+        else { g.vb = 0; g.dS = dS[s.x]; g.dW = WEIGHTED ? dW[s.x] : 0; }
+        return g;
+    }
+    __device__ __forceinline__ void at(const Seg& g, int r, i128& Wv, i128& Sv) const {
+        if constexpr (SMEM) {
+            const int i = g.vb + r;
+            Sv = g.oS + S[i];
+            if constexpr (WEIGHTED) Wv = g.oW + W[i];
+            else Wv = (i128)((int64_t)g.jc * C + P[i]);
+        } else {
+            const size_t i = (size_t)(c0 + g.jc) * ((size_t)C + 1) + r;
+            Sv = g.oS + conv(S[i], g.dS);
+            if constexpr (WEIGHTED) Wv = g.oW + conv(W[i], g.dW);
+            else Wv = (i128)((int64_t)g.jc * C + P[i]);
+        }
+    }
+};
+
+// The turn o -> a -> b is strictly left, exactly.  Unit weights: every W
+// difference is below 2^31 and every S difference below 2^82, so 128-bit
+// products are exact.  Weighted rows: a double-precision determinant decides
+// when it is clear of its rounding bound, the 256-bit products otherwise.
 template <bool WEIGHTED>
-__device__ __forceinline__ Move merge_plan(const MStore<WEIGHTED> V, int j0, int j1) {
+__device__ __forceinline__ bool row_turn(i128 Wo, i128 So, i128 Wa, i128 Sa, i128 Wb, i128 Sb) {
+    const i128 w1 = Wa - Wo, s1 = Sa - So, w2 = Wb - Wo, s2 = Sb - So;
+    if constexpr (!WEIGHTED) {
+        return (i128)(int64_t)w1 * s2 > s1 * (i128)(int64_t)w2;
+    } else {
+        if (fits64(w1) && fits64(s1) && fits64(w2) && fits64(s2))
+            return left_turn<true>((int64_t)w1, (int64_t)s1, (int64_t)w2, (int64_t)s2);
+        const double p = i128_to_double(w1) * i128_to_double(s2);
+        const double q = i128_to_double(s1) * i128_to_double(w2);
+        const double d = p - q;
+        if (fabs(d) > (fabs(p) + fabs(q)) * 0x1p-48) return d > 0.0;
+        return sign_det128(w1, s2, s1, w2) > 0;
+    }
+}
+
+// A position on a list, with its segment and coordinates.
+struct Walker {
+    int k, r;
+    Seg g;
+    i128 W, S;
+};
+
+constexpr int kLinearSteps = 12;   // walk steps before a tangent is found by bisection
+
+// Merge of the lists of the neighbouring nodes starting at j0 and j1
+// (Algorithm 1 of the paper, Lemma 4.2): if the two hulls are convex at their
+// shared point s, R is appended without s; otherwise the bridge is found by
+// alternately moving the left end to its tangent from the right end and the
+// right end to its tangent from the left end, a few steps by walking and then
+// by bisection over the list (first over segments, then inside one).  The two
+// segments the bridge lands in are cut, the merged list's length is set, and
+// the move of the right list's tail is returned.
+template <bool WEIGHTED, bool SMEM>
+__device__ __forceinline__ Move merge_plan(const MView<WEIGHTED, SMEM>& V, int j0, int j1) {
     int4* seg = V.seg;
     const int nL = V.cnt[j0], nR = V.cnt[j1];
     const int kLl = j0 + nL - 1, kR0 = j1, kRl = j1 + nR - 1;
-    const Pos sL = {kLl, seg[kLl].z};
-    const Pos sR = {kR0, seg[kR0].y};
-    auto hasPrev = [&](Pos p) { return p.r > seg[p.k].y || p.k > j0; };
-    auto prev = [&](Pos p) -> Pos {
-        return p.r > seg[p.k].y ? Pos{p.k, p.r - 1} : Pos{p.k - 1, seg[p.k - 1].z};
+    auto turn = [](i128 Wo, i128 So, i128 Wa, i128 Sa, i128 Wb, i128 Sb) {
+        return row_turn<WEIGHTED>(Wo, So, Wa, Sa, Wb, Sb);
     };
-    auto hasNext = [&](Pos p) { return p.r < seg[p.k].z || p.k < kRl; };
-    auto next = [&](Pos p) -> Pos {
-        return p.r < seg[p.k].z ? Pos{p.k, p.r + 1} : Pos{p.k + 1, seg[p.k + 1].y};
-    };
-    const Pos pa = prev(sL);
-    const Pos sb = next(sR);
-    if (V.left(pa, sL, sb)) {
+    // a: the vertex before s on L; b: the vertex after s on R
+    Walker a, b;
+    i128 Ws, Ss;
+    {
+        const Seg gl = V.load(kLl);
+        V.at(gl, gl.hi, Ws, Ss);
+        if (gl.hi > gl.lo) { a.k = kLl; a.g = gl; a.r = gl.hi - 1; }
+        else { a.k = kLl - 1; a.g = V.load(kLl - 1); a.r = a.g.hi; }
+        V.at(a.g, a.r, a.W, a.S);
+        const Seg gr = V.load(kR0);
+        if (gr.hi > gr.lo) { b.k = kR0; b.g = gr; b.r = gr.lo + 1; }
+        else { b.k = kR0 + 1; b.g = V.load(kR0 + 1); b.r = b.g.lo; }
+        V.at(b.g, b.r, b.W, b.S);
+    }
+    if (turn(a.W, a.S, Ws, Ss, b.W, b.S)) {
         // convex at s: append R without its first vertex s
         int first = kR0;
         const int lo = seg[kR0].y + 1;
@@ -265,70 +310,88 @@ __device__ __forceinline__ Move merge_plan(const MStore<WEIGHTED> V, int j0, int
         V.cnt[j0] = nL + len;
         return Move{j0 + nL, first, len};
     }
-    // walk from s's neighbours; the two current ends keep their coordinates in
-    // registers, so a step reads one new vertex
-    Pos a = pa, b = sb;
-    i128 Wa, Sa, Wb, Sb;
-    V.at(a, Wa, Sa);
-    V.at(b, Wb, Sb);
-    int steps = 0;
-    bool gave_up = false;
+    // s is not a vertex of the merged hull: the bridge joins L without s to R
+    // without s, so a stays before s and b after it.
+
+    // g(x): x strictly below the segment from its predecessor to b (true up to
+    // the tangent point of b on L', false after).  Last x in [first, a] with g.
+    auto tanL = [&](Walker& A, const Walker& B) {
+        // the last segment whose first vertex satisfies g (segment j0: always)
+        int lo = j0, hi = A.k;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            const Seg gm = V.load(mid), gp = V.load(mid - 1);
+            i128 Wm, Sm, Wp, Sp;
+            V.at(gm, gm.lo, Wm, Sm);
+            V.at(gp, gp.hi, Wp, Sp);
+            if (turn(Wp, Sp, Wm, Sm, B.W, B.S)) lo = mid; else hi = mid - 1;
+        }
+        const Seg g = lo == A.k ? A.g : V.load(lo);
+        int rlo = g.lo, rhi = lo == A.k ? A.r : g.hi;
+        while (rlo < rhi) {
+            const int mid = (rlo + rhi + 1) >> 1;
+            i128 Wm, Sm, Wp, Sp;
+            V.at(g, mid, Wm, Sm);
+            V.at(g, mid - 1, Wp, Sp);
+            if (turn(Wp, Sp, Wm, Sm, B.W, B.S)) rlo = mid; else rhi = mid - 1;
+        }
+        A.k = lo; A.g = g; A.r = rlo;
+        V.at(g, rlo, A.W, A.S);
+    };
+    // h(x): x strictly below the segment from a to its successor (false before
+    // the tangent point of a on R', true from it on).  First x in [b, last] with h.
+    auto tanR = [&](const Walker& A, Walker& B) {
+        int lo = B.k, hi = kRl;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            const Seg gm = V.load(mid), gn = V.load(mid + 1);
+            i128 Wm, Sm, Wn, Sn;
+            V.at(gm, gm.hi, Wm, Sm);
+            V.at(gn, gn.lo, Wn, Sn);
+            if (turn(A.W, A.S, Wm, Sm, Wn, Sn)) hi = mid; else lo = mid + 1;
+        }
+        const Seg g = lo == B.k ? B.g : V.load(lo);
+        int rlo = lo == B.k ? B.r : g.lo, rhi = g.hi;
+        while (rlo < rhi) {
+            const int mid = (rlo + rhi) >> 1;
+            i128 Wm, Sm, Wn, Sn;
+            V.at(g, mid, Wm, Sm);
+            V.at(g, mid + 1, Wn, Sn);
+            if (turn(A.W, A.S, Wm, Sm, Wn, Sn)) rhi = mid; else rlo = mid + 1;
+        }
+        B.k = lo; B.g = g; B.r = rlo;
+        V.at(g, rlo, B.W, B.S);
+    };
+
     for (;;) {
         bool moved = false;
-        while (hasPrev(a)) {
-            const Pos p = prev(a);
-            i128 Wp, Sp;
-            V.at(p, Wp, Sp);
-            if (V.turn(Wp, Sp, Wa, Sa, Wb, Sb)) break;
-            a = p; Wa = Wp; Sa = Sp; moved = true;
-            if (++steps > kWalkCap) { gave_up = true; break; }
+        // the left end moves to its tangent point from b
+        for (int steps = 0;; ++steps) {
+            const bool hasPrev = a.r > a.g.lo || a.k > j0;
+            if (!hasPrev) break;
+            if (steps == kLinearSteps) { tanL(a, b); break; }
+            Walker p = a;
+            if (a.r > a.g.lo) p.r = a.r - 1;
+            else { p.k = a.k - 1; p.g = V.load(p.k); p.r = p.g.hi; }
+            V.at(p.g, p.r, p.W, p.S);
+            if (turn(p.W, p.S, a.W, a.S, b.W, b.S)) break;
+            a = p;
+            moved = true;
         }
-        if (gave_up) break;
-        while (hasNext(b)) {
-            const Pos q = next(b);
-            i128 Wq, Sq;
-            V.at(q, Wq, Sq);
-            if (V.turn(Wa, Sa, Wb, Sb, Wq, Sq)) break;
-            b = q; Wb = Wq; Sb = Sq; moved = true;
-            if (++steps > kWalkCap) { gave_up = true; break; }
+        // the right end moves to its tangent point from a
+        for (int steps = 0;; ++steps) {
+            const bool hasNext = b.r < b.g.hi || b.k < kRl;
+            if (!hasNext) break;
+            if (steps == kLinearSteps) { tanR(a, b); break; }
+            Walker q = b;
+            if (b.r < b.g.hi) q.r = b.r + 1;
+            else { q.k = b.k + 1; q.g = V.load(q.k); q.r = q.g.lo; }
+            V.at(q.g, q.r, q.W, q.S);
+            if (turn(a.W, a.S, b.W, b.S, q.W, q.S)) break;
+            b = q;
+            moved = true;
         }
-        if (gave_up || !moved) break;
-    }
-    if (gave_up) {
-        // nested bisection (Section 5.2): over the candidates of L, each tested
-        // against its tangent to R, itself found by bisection over R.
-        int totL = 0, totR = 0;
-        for (int k = j0; k <= kLl; ++k) { V.pre[k] = totL; totL += seg[k].z - seg[k].y + 1; }
-        for (int k = kR0; k <= kRl; ++k) { V.pre[k] = totR; totR += seg[k].z - seg[k].y + 1; }
-        auto flatL = [&](int f) -> Pos {
-            int lo = j0, hi = kLl;
-            while (lo < hi) { int mid = (lo + hi + 1) >> 1; if (V.pre[mid] <= f) lo = mid; else hi = mid - 1; }
-            return Pos{lo, seg[lo].y + (f - V.pre[lo])};
-        };
-        auto flatR = [&](int g) -> Pos {
-            int lo = kR0, hi = kRl;
-            while (lo < hi) { int mid = (lo + hi + 1) >> 1; if (V.pre[mid] <= g) lo = mid; else hi = mid - 1; }
-            return Pos{lo, seg[lo].y + (g - V.pre[lo])};
-        };
-        // tangent point of R seen from a vertex of L: the first vertex after s
-        // whose successor lies strictly above the line through it
-        auto tangent = [&](Pos ap) -> int {
-            int lo = 1, hi = totR - 1;
-            while (lo < hi) {
-                int mid = (lo + hi) >> 1;
-                if (V.left(ap, flatR(mid), flatR(mid + 1))) hi = mid; else lo = mid + 1;
-            }
-            return lo;
-        };
-        int lo = 0, hi = totL - 2;   // candidates: every vertex of L before s
-        while (lo < hi) {
-            int mid = (lo + hi) >> 1;
-            const Pos am = flatL(mid);
-            // the next vertex of L strictly below the line from am to its tangent: go right
-            if (V.left(am, flatL(mid + 1), flatR(tangent(am)))) lo = mid + 1; else hi = mid;
-        }
-        a = flatL(lo);
-        b = flatR(tangent(a));
+        if (!moved) break;
     }
     // cut L at a and R at b; R's tail moves down behind L's kept part
     seg[a.k].z = a.r;
@@ -338,40 +401,262 @@ __device__ __forceinline__ Move merge_plan(const MStore<WEIGHTED> V, int j0, int
     return Move{a.k + 1, b.k, len};
 }
 
-// Exclusive block-wide scan of one 128-bit value per thread (blockDim.x <= 1024).
-__device__ __forceinline__ i128 block_excl_scan_i128(i128 v, i128* tmp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    i128 x = v;
+// Exclusive block-wide scan of (S, W, H) per thread (blockDim.x <= 1024, a
+// multiple of 32); also returns the block totals.
+struct Acc3 { i128 s, w; int64_t h; };
+
+__device__ __forceinline__ i128 shfl_up_i128(i128 x, int d) {
+    const uint64_t lo = __shfl_up_sync(kFull, (uint64_t)x, d);
+    const uint64_t hi = __shfl_up_sync(kFull, (uint64_t)((unsigned __int128)x >> 64), d);
+    return (i128)(((unsigned __int128)hi << 64) | lo);
+}
+
+__device__ __forceinline__ Acc3 block_excl_scan3(Acc3 v, Acc3* tmp, Acc3& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    Acc3 x = v;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint64_t lo = __shfl_up_sync(kFull, (uint64_t)x, d);
-        const uint64_t hi = __shfl_up_sync(kFull, (uint64_t)((unsigned __int128)x >> 64), d);
-        if (lane >= d) x += (i128)(((unsigned __int128)hi << 64) | lo);
+        const i128 s = shfl_up_i128(x.s, d);
+        const i128 w = shfl_up_i128(x.w, d);
+        const int64_t h = __shfl_up_sync(kFull, x.h, d);
+        if (lane >= d) { x.s += s; x.w += w; x.h += h; }
     }
     if (lane == 31) tmp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        i128 t = lane < (int)(blockDim.x >> 5) ? tmp[lane] : (i128)0;
+        Acc3 t = lane < nw ? tmp[lane] : Acc3{0, 0, 0};
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
-            const uint64_t lo = __shfl_up_sync(kFull, (uint64_t)t, d);
-            const uint64_t hi = __shfl_up_sync(kFull, (uint64_t)((unsigned __int128)t >> 64), d);
-            if (lane >= d) t += (i128)(((unsigned __int128)hi << 64) | lo);
+            const i128 s = shfl_up_i128(t.s, d);
+            const i128 w = shfl_up_i128(t.w, d);
+            const int64_t h = __shfl_up_sync(kFull, t.h, d);
+            if (lane >= d) { t.s += s; t.w += w; t.h += h; }
         }
-        tmp[lane] = t;
+        if (lane < nw) tmp[lane] = t;
     }
     __syncthreads();
-    const i128 base = warp ? tmp[warp - 1] : (i128)0;
+    Acc3 base = warp ? tmp[warp - 1] : Acc3{0, 0, 0};
+    total = tmp[nw - 1];
     __syncthreads();
-    return base + x - v;
+    base.s += x.s - v.s; base.w += x.w - v.w; base.h += x.h - v.h;
+    return base;
+}
+
+// Shared-memory layout of the merge tree of one row (SMEM variant).
+struct MergeLayout {
+    size_t oSeg, oOffS, oOffW, oCnt, oVb, oSegOf, oNext, oPrev, oS, oW, oP, bytes;
+    __device__ __host__ MergeLayout(int64_t m, int64_t H, bool weighted) {
+        size_t o = 0;
+        auto take = [&](size_t b, size_t al) { o = (o + al - 1) & ~(al - 1); const size_t r = o; o += b; return r; };
+        oSeg = take(16 * m, 16);
+        oOffS = take(16 * m, 16);
+        oOffW = weighted ? take(16 * m, 16) : 0;
+        oS = take(8 * H, 8);
+        oW = weighted ? take(8 * H, 8) : 0;
+        oCnt = take(4 * m, 4);
+        oVb = take(4 * m, 4);
+        oSegOf = take(4 * m, 4);
+        oNext = take(4 * m, 4);
+        oPrev = take(4 * m, 4);
+        oP = weighted ? 0 : take(2 * H, 2);
+        bytes = o;
+    }
+};
+
+template <bool WEIGHTED, bool SMEM>
+__device__ __forceinline__ void merge_row(int64_t m, const LongWs& ws, int64_t c0, int qs, int qw,
+                                          int64_t Htot, Acc3* s_scan) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    MergeLayout L(m, SMEM ? Htot : 0, WEIGHTED);
+    unsigned char* sm = merge_smem;
+    MView<WEIGHTED, SMEM> V;
+    V.c0 = c0;
+    V.C = C;
+    int32_t *segOf, *nextSeg, *prevSeg;
+    i128 *offS, *offW;
+    int32_t* vbw = nullptr;
+    int64_t *Sw = nullptr, *Ww = nullptr;
+    uint16_t* Pw = nullptr;
+    if constexpr (SMEM) {
+        V.seg = reinterpret_cast<int4*>(sm + L.oSeg);
+        V.cnt = reinterpret_cast<int32_t*>(sm + L.oCnt);
+        offS = reinterpret_cast<i128*>(sm + L.oOffS);
+        offW = reinterpret_cast<i128*>(sm + L.oOffW);
+        vbw = reinterpret_cast<int32_t*>(sm + L.oVb);
+        Sw = reinterpret_cast<int64_t*>(sm + L.oS);
+        Ww = reinterpret_cast<int64_t*>(sm + L.oW);
+        Pw = reinterpret_cast<uint16_t*>(sm + L.oP);
+        segOf = reinterpret_cast<int32_t*>(sm + L.oSegOf);
+        nextSeg = reinterpret_cast<int32_t*>(sm + L.oNext);
+        prevSeg = reinterpret_cast<int32_t*>(sm + L.oPrev);
+        V.dS = nullptr; V.dW = nullptr;
+        V.vb = vbw; V.S = Sw; V.W = Ww; V.P = Pw;
+    } else {
+        V.seg = ws.seg + c0;
+        V.cnt = ws.cnt + c0;
+        offS = ws.offS + c0;
+        offW = ws.offW + c0;
+        segOf = ws.segOf + c0;
+        nextSeg = ws.nextSeg + c0;
+        prevSeg = ws.prevSeg + c0;
+        V.dS = ws.dS + c0; V.dW = ws.dW + c0;
+        V.vb = nullptr; V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
+    }
+    V.offS = offS; V.offW = offW;
+
+    // ---- chunk starts in row coordinates (and vertex bases): one scan per
+    // round of blockDim chunks ----
+    Acc3 carry{0, 0, 0};
+    for (int64_t q0 = 0; q0 < m; q0 += nth) {
+        const int64_t j = q0 + tid;
+        const bool valid = j < m;
+        ChunkMeta mt{};
+        if (valid) mt = ws.meta[c0 + j];
+        const int ds = valid ? qs - mt.qs : 0;
+        const int dw = (valid && WEIGHTED) ? qw - mt.qw : 0;
+        Acc3 v;
+        v.s = valid ? (i128)conv(mt.totS, ds) : (i128)0;
+        v.w = valid ? (WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW) : (i128)0;
+        v.h = valid ? mt.h : 0;
+        Acc3 tot;
+        const Acc3 e = block_excl_scan3(v, s_scan, tot);
+        if (valid) {
+            offS[j] = carry.s + e.s;
+            if (WEIGHTED) offW[j] = carry.w + e.w;
+            if (SMEM) vbw[j] = (int32_t)(carry.h + e.h);
+            V.seg[j] = make_int4((int)j, 0, mt.h - 1, 0);
+            V.cnt[j] = 1;
+            ws.dS[c0 + j] = ds;
+            if (WEIGHTED) ws.dW[c0 + j] = dw;
+            if (SMEM) {
+                ws.offS[c0 + j] = carry.s + e.s;
+                if (WEIGHTED) ws.offW[c0 + j] = carry.w + e.w;
+            }
+        }
+        carry.s += tot.s; carry.w += tot.w; carry.h += tot.h;
+    }
+    __syncthreads();
+    if constexpr (SMEM) {
+        // every chunk hull of the row once into shared memory, on the row's
+        // grid: vertex i = tid + t*nth, its chunk by bisection over the bases
+        const int* dSg = ws.dS + c0;
+        const int* dWg = ws.dW + c0;
+        constexpr int U = 4;
+        for (int64_t i0 = tid; i0 < Htot; i0 += (int64_t)U * nth) {
+            int jc[U], r[U];
+            int64_t sv[U], wv[U];
+            uint16_t pv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t i = i0 + (int64_t)u * nth;
+                jc[u] = -1;
+                if (i < Htot) {
+                    int lo = 0, hi = (int)m - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (vbw[mid] <= i) lo = mid; else hi = mid - 1;
+                    }
+                    jc[u] = lo;
+                    r[u] = (int)(i - vbw[lo]);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (jc[u] < 0) continue;
+                const size_t g = (size_t)(c0 + jc[u]) * ((size_t)C + 1) + r[u];
+                sv[u] = ws.slot_S[g];
+                if (WEIGHTED) wv[u] = ws.slot_W[g]; else pv[u] = ws.slot_p[g];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (jc[u] < 0) continue;
+                const int64_t i = i0 + (int64_t)u * nth;
+                Sw[i] = conv(sv[u], dSg[jc[u]]);
+                if (WEIGHTED) Ww[i] = conv(wv[u], dWg[jc[u]]); else Pw[i] = pv[u];
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- the levels.  A team of T threads per merge (T = 1 when merges are
+    // many): its first thread finds the bridge and cuts the lists, then the
+    // team moves the right list's descriptors in rounds of T. ----
+    int4* seg = V.seg;
+    for (int r = 0; ((int64_t)1 << r) < m; ++r) {
+        const int64_t span = (int64_t)2 << r;
+        const int64_t merges = (m + span - 1) / span;
+        int T = 1;
+        while (T < 32 && (int64_t)(2 * T) * merges <= nth) T <<= 1;
+        const int team = tid / T, tl = tid % T, nteams = nth / T;
+        for (int64_t g0 = 0; g0 < merges; g0 += nteams) {
+            const int64_t g = g0 + team;
+            const int64_t j0 = g * span, j1 = j0 + (span >> 1);
+            const bool act = g < merges && j1 < m;
+            Move mv{0, 0, 0};
+            if (act && tl == 0) mv = merge_plan<WEIGHTED, SMEM>(V, (int)j0, (int)j1);
+            if (T == 1) {
+                for (int t = 0; t < mv.len; ++t) seg[mv.dst + t] = seg[mv.src + t];
+            } else {
+                const int lead = (tid & 31) & ~(T - 1);
+                mv.dst = __shfl_sync(kFull, mv.dst, lead);
+                mv.src = __shfl_sync(kFull, mv.src, lead);
+                mv.len = __shfl_sync(kFull, mv.len, lead);
+                int nr = (mv.len + T - 1) / T;
+                for (int d = T; d < 32; d <<= 1) nr = max(nr, __shfl_xor_sync(kFull, nr, d));
+                for (int q = 0; q < nr; ++q) {
+                    const int t = q * T + tl;
+                    int4 d = make_int4(0, 0, 0, 0);
+                    if (t < mv.len) d = seg[mv.src + t];
+                    __syncwarp();
+                    if (t < mv.len) seg[mv.dst + t] = d;
+                    __syncwarp();
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- ends: each chunk's root segment, and the root vertices around it ----
+    const int nroot = V.cnt[0];
+    for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
+    __syncthreads();
+    for (int k = tid; k < nroot; k += nth) {
+        const int cj = seg[k].x;
+        segOf[cj] = k;
+        const int cprev = k > 0 ? seg[k - 1].x : -1;
+        const int cnext = k + 1 < nroot ? seg[k + 1].x : (int)m;
+        for (int q = max(cprev, 0); q < cj; ++q) nextSeg[q] = k;   // chunks in [cprev, cj)
+        for (int q = cj + 1; q <= min(cnext, (int)m - 1); ++q) prevSeg[q] = k;
+    }
+    __syncthreads();
+    for (int64_t j = tid; j < m; j += nth) {
+        ChunkEnds ce;
+        ce.bad = 0;
+        const int sk = segOf[j];
+        if (sk >= 0) { const int4 s = seg[sk]; ce.lo = s.y; ce.hi = s.z; }
+        else { ce.lo = 1; ce.hi = 0; }
+        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
+        ce.pt0_vertex = 0;
+        if (j > 0) {
+            const int pk = prevSeg[j];
+            const Seg gp = V.load(pk);
+            V.at(gp, gp.hi, ce.prevW, ce.prevS);
+            // the previous root vertex is this chunk's first point when it closes chunk j-1
+            ce.pt0_vertex = (gp.jc == j - 1 && gp.hi == ws.meta[c0 + gp.jc].h - 1) ? 1 : 0;
+        }
+        if (j + 1 < m) {
+            const Seg gn = V.load(nextSeg[j]);
+            V.at(gn, gn.lo, ce.nextW, ce.nextS);
+        }
+        ws.ends[c0 + j] = ce;
+    }
 }
 
 template <bool WEIGHTED>
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 1)
 merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
-    constexpr int C = LongCfg<WEIGHTED>::C;
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ i128 s_tmp[32];
+    __shared__ Acc3 s_scan[32];
     __shared__ int s_qs, s_qw, s_bad;
     __shared__ unsigned long long s_H;
     const int64_t row = blockIdx.x;
@@ -415,183 +700,10 @@ merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
         }
         return;
     }
-
-    // ---- shared-memory layout (used only when the whole row fits) ----
-    size_t o = 0;
-    auto take = [&](size_t bytes, size_t al) {
-        o = (o + al - 1) & ~(al - 1);
-        const size_t r = o;
-        o += bytes;
-        return r;
-    };
-    const size_t oOffS = take(sizeof(i128) * m, 16);
-    const size_t oOffW = WEIGHTED ? take(sizeof(i128) * m, 16) : 0;
-    const size_t oSeg = take(sizeof(int4) * m, 16);
-    const size_t oS = take(sizeof(int64_t) * Htot, 8);
-    const size_t oW = WEIGHTED ? take(sizeof(int64_t) * Htot, 8) : 0;
-    const size_t oCnt = take(sizeof(int32_t) * m, 4);
-    const size_t oPre = take(sizeof(int32_t) * m, 4);
-    const size_t oVb = take(sizeof(int32_t) * m, 4);
-    const size_t oDS = take(sizeof(int32_t) * m, 4);
-    const size_t oDW = WEIGHTED ? take(sizeof(int32_t) * m, 4) : 0;
-    const size_t oSegOf = take(sizeof(int32_t) * m, 4);
-    const size_t oNext = take(sizeof(int32_t) * m, 4);
-    const size_t oPrev = take(sizeof(int32_t) * m, 4);
-    const size_t oP = take(sizeof(uint16_t) * Htot, 2);
-    const bool in_smem = o <= (size_t)kMergeSmem;
-
-    i128* offS = in_smem ? (i128*)(smem + oOffS) : ws.offS + c0;
-    i128* offW = in_smem ? (i128*)(smem + oOffW) : ws.offW + c0;
-    int32_t* dS = in_smem ? (int32_t*)(smem + oDS) : ws.dS + c0;
-    int32_t* dW = in_smem ? (int32_t*)(smem + oDW) : ws.dW + c0;
-    int4* seg = in_smem ? (int4*)(smem + oSeg) : ws.seg + c0;
-    int32_t* cnt = in_smem ? (int32_t*)(smem + oCnt) : ws.cnt + c0;
-    int32_t* pre = in_smem ? (int32_t*)(smem + oPre) : ws.pre + c0;
-    int32_t* segOf = in_smem ? (int32_t*)(smem + oSegOf) : ws.segOf + c0;
-    int32_t* nextSeg = in_smem ? (int32_t*)(smem + oNext) : ws.nextSeg + c0;
-    int32_t* prevSeg = in_smem ? (int32_t*)(smem + oPrev) : ws.prevSeg + c0;
-    int32_t* vb = in_smem ? (int32_t*)(smem + oVb) : nullptr;
-    uint16_t* P = in_smem ? (uint16_t*)(smem + oP) : ws.slot_p;
-    int64_t* S = in_smem ? (int64_t*)(smem + oS) : ws.slot_S;
-    int64_t* W = in_smem ? (int64_t*)(smem + oW) : ws.slot_W;
-
-    // ---- chunk starts in row coordinates and vertex bases: scans over chunks,
-    // each thread owning a contiguous range ----
-    const int64_t per = (m + nth - 1) / nth;
-    const int64_t jb = imin64(m, tid * per), je = imin64(m, jb + per);
-    i128 accS = 0, accW = 0, accH = 0;
-    for (int64_t j = jb; j < je; ++j) {
-        const ChunkMeta mt = ws.meta[c0 + j];
-        const int ds = qs - mt.qs, dw = WEIGHTED ? qw - mt.qw : 0;
-        dS[j] = ds;
-        if (WEIGHTED) dW[j] = dw;
-        accS += conv(mt.totS, ds);
-        accW += WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW;
-        accH += mt.h;
-    }
-    i128 bS = block_excl_scan_i128(accS, s_tmp);
-    i128 bW = block_excl_scan_i128(accW, s_tmp);
-    i128 bH = block_excl_scan_i128(accH, s_tmp);
-    for (int64_t j = jb; j < je; ++j) {
-        const ChunkMeta mt = ws.meta[c0 + j];
-        offS[j] = bS;
-        if (WEIGHTED) offW[j] = bW;
-        if (vb) vb[j] = (int32_t)bH;
-        bS += conv(mt.totS, dS[j]);
-        bW += WEIGHTED ? (i128)conv(mt.totW, dW[j]) : (i128)mt.totW;
-        bH += mt.h;
-        seg[j] = make_int4((int)j, 0, mt.h - 1, 0);
-        cnt[j] = 1;
-    }
-    __syncthreads();
-    if (in_smem) {
-        // read every chunk hull of the row once into shared memory; each thread
-        // copies a contiguous range of vertices
-        const size_t cap = (size_t)C + 1;
-        const int64_t pv = (Htot + nth - 1) / nth;
-        const int64_t i0 = imin64(Htot, tid * pv), i1 = imin64(Htot, i0 + pv);
-        if (i0 < i1) {
-            int lo = 0, hi = (int)m - 1;        // chunk holding vertex i0
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (vb[mid] <= i0) lo = mid; else hi = mid - 1;
-            }
-            int jc = lo;
-            int nextb = jc + 1 < m ? vb[jc + 1] : (int)Htot;
-#pragma unroll 4
-            for (int64_t i = i0; i < i1; ++i) {
-                while (i >= nextb) { ++jc; nextb = jc + 1 < m ? vb[jc + 1] : (int)Htot; }
-                const size_t g = (size_t)(c0 + jc) * cap + (size_t)(i - vb[jc]);
-                P[i] = ws.slot_p[g];
-                S[i] = ws.slot_S[g];
-                if (WEIGHTED) W[i] = ws.slot_W[g];
-            }
-        }
-    }
-    __syncthreads();
-
-    MStore<WEIGHTED> V;
-    V.vb = vb; V.P = P; V.S = S; V.W = W;
-    V.offS = offS; V.offW = offW; V.dS = dS; V.dW = dW;
-    V.seg = seg; V.cnt = cnt; V.pre = pre;
-    V.c0 = c0; V.C = C;
-    // Levels with many merges run one thread per merge; the others one warp per
-    // merge, whose lanes move the descriptors in coalesced rounds of 32
-    // (Section 6, "Merge levels").
-    const int warp = tid >> 5, wl = tid & 31, nw = nth >> 5;
-    for (int r = 0; ((int64_t)1 << r) < m; ++r) {
-        const int64_t span = (int64_t)2 << r;
-        const int64_t merges = (m + span - 1) / span;
-        if (merges >= nw) {
-            for (int64_t g = tid; g < merges; g += nth) {
-                const int64_t j0 = g * span, j1 = j0 + (span >> 1);
-                if (j1 < m) {
-                    const Move mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
-                    for (int t = 0; t < mv.len; ++t) seg[mv.dst + t] = seg[mv.src + t];
-                }
-            }
-        } else {
-            for (int64_t g = warp; g < merges; g += nw) {
-                const int64_t j0 = g * span, j1 = j0 + (span >> 1);
-                if (j1 >= m) continue;
-                Move mv{0, 0, 0};
-                if (wl == 0) mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
-                mv.dst = __shfl_sync(kFull, mv.dst, 0);
-                mv.src = __shfl_sync(kFull, mv.src, 0);
-                mv.len = __shfl_sync(kFull, mv.len, 0);
-                __syncwarp();
-                for (int t0 = 0; t0 < mv.len; t0 += 32) {
-                    const int t = t0 + wl;
-                    int4 d = make_int4(0, 0, 0, 0);
-                    if (t < mv.len) d = seg[mv.src + t];
-                    __syncwarp();
-                    if (t < mv.len) seg[mv.dst + t] = d;
-                    __syncwarp();
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- ends: each chunk's root segment, and the root vertices around it ----
-    const int nroot = cnt[0];
-    for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
-    __syncthreads();
-    for (int k = tid; k < nroot; k += nth) {
-        const int cj = seg[k].x;
-        segOf[cj] = k;
-        const int cprev = k > 0 ? seg[k - 1].x : -1;
-        const int cnext = k + 1 < nroot ? seg[k + 1].x : (int)m;
-        for (int q = max(cprev, 0); q < cj; ++q) nextSeg[q] = k;   // chunks in [cprev, cj)
-        for (int q = cj + 1; q <= min(cnext, (int)m - 1); ++q) prevSeg[q] = k;
-    }
-    __syncthreads();
-    for (int64_t j = tid; j < m; j += nth) {
-        ChunkEnds ce;
-        ce.bad = 0;
-        const int sk = segOf[j];
-        if (sk >= 0) { ce.lo = seg[sk].y; ce.hi = seg[sk].z; }
-        else { ce.lo = 1; ce.hi = 0; }
-        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
-        ce.pt0_vertex = 0;
-        if (j > 0) {
-            const int pk = prevSeg[j];
-            const int pc = seg[pk].x, pr = seg[pk].z;
-            V.vertex(pc, pr, ce.prevW, ce.prevS);
-            // the previous root vertex is this chunk's first point when it closes chunk j-1
-            ce.pt0_vertex = (pc == j - 1 && pr == ws.meta[c0 + pc].h - 1) ? 1 : 0;
-        }
-        if (j + 1 < m) {
-            const int nk = nextSeg[j];
-            V.vertex(seg[nk].x, seg[nk].y, ce.nextW, ce.nextS);
-        }
-        ws.ends[c0 + j] = ce;
-        if (in_smem) {
-            ws.offS[c0 + j] = offS[j];
-            ws.dS[c0 + j] = dS[j];
-            if (WEIGHTED) { ws.offW[c0 + j] = offW[j]; ws.dW[c0 + j] = dW[j]; }
-        }
-    }
+    if (MergeLayout(m, Htot, WEIGHTED).bytes <= (size_t)kMergeSmem)
+        merge_row<WEIGHTED, true>(m, ws, c0, qs, qw, Htot, s_scan);
+    else
+        merge_row<WEIGHTED, false>(m, ws, c0, qs, qw, Htot, s_scan);
 }
 
 // ---------------------------------------------------------------------------

@@ -279,6 +279,7 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     int64_t s = 0, wsum = 0;
     uint32_t cand = 0;
     {
+        const Quant qy(emax), qw(ewmax);
         int64_t up = 0, op = 1;   // previous element's value and weight
         myS[0] = 0;
         if constexpr (WEIGHTED) myW[0] = 0;
@@ -288,11 +289,11 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
             int64_t uk, ok;
             if constexpr (WEIGHTED) {
                 uk = in ? quant_prod(wv[k], yv[k], pemax) : 0;
-                ok = in ? max(quant(wv[k], ewmax), (int64_t)1) : 0;
+                ok = in ? max(qw(wv[k]), (int64_t)1) : 0;
                 // point k is locally convex: mean of element k-1 < mean of element k
                 if (k > 0 && in && (__int128)up * ok < (__int128)uk * op) cand |= 1u << k;
             } else {
-                uk = in ? quant(yv[k], emax) : 0;
+                uk = in ? qy(yv[k]) : 0;
                 ok = in ? 1 : 0;
                 if (k > 0 && in && up < uk) cand |= 1u << k;
             }
@@ -366,10 +367,18 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         int64_t* WB = SB + SM::kCapB;
         int32_t* PA = reinterpret_cast<int32_t*>(WB + SM::kCapB);
         int32_t* PB = PA + SM::kCapA;
-        int64_t* cS[2] = {SA + tile * capA, SB + tile * capB};
-        int64_t* cW[2] = {WA + tile * capA, WB + tile * capB};
-        int32_t* cP[2] = {PA + tile * capA, PB + tile * capB};
-        const int cap[2] = {capA, capB};
+        // list b (0 or 1) of this tile; selects, not arrays, so that nothing
+        // is indexed at run time
+        int64_t* const cS0 = SA + tile * capA;
+        int64_t* const cS1 = SB + tile * capB;
+        int64_t* const cW0 = WA + tile * capA;
+        int64_t* const cW1 = WB + tile * capB;
+        int32_t* const cP0 = PA + tile * capA;
+        int32_t* const cP1 = PB + tile * capB;
+        auto lS = [&](int b) { return b ? cS1 : cS0; };
+        auto lW = [&](int b) { return b ? cW1 : cW0; };
+        auto lP = [&](int b) { return b ? cP1 : cP0; };
+        auto lcap = [&](int b) { return b ? capB : capA; };
 
         // entry j of a list lives at j + j/32, and an entry that starts a group of
         // 32 (j = 32g, g > 0) is also copied just before it, where the previous
@@ -377,11 +386,14 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         auto lpos = [](int j) { return j + (j >> 5); };
         auto put = [&](int b, int j, int64_t sv, int64_t wv, int32_t pv) {
             const int x = lpos(j);
-            cS[b][x] = sv; cW[b][x] = wv;
-            if (WEIGHTED) cP[b][x] = pv;
+            int64_t* const S_ = lS(b);
+            int64_t* const W_ = lW(b);
+            int32_t* const P_ = lP(b);
+            S_[x] = sv; W_[x] = wv;
+            if (WEIGHTED) P_[x] = pv;
             if (j > 0 && (j & 31) == 0) {
-                cS[b][x - 1] = sv; cW[b][x - 1] = wv;
-                if (WEIGHTED) cP[b][x - 1] = pv;
+                S_[x - 1] = sv; W_[x - 1] = wv;
+                if (WEIGHTED) P_[x - 1] = pv;
             }
         };
         const int cnt = __popc(mask);
@@ -413,29 +425,32 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                 uint32_t gm = 0;
                 if (lane < G) {
                     const int e = min(32, n - 1 - (lane << 5));
-                    gm = list_chain<WEIGHTED>(cS[cur] + 33 * lane, cW[cur] + 33 * lane, e);
+                    gm = list_chain<WEIGHTED>(lS(cur) + 33 * lane, lW(cur) + 33 * lane, e);
                 }
                 const int gc = __popc(gm);
                 const int64_t gi = tile_scan_incl<NT>((int64_t)gc, lane, L, scan);
                 if (lane == L - 1) info[tile * 4 + 1] = (int)gi;
                 __syncthreads();
                 const int n2 = more ? info[tile * 4 + 1] + 1 : n;
-                const bool fits = !more || (lpos(n2 - 1) + 1 <= cap[cur ^ 1] && (n2 <= 33 || 2 * n2 <= n + 2));
+                const bool fits = !more || (lpos(n2 - 1) + 1 <= lcap(cur ^ 1) && (n2 <= 33 || 2 * n2 <= n + 2));
                 if (!__syncthreads_and(fits)) { fast = false; break; }
                 if (more) {
                     const int nx = cur ^ 1;
+                    const int64_t* const S_ = lS(cur);
+                    const int64_t* const W_ = lW(cur);
+                    const int32_t* const P_ = lP(cur);
                     int i = (int)(gi - gc);
                     uint32_t mm = gm;
                     while (mm) {
                         const int k = __ffs(mm) - 1;
                         mm &= mm - 1u;
                         const int src = 33 * lane + k;
-                        put(nx, i, cS[cur][src], cW[cur][src], WEIGHTED ? cP[cur][src] : 0);
+                        put(nx, i, S_[src], W_[src], WEIGHTED ? P_[src] : 0);
                         ++i;
                     }
                     if (lane == 0) {
                         const int src = lpos(n - 1);
-                        put(nx, n2 - 1, cS[cur][src], cW[cur][src], WEIGHTED ? cP[cur][src] : 0);
+                        put(nx, n2 - 1, S_[src], W_[src], WEIGHTED ? P_[src] : 0);
                     }
                     n = n2;
                     cur = nx;
@@ -446,7 +461,7 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
             // one chain over the last list; its kept entries are the tile hull
             __syncthreads();
             uint32_t fm = 0;
-            if (work && lane == 0) fm = list_chain<WEIGHTED>(cS[cur], cW[cur], n - 1);
+            if (work && lane == 0) fm = list_chain<WEIGHTED>(lS(cur), lW(cur), n - 1);
             mask = 0u;
             maska[gl] = 0u;
             __syncthreads();
@@ -454,7 +469,7 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                 while (fm) {
                     const int k = __ffs(fm) - 1;      // entries 0..31: stored at k
                     fm &= fm - 1u;
-                    const int p = WEIGHTED ? cP[cur][k] : (int)cW[cur][k];
+                    const int p = WEIGHTED ? lP(cur)[k] : (int)lW(cur)[k];
                     if (p < nt) T.mask[p >> 5] |= 1u << (p & 31);
                 }
             }
