@@ -300,43 +300,6 @@ __device__ __forceinline__ int tile_succ(const Tile& T, int p, int hi_lane, int 
     return (q << 5) + __ffs(T.mask[q]) - 1;
 }
 
-// Monotone chain over entries 0..e (e <= 32) of a list of points with
-// explicit coordinates, every entry a candidate.  Same stack discipline as
-// lane_hull; returns the mask of kept entries among 0..e-1 (entry e, the end,
-// is always kept).  Unit-weight lists carry point indices as W (|dW| < 2^14).
-template <bool WEIGHTED>
-__device__ __forceinline__ uint32_t list_chain(const int64_t* S, const int64_t* W, int e) {
-    if (e <= 0) return 0u;
-    auto turn = [](int64_t Wo, int64_t So, int64_t Wa, int64_t Sa, int64_t Wb, int64_t Sb) {
-        if constexpr (WEIGHTED) return left_turn<true>(Wa - Wo, Sa - So, Wb - Wo, Sb - So);
-        else return left_turn_w32((int)(Wa - Wo), Sa - So, (int)(Wb - Wo), Sb - So);
-    };
-    uint32_t mask = 1u;
-    int t = 0, b = -1, k = 1;
-    int64_t St = S[0], Wt = W[0], Sb = 0, Wb = 0;
-    int64_t Sk = S[1], Wk = W[1];
-    for (int it = 0; it < 2 * kPts + 2; ++it) {
-        const int k2 = k < e ? k + 1 : e;
-        const uint32_t below = b > 0 ? (mask & ((1u << b) - 1u)) : 0u;
-        const int b2 = below ? (31 - __clz(below)) : -1;
-        const int bl = b2 < 0 ? 0 : b2;
-        const int64_t Sk2 = S[k2], Wk2 = W[k2], Sb2 = S[bl], Wb2 = W[bl];
-        const bool push = (b < 0) || turn(Wb, Sb, Wt, St, Wk, Sk);
-        if (push) {
-            if (k >= e) break;
-            mask |= 1u << k;
-            b = t; Sb = St; Wb = Wt;
-            t = k; St = Sk; Wt = Wk;
-            k = k2; Sk = Sk2; Wk = Wk2;
-        } else {
-            mask &= ~(1u << t);
-            t = b; St = Sb; Wt = Wb;
-            b = b2; Sb = Sb2; Wb = Wb2;
-        }
-    }
-    return mask;
-}
-
 // Predecessor / successor vertex for merge groups that lie inside one warp:
 // `word` is the warp's non-empty-lane word, so no loop over lanes is needed
 // and the leaders of all groups of a warp run the same instructions.
@@ -406,6 +369,78 @@ __device__ __forceinline__ void tile_bridge(const Tile& T, int A0, int B0, int B
         if (!moved) break;
     }
     ra = a; rb = b;
+}
+
+// Merge of two neighbouring hulls stored as compact lists (point indices P,
+// tile-relative S, and W for weighted tiles): L = entries 0..cL-1, R = entries
+// 0..cR-1, where L's last entry and R's first are the same point s (Lemma
+// 4.2).  If the chain is convex at s, R is appended without s.  Otherwise the
+// two ends walk to their tangent points in turn, from s's neighbours; a walk
+// longer than kCompactLinear steps finishes by bisection over the list.  The
+// merged list is L[0..a] followed by R[b..cR-1]; the caller moves the tail
+// (returned as dst in L's list, src in R's list, len) and the new count is
+// stored in *cntL.
+constexpr int kCompactLinear = 8;
+
+template <bool WEIGHTED>
+__device__ __forceinline__ void compact_merge(const int64_t* SL, const int64_t* WL,
+                                              const uint16_t* PL, int* cntL, const int64_t* SR,
+                                              const int64_t* WR, const uint16_t* PR, int cR,
+                                              int& dst, int& src, int& len) {
+    const int cL = *cntL;
+    auto wl = [&](int i) -> int64_t {
+        if constexpr (WEIGHTED) return WL[i]; else return (int64_t)PL[i];
+    };
+    auto wr = [&](int j) -> int64_t {
+        if constexpr (WEIGHTED) return WR[j]; else return (int64_t)PR[j];
+    };
+    int a = cL - 2, b = 1;
+    int64_t Wa = wl(a), Sa = SL[a], Wb = wr(b), Sb = SR[b];
+    if (tile_turn<WEIGHTED>(Wa, Sa, wl(cL - 1), SL[cL - 1], Wb, Sb)) {
+        dst = cL; src = 1; len = cR - 1;
+        *cntL = cL + cR - 1;
+        return;
+    }
+    for (;;) {
+        bool moved = false;
+        // the left end: the last vertex i <= a strictly below the segment from
+        // its predecessor to b
+        for (int steps = 0; a > 0; ++steps) {
+            if (steps == kCompactLinear) {
+                int lo = 0, hi = a;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (tile_turn<WEIGHTED>(wl(mid - 1), SL[mid - 1], wl(mid), SL[mid], Wb, Sb)) lo = mid;
+                    else hi = mid - 1;
+                }
+                a = lo; Wa = wl(a); Sa = SL[a];
+                break;
+            }
+            const int64_t Wp = wl(a - 1), Sp = SL[a - 1];
+            if (tile_turn<WEIGHTED>(Wp, Sp, Wa, Sa, Wb, Sb)) break;
+            --a; Wa = Wp; Sa = Sp; moved = true;
+        }
+        // the right end: the first vertex j >= b strictly below the segment
+        // from a to its successor
+        for (int steps = 0; b < cR - 1; ++steps) {
+            if (steps == kCompactLinear) {
+                int lo = b, hi = cR - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (tile_turn<WEIGHTED>(Wa, Sa, wr(mid), SR[mid], wr(mid + 1), SR[mid + 1])) hi = mid;
+                    else lo = mid + 1;
+                }
+                b = lo; Wb = wr(b); Sb = SR[b];
+                break;
+            }
+            const int64_t Wq = wr(b + 1), Sq = SR[b + 1];
+            if (tile_turn<WEIGHTED>(Wa, Sa, Wb, Sb, Wq, Sq)) break;
+            ++b; Wb = Wq; Sb = Sq; moved = true;
+        }
+        if (!moved) break;
+    }
+    dst = a + 1; src = b; len = cR - b;
+    *cntL = a + 1 + cR - b;
 }
 
 // Clear this lane's vertex bits strictly between a and b.

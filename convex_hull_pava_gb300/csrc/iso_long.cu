@@ -141,31 +141,21 @@ chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int6
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, false, 1>(yr, wr, nt, true, !increasing, NT, smem, H);
 
-    // ranks of the vertices: exclusive scan of the lanes' vertex counts
-    int64_t* scan = reinterpret_cast<int64_t*>(smem + SM::oScan);
-    const uint32_t mask = H.T.mask[H.lane];
-    const int cntl = __popc(mask);
-    const int64_t inc = tile_scan_incl<NT>((int64_t)cntl, H.lane, NT, scan);
-    int rank = (int)(inc - cntl);
+    // the chunk hull is the compact list of lane 0's row: copy it to the slot
+    const int64_t* Sx = reinterpret_cast<const int64_t*>(smem + SM::oSx);
+    const int64_t* Wx = reinterpret_cast<const int64_t*>(smem + SM::oWx);
+    const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
+    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] : 0;
     const size_t cap = (size_t)C + 1;
     uint16_t* sp = ws.slot_p + c * cap;
     int64_t* sS = ws.slot_S + c * cap;
     int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
-    if (H.bad == 0) {
-        uint32_t mm = mask;
-        while (mm) {
-            const int k = __ffs(mm) - 1;
-            mm &= mm - 1u;
-            const int p = (H.lane << 5) + k;
-            sp[rank] = (uint16_t)p;
-            sS[rank] = tile_S<WEIGHTED>(H.T, p);
-            if constexpr (WEIGHTED) sW[rank] = tile_W<WEIGHTED>(H.T, p);
-            ++rank;
-        }
+    for (int j = threadIdx.x; j < h; j += NT) {
+        sp[j] = Px[j];
+        sS[j] = Sx[j];
+        if constexpr (WEIGHTED) sW[j] = Wx[j];
     }
-    if (threadIdx.x == NT - 1) {
-        // the chunk's end point closes the list
-        const int h = (int)inc + 1;
+    if (threadIdx.x == 0) {
         ChunkMeta mt;
         mt.h = h;
         mt.bad = (int32_t)H.bad;
@@ -173,11 +163,6 @@ chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int6
         mt.qw = H.qw;
         mt.totS = H.T.LS[NT];
         mt.totW = WEIGHTED ? H.T.LW[NT] : (int64_t)nt;
-        if (H.bad == 0) {
-            sp[h - 1] = (uint16_t)nt;
-            sS[h - 1] = mt.totS;
-            if constexpr (WEIGHTED) sW[h - 1] = mt.totW;
-        }
         ws.meta[c] = mt;
     }
 }

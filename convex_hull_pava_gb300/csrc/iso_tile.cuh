@@ -21,21 +21,17 @@ __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ g
 // tiles of L lanes.  The input staging lives inside the lane-relative sums
 // array Sx (2 x 128 B per lane fit in its 264 B per lane): it is read into
 // registers before Sx is written.  Kernels that write the fit (EMIT) keep y in
-// a separate area, which later holds each vertex's edge slope.
+// a separate area, which later holds each vertex's edge slope, and merge the
+// lane hulls by walking over vertex masks.  The others (chunks of long rows)
+// compact each lane hull into the front of its row, with the points' indices
+// in Px, and merge the compact lists.
 template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 struct TileSmem {
-    // lists of the multi-level chains: capacities (entries) for the whole CTA
-    // (entry j of a list lives at j + j/32: groups of 32 entries start 33 apart,
-    // so the lanes of a level read different banks)
-    static constexpr int kCapA = (WEIGHTED ? 4 : 5) * NT;
-    static constexpr int kCapB = kCapA / 2;
-    static constexpr int kEntB = WEIGHTED ? 20 : 16;            // S, W (and the point index)
-    static constexpr int kListBytes = (kCapA + kCapB) * kEntB;
     static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
-    // EMIT: slope per vertex at emission; before that, the lists
-    static constexpr int kYB = EMIT ? (NT * 128 > kListBytes ? NT * 128 : kListBytes) : 0;
-    static constexpr int kOwnListB = EMIT ? 0 : kListBytes;
+    static constexpr int kYB = EMIT ? NT * 128 : 0;             // slope per vertex (EMIT)
+    static constexpr int kPxB = EMIT ? 0 : ((NT * kRow * 2 + 15) / 16) * 16;   // point indices
+    static constexpr int kCntB = EMIT ? 0 : NT * 4;             // entries of each compact list
     static constexpr int kLSB = (NT + RMAX) * 8;                // lane starts, L+1 per tile
     static constexpr int kLWB = WEIGHTED ? kLSB : 0;
     static constexpr int kMaskB = NT * 4;
@@ -46,8 +42,9 @@ struct TileSmem {
     static constexpr int oSx = 0;
     static constexpr int oWx = oSx + kSxB;
     static constexpr int oY = oWx + kWxB;
-    static constexpr int oOwnList = oY + kYB;
-    static constexpr int oLS = oOwnList + kOwnListB;
+    static constexpr int oPx = oY + kYB;
+    static constexpr int oCnt = oPx + kPxB;
+    static constexpr int oLS = oCnt + kCntB;
     static constexpr int oLW = oLS + kLSB;
     static constexpr int oMask = oLW + kLWB;
     static constexpr int oSumm = oMask + kMaskB;
@@ -58,7 +55,6 @@ struct TileSmem {
     // staging: y at the start of Sx, w after it (2 x 128 B per lane < 264 B)
     static constexpr int oStageY = oSx;
     static constexpr int oStageW = oSx + NT * 128;
-    static constexpr int oList = EMIT ? oY : oOwnList;
 };
 
 // Per-tile reduction slots in the info area.
@@ -319,25 +315,10 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         }
     }
 
-    // ---- lane hulls in bit masks, on lane-relative sums; then the lane's row
-    // becomes tile-relative for the merges ----
+    // ---- lane hulls in bit masks, on lane-relative sums ----
     uint32_t mask = lane_hull<WEIGHTED>(myS, myW, cand, e);
-    {
-        const int64_t ls = LSa[tile * (L + 1) + lane];
-#pragma unroll
-        for (int k = 0; k <= 32; ++k) myS[k] += ls;
-        if constexpr (WEIGHTED) {
-            const int64_t lw = LWa[tile * (L + 1) + lane];
-#pragma unroll
-            for (int k = 0; k <= 32; ++k) myW[k] += lw;
-        }
-    }
-    maska[gl] = mask;
-    {
-        const uint32_t bal = __ballot_sync(kFull, mask != 0u);
-        if ((tid & 31) == 0) summ[tid >> 5] = bal;
-    }
-    __syncthreads();
+    const int64_t ls = LSa[tile * (L + 1) + lane];
+    const int64_t lw = WEIGHTED ? LWa[tile * (L + 1) + lane] : 0;
 
     Tile& T = H.T;
     T.Sx = Sx + tile * L * kRow;
@@ -350,166 +331,125 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     T.L = L;
     T.nt = nt;
 
-    // ---- the tile hull from the lane hulls.  When the lane hulls are small
-    // (few vertices survive, as on noisy data), their vertices are listed and
-    // hulled again by lane chains over groups of 32 entries, level after level,
-    // until one chain finishes the tile: every level discards only points that
-    // are not vertices of a subset's hull (Lemma 4.1).  Otherwise, or when a
-    // level does not halve the list, the lane hulls are merged in rounds by
-    // walking to the bridges (Section 3.2). ----
-    bool fast = false;
-    {
-        const int R = NT / L;
-        const int capA = SM::kCapA / R, capB = SM::kCapB / R;
-        int64_t* SA = reinterpret_cast<int64_t*>(smem + SM::oList);
-        int64_t* WA = SA + SM::kCapA;
-        int64_t* SB = WA + SM::kCapA;
-        int64_t* WB = SB + SM::kCapB;
-        int32_t* PA = reinterpret_cast<int32_t*>(WB + SM::kCapB);
-        int32_t* PB = PA + SM::kCapA;
-        // list b (0 or 1) of this tile; selects, not arrays, so that nothing
-        // is indexed at run time
-        int64_t* const cS0 = SA + tile * capA;
-        int64_t* const cS1 = SB + tile * capB;
-        int64_t* const cW0 = WA + tile * capA;
-        int64_t* const cW1 = WB + tile * capB;
-        int32_t* const cP0 = PA + tile * capA;
-        int32_t* const cP1 = PB + tile * capB;
-        auto lS = [&](int b) { return b ? cS1 : cS0; };
-        auto lW = [&](int b) { return b ? cW1 : cW0; };
-        auto lP = [&](int b) { return b ? cP1 : cP0; };
-        auto lcap = [&](int b) { return b ? capB : capA; };
-
-        // entry j of a list lives at j + j/32, and an entry that starts a group of
-        // 32 (j = 32g, g > 0) is also copied just before it, where the previous
-        // group reads its shared end: every group is 33 contiguous entries
-        auto lpos = [](int j) { return j + (j >> 5); };
-        auto put = [&](int b, int j, int64_t sv, int64_t wv, int32_t pv) {
-            const int x = lpos(j);
-            int64_t* const S_ = lS(b);
-            int64_t* const W_ = lW(b);
-            int32_t* const P_ = lP(b);
-            S_[x] = sv; W_[x] = wv;
-            if (WEIGHTED) P_[x] = pv;
-            if (j > 0 && (j & 31) == 0) {
-                S_[x - 1] = sv; W_[x - 1] = wv;
-                if (WEIGHTED) P_[x - 1] = pv;
-            }
-        };
-        const int cnt = __popc(mask);
-        const int64_t ci = tile_scan_incl<NT>((int64_t)cnt, lane, L, scan);
-        if (lane == L - 1) info[tile * 4 + 0] = (int)ci;
-        __syncthreads();
-        const int V1 = info[tile * 4 + 0];
-        const bool ok = !work || (lpos(V1) + 1 <= capA);
-        fast = __syncthreads_and(ok) != 0;
-        int n = work ? V1 + 1 : 0;
-        int cur = 0;
-        if (fast) {
-            if (work) {
-                uint32_t mm = mask;
-                int i = (int)(ci - cnt);
-                while (mm) {
-                    const int k = __ffs(mm) - 1;
-                    mm &= mm - 1u;
-                    put(0, i, myS[k], WEIGHTED ? myW[k] : (int64_t)((lane << 5) + k), (lane << 5) + k);
-                    ++i;
-                }
-                if (lane == L - 1)
-                    put(0, V1, LSa[tile * (L + 1) + L], WEIGHTED ? LWa[tile * (L + 1) + L] : (int64_t)nt, nt);
-            }
-            for (int level = 0; level < 12; ++level) {
-                const bool more = work && n > 33;
-                if (!__syncthreads_or(more)) break;
-                const int G = more ? (n - 1 + 31) >> 5 : 0;
-                uint32_t gm = 0;
-                if (lane < G) {
-                    const int e = min(32, n - 1 - (lane << 5));
-                    gm = list_chain<WEIGHTED>(lS(cur) + 33 * lane, lW(cur) + 33 * lane, e);
-                }
-                const int gc = __popc(gm);
-                const int64_t gi = tile_scan_incl<NT>((int64_t)gc, lane, L, scan);
-                if (lane == L - 1) info[tile * 4 + 1] = (int)gi;
-                __syncthreads();
-                const int n2 = more ? info[tile * 4 + 1] + 1 : n;
-                const bool fits = !more || (lpos(n2 - 1) + 1 <= lcap(cur ^ 1) && (n2 <= 33 || 2 * n2 <= n + 2));
-                if (!__syncthreads_and(fits)) { fast = false; break; }
-                if (more) {
-                    const int nx = cur ^ 1;
-                    const int64_t* const S_ = lS(cur);
-                    const int64_t* const W_ = lW(cur);
-                    const int32_t* const P_ = lP(cur);
-                    int i = (int)(gi - gc);
-                    uint32_t mm = gm;
-                    while (mm) {
-                        const int k = __ffs(mm) - 1;
-                        mm &= mm - 1u;
-                        const int src = 33 * lane + k;
-                        put(nx, i, S_[src], W_[src], WEIGHTED ? P_[src] : 0);
-                        ++i;
-                    }
-                    if (lane == 0) {
-                        const int src = lpos(n - 1);
-                        put(nx, n2 - 1, S_[src], W_[src], WEIGHTED ? P_[src] : 0);
-                    }
-                    n = n2;
-                    cur = nx;
-                }
-            }
+    if constexpr (EMIT) {
+        // ---- rows become tile-relative; the lane hulls are merged in rounds
+        // by walking over the vertex masks: pairs of 2^r lanes, up to the
+        // whole tile (Section 3.2).  Rounds whose groups lie inside one warp
+        // synchronise the warp only. ----
+#pragma unroll
+        for (int k = 0; k <= 32; ++k) myS[k] += ls;
+        if constexpr (WEIGHTED) {
+#pragma unroll
+            for (int k = 0; k <= 32; ++k) myW[k] += lw;
         }
-        if (fast) {
-            // one chain over the last list; its kept entries are the tile hull
-            __syncthreads();
-            uint32_t fm = 0;
-            if (work && lane == 0) fm = list_chain<WEIGHTED>(lS(cur), lW(cur), n - 1);
-            mask = 0u;
-            maska[gl] = 0u;
-            __syncthreads();
-            if (work && lane == 0) {
-                while (fm) {
-                    const int k = __ffs(fm) - 1;      // entries 0..31: stored at k
-                    fm &= fm - 1u;
-                    const int p = WEIGHTED ? lP(cur)[k] : (int)lW(cur)[k];
-                    if (p < nt) T.mask[p >> 5] |= 1u << (p & 31);
-                }
-            }
-            __syncthreads();
-            mask = maska[gl];
+        maska[gl] = mask;
+        {
             const uint32_t bal = __ballot_sync(kFull, mask != 0u);
             if ((tid & 31) == 0) summ[tid >> 5] = bal;
         }
-    }
-
-    // ---- merge rounds: pairs of 2^r lanes, up to the whole tile.  Rounds whose
-    // groups lie inside one warp synchronise the warp only. ----
-    for (int r = 0; !fast && (1 << r) < L; ++r) {
-        const int grp = lane >> (r + 1);
-        const int A0 = grp << (r + 1);
-        const int B0 = A0 + (1 << r);
-        const int Bend = A0 + (2 << r);
-        const bool active = work && ((B0 << 5) < nt);
-        // one slot per group; rounds inside a warp use slots of their own warp
-        // only, since warps are not synchronised with each other there
-        const int slot = r < 5 ? ((tid >> 5) << 4) + ((tid & 31) >> (r + 1)) : (tid >> (r + 1));
-        if (active && lane == A0) {
-            int a, b;
-            if (r < 5) tile_bridge<WEIGHTED, true>(T, A0, B0, Bend, a, b);
-            else tile_bridge<WEIGHTED, false>(T, A0, B0, Bend, a, b);
-            bridge[slot] = make_int2(a, b);
+        __syncthreads();
+        for (int r = 0; (1 << r) < L; ++r) {
+            const int grp = lane >> (r + 1);
+            const int A0 = grp << (r + 1);
+            const int B0 = A0 + (1 << r);
+            const int Bend = A0 + (2 << r);
+            const bool active = work && ((B0 << 5) < nt);
+            // one slot per group; rounds inside a warp use slots of their own warp
+            // only, since warps are not synchronised with each other there
+            const int slot = r < 5 ? ((tid >> 5) << 4) + ((tid & 31) >> (r + 1)) : (tid >> (r + 1));
+            if (active && lane == A0) {
+                int a, b;
+                if (r < 5) tile_bridge<WEIGHTED, true>(T, A0, B0, Bend, a, b);
+                else tile_bridge<WEIGHTED, false>(T, A0, B0, Bend, a, b);
+                bridge[slot] = make_int2(a, b);
+            }
+            if (r < 5) __syncwarp(); else __syncthreads();
+            if (active) {
+                const int2 ab = bridge[slot];
+                if (ab.x != ab.y) {
+                    mask = clear_between(mask, lane, ab.x, ab.y);
+                    maska[gl] = mask;
+                }
+            }
+            const uint32_t bal = __ballot_sync(kFull, mask != 0u);
+            if ((tid & 31) == 0) summ[tid >> 5] = bal;
+            if (r + 1 < 5) __syncwarp(); else __syncthreads();
         }
-        if (r < 5) __syncwarp(); else __syncthreads();
-        if (active) {
-            const int2 ab = bridge[slot];
-            if (ab.x != ab.y) {
-                mask = clear_between(mask, lane, ab.x, ab.y);
-                maska[gl] = mask;
+        __syncthreads();
+    } else {
+        // ---- each lane hull moves to the front of its row, tile-relative,
+        // with its points' indices, its end point included ----
+        uint16_t* Px = reinterpret_cast<uint16_t*>(smem + SM::oPx);
+        int* cnt = reinterpret_cast<int*>(smem + SM::oCnt);
+        uint16_t* myP = Px + gl * kRow;
+        int c = 0;
+        if (e > 0) {
+            const int64_t Se = myS[e] + ls;
+            const int64_t We = WEIGHTED ? myW[e] + lw : 0;
+            uint32_t mm = mask;
+            while (mm) {
+                const int k = __ffs(mm) - 1;
+                mm &= mm - 1u;
+                myS[c] = myS[k] + ls;
+                if constexpr (WEIGHTED) myW[c] = myW[k] + lw;
+                myP[c] = (uint16_t)((lane << 5) + k);
+                ++c;
+            }
+            myS[c] = Se;
+            if constexpr (WEIGHTED) myW[c] = We;
+            myP[c] = (uint16_t)((lane << 5) + e);
+            ++c;
+        }
+        cnt[gl] = c;
+        __syncwarp();
+        // ---- merge rounds over the compact lists: pairs of 2^r lanes.  The
+        // group's first lane finds the bridge; the group's lanes in its first
+        // warp move the right list's kept tail behind the left list's kept
+        // head (the copy the paper's segment lists avoid; here the lists are
+        // short and in shared memory). ----
+        for (int r = 0; (1 << r) < L; ++r) {
+            const bool cross = (2 << r) > 32;
+            if (cross) __syncthreads();
+            const int A0 = (lane >> (r + 1)) << (r + 1);
+            const int B0 = A0 + (1 << r);
+            const int T_ = cross ? 32 : (2 << r);
+            int dst = 0, src = 0, len = 0;
+            if (work && lane == A0 && (B0 << 5) < nt) {
+                const int base = tile * L;
+                compact_merge<WEIGHTED>(Sx + (base + A0) * kRow, Wx + (base + A0) * kRow,
+                                        Px + (base + A0) * kRow, cnt + base + A0,
+                                        Sx + (base + B0) * kRow, Wx + (base + B0) * kRow,
+                                        Px + (base + B0) * kRow, cnt[base + B0], dst, src, len);
+                dst += (base + A0) * kRow;
+                src += (base + B0) * kRow;
+            }
+            const int lead = (tid & 31) & ~(T_ - 1);
+            dst = __shfl_sync(kFull, dst, lead);
+            src = __shfl_sync(kFull, src, lead);
+            len = __shfl_sync(kFull, len, lead);
+            const int tl = (tid & 31) & (T_ - 1);
+            int nr = (len + T_ - 1) / T_;
+            for (int d = T_; d < 32; d <<= 1) nr = max(nr, __shfl_xor_sync(kFull, nr, d));
+            for (int q = 0; q < nr; ++q) {
+                const int t = q * T_ + tl;
+                int64_t sv = 0, wv = 0;
+                uint16_t pv = 0;
+                if (t < len) {
+                    sv = Sx[src + t];
+                    if constexpr (WEIGHTED) wv = Wx[src + t];
+                    pv = Px[src + t];
+                }
+                __syncwarp();
+                if (t < len) {
+                    Sx[dst + t] = sv;
+                    if constexpr (WEIGHTED) Wx[dst + t] = wv;
+                    Px[dst + t] = pv;
+                }
+                __syncwarp();
             }
         }
-        const uint32_t bal = __ballot_sync(kFull, mask != 0u);
-        if ((tid & 31) == 0) summ[tid >> 5] = bal;
-        if (r + 1 < 5) __syncwarp(); else __syncthreads();
+        __syncthreads();
     }
-    __syncthreads();
 }
 
 // Slope of the edge between tile points a < b, rounded to float32 from the
