@@ -235,7 +235,7 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
                 const int gll = tile * L + (cur_last >> 5);
                 const int64_t G = Px[gll * kRow + (cur_last & 31)];
                 const int64_t Wb = Qx[gll * kRow + (cur_last & 31)];
-                ratio = ldexpf(__ll2float_rn(G) / __ll2float_rn(Wb), qd);
+                ratio = ldexpf(i64_to_f32(G) / i64_to_f32(Wb), qd);
                 if (B.nan) ratio = __int_as_float(0x7fffffff);
             }
             stage[spos(gl, k)] = WEIGHTED ? stagew[spos(gl, k)] * ratio : ratio;

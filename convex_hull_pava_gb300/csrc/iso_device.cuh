@@ -55,6 +55,16 @@ struct Quant {
 
 __device__ __forceinline__ int64_t quant(float v, int emax) { return Quant(emax)(v); }
 
+// float32 of a 64-bit integer from two 32-bit conversions and one fused
+// multiply-add on the magnitude: exact when the value is representable, else
+// within 1.5 ulp.
+__device__ __forceinline__ float i64_to_f32(int64_t x) {
+    const uint64_t u = x < 0 ? (uint64_t)0 - (uint64_t)x : (uint64_t)x;
+    const float f = __fmaf_rn(__uint2float_rn((unsigned)(u >> 32)), 4294967296.0f,
+                              __uint2float_rn((unsigned)u));
+    return x < 0 ? -f : f;
+}
+
 // round(w*y / 2^(pemax - 302)) from the exact 48-bit product of the mantissas:
 // |result| < 2^50 when bexp(w) + bexp(y) <= pemax.
 __device__ __forceinline__ int64_t quant_prod(float w, float y, int pemax) {
@@ -95,6 +105,15 @@ __device__ __forceinline__ bool left_turn(int64_t w1, int64_t s1, int64_t w2, in
     } else {
         return w1 * s2 > s1 * w2;
     }
+}
+
+// Exact sign test w1*s2 - w2*s1 > 0 for |w| < 2^30 (point counts of a tile):
+// 32 x 64-bit products split in two halves, without 128-bit arithmetic.
+__device__ __forceinline__ bool left_turn_w32(int w1, int64_t s1, int w2, int64_t s2) {
+    const int64_t h = (int64_t)w1 * (int32_t)(s2 >> 32) - (int64_t)w2 * (int32_t)(s1 >> 32);
+    const int64_t l = (int64_t)w1 * (int64_t)(uint32_t)s2 - (int64_t)w2 * (int64_t)(uint32_t)s1;
+    const int64_t H = h + (l >> 32);
+    return H > 0 || (H == 0 && (uint32_t)l != 0u);
 }
 
 // Exact sign of a*b - c*d for signed 128-bit operands (products up to 256 bits),
@@ -225,15 +244,6 @@ __device__ __forceinline__ int64_t tile_W(const Tile& T, int p) {
     } else {
         return (int64_t)p;
     }
-}
-
-// Exact sign test w1*s2 - w2*s1 > 0 for |w| < 2^30 (point counts of a tile):
-// 32 x 64-bit products split in two halves, without 128-bit arithmetic.
-__device__ __forceinline__ bool left_turn_w32(int w1, int64_t s1, int w2, int64_t s2) {
-    const int64_t h = (int64_t)w1 * (int32_t)(s2 >> 32) - (int64_t)w2 * (int32_t)(s1 >> 32);
-    const int64_t l = (int64_t)w1 * (int64_t)(uint32_t)s2 - (int64_t)w2 * (int64_t)(uint32_t)s1;
-    const int64_t H = h + (l >> 32);
-    return H > 0 || (H == 0 && (uint32_t)l != 0u);
 }
 
 // Turn test on tile points, with the differences taken from o.

@@ -770,7 +770,7 @@ expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict
                 // both ends in the chunk: chunk-relative coordinates, chunk quanta
                 const int64_t dS_ = sS[r + 1] - sS[r];
                 const int64_t dW_ = WEIGHTED ? sW[r + 1] - sW[r] : (int64_t)(sp[r + 1] - p);
-                sl = ldexpf(__ll2float_rn(dS_) / __ll2float_rn(dW_), mt.qs - (WEIGHTED ? mt.qw : 0));
+                sl = ldexpf(i64_to_f32(dS_) / i64_to_f32(dW_), mt.qs - (WEIGHTED ? mt.qw : 0));
             } else {
                 i128 Wa, Sa;
                 vrow(r, Wa, Sa);

@@ -458,7 +458,7 @@ template <bool WEIGHTED>
 __device__ __forceinline__ float tile_slope(const Tile& T, int a, int b, int qs, int qw) {
     const int64_t dS = tile_S<WEIGHTED>(T, b) - tile_S<WEIGHTED>(T, a);
     const int64_t dW = tile_W<WEIGHTED>(T, b) - tile_W<WEIGHTED>(T, a);
-    const float f = __ll2float_rn(dS) / __ll2float_rn(dW);
+    const float f = i64_to_f32(dS) / i64_to_f32(dW);
     return ldexpf(f, qs - qw);
 }
 
