@@ -8,7 +8,7 @@ before every timed step, outside the timed interval; each step is timed with
 CUDA events on the launching stream.
 
 Prints one JSON line.  `--impl reference` times the fp64 CPU oracle instead
-(the reference arm of this build), on the host cores.
+(the reference arm), on the host cores.
 """
 from __future__ import annotations
 
