@@ -267,7 +267,8 @@ def run_gpu(args):
         # write the fit
         "expand": W.elements * 4,
         # descriptor lists only; no per-element traffic
-        "merge": 0,
+        "merge_groups": 0,
+        "merge_top": 0,
     }
     ab = alg_bytes.get(dom, W.elements * (12 if W.weighted else 8))
     achieved = ab / (kavg[dom] * 1e-3) / 1e9

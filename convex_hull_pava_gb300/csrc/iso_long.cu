@@ -3,18 +3,18 @@
 //  1. chunk_hull_kernel: one CTA per chunk builds the chunk's hull (lanes ->
 //     warps -> CTA, Sections 3.1-3.2) and writes its vertices once into the
 //     chunk's slot, with coordinates relative to the chunk (Section 3.3).
-//  2. merge_kernel: one CTA per row merges the chunk hulls in a tree.  A node
-//     is a list of segments (chunk, first vertex, last vertex), at most one per
-//     chunk (Definition 4.3, Theorem 4.4); a merge finds the bridge by moving
-//     its two ends to their tangent points in turn, a few steps by walking and
-//     then by bisection over the list, cuts two segments and moves the right
-//     list's descriptors down.  No
-//     vertex is ever copied between levels.  When a row's chunk hulls fit in
-//     shared memory (noisy rows keep few vertices) they are read once into it
-//     and the whole tree runs there; otherwise the tree reads them from the
-//     slots in global memory.  The kernel then finds each chunk's range in the
-//     root list and the root vertices before and after it (Section 3.4,
-//     Corollary 4.5).
+//  2. merge_groups_kernel and merge_top_kernel: the chunk hulls are merged in
+//     a tree.  A node is a list of segments (chunk, first vertex, last vertex),
+//     at most one per chunk (Definition 4.3, Theorem 4.4); a merge finds the
+//     bridge by moving its two ends to their tangent points in turn, a few
+//     steps by walking and then by bisection over the list, cuts two segments
+//     and moves the right list's descriptors down.  No vertex is ever copied
+//     between levels.  The first levels run in one CTA per group of 32 chunks,
+//     all groups at once; the rest in one CTA per row.  A CTA reads the hull
+//     vertices it needs into shared memory when they fit (noisy rows keep few
+//     vertices), else it reads them from the slots in global memory.  The top
+//     kernel then finds each chunk's range in the root list and the root
+//     vertices before and after it (Section 3.4, Corollary 4.5).
 //  3. expand_kernel: one CTA per chunk writes every element's slope and its
 //     block-start byte (Section 3.4).
 #include "iso_internal.h"
@@ -427,157 +427,89 @@ __device__ __forceinline__ Acc3 block_excl_scan3(Acc3 v, Acc3* tmp, Acc3& total)
     return base;
 }
 
-// Shared-memory layout of the merge tree of one row (SMEM variant).
+// The merge tree runs in two kernels.  merge_groups_kernel: one CTA per group
+// of kGroup consecutive chunks merges them (the tree's first levels), many
+// groups at a time across the GPU.  merge_top_kernel: one CTA per row merges
+// the groups' lists (the remaining levels) and finds each chunk's root segment.
+// Each CTA reads its chunk hulls into shared memory when they fit (noisy rows
+// keep few vertices; the top kernel reads only the vertices still inside a
+// segment), else it reads them from the slots in global memory.
+constexpr int kGroup = 32;
+constexpr int kGroupThreads = 256;
+constexpr int kGroupSmem = 48 * 1024;
+
+// Shared-memory layout for mc chunks and H vertices.
 struct MergeLayout {
     size_t oSeg, oOffS, oOffW, oCnt, oVb, oSegOf, oNext, oPrev, oS, oW, oP, bytes;
-    __device__ __host__ MergeLayout(int64_t m, int64_t H, bool weighted) {
+    __device__ __host__ MergeLayout(int64_t mc, int64_t H, bool weighted, bool ends) {
         size_t o = 0;
         auto take = [&](size_t b, size_t al) { o = (o + al - 1) & ~(al - 1); const size_t r = o; o += b; return r; };
-        oSeg = take(16 * m, 16);
-        oOffS = take(16 * m, 16);
-        oOffW = weighted ? take(16 * m, 16) : 0;
+        oSeg = take(16 * mc, 16);
+        oOffS = take(16 * mc, 16);
+        oOffW = weighted ? take(16 * mc, 16) : 0;
         oS = take(8 * H, 8);
         oW = weighted ? take(8 * H, 8) : 0;
-        oCnt = take(4 * m, 4);
-        oVb = take(4 * m, 4);
-        oSegOf = take(4 * m, 4);
-        oNext = take(4 * m, 4);
-        oPrev = take(4 * m, 4);
+        oCnt = take(4 * mc, 4);
+        oVb = take(4 * mc, 4);
+        oSegOf = ends ? take(4 * mc, 4) : 0;
+        oNext = ends ? take(4 * mc, 4) : 0;
+        oPrev = ends ? take(4 * mc, 4) : 0;
         oP = weighted ? 0 : take(2 * H, 2);
         bytes = o;
     }
 };
 
-template <bool WEIGHTED, bool SMEM>
-__device__ __forceinline__ void merge_row(int64_t m, const LongWs& ws, int64_t c0, int qs, int qw,
-                                          int64_t Htot, Acc3* s_scan) {
-    constexpr int C = LongCfg<WEIGHTED>::C;
-    const int tid = threadIdx.x, nth = blockDim.x;
-    MergeLayout L(m, SMEM ? Htot : 0, WEIGHTED);
-    unsigned char* sm = merge_smem;
-    MView<WEIGHTED, SMEM> V;
-    V.c0 = c0;
-    V.C = C;
-    int32_t *segOf, *nextSeg, *prevSeg;
-    i128 *offS, *offW;
-    int32_t* vbw = nullptr;
-    int64_t *Sw = nullptr, *Ww = nullptr;
-    uint16_t* Pw = nullptr;
-    if constexpr (SMEM) {
-        V.seg = reinterpret_cast<int4*>(sm + L.oSeg);
-        V.cnt = reinterpret_cast<int32_t*>(sm + L.oCnt);
-        offS = reinterpret_cast<i128*>(sm + L.oOffS);
-        offW = reinterpret_cast<i128*>(sm + L.oOffW);
-        vbw = reinterpret_cast<int32_t*>(sm + L.oVb);
-        Sw = reinterpret_cast<int64_t*>(sm + L.oS);
-        Ww = reinterpret_cast<int64_t*>(sm + L.oW);
-        Pw = reinterpret_cast<uint16_t*>(sm + L.oP);
-        segOf = reinterpret_cast<int32_t*>(sm + L.oSegOf);
-        nextSeg = reinterpret_cast<int32_t*>(sm + L.oNext);
-        prevSeg = reinterpret_cast<int32_t*>(sm + L.oPrev);
-        V.dS = nullptr; V.dW = nullptr;
-        V.vb = vbw; V.S = Sw; V.W = Ww; V.P = Pw;
-    } else {
-        V.seg = ws.seg + c0;
-        V.cnt = ws.cnt + c0;
-        offS = ws.offS + c0;
-        offW = ws.offW + c0;
-        segOf = ws.segOf + c0;
-        nextSeg = ws.nextSeg + c0;
-        prevSeg = ws.prevSeg + c0;
-        V.dS = ws.dS + c0; V.dW = ws.dW + c0;
-        V.vb = nullptr; V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
-    }
-    V.offS = offS; V.offW = offW;
+// Row quanta and status: the largest chunk quanta and the or of the chunks'
+// status bits, over the m chunks of the row (every thread of the CTA calls it).
+struct RowQ { int qs, qw, bad; };
 
-    // ---- chunk starts in row coordinates (and vertex bases): one scan per
-    // round of blockDim chunks ----
-    Acc3 carry{0, 0, 0};
-    for (int64_t q0 = 0; q0 < m; q0 += nth) {
-        const int64_t j = q0 + tid;
-        const bool valid = j < m;
-        ChunkMeta mt{};
-        if (valid) mt = ws.meta[c0 + j];
-        const int ds = valid ? qs - mt.qs : 0;
-        const int dw = (valid && WEIGHTED) ? qw - mt.qw : 0;
-        Acc3 v;
-        v.s = valid ? (i128)conv(mt.totS, ds) : (i128)0;
-        v.w = valid ? (WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW) : (i128)0;
-        v.h = valid ? mt.h : 0;
-        Acc3 tot;
-        const Acc3 e = block_excl_scan3(v, s_scan, tot);
-        if (valid) {
-            offS[j] = carry.s + e.s;
-            if (WEIGHTED) offW[j] = carry.w + e.w;
-            if (SMEM) vbw[j] = (int32_t)(carry.h + e.h);
-            V.seg[j] = make_int4((int)j, 0, mt.h - 1, 0);
-            V.cnt[j] = 1;
-            ws.dS[c0 + j] = ds;
-            if (WEIGHTED) ws.dW[c0 + j] = dw;
-            if (SMEM) {
-                ws.offS[c0 + j] = carry.s + e.s;
-                if (WEIGHTED) ws.offW[c0 + j] = carry.w + e.w;
-            }
-        }
-        carry.s += tot.s; carry.w += tot.w; carry.h += tot.h;
+__device__ __forceinline__ RowQ row_quanta(int64_t m, const LongWs& ws, int64_t c0, int* red) {
+    const int tid = threadIdx.x, nth = blockDim.x;
+    if (tid == 0) { red[0] = -100000; red[1] = -100000; red[2] = 0; }
+    __syncthreads();
+    int qs = -100000, qw = -100000, bad = 0;
+    for (int64_t j = tid; j < m; j += nth) {
+        const ChunkMeta mt = ws.meta[c0 + j];
+        qs = max(qs, mt.qs); qw = max(qw, mt.qw); bad |= mt.bad;
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+        qs = max(qs, __shfl_xor_sync(kFull, qs, d));
+        qw = max(qw, __shfl_xor_sync(kFull, qw, d));
+        bad |= __shfl_xor_sync(kFull, bad, d);
+    }
+    if ((tid & 31) == 0) {
+        atomicMax(&red[0], qs);
+        atomicMax(&red[1], qw);
+        if (bad) atomicOr(&red[2], bad);
     }
     __syncthreads();
-    if constexpr (SMEM) {
-        // every chunk hull of the row once into shared memory, on the row's
-        // grid: vertex i = tid + t*nth, its chunk by bisection over the bases
-        const int* dSg = ws.dS + c0;
-        const int* dWg = ws.dW + c0;
-        constexpr int U = 4;
-        for (int64_t i0 = tid; i0 < Htot; i0 += (int64_t)U * nth) {
-            int jc[U], r[U];
-            int64_t sv[U], wv[U];
-            uint16_t pv[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t i = i0 + (int64_t)u * nth;
-                jc[u] = -1;
-                if (i < Htot) {
-                    int lo = 0, hi = (int)m - 1;
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (vbw[mid] <= i) lo = mid; else hi = mid - 1;
-                    }
-                    jc[u] = lo;
-                    r[u] = (int)(i - vbw[lo]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (jc[u] < 0) continue;
-                const size_t g = (size_t)(c0 + jc[u]) * ((size_t)C + 1) + r[u];
-                sv[u] = ws.slot_S[g];
-                if (WEIGHTED) wv[u] = ws.slot_W[g]; else pv[u] = ws.slot_p[g];
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (jc[u] < 0) continue;
-                const int64_t i = i0 + (int64_t)u * nth;
-                Sw[i] = conv(sv[u], dSg[jc[u]]);
-                if (WEIGHTED) Ww[i] = conv(wv[u], dWg[jc[u]]); else Pw[i] = pv[u];
-            }
-        }
-        __syncthreads();
-    }
+    const RowQ r{red[0], red[1], red[2]};
+    __syncthreads();
+    return r;
+}
 
-    // ---- the levels.  A team of T threads per merge (T = 1 when merges are
-    // many): its first thread finds the bridge and cuts the lists, then the
-    // team moves the right list's descriptors in rounds of T. ----
+// The levels of the tree whose nodes start at multiples of `span0` chunks,
+// inside chunks [jb, je): merges of nodes (j0, j0 + span) for span = span0,
+// 2 span0, ... while a node of span chunks is smaller than the range.  A team
+// of T threads per merge (T = 1 when merges are many): its first thread finds
+// the bridge and cuts the lists, then the team moves the right list's
+// descriptors in rounds of T.
+template <bool WEIGHTED, bool SMEM>
+__device__ __forceinline__ void merge_levels(const MView<WEIGHTED, SMEM>& V, int64_t jb, int64_t je,
+                                             int64_t span0) {
+    const int tid = threadIdx.x, nth = blockDim.x;
     int4* seg = V.seg;
-    for (int r = 0; ((int64_t)1 << r) < m; ++r) {
-        const int64_t span = (int64_t)2 << r;
-        const int64_t merges = (m + span - 1) / span;
+    for (int64_t half = span0; half < je - jb; half <<= 1) {
+        const int64_t span = half << 1;
+        const int64_t merges = (je - jb + span - 1) / span;
         int T = 1;
         while (T < 32 && (int64_t)(2 * T) * merges <= nth) T <<= 1;
         const int team = tid / T, tl = tid % T, nteams = nth / T;
         for (int64_t g0 = 0; g0 < merges; g0 += nteams) {
             const int64_t g = g0 + team;
-            const int64_t j0 = g * span, j1 = j0 + (span >> 1);
-            const bool act = g < merges && j1 < m;
+            const int64_t j0 = jb + g * span, j1 = j0 + half;
+            const bool act = g < merges && j1 < je;
             Move mv{0, 0, 0};
             if (act && tl == 0) mv = merge_plan<WEIGHTED, SMEM>(V, (int)j0, (int)j1);
             if (T == 1) {
@@ -601,8 +533,255 @@ __device__ __forceinline__ void merge_row(int64_t m, const LongWs& ws, int64_t c
         }
         __syncthreads();
     }
+}
+
+// Vertices (chunk jc, ranks lo..lo+len-1) into shared memory at base, on the
+// row's grid, for the chunks of [jb, je) with len > 0: vertex i of the range
+// total is found by bisection over the bases; four vertices per thread in
+// flight.
+template <bool WEIGHTED>
+__device__ __forceinline__ void copy_vertices(const LongWs& ws, int64_t c0, int jb, int je,
+                                              const int32_t* base, const int32_t* lo0, int64_t H,
+                                              int64_t* Sw, int64_t* Ww, uint16_t* Pw) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    constexpr int U = 4;
+    for (int64_t i0 = tid; i0 < H; i0 += (int64_t)U * nth) {
+        int jc[U], r[U];
+        int64_t sv[U], wv[U];
+        uint16_t pv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + (int64_t)u * nth;
+            jc[u] = -1;
+            if (i < H) {
+                int lo = jb, hi = je - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (base[mid] <= i) lo = mid; else hi = mid - 1;
+                }
+                jc[u] = lo;
+                r[u] = (int)(i - base[lo]) + lo0[lo];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (jc[u] < 0) continue;
+            const size_t g = (size_t)(c0 + jc[u]) * ((size_t)C + 1) + r[u];
+            sv[u] = ws.slot_S[g];
+            if (WEIGHTED) wv[u] = ws.slot_W[g]; else pv[u] = ws.slot_p[g];
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (jc[u] < 0) continue;
+            const int64_t i = i0 + (int64_t)u * nth;
+            Sw[i] = conv(sv[u], ws.dS[c0 + jc[u]]);
+            if (WEIGHTED) Ww[i] = conv(wv[u], ws.dW[c0 + jc[u]]); else Pw[i] = pv[u];
+        }
+    }
+}
+
+template <bool WEIGHTED, bool SMEM>
+__device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t c0, int jb, int je,
+                                            const i128* gS, const i128* gW, const int32_t* gH,
+                                            int64_t Hg) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int tid = threadIdx.x;
+    const int mg = je - jb;
+    MergeLayout L(mg, SMEM ? Hg : 0, WEIGHTED, false);
+    unsigned char* sm = merge_smem;
+    MView<WEIGHTED, SMEM> V;
+    V.c0 = c0;
+    V.C = C;
+    if constexpr (SMEM) {
+        // arrays of the group's chunks, indexed by the chunk's index in the row
+        V.seg = reinterpret_cast<int4*>(sm + L.oSeg) - jb;
+        V.cnt = reinterpret_cast<int32_t*>(sm + L.oCnt) - jb;
+        V.offS = reinterpret_cast<i128*>(sm + L.oOffS) - jb;
+        V.offW = reinterpret_cast<i128*>(sm + L.oOffW) - jb;
+        V.vb = reinterpret_cast<int32_t*>(sm + L.oVb) - jb;
+        V.S = reinterpret_cast<int64_t*>(sm + L.oS);
+        V.W = reinterpret_cast<int64_t*>(sm + L.oW);
+        V.P = reinterpret_cast<uint16_t*>(sm + L.oP);
+        V.dS = nullptr; V.dW = nullptr;
+    } else {
+        V.seg = ws.seg + c0;
+        V.cnt = ws.cnt + c0;
+        V.offS = ws.offS + c0;
+        V.offW = ws.offW + c0;
+        V.vb = nullptr;
+        V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
+        V.dS = ws.dS + c0; V.dW = ws.dW + c0;
+    }
+    if (tid < mg) {
+        const int j = jb + tid;
+        const ChunkMeta mt = ws.meta[c0 + j];
+        const_cast<i128*>(V.offS)[j] = gS[tid];
+        if (WEIGHTED) const_cast<i128*>(V.offW)[j] = gW[tid];
+        if (SMEM) const_cast<int32_t*>(V.vb)[j] = gH[tid];
+        V.seg[j] = make_int4(j, 0, mt.h - 1, 0);
+        V.cnt[j] = 1;
+    }
+    __syncthreads();
+    if constexpr (SMEM) {
+        __shared__ int32_t s_lo0[kGroup];
+        if (tid < mg) s_lo0[tid] = 0;
+        __syncthreads();
+        copy_vertices<WEIGHTED>(ws, c0, jb, je, V.vb, s_lo0 - jb, Hg,
+                                const_cast<int64_t*>(V.S), const_cast<int64_t*>(V.W),
+                                const_cast<uint16_t*>(V.P));
+        __syncthreads();
+    }
+    merge_levels<WEIGHTED, SMEM>(V, jb, je, 1);
+    if constexpr (SMEM) {
+        // the group's list back to the workspace
+        const int n = V.cnt[jb];
+        for (int k = tid; k < n; k += blockDim.x) ws.seg[c0 + jb + k] = V.seg[jb + k];
+        if (tid == 0) ws.cnt[c0 + jb] = n;
+    }
+}
+
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(kGroupThreads)
+merge_groups_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
+    __shared__ int s_red[3];
+    __shared__ i128 s_part[2][kGroupThreads / 32];
+    __shared__ i128 s_gS[kGroup], s_gW[kGroup];
+    __shared__ int32_t s_gH[kGroup];
+    __shared__ long long s_Hg;
+    const int64_t row = blockIdx.x;
+    const int64_t c0 = row * m;
+    const int jb = blockIdx.y * kGroup;
+    const int je = (int)imin64(jb + kGroup, m);
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const RowQ q = row_quanta(m, ws, c0, s_red);
+    if (blockIdx.y == 0 && tid == 0) {
+        ws.rowq[row * 4 + 0] = q.qs; ws.rowq[row * 4 + 1] = q.qw; ws.rowq[row * 4 + 2] = q.bad;
+        if (row_status) row_status[row] = (uint32_t)q.bad;
+    }
+    if (q.bad) {
+        for (int j = jb + tid; j < je; j += nth) {
+            ChunkEnds ce{};
+            ce.lo = 1; ce.hi = 0; ce.bad = q.bad;
+            ws.ends[c0 + j] = ce;
+        }
+        return;
+    }
+    // the group's start in row coordinates: the converted totals of the chunks before it
+    {
+        i128 aS = 0, aW = 0;
+        for (int64_t j = tid; j < jb; j += nth) {
+            const ChunkMeta mt = ws.meta[c0 + j];
+            aS += conv(mt.totS, q.qs - mt.qs);
+            aW += WEIGHTED ? (i128)conv(mt.totW, q.qw - mt.qw) : (i128)mt.totW;
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            aS += (i128)(((unsigned __int128)__shfl_xor_sync(kFull, (uint64_t)((unsigned __int128)aS >> 64), d) << 64) |
+                         __shfl_xor_sync(kFull, (uint64_t)aS, d));
+            aW += (i128)(((unsigned __int128)__shfl_xor_sync(kFull, (uint64_t)((unsigned __int128)aW >> 64), d) << 64) |
+                         __shfl_xor_sync(kFull, (uint64_t)aW, d));
+        }
+        if ((tid & 31) == 0) { s_part[0][tid >> 5] = aS; s_part[1][tid >> 5] = aW; }
+        __syncthreads();
+        if (tid < 32) {
+            // the group's chunks: starts, shifts and vertex bases by a warp scan
+            i128 bS = 0, bW = 0;
+            for (int w = 0; w < nth / 32; ++w) { bS += s_part[0][w]; bW += s_part[1][w]; }
+            const int j = jb + tid;
+            const bool valid = j < je;
+            ChunkMeta mt{};
+            if (valid) mt = ws.meta[c0 + j];
+            const int ds = valid ? q.qs - mt.qs : 0;
+            const int dw = (valid && WEIGHTED) ? q.qw - mt.qw : 0;
+            const i128 vS = valid ? (i128)conv(mt.totS, ds) : (i128)0;
+            const i128 vW = valid ? (WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW) : (i128)0;
+            int vH = valid ? mt.h : 0;
+            i128 xS = vS, xW = vW;
+            int xH = vH;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const i128 oS = shfl_up_i128(xS, d), oW = shfl_up_i128(xW, d);
+                const int oH = __shfl_up_sync(kFull, xH, d);
+                if (tid >= d) { xS += oS; xW += oW; xH += oH; }
+            }
+            if (valid) {
+                s_gS[tid] = bS + xS - vS;
+                s_gW[tid] = bW + xW - vW;
+                s_gH[tid] = xH - vH;
+                ws.offS[c0 + j] = bS + xS - vS;
+                if (WEIGHTED) ws.offW[c0 + j] = bW + xW - vW;
+                ws.dS[c0 + j] = ds;
+                if (WEIGHTED) ws.dW[c0 + j] = dw;
+            }
+            if (tid == 31) s_Hg = xH;
+        }
+        __syncthreads();
+    }
+    const int64_t Hg = s_Hg;
+    if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
+        merge_group<WEIGHTED, true>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
+    else
+        merge_group<WEIGHTED, false>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
+}
+
+template <bool WEIGHTED, bool SMEM>
+__device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c0, int64_t Hs,
+                                          int32_t* s_len, int32_t* s_lo) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    MergeLayout L(m, SMEM ? Hs : 0, WEIGHTED, true);
+    unsigned char* sm = merge_smem;
+    MView<WEIGHTED, SMEM> V;
+    V.c0 = c0;
+    V.C = C;
+    int32_t *segOf, *nextSeg, *prevSeg;
+    if constexpr (SMEM) {
+        V.seg = reinterpret_cast<int4*>(sm + L.oSeg);
+        V.cnt = reinterpret_cast<int32_t*>(sm + L.oCnt);
+        V.offS = reinterpret_cast<i128*>(sm + L.oOffS);
+        V.offW = reinterpret_cast<i128*>(sm + L.oOffW);
+        V.vb = reinterpret_cast<int32_t*>(sm + L.oVb);
+        V.S = reinterpret_cast<int64_t*>(sm + L.oS);
+        V.W = reinterpret_cast<int64_t*>(sm + L.oW);
+        V.P = reinterpret_cast<uint16_t*>(sm + L.oP);
+        V.dS = nullptr; V.dW = nullptr;
+        segOf = reinterpret_cast<int32_t*>(sm + L.oSegOf);
+        nextSeg = reinterpret_cast<int32_t*>(sm + L.oNext);
+        prevSeg = reinterpret_cast<int32_t*>(sm + L.oPrev);
+        // chunk starts, and the lists of the groups
+        for (int64_t j = tid; j < m; j += nth) {
+            const_cast<i128*>(V.offS)[j] = ws.offS[c0 + j];
+            if (WEIGHTED) const_cast<i128*>(V.offW)[j] = ws.offW[c0 + j];
+            V.seg[j] = ws.seg[c0 + j];
+            V.cnt[j] = ws.cnt[c0 + j];
+        }
+        // vertex bases (s_len: the surviving segments' lengths scanned in chunk
+        // order) and first ranks (s_lo), staged in the ends scratch; vertex
+        // (jc, r) then lives at vb[jc] + r
+        for (int64_t j = tid; j < m; j += nth) { segOf[j] = s_len[j]; prevSeg[j] = s_lo[j]; }
+        __syncthreads();
+        copy_vertices<WEIGHTED>(ws, c0, 0, (int)m, segOf, prevSeg, Hs, const_cast<int64_t*>(V.S),
+                                const_cast<int64_t*>(V.W), const_cast<uint16_t*>(V.P));
+        for (int64_t j = tid; j < m; j += nth)
+            const_cast<int32_t*>(V.vb)[j] = segOf[j] - prevSeg[j];
+        __syncthreads();
+    } else {
+        V.seg = ws.seg + c0;
+        V.cnt = ws.cnt + c0;
+        V.offS = ws.offS + c0;
+        V.offW = ws.offW + c0;
+        V.vb = nullptr;
+        V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
+        V.dS = ws.dS + c0; V.dW = ws.dW + c0;
+        segOf = ws.segOf + c0;
+        nextSeg = ws.nextSeg + c0;
+        prevSeg = ws.prevSeg + c0;
+    }
+    merge_levels<WEIGHTED, SMEM>(V, 0, m, kGroup);
 
     // ---- ends: each chunk's root segment, and the root vertices around it ----
+    const int4* seg = V.seg;
     const int nroot = V.cnt[0];
     for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
     __syncthreads();
@@ -640,55 +819,43 @@ __device__ __forceinline__ void merge_row(int64_t m, const LongWs& ws, int64_t c
 
 template <bool WEIGHTED>
 __global__ void __launch_bounds__(kMergeThreads, 1)
-merge_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
+merge_top_kernel(int64_t m, LongWs ws) {
     __shared__ Acc3 s_scan[32];
-    __shared__ int s_qs, s_qw, s_bad;
-    __shared__ unsigned long long s_H;
     const int64_t row = blockIdx.x;
     const int64_t c0 = row * m;
     const int tid = threadIdx.x, nth = blockDim.x;
-    if (tid == 0) { s_qs = -100000; s_qw = -100000; s_bad = 0; s_H = 0; }
+    if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
+    // the chunks' surviving segments (each chunk in at most one): lengths into
+    // segOf, first ranks into prevSeg (scratch), then bases by a scan
+    int32_t* len = ws.segOf + c0;
+    int32_t* lo0 = ws.prevSeg + c0;
+    for (int64_t j = tid; j < m; j += nth) { len[j] = 0; lo0[j] = 0; }
     __syncthreads();
-    {
-        int qs = -100000, qw = -100000, bad = 0;
-        unsigned long long hsum = 0;
-        for (int64_t j = tid; j < m; j += nth) {
-            const ChunkMeta mt = ws.meta[c0 + j];
-            qs = max(qs, mt.qs); qw = max(qw, mt.qw); bad |= mt.bad; hsum += (unsigned)mt.h;
-        }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) {
-            qs = max(qs, __shfl_xor_sync(kFull, qs, d));
-            qw = max(qw, __shfl_xor_sync(kFull, qw, d));
-            bad |= __shfl_xor_sync(kFull, bad, d);
-            hsum += __shfl_xor_sync(kFull, hsum, d);
-        }
-        if ((tid & 31) == 0) {
-            atomicMax(&s_qs, qs);
-            atomicMax(&s_qw, qw);
-            if (bad) atomicOr(&s_bad, bad);
-            atomicAdd(&s_H, hsum);
+    for (int64_t g = (int64_t)(tid >> 5) * kGroup; g < m; g += (int64_t)(nth >> 5) * kGroup) {
+        const int n = ws.cnt[c0 + g];
+        for (int k = tid & 31; k < n; k += 32) {
+            const int4 sg = ws.seg[c0 + g + k];
+            len[sg.x] = sg.z - sg.y + 1;
+            lo0[sg.x] = sg.y;
         }
     }
     __syncthreads();
-    const int qs = s_qs, qw = s_qw, bad = s_bad;
-    const int64_t Htot = (int64_t)s_H;
-    if (tid == 0) {
-        ws.rowq[row * 4 + 0] = qs; ws.rowq[row * 4 + 1] = qw; ws.rowq[row * 4 + 2] = bad;
-        if (row_status) row_status[row] = (uint32_t)bad;
+    Acc3 carry{0, 0, 0};
+    for (int64_t q0 = 0; q0 < m; q0 += nth) {
+        const int64_t j = q0 + tid;
+        Acc3 v{0, 0, j < m ? (int64_t)len[j] : 0};
+        Acc3 tot;
+        const Acc3 e = block_excl_scan3(v, s_scan, tot);
+        __syncthreads();
+        if (j < m) len[j] = (int32_t)(carry.h + e.h);     // now the base of chunk j
+        carry.h += tot.h;
     }
-    if (bad) {
-        for (int64_t j = tid; j < m; j += nth) {
-            ChunkEnds ce{};
-            ce.lo = 1; ce.hi = 0; ce.bad = bad;
-            ws.ends[c0 + j] = ce;
-        }
-        return;
-    }
-    if (MergeLayout(m, Htot, WEIGHTED).bytes <= (size_t)kMergeSmem)
-        merge_row<WEIGHTED, true>(m, ws, c0, qs, qw, Htot, s_scan);
+    __syncthreads();
+    const int64_t Hs = carry.h;
+    if (MergeLayout(m, Hs, WEIGHTED, true).bytes <= (size_t)kMergeSmem)
+        merge_top<WEIGHTED, true>(m, ws, c0, Hs, len, lo0);
     else
-        merge_row<WEIGHTED, false>(m, ws, c0, qs, qw, Htot, s_scan);
+        merge_top<WEIGHTED, false>(m, ws, c0, Hs, len, lo0);
 }
 
 // ---------------------------------------------------------------------------
@@ -880,12 +1047,20 @@ static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int6
     chunk_hull_kernel<WEIGHTED><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, n, m, increasing, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "chunk_hull");
-    err = cudaFuncSetAttribute(merge_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
+    if (err != cudaSuccess) return err;
+    const int64_t ng = (m + kGroup - 1) / kGroup;
+    merge_groups_kernel<WEIGHTED><<<dim3((unsigned)rows, (unsigned)ng), kGroupThreads, kGroupSmem,
+                                    stream>>>(m, ws, row_status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "merge_groups");
+    err = cudaFuncSetAttribute(merge_top_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kMergeSmem);
     if (err != cudaSuccess) return err;
-    merge_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, kMergeSmem, stream>>>(m, ws, row_status);
+    merge_top_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, kMergeSmem, stream>>>(m, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    prof_mark(stream, "merge");
+    prof_mark(stream, "merge_top");
     err = cudaFuncSetAttribute(expand_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                ExpandSmem<WEIGHTED>::kBytes);
     if (err != cudaSuccess) return err;
