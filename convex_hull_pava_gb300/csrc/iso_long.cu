@@ -28,7 +28,10 @@ constexpr int kMergeThreads = 512;
 constexpr int kMergeSmem = 210 * 1024;    // shared memory of the merge kernel
 
 template <bool WEIGHTED> struct LongCfg;
-template <> struct LongCfg<false> { static constexpr int NT = 256; static constexpr int C = 8192; };
+#ifndef ISO_UNIT_NT
+#define ISO_UNIT_NT 128
+#endif
+template <> struct LongCfg<false> { static constexpr int NT = ISO_UNIT_NT; static constexpr int C = 32 * ISO_UNIT_NT; };
 template <> struct LongCfg<true> { static constexpr int NT = 128; static constexpr int C = 4096; };
 
 typedef __int128 i128;
@@ -434,7 +437,10 @@ __device__ __forceinline__ Acc3 block_excl_scan3(Acc3 v, Acc3* tmp, Acc3& total)
 // Each CTA reads its chunk hulls into shared memory when they fit (noisy rows
 // keep few vertices; the top kernel reads only the vertices still inside a
 // segment), else it reads them from the slots in global memory.
-constexpr int kGroup = 32;
+#ifndef ISO_GROUP
+#define ISO_GROUP 64
+#endif
+constexpr int kGroup = ISO_GROUP;
 constexpr int kGroupThreads = 256;
 constexpr int kGroupSmem = 48 * 1024;
 
@@ -644,6 +650,7 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
 template <bool WEIGHTED>
 __global__ void __launch_bounds__(kGroupThreads)
 merge_groups_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
+    __shared__ Acc3 s_scan[32];
     __shared__ int s_red[3];
     __shared__ i128 s_part[2][kGroupThreads / 32];
     __shared__ i128 s_gS[kGroup], s_gW[kGroup];
@@ -684,38 +691,31 @@ merge_groups_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
         }
         if ((tid & 31) == 0) { s_part[0][tid >> 5] = aS; s_part[1][tid >> 5] = aW; }
         __syncthreads();
-        if (tid < 32) {
-            // the group's chunks: starts, shifts and vertex bases by a warp scan
-            i128 bS = 0, bW = 0;
-            for (int w = 0; w < nth / 32; ++w) { bS += s_part[0][w]; bW += s_part[1][w]; }
-            const int j = jb + tid;
-            const bool valid = j < je;
-            ChunkMeta mt{};
-            if (valid) mt = ws.meta[c0 + j];
-            const int ds = valid ? q.qs - mt.qs : 0;
-            const int dw = (valid && WEIGHTED) ? q.qw - mt.qw : 0;
-            const i128 vS = valid ? (i128)conv(mt.totS, ds) : (i128)0;
-            const i128 vW = valid ? (WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW) : (i128)0;
-            int vH = valid ? mt.h : 0;
-            i128 xS = vS, xW = vW;
-            int xH = vH;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const i128 oS = shfl_up_i128(xS, d), oW = shfl_up_i128(xW, d);
-                const int oH = __shfl_up_sync(kFull, xH, d);
-                if (tid >= d) { xS += oS; xW += oW; xH += oH; }
-            }
-            if (valid) {
-                s_gS[tid] = bS + xS - vS;
-                s_gW[tid] = bW + xW - vW;
-                s_gH[tid] = xH - vH;
-                ws.offS[c0 + j] = bS + xS - vS;
-                if (WEIGHTED) ws.offW[c0 + j] = bW + xW - vW;
-                ws.dS[c0 + j] = ds;
-                if (WEIGHTED) ws.dW[c0 + j] = dw;
-            }
-            if (tid == 31) s_Hg = xH;
+        // the group's chunks: starts, shifts and vertex bases by a block scan
+        i128 bS = 0, bW = 0;
+        for (int w = 0; w < nth / 32; ++w) { bS += s_part[0][w]; bW += s_part[1][w]; }
+        const int j = jb + tid;
+        const bool valid = tid < kGroup && j < je;
+        ChunkMeta mt{};
+        if (valid) mt = ws.meta[c0 + j];
+        const int ds = valid ? q.qs - mt.qs : 0;
+        const int dw = (valid && WEIGHTED) ? q.qw - mt.qw : 0;
+        Acc3 v;
+        v.s = valid ? (i128)conv(mt.totS, ds) : (i128)0;
+        v.w = valid ? (WEIGHTED ? (i128)conv(mt.totW, dw) : (i128)mt.totW) : (i128)0;
+        v.h = valid ? mt.h : 0;
+        Acc3 tot;
+        const Acc3 e = block_excl_scan3(v, s_scan, tot);
+        if (valid) {
+            s_gS[tid] = bS + e.s;
+            s_gW[tid] = bW + e.w;
+            s_gH[tid] = (int32_t)e.h;
+            ws.offS[c0 + j] = bS + e.s;
+            if (WEIGHTED) ws.offW[c0 + j] = bW + e.w;
+            ws.dS[c0 + j] = ds;
+            if (WEIGHTED) ws.dW[c0 + j] = dw;
         }
+        if (tid == 0) s_Hg = tot.h;
         __syncthreads();
     }
     const int64_t Hg = s_Hg;
