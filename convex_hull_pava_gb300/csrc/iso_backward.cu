@@ -16,61 +16,73 @@ namespace isodev {
 
 namespace {
 
-// Shared memory of a backward tile of NT lanes: grad and w staging, the
-// block-prefix sums of both, masks of block starts and scan scratch.
-template <int NT>
+// Shared memory of a backward CTA of NT lanes: grad (and w) staging, which
+// later holds each run's ratio and then the output, and the lanes' carries of
+// the two segmented scans.
+template <int NT, bool WEIGHTED>
 struct BwdSmem {
-    static constexpr int oStage = 0;                              // grad (later the output)
-    static constexpr int oStageW = oStage + NT * 128;             // w
-    static constexpr int oSx = oStageW + NT * 128;                // block prefix of grad
-    static constexpr int oWx = oSx + NT * kRow * 8;               // block prefix of w
-    static constexpr int oMask = oWx + NT * kRow * 8;
-    static constexpr int oSumm = oMask + NT * 4;
-    static constexpr int oInfo = oSumm + ((NT + 63) / 64) * 8;
-    static constexpr int oScan = oInfo + NT * 16;
-    static constexpr int oLS = oScan + (NT / 16 + 2) * 8;         // per-lane inclusive carries
-    static constexpr int oLW = oLS + NT * 8;
-    static constexpr int oBridge = oLW + NT * 8;                  // scan flags
-    static constexpr int kBytes = ((oBridge + NT * 4 + 127) / 128) * 128;
+    static constexpr int oStage = 0;                                  // grad, ratios, output
+    static constexpr int oStageW = oStage + NT * 128;                 // w
+    static constexpr int oCarry = oStageW + (WEIGHTED ? NT * 128 : 0);   // [4][NT] int64
+    static constexpr int oWarp = oCarry + 4 * NT * 8;                 // [4][NT/32] int64 + flags
+    static constexpr int oWarpF = oWarp + 4 * (NT / 32) * 8;          // [2][NT/32] int
+    static constexpr int oInfo = oWarpF + 2 * (NT / 32) * 4;          // per tile: 8 int64
+    static constexpr int kBytes = ((oInfo + NT * 8 * 8 + 127) / 128) * 128;
 };
 
-// Block sums of one tile: on return, stage holds, for every element whose
-// block both starts and ends inside the tile, its output value; `Px`/`Qx` hold
-// the block-prefix sums (fixed point) of grad and w, restarting at each block
-// start and at the tile's first element.  Tail/head information is returned
-// for the long-row path.
+// Result of a backward tile.  hG/hW: sums (fixed point) of the elements before
+// the tile's first block start (the whole tile if it has none); tG/tW: sums
+// from its last block start to its end.
 struct BwdTile {
     int first_start;   // first block start in the tile, or -1
     int last_start;    // last block start in the tile, or -1
     int qg, qw;        // quantum exponents of grad and w
     bool nan;          // a non-finite grad or an invalid weight in the tile
+    int64_t hG, hW, tG, tW;
 };
 
+// Per-tile info: ints 0..4 (exponent maxima, status, first and last start),
+// then 64-bit slots for the tile's head and tail sums.
+enum { kBInfoG = 0, kBInfoW = 1, kBInfoBad = 2, kBInfoFs = 3, kBInfoLs = 4 };
+enum { kSlotTW = 4, kSlotHG = 5, kSlotHW = 6, kSlotTG = 7 };
+
+// One tile of L lanes (32 elements each): every element gets w_i G / W of its
+// block, where the block's sums come from the lane's own run sums and, for
+// runs that cross lanes, from a forward segmented scan (the part before the
+// lane) and a backward one (the part after it) over the lanes' sums.  Each
+// run's ratio is written at the run's last element and spread back over the
+// run by a reverse pass.  Runs that cross the tile's edges get only the
+// tile's part; the long-row path completes them.  All threads of the CTA call
+// it.  On return, stage holds the output of the tile's elements.
 template <int NT, bool WEIGHTED>
 __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
                                                const uint8_t* __restrict__ br,
                                                const float* __restrict__ wr, int nt, bool live,
                                                bool first_is_start, int L, unsigned char* smem,
                                                BwdTile& B) {
-    using SM = BwdSmem<NT>;
+    using SM = BwdSmem<NT, WEIGHTED>;
     float* stage = reinterpret_cast<float*>(smem + SM::oStage);
-    int64_t* Px = reinterpret_cast<int64_t*>(smem + SM::oSx);
-    int64_t* Qx = reinterpret_cast<int64_t*>(smem + SM::oWx);
     float* stagew = reinterpret_cast<float*>(smem + SM::oStageW);
-    uint32_t* maska = reinterpret_cast<uint32_t*>(smem + SM::oMask);
-    uint32_t* summ = reinterpret_cast<uint32_t*>(smem + SM::oSumm);
-    int* info = reinterpret_cast<int*>(smem + SM::oInfo);
-    int64_t* scan = reinterpret_cast<int64_t*>(smem + SM::oScan);
-    int64_t* incl = reinterpret_cast<int64_t*>(smem + SM::oLS);
-    int64_t* inclw = reinterpret_cast<int64_t*>(smem + SM::oLW);
-    int* scanf = reinterpret_cast<int*>(smem + SM::oBridge);
+    int64_t* carry = reinterpret_cast<int64_t*>(smem + SM::oCarry);
+    int64_t* wsum = reinterpret_cast<int64_t*>(smem + SM::oWarp);
+    int* wflag = reinterpret_cast<int*>(smem + SM::oWarpF);
+    int64_t* info64 = reinterpret_cast<int64_t*>(smem + SM::oInfo);
 
     const int tid = threadIdx.x;
     const int tile = tid / L;
     const int lane = tid - tile * L;
     const int gl = tid;
+    const int wl = tid & 31, warp = tid >> 5;
+    const int seg = L < 32 ? L : 32;
+    const int lseg = wl & (seg - 1);
+    int* info = reinterpret_cast<int*>(info64 + tile * 8);
 
-    for (int i = lane; i < 4; i += L) info[tile * 4 + i] = 0;
+    if (lane == 0) {
+        info[kBInfoG] = 0; info[kBInfoW] = 0; info[kBInfoBad] = 0;
+        info[kBInfoFs] = 0x7fffffff; info[kBInfoLs] = -1;
+        info64[tile * 8 + kSlotHG] = 0; info64[tile * 8 + kSlotHW] = 0;
+        info64[tile * 8 + kSlotTG] = 0; info64[tile * 8 + kSlotTW] = 0;
+    }
     __syncthreads();
     int gmax = 0, ewmax = 0;
     uint32_t bad = 0;
@@ -101,29 +113,28 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
         }
         if (lane == 0 && first_is_start) starts |= 1u;
     }
-    maska[gl] = starts;
     gmax = tile_warp_max(gmax, L);
     if (WEIGHTED) ewmax = tile_warp_max(ewmax, L);
     const int bad_or = tile_warp_or((int)bad, L);
-    const int seg = L < 32 ? L : 32;
-    if (live && ((tid & 31) & (seg - 1)) == 0) {
-        atomicMax(&info[tile * 4 + 0], gmax);
-        if (WEIGHTED) atomicMax(&info[tile * 4 + 1], ewmax);
-        if (bad_or) atomicOr(&info[tile * 4 + 2], 1);
+    if (live && lseg == 0) {
+        atomicMax(&info[kBInfoG], gmax);
+        if (WEIGHTED) atomicMax(&info[kBInfoW], ewmax);
+        if (bad_or) atomicOr(&info[kBInfoBad], 1);
+    }
+    if (starts) {
+        atomicMin(&info[kBInfoFs], (lane << 5) + __ffs(starts) - 1);
+        atomicMax(&info[kBInfoLs], (lane << 5) + 31 - __clz(starts));
     }
     __syncthreads();
-    gmax = max(info[tile * 4 + 0], 1);
-    ewmax = max(info[tile * 4 + 1], 1);
-    B.nan = info[tile * 4 + 2] != 0;
+    gmax = max(info[kBInfoG], 1);
+    ewmax = max(info[kBInfoW], 1);
+    B.nan = info[kBInfoBad] != 0;
     B.qg = qexp_unit(gmax);
     B.qw = WEIGHTED ? qexp_unit(ewmax) : 0;
-    {
-        const uint32_t bal = __ballot_sync(kFull, starts != 0u);
-        if ((tid & 31) == 0) summ[tid >> 5] = bal;
-    }
+    B.first_start = info[kBInfoFs] == 0x7fffffff ? -1 : info[kBInfoFs];
+    B.last_start = info[kBInfoLs];
+    const Quant qg(gmax), qwt(ewmax);
 
-    // one pass over the lane's staged values: fixed-point grad and w, and the
-    // sums after the lane's last block start (or the lane totals)
     const float4* st4 = reinterpret_cast<const float4*>(stage);
     const float4* sw4 = reinterpret_cast<const float4*>(stagew);
     auto lane_values = [&](int q, float (&vv)[4], float (&ww)[4]) {
@@ -136,60 +147,18 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
             ww[0] = t.x; ww[1] = t.y; ww[2] = t.z; ww[3] = t.w;
         }
     };
-    int64_t sg = 0, sw = 0;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        float vv[4], ww[4];
-        lane_values(q, vv, ww);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k = 4 * q + j;
-            if ((starts >> k) & 1u) { sg = 0; sw = 0; }
-            if (k < e) {
-                sg += quant(vv[j], gmax);
-                sw += WEIGHTED ? quant(ww[j], ewmax) : 1;
-            }
-        }
-    }
-    int64_t cg, cw;
+    const int qd = B.qg - B.qw;
+    const float qnan = __int_as_float(0x7fffffff);
+    auto ratio = [&](int64_t G, int64_t Wt) {
+        return B.nan ? qnan : ldexpf(i64_to_f32(G) / i64_to_f32(Wt), qd);
+    };
+    // pass 1: the lane's head (before its first start) and tail (from its
+    // last start) sums, a lane without a start having head = tail = its total;
+    // the ratio of every run between two starts of the lane is written over the
+    // run's last element
+    int64_t hg = 0, hw = 0, tg = 0, tw = 0;
     {
-        int64_t vg = sg, vw = sw;
-        int fl = starts ? 1 : 0;
-        const int wl = tid & 31;
-        const int seg = L < 32 ? L : 32;
-        const int lseg = wl & (seg - 1);
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            int64_t og = __shfl_up_sync(kFull, vg, d);
-            int64_t ow = __shfl_up_sync(kFull, vw, d);
-            int of = __shfl_up_sync(kFull, fl, d);
-            if (d < seg && lseg >= d) {
-                if (!fl) { vg += og; vw += ow; }
-                fl |= of;
-            }
-        }
-        if (L > 32) {
-            const int warp = tid >> 5;
-            if (wl == 31) { scan[warp] = vg; scanf[warp] = fl; scan[NT / 32 + warp] = vw; }
-            __syncthreads();
-            const int w0 = warp - (lane >> 5);
-            int64_t ag = 0, aw = 0;
-            for (int q = w0; q < warp; ++q) {
-                if (scanf[q]) { ag = scan[q]; aw = scan[NT / 32 + q]; }
-                else { ag += scan[q]; aw += scan[NT / 32 + q]; }
-            }
-            if (!fl) { vg += ag; vw += aw; }
-        }
-        incl[gl] = vg;
-        inclw[gl] = vw;
-        __syncthreads();
-        cg = lane ? incl[gl - 1] : 0;
-        cw = lane ? inclw[gl - 1] : 0;
-    }
-    {
-        int64_t pg = cg, pw = cw;
-        int64_t* myP = Px + gl * kRow;
-        int64_t* myQ = Qx + gl * kRow;
+        bool seen = false;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             float vv[4], ww[4];
@@ -197,51 +166,123 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int k = 4 * q + j;
-                if ((starts >> k) & 1u) { pg = 0; pw = 0; }
-                if (k < e) {
-                    pg += quant(vv[j], gmax);
-                    pw += WEIGHTED ? quant(ww[j], ewmax) : 1;
+                if ((starts >> k) & 1u) {
+                    if (seen) stage[spos(gl, k - 1)] = ratio(tg, tw);
+                    else { hg = tg; hw = tw; seen = true; }
+                    tg = 0; tw = 0;
                 }
-                myP[k] = pg;
-                myQ[k] = pw;
+                if (k < e) {
+                    tg += qg(vv[j]);
+                    tw += WEIGHTED ? qwt(ww[j]) : 1;
+                }
             }
         }
+        if (!seen) { hg = tg; hw = tw; }
     }
-    __syncthreads();
-
-    Tile T;
-    T.Sx = Px; T.Wx = Qx; T.LS = nullptr; T.LW = nullptr;
-    T.mask = maska + tile * L; T.summ = summ; T.sbase = tile * L; T.L = L; T.nt = nt;
+    const int fl0 = starts ? 1 : 0;
+    int64_t* inG = carry;            // forward inclusive
+    int64_t* inW = carry + NT;
+    int64_t* bkG = carry + 2 * NT;   // backward inclusive
+    int64_t* bkW = carry + 3 * NT;
     {
-        // first / last block start of the tile (scan of the starts masks)
-        const int fl = next_nonempty(T, 0, L);
-        const int ll = prev_nonempty(T, 0, L);
-        B.first_start = fl < 0 ? -1 : (fl << 5) + __ffs(T.mask[fl]) - 1;
-        B.last_start = ll < 0 ? -1 : (ll << 5) + 31 - __clz(T.mask[ll]);
-    }
-
-    // each element inside the tile's complete blocks: the block sums are the
-    // prefixes at the block's last element, one before the next start
-    const int p0 = lane << 5;
-    const int qd = B.qg - B.qw;
-    int cur_last = -1;
-    float ratio = 0.0f;
+        // forward: I_l = f_l ? tail_l : I_{l-1} + total_l
+        int64_t vg = tg, vw = tw;
+        int fl = fl0;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        if (k < e) {
-            if (p0 + k > cur_last) {
-                const int nxt = tile_succ(T, p0 + k, L, nt);
-                cur_last = nxt - 1;
-                const int gll = tile * L + (cur_last >> 5);
-                const int64_t G = Px[gll * kRow + (cur_last & 31)];
-                const int64_t Wb = Qx[gll * kRow + (cur_last & 31)];
-                ratio = ldexpf(i64_to_f32(G) / i64_to_f32(Wb), qd);
-                if (B.nan) ratio = __int_as_float(0x7fffffff);
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t og = __shfl_up_sync(kFull, vg, d);
+            const int64_t ow = __shfl_up_sync(kFull, vw, d);
+            const int of = __shfl_up_sync(kFull, fl, d);
+            if (d < seg && lseg >= d) {
+                if (!fl) { vg += og; vw += ow; }
+                fl |= of;
             }
-            stage[spos(gl, k)] = WEIGHTED ? stagew[spos(gl, k)] * ratio : ratio;
+        }
+        // backward: J_l = f_l ? head_l : total_l + J_{l+1}
+        int64_t ug = hg, uw = hw;
+        int fr = fl0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int64_t og = __shfl_down_sync(kFull, ug, d);
+            const int64_t ow = __shfl_down_sync(kFull, uw, d);
+            const int of = __shfl_down_sync(kFull, fr, d);
+            if (d < seg && lseg + d < seg) {
+                if (!fr) { ug += og; uw += ow; }
+                fr |= of;
+            }
+        }
+        if (L > 32) {
+            const int nw = NT / 32;
+            if (wl == 31) { wsum[warp] = vg; wsum[nw + warp] = vw; wflag[warp] = fl; }
+            if (wl == 0) { wsum[2 * nw + warp] = ug; wsum[3 * nw + warp] = uw; wflag[nw + warp] = fr; }
+            __syncthreads();
+            const int w0 = warp - (lane >> 5);            // first warp of this tile
+            const int w1 = w0 + (L >> 5);                 // one past its last
+            if (!fl) {
+                int64_t ag = 0, aw = 0;
+                for (int q = warp - 1; q >= w0; --q) {
+                    ag += wsum[q]; aw += wsum[nw + q];
+                    if (wflag[q]) break;
+                }
+                vg += ag; vw += aw;
+            }
+            if (!fr) {
+                int64_t ag = 0, aw = 0;
+                for (int q = warp + 1; q < w1; ++q) {
+                    ag += wsum[2 * nw + q]; aw += wsum[3 * nw + q];
+                    if (wflag[nw + q]) break;
+                }
+                ug += ag; uw += aw;
+            }
+        }
+        inG[gl] = vg; inW[gl] = vw;
+        bkG[gl] = ug; bkW[gl] = uw;
+    }
+    __syncthreads();
+    // the part of the lane's first run before the lane, and of its last run after it
+    const int64_t cing = lane ? inG[gl - 1] : 0, cinw = lane ? inW[gl - 1] : 0;
+    const int64_t coutg = lane + 1 < L ? bkG[gl + 1] : 0, coutw = lane + 1 < L ? bkW[gl + 1] : 0;
+    // the tile's head and tail sums, from the lanes that hold its first and last start
+    if (B.first_start >= 0 && lane == (B.first_start >> 5)) {
+        info64[tile * 8 + kSlotHG] = cing + hg;
+        info64[tile * 8 + kSlotHW] = cinw + hw;
+    }
+    if (B.first_start < 0 && lane == L - 1) {
+        info64[tile * 8 + kSlotHG] = inG[gl];
+        info64[tile * 8 + kSlotHW] = inW[gl];
+    }
+    if (B.last_start >= 0 && lane == (B.last_start >> 5)) {
+        info64[tile * 8 + kSlotTG] = tg + coutg;
+        info64[tile * 8 + kSlotTW] = tw + coutw;
+    }
+    // the lane's first and last runs, which may reach into other lanes
+    if (e > 0) {
+        if (starts) {
+            const int f = __ffs(starts) - 1;
+            if (f > 0) stage[spos(gl, f - 1)] = ratio(cing + hg, cinw + hw);
+            stage[spos(gl, e - 1)] = ratio(tg + coutg, tw + coutw);
+        } else {
+            stage[spos(gl, e - 1)] = ratio(cing + tg + coutg, cinw + tw + coutw);
+        }
+    }
+    // pass 2, backwards: each element takes the ratio of its run (times w)
+    {
+        float r = 0.0f;
+#pragma unroll
+        for (int k = 31; k >= 0; --k) {
+            if (k < e) {
+                const bool last = k == e - 1 || ((starts >> (k + 1)) & 1u);
+                const int p = spos(gl, k);
+                if (last) r = stage[p];
+                stage[p] = WEIGHTED ? stagew[p] * r : r;
+            }
         }
     }
     __syncthreads();
+    B.hG = info64[tile * 8 + kSlotHG];
+    B.hW = info64[tile * 8 + kSlotHW];
+    B.tG = info64[tile * 8 + kSlotTG];
+    B.tW = info64[tile * 8 + kSlotTW];
 }
 
 template <int NT, bool WEIGHTED>
@@ -250,7 +291,7 @@ rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__
                      const float* __restrict__ w, int64_t rows, int n, int L,
                      float* __restrict__ out) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = BwdSmem<NT>;
+    using SM = BwdSmem<NT, WEIGHTED>;
     const int R = NT / L;
     const int tile = threadIdx.x / L;
     const int lane = threadIdx.x - tile * L;
@@ -290,7 +331,7 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
                       const float* __restrict__ w, int64_t n, int64_t m, float* __restrict__ out,
                       BwdRec* __restrict__ rec) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = BwdSmem<kBNT>;
+    using SM = BwdSmem<kBNT, WEIGHTED>;
     const int64_t c = blockIdx.x;
     const int64_t row = c / m;
     const int64_t j = c - row * m;
@@ -301,8 +342,6 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
     bwd_tile_phase<kBNT, WEIGHTED>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, nt,
                                    true, j == 0, kBNT, smem, B);
     const float* stage = reinterpret_cast<const float*>(smem + SM::oStage);
-    const int64_t* Px = reinterpret_cast<const int64_t*>(smem + SM::oSx);
-    const int64_t* Qx = reinterpret_cast<const int64_t*>(smem + SM::oWx);
     // elements of complete blocks: from the first start to one before the last start
     const int lo = B.first_start < 0 ? nt : B.first_start;
     const int hi = B.last_start < 0 ? nt : B.last_start;
@@ -315,17 +354,11 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
         r.nan = B.nan ? 1 : 0;
         r.pad = 0;
         const double sg = ldexp(1.0, B.qg), sw = ldexp(1.0, B.qw);
-        const int hl = (B.first_start < 0 ? nt : B.first_start) - 1;   // last element of the head
-        if (hl >= 0) {
-            r.hG = (double)Px[(hl >> 5) * kRow + (hl & 31)] * sg;
-            r.hW = (double)Qx[(hl >> 5) * kRow + (hl & 31)] * sw;
-        } else {
-            r.hG = 0.0; r.hW = 0.0;
-        }
+        r.hG = (double)B.hG * sg;
+        r.hW = (double)B.hW * sw;
         if (B.last_start >= 0) {
-            const int tl = nt - 1;
-            r.tG = (double)Px[(tl >> 5) * kRow + (tl & 31)] * sg;
-            r.tW = (double)Qx[(tl >> 5) * kRow + (tl & 31)] * sw;
+            r.tG = (double)B.tG * sg;
+            r.tW = (double)B.tW * sw;
         } else {
             r.tG = 0.0; r.tW = 0.0;
         }
@@ -398,7 +431,7 @@ __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(25
 template <int NT, bool WEIGHTED>
 cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const float* w,
                             int64_t rows, int n, int L, float* out, cudaStream_t stream) {
-    using SM = BwdSmem<NT>;
+    using SM = BwdSmem<NT, WEIGHTED>;
     auto kern = rows_backward_kernel<NT, WEIGHTED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
@@ -413,7 +446,7 @@ cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const floa
 template <bool WEIGHTED>
 cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
                        int64_t n, float* out, void* ws, cudaStream_t stream) {
-    using SM = BwdSmem<kBNT>;
+    using SM = BwdSmem<kBNT, WEIGHTED>;
     const int64_t m = (n + kBT - 1) / kBT;
     const int64_t M = rows * m;
     BwdRec* rec = static_cast<BwdRec*>(ws);
