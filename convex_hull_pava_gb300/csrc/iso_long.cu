@@ -928,10 +928,15 @@ expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict
     // each with the slope of the root edge leaving it
     const bool has = ce.lo <= ce.hi;
     if (has) {
-        for (int r = ce.lo + tid; r <= ce.hi; r += NT) {
-            const int p = sp[r];
+        for (int r0 = ce.lo; r0 <= ce.hi; r0 += NT) {
+            const int r = r0 + tid;
+            const int p = r <= ce.hi ? sp[r] : nt;
+            // the warp's start bits, one atomic per distinct mask word
+            const int word = p < nt ? p >> 5 : -1;
+            const unsigned grp = __match_any_sync(kFull, word);
+            const unsigned bits = __reduce_or_sync(grp, p < nt ? 1u << (p & 31) : 0u);
+            if (word >= 0 && (tid & 31) == __ffs(grp) - 1) atomicOr(&s_mask[word], bits);
             if (p >= nt) continue;
-            atomicOr(&s_mask[p >> 5], 1u << (p & 31));
             float sl;
             if (r < ce.hi) {
                 // both ends in the chunk: chunk-relative coordinates, chunk quanta
