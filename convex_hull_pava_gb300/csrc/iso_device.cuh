@@ -382,33 +382,40 @@ __device__ __forceinline__ void tile_bridge(const Tile& T, int A0, int B0, int B
 }
 
 // Merge of two neighbouring hulls stored as compact lists (point indices P,
-// tile-relative S, and W for weighted tiles): L = entries 0..cL-1, R = entries
-// 0..cR-1, where L's last entry and R's first are the same point s (Lemma
-// 4.2).  If the chain is convex at s, R is appended without s.  Otherwise the
-// two ends walk to their tangent points in turn, from s's neighbours; a walk
-// longer than kCompactLinear steps finishes by bisection over the list.  The
-// merged list is L[0..a] followed by R[b..cR-1]; the caller moves the tail
-// (returned as dst in L's list, src in R's list, len) and the new count is
-// stored in *cntL.
+// tile-relative S, and W for weighted tiles; flat entry f at f + f/32), each
+// list holding a group's vertices before its end point: L = the cL entries
+// from flat fL, R = the cR entries from flat fR, R's
+// first entry being L's end point s, and (SE, WE) the end point of R (W: the
+// point index for unit weights), index cR below.  If the chain is convex at s,
+// R follows L unchanged.  Otherwise the two ends walk to their tangent points
+// in turn, from s's neighbours (Lemma 4.2); a walk longer than kCompactLinear
+// steps finishes by bisection over the list.  The merged list is L[0..a]
+// followed by R[b..cR-1]; the caller moves that tail (returned as flat dst,
+// src and len) and the new count is stored in *cntL.
 constexpr int kCompactLinear = 8;
 
 template <bool WEIGHTED>
-__device__ __forceinline__ void compact_merge(const int64_t* SL, const int64_t* WL,
-                                              const uint16_t* PL, int* cntL, const int64_t* SR,
-                                              const int64_t* WR, const uint16_t* PR, int cR,
-                                              int& dst, int& src, int& len) {
+__device__ __forceinline__ void compact_merge(const int64_t* S, const int64_t* W,
+                                              const uint16_t* P, int fL, int* cntL, int fR, int cR,
+                                              int64_t SE, int64_t WE, int& dst, int& src,
+                                              int& len) {
+    // flat entry f lives at f + f/32
     const int cL = *cntL;
+    auto at = [](int f) { return f + (f >> 5); };
+    auto SL = [&](int i) -> int64_t { return S[at(fL + i)]; };
     auto wl = [&](int i) -> int64_t {
-        if constexpr (WEIGHTED) return WL[i]; else return (int64_t)PL[i];
+        if constexpr (WEIGHTED) return W[at(fL + i)]; else return (int64_t)P[at(fL + i)];
     };
+    auto sr = [&](int j) -> int64_t { return j < cR ? S[at(fR + j)] : SE; };
     auto wr = [&](int j) -> int64_t {
-        if constexpr (WEIGHTED) return WR[j]; else return (int64_t)PR[j];
+        if constexpr (WEIGHTED) return j < cR ? W[at(fR + j)] : WE;
+        else return j < cR ? (int64_t)P[at(fR + j)] : WE;
     };
-    int a = cL - 2, b = 1;
-    int64_t Wa = wl(a), Sa = SL[a], Wb = wr(b), Sb = SR[b];
-    if (tile_turn<WEIGHTED>(Wa, Sa, wl(cL - 1), SL[cL - 1], Wb, Sb)) {
-        dst = cL; src = 1; len = cR - 1;
-        *cntL = cL + cR - 1;
+    int a = cL - 1, b = 1;
+    int64_t Wa = wl(a), Sa = SL(a), Wb = wr(b), Sb = sr(b);
+    if (tile_turn<WEIGHTED>(Wa, Sa, wr(0), sr(0), Wb, Sb)) {
+        dst = fL + cL; src = fR; len = cR;
+        *cntL = cL + cR;
         return;
     }
     for (;;) {
@@ -420,36 +427,36 @@ __device__ __forceinline__ void compact_merge(const int64_t* SL, const int64_t* 
                 int lo = 0, hi = a;
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
-                    if (tile_turn<WEIGHTED>(wl(mid - 1), SL[mid - 1], wl(mid), SL[mid], Wb, Sb)) lo = mid;
+                    if (tile_turn<WEIGHTED>(wl(mid - 1), SL(mid - 1), wl(mid), SL(mid), Wb, Sb)) lo = mid;
                     else hi = mid - 1;
                 }
-                a = lo; Wa = wl(a); Sa = SL[a];
+                a = lo; Wa = wl(a); Sa = SL(a);
                 break;
             }
-            const int64_t Wp = wl(a - 1), Sp = SL[a - 1];
+            const int64_t Wp = wl(a - 1), Sp = SL(a - 1);
             if (tile_turn<WEIGHTED>(Wp, Sp, Wa, Sa, Wb, Sb)) break;
             --a; Wa = Wp; Sa = Sp; moved = true;
         }
         // the right end: the first vertex j >= b strictly below the segment
-        // from a to its successor
-        for (int steps = 0; b < cR - 1; ++steps) {
+        // from a to its successor (R's end point always qualifies)
+        for (int steps = 0; b < cR; ++steps) {
             if (steps == kCompactLinear) {
-                int lo = b, hi = cR - 1;
+                int lo = b, hi = cR;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
-                    if (tile_turn<WEIGHTED>(Wa, Sa, wr(mid), SR[mid], wr(mid + 1), SR[mid + 1])) hi = mid;
+                    if (tile_turn<WEIGHTED>(Wa, Sa, wr(mid), sr(mid), wr(mid + 1), sr(mid + 1))) hi = mid;
                     else lo = mid + 1;
                 }
-                b = lo; Wb = wr(b); Sb = SR[b];
+                b = lo; Wb = wr(b); Sb = sr(b);
                 break;
             }
-            const int64_t Wq = wr(b + 1), Sq = SR[b + 1];
+            const int64_t Wq = wr(b + 1), Sq = sr(b + 1);
             if (tile_turn<WEIGHTED>(Wa, Sa, Wb, Sb, Wq, Sq)) break;
             ++b; Wb = Wq; Sb = Sq; moved = true;
         }
         if (!moved) break;
     }
-    dst = a + 1; src = b; len = cR - b;
+    dst = fL + a + 1; src = fR + b; len = cR - b;
     *cntL = a + 1 + cR - b;
 }
 

@@ -144,19 +144,22 @@ chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int6
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, false, 1>(yr, wr, nt, true, !increasing, NT, smem, H);
 
-    // the chunk hull is the compact list of lane 0's row: copy it to the slot
+    // the chunk hull is the compact list of lane 0's row and the chunk's end
+    // point: copy them to the slot
     const int64_t* Sx = reinterpret_cast<const int64_t*>(smem + SM::oSx);
     const int64_t* Wx = reinterpret_cast<const int64_t*>(smem + SM::oWx);
     const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
-    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] : 0;
+    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] + 1 : 0;
     const size_t cap = (size_t)C + 1;
     uint16_t* sp = ws.slot_p + c * cap;
     int64_t* sS = ws.slot_S + c * cap;
     int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
     for (int j = threadIdx.x; j < h; j += NT) {
-        sp[j] = Px[j];
-        sS[j] = Sx[j];
-        if constexpr (WEIGHTED) sW[j] = Wx[j];
+        const bool endp = j == h - 1;
+        const int f = j + (j >> 5);                    // flat entry j
+        sp[j] = endp ? (uint16_t)nt : Px[f];
+        sS[j] = endp ? H.T.LS[NT] : Sx[f];
+        if constexpr (WEIGHTED) sW[j] = endp ? H.T.LW[NT] : Wx[f];
     }
     if (threadIdx.x == 0) {
         ChunkMeta mt;

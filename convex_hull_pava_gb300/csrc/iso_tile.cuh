@@ -27,6 +27,10 @@ __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ g
 // in Px, and merge the compact lists.
 template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
 struct TileSmem {
+    // 33 entries per lane row (an odd stride: the lanes' rows start in
+    // different banks), points 0..32 of the lane.  Compact lists use the first
+    // 32 entries of each row, flat entry i living at i + i/32, so that the
+    // lists of neighbouring lanes are contiguous in flat order.
     static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
     static constexpr int kYB = EMIT ? NT * 128 : 0;             // slope per vertex (EMIT)
@@ -52,7 +56,7 @@ struct TileSmem {
     static constexpr int oInfo = oBridge + kBridgeB;
     static constexpr int oScan = oInfo + kInfoB;
     static constexpr int kBytes = ((oScan + kScanB + 127) / 128) * 128;
-    // staging: y at the start of Sx, w after it (2 x 128 B per lane < 264 B)
+    // staging: y at the start of Sx, w after it (2 x 128 B per lane <= 256 B)
     static constexpr int oStageY = oSx;
     static constexpr int oStageW = oSx + NT * 128;
 };
@@ -378,26 +382,19 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         __syncthreads();
     } else {
         // ---- each lane hull moves to the front of its row, tile-relative,
-        // with its points' indices, its end point included ----
+        // with its points' indices; the end point of a group of lanes is the
+        // next group's first point (lane starts LS, LW) ----
         uint16_t* Px = reinterpret_cast<uint16_t*>(smem + SM::oPx);
         int* cnt = reinterpret_cast<int*>(smem + SM::oCnt);
         uint16_t* myP = Px + gl * kRow;
         int c = 0;
-        if (e > 0) {
-            const int64_t Se = myS[e] + ls;
-            const int64_t We = WEIGHTED ? myW[e] + lw : 0;
-            uint32_t mm = mask;
-            while (mm) {
-                const int k = __ffs(mm) - 1;
-                mm &= mm - 1u;
-                myS[c] = myS[k] + ls;
-                if constexpr (WEIGHTED) myW[c] = myW[k] + lw;
-                myP[c] = (uint16_t)((lane << 5) + k);
-                ++c;
-            }
-            myS[c] = Se;
-            if constexpr (WEIGHTED) myW[c] = We;
-            myP[c] = (uint16_t)((lane << 5) + e);
+        uint32_t mm = mask;
+        while (mm) {
+            const int k = __ffs(mm) - 1;
+            mm &= mm - 1u;
+            myS[c] = myS[k] + ls;
+            if constexpr (WEIGHTED) myW[c] = myW[k] + lw;
+            myP[c] = (uint16_t)((lane << 5) + k);
             ++c;
         }
         cnt[gl] = c;
@@ -406,7 +403,8 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
         // group's first lane finds the bridge; the group's lanes in its first
         // warp move the right list's kept tail behind the left list's kept
         // head (the copy the paper's segment lists avoid; here the lists are
-        // short and in shared memory). ----
+        // short and in shared memory, and on a chain convex at the junction
+        // the lists are already adjacent). ----
         for (int r = 0; (1 << r) < L; ++r) {
             const bool cross = (2 << r) > 32;
             if (cross) __syncthreads();
@@ -416,17 +414,19 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
             int dst = 0, src = 0, len = 0;
             if (work && lane == A0 && (B0 << 5) < nt) {
                 const int base = tile * L;
-                compact_merge<WEIGHTED>(Sx + (base + A0) * kRow, Wx + (base + A0) * kRow,
-                                        Px + (base + A0) * kRow, cnt + base + A0,
-                                        Sx + (base + B0) * kRow, Wx + (base + B0) * kRow,
-                                        Px + (base + B0) * kRow, cnt[base + B0], dst, src, len);
-                dst += (base + A0) * kRow;
-                src += (base + B0) * kRow;
+                const int eb = min(A0 + (2 << r), L);          // R's end point: lane eb's start
+                const int64_t SE = LSa[tile * (L + 1) + eb];
+                const int64_t WE = WEIGHTED ? LWa[tile * (L + 1) + eb] : (int64_t)min(eb << 5, nt);
+                dst = (base + A0) << 5;                         // flat list starts
+                src = (base + B0) << 5;
+                compact_merge<WEIGHTED>(Sx, Wx, Px, dst, cnt + base + A0, src, cnt[base + B0],
+                                        SE, WE, dst, src, len);
             }
             const int lead = (tid & 31) & ~(T_ - 1);
             dst = __shfl_sync(kFull, dst, lead);
             src = __shfl_sync(kFull, src, lead);
             len = __shfl_sync(kFull, len, lead);
+            if (dst == src) len = 0;                           // already in place
             const int tl = (tid & 31) & (T_ - 1);
             int nr = (len + T_ - 1) / T_;
             for (int d = T_; d < 32; d <<= 1) nr = max(nr, __shfl_xor_sync(kFull, nr, d));
@@ -434,16 +434,17 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
                 const int t = q * T_ + tl;
                 int64_t sv = 0, wv = 0;
                 uint16_t pv = 0;
+                const int fs = src + t, fd = dst + t;           // flat entries
                 if (t < len) {
-                    sv = Sx[src + t];
-                    if constexpr (WEIGHTED) wv = Wx[src + t];
-                    pv = Px[src + t];
+                    sv = Sx[fs + (fs >> 5)];
+                    if constexpr (WEIGHTED) wv = Wx[fs + (fs >> 5)];
+                    pv = Px[fs + (fs >> 5)];
                 }
                 __syncwarp();
                 if (t < len) {
-                    Sx[dst + t] = sv;
-                    if constexpr (WEIGHTED) Wx[dst + t] = wv;
-                    Px[dst + t] = pv;
+                    Sx[fd + (fd >> 5)] = sv;
+                    if constexpr (WEIGHTED) Wx[fd + (fd >> 5)] = wv;
+                    Px[fd + (fd >> 5)] = pv;
                 }
                 __syncwarp();
             }
