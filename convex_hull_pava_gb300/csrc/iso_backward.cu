@@ -147,10 +147,10 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
             ww[0] = t.x; ww[1] = t.y; ww[2] = t.z; ww[3] = t.w;
         }
     };
-    const int qd = B.qg - B.qw;
+    const Pow2 scale(B.qg - B.qw);
     const float qnan = __int_as_float(0x7fffffff);
     auto ratio = [&](int64_t G, int64_t Wt) {
-        return B.nan ? qnan : ldexpf(i64_to_f32(G) / i64_to_f32(Wt), qd);
+        return B.nan ? qnan : scale(i64_to_f32(G) / i64_to_f32(Wt));
     };
     // pass 1: the lane's head (before its first start) and tail (from its
     // last start) sums, a lane without a start having head = tail = its total;

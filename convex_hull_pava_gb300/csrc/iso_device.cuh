@@ -55,6 +55,19 @@ struct Quant {
 
 __device__ __forceinline__ int64_t quant(float v, int emax) { return Quant(emax)(v); }
 
+// Multiplication by 2^k in float32 as two exact scalings (k within [-252, 254]),
+// the product rounded like ldexpf unless it falls below the normal range.
+struct Pow2 {
+    float a, b;
+    __device__ __forceinline__ explicit Pow2(int k) {
+        const int k1 = max(min(k, 127), -126);
+        const int k2 = max(min(k - k1, 127), -126);
+        a = __int_as_float((k1 + 127) << 23);
+        b = __int_as_float((k2 + 127) << 23);
+    }
+    __device__ __forceinline__ float operator()(float x) const { return (x * a) * b; }
+};
+
 // float32 of a 64-bit integer from two 32-bit conversions and one fused
 // multiply-add on the magnitude: exact when the value is representable, else
 // within 1.5 ulp.

@@ -916,6 +916,7 @@ expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict
     const i128 offW = WEIGHTED ? ws.offW[c] : (i128)0;
     const int ds = ws.dS[c], dw = WEIGHTED ? ws.dW[c] : 0;
 
+    const Pow2 cscale(mt.qs - (WEIGHTED ? mt.qw : 0));   // chunk quanta to values
     s_mask[tid] = 0u;
     __syncthreads();
     auto row_slope = [&](i128 Wa, i128 Sa, i128 Wb, i128 Sb) -> float {
@@ -945,7 +946,7 @@ expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict
                 // both ends in the chunk: chunk-relative coordinates, chunk quanta
                 const int64_t dS_ = sS[r + 1] - sS[r];
                 const int64_t dW_ = WEIGHTED ? sW[r + 1] - sW[r] : (int64_t)(sp[r + 1] - p);
-                sl = ldexpf(i64_to_f32(dS_) / i64_to_f32(dW_), mt.qs - (WEIGHTED ? mt.qw : 0));
+                sl = cscale(i64_to_f32(dS_) / i64_to_f32(dW_));
             } else {
                 i128 Wa, Sa;
                 vrow(r, Wa, Sa);

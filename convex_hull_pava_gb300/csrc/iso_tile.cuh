@@ -460,7 +460,7 @@ __device__ __forceinline__ float tile_slope(const Tile& T, int a, int b, int qs,
     const int64_t dS = tile_S<WEIGHTED>(T, b) - tile_S<WEIGHTED>(T, a);
     const int64_t dW = tile_W<WEIGHTED>(T, b) - tile_W<WEIGHTED>(T, a);
     const float f = i64_to_f32(dS) / i64_to_f32(dW);
-    return ldexpf(f, qs - qw);
+    return Pow2(qs - qw)(f);
 }
 
 }  // namespace isodev
