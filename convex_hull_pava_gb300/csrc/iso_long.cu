@@ -876,8 +876,8 @@ struct ExpandSmem {
 
 template <bool WEIGHTED>
 __global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
-expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict__ out,
-              uint8_t* __restrict__ blocks) {
+expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing, LongWs ws,
+              float* __restrict__ out, uint8_t* __restrict__ blocks) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
     using XS = ExpandSmem<WEIGHTED>;
@@ -909,6 +909,32 @@ expand_kernel(int64_t n, int64_t m, int increasing, LongWs ws, float* __restrict
     const uint16_t* sp = ws.slot_p + c * cap;
     const int64_t* sS = ws.slot_S + c * cap;
     const int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
+    // Every point of the chunk a root vertex (a dense hull): every element is a
+    // one-element block, fitted by its own value (an edge's slope is its
+    // element's mean; for a decreasing fit the negations cancel).
+    if (ce.lo <= ce.hi && ce.hi - ce.lo + sp[ce.lo] == nt && sp[ce.hi] == nt &&
+        (sp[ce.lo] == 0 || (sp[ce.lo] == 1 && ce.pt0_vertex))) {
+        const float* yrow = y + row * n + e0;
+        if ((reinterpret_cast<uintptr_t>(yrow) & 15u) == 0 &&
+            (reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
+            const int n4 = nt >> 2;
+            for (int i = tid; i < n4; i += NT)
+                reinterpret_cast<float4*>(orow)[i] = __ldg(reinterpret_cast<const float4*>(yrow) + i);
+            for (int i = (n4 << 2) + tid; i < nt; i += NT) orow[i] = __ldg(yrow + i);
+        } else {
+            for (int i = tid; i < nt; i += NT) orow[i] = __ldg(yrow + i);
+        }
+        if (brow) {
+            if ((reinterpret_cast<uintptr_t>(brow) & 3u) == 0) {
+                const int n4 = nt >> 2;
+                for (int i = tid; i < n4; i += NT) reinterpret_cast<uint32_t*>(brow)[i] = 0x01010101u;
+                for (int i = (n4 << 2) + tid; i < nt; i += NT) brow[i] = 1;
+            } else {
+                for (int i = tid; i < nt; i += NT) brow[i] = 1;
+            }
+        }
+        return;
+    }
     const int qs_row = ws.rowq[row * 4 + 0];
     const int qw_row = WEIGHTED ? ws.rowq[row * 4 + 1] : 0;
     const ChunkMeta mt = ws.meta[c];
@@ -1074,7 +1100,7 @@ static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int6
                                ExpandSmem<WEIGHTED>::kBytes);
     if (err != cudaSuccess) return err;
     expand_kernel<WEIGHTED><<<(unsigned)M, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
-        n, m, increasing, ws, out, blocks);
+        y, n, m, increasing, ws, out, blocks);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "expand");
     return cudaSuccess;

@@ -320,7 +320,12 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     }
 
     // ---- lane hulls in bit masks, on lane-relative sums ----
-    uint32_t mask = lane_hull<WEIGHTED>(myS, myW, cand, e);
+    // Each edge's slope is its element's mean, so a lane whose every interior
+    // point is locally convex (strictly increasing means) is a strictly convex
+    // chain: all its points are vertices and the monotone chain is not needed.
+    const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+    uint32_t mask = ((cand | 1u) & allp) == allp ? (e > 0 ? allp : 0u)
+                                                 : lane_hull<WEIGHTED>(myS, myW, cand, e);
     const int64_t ls = LSa[tile * (L + 1) + lane];
     const int64_t lw = WEIGHTED ? LWa[tile * (L + 1) + lane] : 0;
 
