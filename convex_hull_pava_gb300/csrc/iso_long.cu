@@ -32,7 +32,10 @@ template <bool WEIGHTED> struct LongCfg;
 #define ISO_UNIT_NT 128
 #endif
 template <> struct LongCfg<false> { static constexpr int NT = ISO_UNIT_NT; static constexpr int C = 32 * ISO_UNIT_NT; };
-template <> struct LongCfg<true> { static constexpr int NT = 128; static constexpr int C = 4096; };
+#ifndef ISO_WEIGHTED_NT
+#define ISO_WEIGHTED_NT 128
+#endif
+template <> struct LongCfg<true> { static constexpr int NT = ISO_WEIGHTED_NT; static constexpr int C = 32 * ISO_WEIGHTED_NT; };
 
 typedef __int128 i128;
 
@@ -870,7 +873,7 @@ struct ExpandSmem {
     static constexpr int C = LongCfg<WEIGHTED>::C;
     static constexpr int oMask = 0;
     static constexpr int oTmp = oMask + NT * 4;
-    static constexpr int oSlope = oTmp + (NT / 32 + 2) * 8;
+    static constexpr int oSlope = ((oTmp + (NT / 32 + 2) * 8 + 15) / 16) * 16;   // float4 rows
     static constexpr int kBytes = oSlope + C * 4;
 };
 
