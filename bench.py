@@ -36,6 +36,24 @@ def dist_env():
     return rank, world, local
 
 
+def cross_rank_max(x, device):
+    """The largest x over the ranks of the default process group (x itself
+    with no group): the job's step time is its slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(elements_per_rank, world, ms_max):
+    """Whole-job throughput: every rank processed its own copy of the
+    workload (weak scaling) in at most ms_max per step."""
+    return world * elements_per_rank / (ms_max * 1e-3)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -251,12 +269,8 @@ def run_gpu(args):
     clocks = sampler.stop()
     chp.profile_enable(False)
 
-    ms_step = float(np.mean(step_ms))
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * W.elements / (ms_step * 1e-3)
+    ms_step = cross_rank_max(float(np.mean(step_ms)), dev)
+    value = job_value(W.elements, world, ms_step)
 
     # dominant kernel and its roofline: algorithmic bytes of that kernel per launch
     kavg = {k: float(np.mean(v)) for k, v in kern.items()}
@@ -296,7 +310,7 @@ def run_gpu(args):
         b.synchronize()
         if i >= 2:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_val = world * W.elements / (float(np.mean(e2e_ms)) * 1e-3)
+    e2e_val = job_value(W.elements, world, cross_rank_max(float(np.mean(e2e_ms)), dev))
 
     # ---- the other named workloads (parity-test configurations), for context ----
     also = {}
