@@ -32,8 +32,8 @@ ISO_ROW_BAD_Y = 1
 ISO_ROW_BAD_W = 2
 
 EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
-           "iso_backward_workspace_bytes", "iso_backward", "iso_backward_noalloc",
-           "iso_profile_enable", "iso_profile_read")
+           "iso_backward_workspace_bytes", "iso_backward", "iso_backward_w",
+           "iso_backward_noalloc", "iso_profile_enable", "iso_profile_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -69,6 +69,8 @@ def load_library(path: str | None = None):
         lib.iso_fit.restype = ci
         lib.iso_backward.argtypes = [vp, vp, vp, i64, i64, vp, vp, sz, vp]
         lib.iso_backward.restype = ci
+        lib.iso_backward_w.argtypes = [vp, vp, vp, vp, vp, i64, i64, vp, vp, vp, sz, vp]
+        lib.iso_backward_w.restype = ci
         lib.iso_backward_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp]
         lib.iso_backward_noalloc.restype = ci
         lib.iso_profile_enable.argtypes = [ci]
@@ -199,6 +201,34 @@ def iso_backward(grad, blocks, w=None, *, out=None, workspace=None, stream=None)
     return out
 
 
+def iso_backward_w(grad, blocks, w, y, fit, *, out_dy=None, out_dw=None, want_dy=True,
+                   workspace=None, stream=None):
+    """Gradients with respect to y and to the weights: ``d/dy_i = w_i * G / W`` and
+    ``d/dw_i = (y_i - z_i) * G / W`` over the blocks of ``blocks`` (``w`` may be
+    None: unit weights).  Returns ``(dy or None, dw)``."""
+    torch = _torch()
+    _check_dev(grad, "grad", torch.float32)
+    _check_dev(blocks, "blocks", torch.uint8)
+    _check_dev(y, "y", torch.float32)
+    _check_dev(fit, "fit", torch.float32)
+    rows, n = _shape2(grad)
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+    if want_dy and out_dy is None:
+        out_dy = torch.empty_like(grad)
+    if out_dw is None:
+        out_dw = torch.empty_like(grad)
+    nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
+    ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
+    st = load_library().iso_backward_w(
+        grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), y.data_ptr(),
+        fit.data_ptr(), rows, n, None if out_dy is None else out_dy.data_ptr(),
+        out_dw.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_backward_w")
+    return out_dy, out_dw
+
+
 def iso_backward_noalloc(grad, blocks, w=None, *, out=None, stream=None):
     """Backward without a workspace, for callers that cannot allocate device
     memory: long rows use a fixed scratch array inside the library (limit:
@@ -226,16 +256,20 @@ def _make_function():
     class _Isotonic(torch.autograd.Function):
         @staticmethod
         def forward(ctx, y, w, increasing):
-            out, blocks, _ = iso_fit(y.contiguous(), None if w is None else w.contiguous(),
-                                     increasing)
-            ctx.save_for_backward(blocks, w)
+            y = y.contiguous()
+            w = None if w is None else w.contiguous()
+            out, blocks, _ = iso_fit(y, w, increasing)
+            ctx.save_for_backward(blocks, w, y, out)
             return out
 
         @staticmethod
         def backward(ctx, g):
-            blocks, w = ctx.saved_tensors
-            gy = iso_backward(g.contiguous(), blocks, w)
-            return gy, None, None
+            blocks, w, y, out = ctx.saved_tensors
+            g = g.contiguous()
+            if w is not None and ctx.needs_input_grad[1]:
+                gy, gw = iso_backward_w(g, blocks, w, y, out, want_dy=ctx.needs_input_grad[0])
+                return gy, gw, None
+            return iso_backward(g, blocks, w), None, None
 
     return _Isotonic
 
@@ -244,9 +278,9 @@ _Fn = None
 
 
 def isotonic(y, w=None, increasing: bool = True):
-    """Differentiable isotonic regression of each row of ``y`` (gradient with
-    respect to ``y``).  Host tensors are copied to the current CUDA device and
-    the result is copied back."""
+    """Differentiable isotonic regression of each row of ``y`` (gradients with
+    respect to ``y`` and, when it requires one, to ``w``).  Host tensors are
+    copied to the current CUDA device and the result is copied back."""
     global _Fn
     torch = _torch()
     if _Fn is None:

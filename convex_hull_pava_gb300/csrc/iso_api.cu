@@ -96,13 +96,31 @@ iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     isodev::prof_start(st);
     if (n <= isodev::kRowMax)
-        return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out, st));
+        return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out, nullptr, nullptr,
+                                               nullptr, st));
     const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
     if (need > 0 && (!workspace || workspace_bytes < need ||
                      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
         return ISO_ERR_WORKSPACE;
-    return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out, workspace,
-                                           workspace_bytes, st));
+    return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out, nullptr, nullptr, nullptr,
+                                           workspace, workspace_bytes, st));
+}
+
+iso_status iso_backward_w(const float* grad, const uint8_t* blocks, const float* w, const float* y,
+                          const float* fit, int64_t rows, int64_t n, float* out_dy, float* out_dw,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+    if (!grad || !blocks || !y || !fit || !out_dw || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    if (n <= isodev::kRowMax)
+        return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out_dy, y, fit, out_dw,
+                                               st));
+    const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return ISO_ERR_WORKSPACE;
+    return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out_dy, y, fit, out_dw,
+                                           workspace, workspace_bytes, st));
 }
 
 int iso_profile_enable(int on) {

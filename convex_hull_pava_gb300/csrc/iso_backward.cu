@@ -46,6 +46,14 @@ struct BwdTile {
 enum { kBInfoG = 0, kBInfoW = 1, kBInfoBad = 2, kBInfoFs = 3, kBInfoLs = 4 };
 enum { kSlotTW = 4, kSlotHG = 5, kSlotHW = 6, kSlotTG = 7 };
 
+// Optional weight gradient: d/dw_i = (y_i - z_i) G / W (the paper's Section 6,
+// "Gradient"), from the fit z of the forward pass.
+struct WGrad {
+    const float* y;      // the forward pass's input, [rows, n]
+    const float* fit;    // its output z, [rows, n]
+    float* dw;           // nullptr: not wanted
+};
+
 // One tile of L lanes (32 elements each): every element gets w_i G / W of its
 // block, where the block's sums come from the lane's own run sums and, for
 // runs that cross lanes, from a forward segmented scan (the part before the
@@ -53,7 +61,8 @@ enum { kSlotTW = 4, kSlotHG = 5, kSlotHW = 6, kSlotTG = 7 };
 // run's ratio is written at the run's last element and spread back over the
 // run by a reverse pass.  Runs that cross the tile's edges get only the
 // tile's part; the long-row path completes them.  All threads of the CTA call
-// it.  On return, stage holds the output of the tile's elements.
+// it.  On return, stage holds the output of the tile's elements and, for
+// weighted tiles, the w staging holds each element's ratio G / W.
 template <int NT, bool WEIGHTED>
 __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
                                                const uint8_t* __restrict__ br,
@@ -274,7 +283,12 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
                 const bool last = k == e - 1 || ((starts >> (k + 1)) & 1u);
                 const int p = spos(gl, k);
                 if (last) r = stage[p];
-                stage[p] = WEIGHTED ? stagew[p] * r : r;
+                if constexpr (WEIGHTED) {
+                    stage[p] = stagew[p] * r;
+                    stagew[p] = r;          // the ratio G / W, for the weight gradient
+                } else {
+                    stage[p] = r;
+                }
             }
         }
     }
@@ -289,7 +303,7 @@ template <int NT, bool WEIGHTED>
 __global__ void __launch_bounds__(NT)
 rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__ blocks,
                      const float* __restrict__ w, int64_t rows, int n, int L,
-                     float* __restrict__ out) {
+                     float* __restrict__ out, WGrad wg) {
     extern __shared__ __align__(128) unsigned char smem[];
     using SM = BwdSmem<NT, WEIGHTED>;
     const int R = NT / L;
@@ -302,9 +316,19 @@ rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__
     bwd_tile_phase<NT, WEIGHTED>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, n, live,
                                  true, L, smem, B);
     const float* stage = reinterpret_cast<const float*>(smem + SM::oStage);
+    const float* ratio = reinterpret_cast<const float*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
     if (live) {
-        float* orow = out + off;
-        for (int i = lane; i < n; i += L) orow[i] = stage[spos(tile * L + (i >> 5), i & 31)];
+        if (out) {
+            float* orow = out + off;
+            for (int i = lane; i < n; i += L) orow[i] = stage[spos(tile * L + (i >> 5), i & 31)];
+        }
+        if (wg.dw) {
+            const float* yrow = wg.y + off;
+            const float* zrow = wg.fit + off;
+            float* drow = wg.dw + off;
+            for (int i = lane; i < n; i += L)
+                drow[i] = (__ldg(yrow + i) - __ldg(zrow + i)) * ratio[spos(tile * L + (i >> 5), i & 31)];
+        }
     }
 }
 
@@ -329,6 +353,7 @@ template <bool WEIGHTED>
 __global__ void __launch_bounds__(kBNT)
 long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict__ blocks,
                       const float* __restrict__ w, int64_t n, int64_t m, float* __restrict__ out,
+                      WGrad wg,
                       BwdRec* __restrict__ rec) {
     extern __shared__ __align__(128) unsigned char smem[];
     using SM = BwdSmem<kBNT, WEIGHTED>;
@@ -345,8 +370,15 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
     // elements of complete blocks: from the first start to one before the last start
     const int lo = B.first_start < 0 ? nt : B.first_start;
     const int hi = B.last_start < 0 ? nt : B.last_start;
-    float* o = out + off;
-    for (int i = lo + threadIdx.x; i < hi; i += kBNT) o[i] = stage[spos(i >> 5, i & 31)];
+    if (out) {
+        float* o = out + off;
+        for (int i = lo + threadIdx.x; i < hi; i += kBNT) o[i] = stage[spos(i >> 5, i & 31)];
+    }
+    if (wg.dw) {
+        const float* ratio = reinterpret_cast<const float*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
+        for (int i = lo + threadIdx.x; i < hi; i += kBNT)
+            wg.dw[off + i] = (__ldg(wg.y + off + i) - __ldg(wg.fit + off + i)) * ratio[spos(i >> 5, i & 31)];
+    }
     if (threadIdx.x == 0) {
         BwdRec r;
         r.fs = B.first_start;
@@ -404,7 +436,7 @@ template <bool WEIGHTED>
 __global__ void __launch_bounds__(kBNT)
 long_bwd_fill_kernel(const float* __restrict__ w, int64_t n, int64_t m,
                      const BwdRec* __restrict__ rec, const BwdTot* __restrict__ tot,
-                     float* __restrict__ out) {
+                     float* __restrict__ out, WGrad wg) {
     const int64_t c = blockIdx.x;
     const int64_t row = c / m;
     const int64_t j = c - row * m;
@@ -413,24 +445,34 @@ long_bwd_fill_kernel(const float* __restrict__ w, int64_t n, int64_t m,
     const BwdRec r = rec[c];
     const BwdTot t = tot[c];
     const int64_t off = row * n + e0;
-    float* o = out + off;
+    float* o = out ? out + off : nullptr;
     const float* wr = WEIGHTED ? w + off : nullptr;
     const float qnan = __int_as_float(0x7fffffff);
     const float rh = t.nan ? qnan : (float)(t.headG / t.headW);
     const float rt = t.nan ? qnan : (float)(t.tailG / t.tailW);
     const int hend = r.fs < 0 ? nt : r.fs;
-    for (int i = threadIdx.x; i < hend; i += kBNT) o[i] = WEIGHTED ? __ldg(wr + i) * rh : rh;
-    if (r.ls >= 0)
-        for (int i = r.ls + threadIdx.x; i < nt; i += kBNT) o[i] = WEIGHTED ? __ldg(wr + i) * rt : rt;
+    const int tbeg = r.ls >= 0 ? r.ls : nt;
+    // the head (elements before the tile's first start) and the tail (from its
+    // last start) belong to blocks that cross tiles; a bad row is NaN throughout
+    auto put = [&](int i, float rt) {
+        if (o) o[i] = WEIGHTED ? __ldg(wr + i) * rt : rt;
+        if (wg.dw) wg.dw[off + i] = (__ldg(wg.y + off + i) - __ldg(wg.fit + off + i)) * rt;
+    };
+    for (int i = threadIdx.x; i < hend; i += kBNT) put(i, rh);
+    for (int i = tbeg + threadIdx.x; i < nt; i += kBNT) put(i, rt);
     if (t.nan)
-        for (int i = hend + threadIdx.x; i < (r.ls >= 0 ? r.ls : nt); i += kBNT) o[i] = qnan;
+        for (int i = hend + threadIdx.x; i < tbeg; i += kBNT) {
+            if (o) o[i] = qnan;
+            if (wg.dw) wg.dw[off + i] = qnan;
+        }
 }
 
 __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 template <int NT, bool WEIGHTED>
 cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const float* w,
-                            int64_t rows, int n, int L, float* out, cudaStream_t stream) {
+                            int64_t rows, int n, int L, float* out, WGrad wg,
+                            cudaStream_t stream) {
     using SM = BwdSmem<NT, WEIGHTED>;
     auto kern = rows_backward_kernel<NT, WEIGHTED>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -438,14 +480,14 @@ cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const floa
     if (err != cudaSuccess) return err;
     const int R = NT / L;
     const int64_t grid = (rows + R - 1) / R;
-    kern<<<(unsigned)grid, NT, SM::kBytes, stream>>>(grad, blocks, w, rows, n, L, out);
+    kern<<<(unsigned)grid, NT, SM::kBytes, stream>>>(grad, blocks, w, rows, n, L, out, wg);
     prof_mark(stream, "rows_backward");
     return cudaGetLastError();
 }
 
 template <bool WEIGHTED>
 cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                       int64_t n, float* out, void* ws, cudaStream_t stream) {
+                       int64_t n, float* out, WGrad wg, void* ws, cudaStream_t stream) {
     using SM = BwdSmem<kBNT, WEIGHTED>;
     const int64_t m = (n + kBT - 1) / kBT;
     const int64_t M = rows * m;
@@ -455,13 +497,13 @@ cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w,
     cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
     if (err != cudaSuccess) return err;
-    k1<<<(unsigned)M, kBNT, SM::kBytes, stream>>>(grad, blocks, w, n, m, out, rec);
+    k1<<<(unsigned)M, kBNT, SM::kBytes, stream>>>(grad, blocks, w, n, m, out, wg, rec);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "bwd_tiles");
     long_bwd_totals_kernel<<<(unsigned)((rows + 63) / 64), 64, 0, stream>>>(rows, m, rec, tot);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "bwd_totals");
-    long_bwd_fill_kernel<WEIGHTED><<<(unsigned)M, kBNT, 0, stream>>>(w, n, m, rec, tot, out);
+    long_bwd_fill_kernel<WEIGHTED><<<(unsigned)M, kBNT, 0, stream>>>(w, n, m, rec, tot, out, wg);
     prof_mark(stream, "bwd_fill");
     return cudaGetLastError();
 }
@@ -469,21 +511,20 @@ cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w,
 }  // namespace
 
 cudaError_t rows_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int n, float* out, cudaStream_t stream) {
+                          int n, float* out, const float* y, const float* fit, float* dw,
+                          cudaStream_t stream) {
     int L = 1;
     while (32 * L < n) L <<= 1;
+    const WGrad wg{y, fit, dw};
     const bool weighted = w != nullptr;
-    if (L <= 32)
-        return weighted ? launch_rows_bwd<128, true>(grad, blocks, w, rows, n, L, out, stream)
-                        : launch_rows_bwd<128, false>(grad, blocks, w, rows, n, L, out, stream);
-    if (L <= 64)
-        return weighted ? launch_rows_bwd<64, true>(grad, blocks, w, rows, n, L, out, stream)
-                        : launch_rows_bwd<64, false>(grad, blocks, w, rows, n, L, out, stream);
-    if (L <= 128)
-        return weighted ? launch_rows_bwd<128, true>(grad, blocks, w, rows, n, L, out, stream)
-                        : launch_rows_bwd<128, false>(grad, blocks, w, rows, n, L, out, stream);
-    return weighted ? launch_rows_bwd<256, true>(grad, blocks, w, rows, n, L, out, stream)
-                    : launch_rows_bwd<256, false>(grad, blocks, w, rows, n, L, out, stream);
+#define ISO_BWD_LAUNCH(NT_)                                                                     \
+    return weighted ? launch_rows_bwd<NT_, true>(grad, blocks, w, rows, n, L, out, wg, stream)  \
+                    : launch_rows_bwd<NT_, false>(grad, blocks, w, rows, n, L, out, wg, stream)
+    if (L <= 32) { ISO_BWD_LAUNCH(128); }
+    if (L <= 64) { ISO_BWD_LAUNCH(64); }
+    if (L <= 128) { ISO_BWD_LAUNCH(128); }
+    ISO_BWD_LAUNCH(256);
+#undef ISO_BWD_LAUNCH
 }
 
 size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted) {
@@ -493,10 +534,12 @@ size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted) {
 }
 
 cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int64_t n, float* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                          int64_t n, float* out, const float* y, const float* fit, float* dw,
+                          void* ws, size_t ws_bytes, cudaStream_t stream) {
     (void)ws_bytes;
-    return w ? long_bwd_t<true>(grad, blocks, w, rows, n, out, ws, stream)
-             : long_bwd_t<false>(grad, blocks, w, rows, n, out, ws, stream);
+    const WGrad wg{y, fit, dw};
+    return w ? long_bwd_t<true>(grad, blocks, w, rows, n, out, wg, ws, stream)
+             : long_bwd_t<false>(grad, blocks, w, rows, n, out, wg, ws, stream);
 }
 
 }  // namespace isodev

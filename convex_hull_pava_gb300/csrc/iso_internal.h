@@ -18,8 +18,11 @@ constexpr int kRowMax = 8192;
 cudaError_t rows_fit(const float* y, const float* w, int64_t rows, int n, int increasing,
                      float* out, uint8_t* blocks, uint32_t* row_status, cudaStream_t stream);
 
+// Backward: out (may be null) gets d/dy; dw, when not null, gets d/dw from the
+// forward's input y and fit.
 cudaError_t rows_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int n, float* out, cudaStream_t stream);
+                          int n, float* out, const float* y, const float* fit, float* dw,
+                          cudaStream_t stream);
 
 // Long rows (n > kRowMax): chunk hulls, segment-list merge tree, expansion.
 size_t long_fit_workspace(int64_t rows, int64_t n, bool weighted);
@@ -29,6 +32,7 @@ cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, in
 
 size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted);
 cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int64_t n, float* out, void* ws, size_t ws_bytes, cudaStream_t stream);
+                          int64_t n, float* out, const float* y, const float* fit, float* dw,
+                          void* ws, size_t ws_bytes, cudaStream_t stream);
 
 }  // namespace isodev

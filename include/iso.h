@@ -121,6 +121,35 @@ iso_status iso_backward(const float *grad, const uint8_t *blocks, const float *w
                         void *stream);
 
 /*
+ * iso_backward_w -- the vector-Jacobian products of the fit with respect to y
+ * and to the weights w.
+ *
+ * The paper's Section 6 "Gradient": on element i's block, with G and W the
+ * sums of grad and of w over the block and z_i the block's weighted mean (the
+ * fit), d/dy_i = w_i * G / W and d/dw_i = (y_i - z_i) * G / W.  The same
+ * formulas hold for increasing and decreasing fits.
+ *
+ *  grad       [rows, n] float32, device: gradient with respect to the fit.
+ *  blocks     [rows, n] uint8, device: block starts as written by iso_fit.
+ *  w          [rows, n] float32 or NULL (unit weights), as given to iso_fit.
+ *  y          [rows, n] float32, device: the input given to iso_fit.
+ *  fit        [rows, n] float32, device: the fit iso_fit wrote.
+ *  out_dy     [rows, n] float32, device, written; may be NULL (not wanted).
+ *  out_dw     [rows, n] float32, device, written.
+ *  workspace  as for iso_backward, of iso_backward_workspace_bytes(rows, n,
+ *             w != NULL) bytes.
+ *  stream     cudaStream_t.
+ *
+ * Errors: ISO_ERR_INVALID_ARG for a NULL grad, blocks, y, fit or out_dw or a
+ * bad shape, ISO_ERR_WORKSPACE as for iso_backward, ISO_ERR_CUDA for a launch
+ * failure.  A row whose forward pass was rejected (its fit is NaN) gets NaN.
+ */
+iso_status iso_backward_w(const float *grad, const uint8_t *blocks, const float *w,
+                          const float *y, const float *fit, int64_t rows, int64_t n,
+                          float *out_dy, float *out_dw, void *workspace, size_t workspace_bytes,
+                          void *stream);
+
+/*
  * iso_backward_noalloc -- iso_backward for callers that cannot allocate device
  * memory (no counterpart in the paper: it is an interface addition).
  *

@@ -90,3 +90,94 @@ def test_host_tensors_round_trip(cuda_ok):
     assert not z.is_cuda
     zo, _, _ = oracle.pava(y.numpy())
     assert np.abs(z.numpy() - zo).max() <= 1e-5 * (1 + np.abs(y.numpy()).max())
+
+
+# ---- the weight gradient, d/dw_i = (y_i - z_i) G / W (paper Section 6, "Gradient") ----
+def run_w(y, w, g, increasing=True):
+    import torch
+    import convex_hull_pava_gb300 as chp
+    yt = torch.from_numpy(np.ascontiguousarray(y)).cuda()
+    wt = None if w is None else torch.from_numpy(np.ascontiguousarray(w)).cuda()
+    gt = torch.from_numpy(np.ascontiguousarray(g)).cuda()
+    z, blocks, _ = chp.iso_fit(yt, wt, increasing)
+    dy, dw = chp.iso_backward_w(gt, blocks, wt, yt, z)
+    torch.cuda.synchronize()
+    return blocks.cpu().numpy(), z.cpu().numpy(), dy.cpu().numpy(), dw.cpu().numpy()
+
+
+def check_w(y, w, g, increasing=True, label=""):
+    """Both gradients against the oracle, over the CUDA forward's blocks and fit
+    (the weight gradient's formula takes the fit as given)."""
+    blocks, z, dy, dw = run_w(y, w, g, increasing)
+    ref_dy = oracle.backward(g, blocks, w)
+    for r in range(y.shape[0]):
+        wr = None if w is None else w[r]
+        ref = oracle.backward_w(g[r], blocks[r], wr, y[r], z[r].astype(np.float64))
+        err = np.abs(dw[r].astype(np.float64) - ref)
+        assert err.max() <= TOL * (1.0 + np.abs(ref).max()), f"{label} row {r}: dw err {err.max():.3e}"
+        e2 = np.abs(dy[r].astype(np.float64) - ref_dy[r])
+        assert e2.max() <= TOL * (1.0 + np.abs(ref_dy[r]).max()), f"{label} row {r}: dy err {e2.max():.3e}"
+    return blocks, z, dy, dw
+
+
+@pytest.mark.parametrize("n", [1, 2, 33, 1000, 4096, 8192])
+@pytest.mark.parametrize("weighting", ["none", "uniform", "extreme"])
+def test_weight_gradient_rows(cuda_ok, n, weighting):
+    rows = 7
+    y = wl.noisy_ramp(rows, n, seed=n + 7)
+    w = wl.weights(weighting, rows, n, seed=n + 7)
+    g = wl.normal((rows, n), seed=n + 8)
+    for inc in (True, False):
+        check_w(y, w, g, inc, f"dw rows n={n} {weighting} inc={inc}")
+
+
+@pytest.mark.parametrize("n", [8193, 100003])
+@pytest.mark.parametrize("fam", ["noise", "increasing", "sawtooth"])
+@pytest.mark.parametrize("weighting", ["none", "uniform", "extreme"])
+def test_weight_gradient_long_rows(cuda_ok, n, fam, weighting):
+    y = wl.family(fam, 2, n, seed=13)
+    w = wl.weights(weighting, 2, n, seed=13)
+    g = wl.normal((2, n), seed=14)
+    for inc in (True, False):
+        check_w(y, w, g, inc, f"dw long n={n} {fam} {weighting} inc={inc}")
+
+
+def test_weight_gradient_sums_to_zero_on_each_block(cuda_ok):
+    """sum_B (y_i - z_i) = 0 for unit weights (z is the block mean), so the unit
+    weight gradient sums to zero over every block."""
+    y = wl.noisy_ramp(3, 20000, 21)
+    g = wl.normal((3, 20000), 22)
+    blocks, z, dy, dw = check_w(y, None, g, True, "dw block sums")
+    for r in range(3):
+        ids = np.cumsum(blocks[r].astype(np.int64)) - 1
+        sums = np.bincount(ids, weights=dw[r].astype(np.float64))
+        assert np.abs(sums).max() <= 1e-3 * (1 + np.abs(dw[r]).max())
+
+
+def test_weight_gradient_bad_row_is_nan(cuda_ok):
+    y = wl.noisy_ramp(3, 5000, 23)
+    y[1, 17] = np.nan
+    w = wl.weights("uniform", 3, 5000, 23)
+    g = wl.normal((3, 5000), 24)
+    blocks, z, dy, dw = run_w(y, w, g)
+    assert np.isnan(dw[1]).all()
+    assert np.isfinite(dw[[0, 2]]).all()
+
+
+def test_autograd_weight_gradient(cuda_ok):
+    import torch
+    import convex_hull_pava_gb300 as chp
+    y0 = wl.noisy_ramp(2, 9000, 25)
+    w0 = wl.weights("uniform", 2, 9000, 25)
+    y = torch.from_numpy(y0).cuda().requires_grad_(True)
+    w = torch.from_numpy(w0).cuda().requires_grad_(True)
+    z = chp.isotonic(y, w)
+    g = torch.randn_like(z)
+    z.backward(g)
+    zt, blocks, _ = chp.iso_fit(y.detach(), w.detach())
+    gn, bn, zn = g.cpu().numpy(), blocks.cpu().numpy(), zt.cpu().numpy().astype(np.float64)
+    for r in range(2):
+        ref = oracle.backward_w(gn[r], bn[r], w0[r], y0[r], zn[r])
+        assert np.abs(w.grad[r].cpu().numpy() - ref).max() <= TOL * (1 + np.abs(ref).max())
+    ref_dy = oracle.backward(gn, bn, w0)
+    assert np.abs(y.grad.cpu().numpy() - ref_dy).max() <= TOL * (1 + np.abs(ref_dy).max())
