@@ -356,6 +356,26 @@ def run_gpu(args):
                                    "gbs": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak}
             also[name] = rec
             del yv, wv, ov, bv, wsv
+        # the soft rank end to end (sort, non-increasing fit, gather; backward
+        # through the block averaging), 1,024 rows x 8,192 N(0,1) values
+        from convex_hull_pava_gb300.soft_rank import soft_rank
+        xs = torch.from_numpy(wl.normal((1024, 8192), 31)).to(dev)
+        gs = torch.from_numpy(wl.normal((1024, 8192), 32)).to(dev)
+        sr = {}
+        for tag, eps in (("eps_1", 1.0), ("eps_1_over_n", 1.0 / 8192)):
+            ts = []
+            for i in range(13):
+                flush.zero_()
+                x = xs.clone().requires_grad_(True)
+                a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                soft_rank(x, eps).backward(gs)
+                b.record(stream); b.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(b))
+            t = float(np.median(ts)) * 1e-3
+            sr[tag] = {"ms_fwd_bwd": t * 1e3, "elements_per_s": xs.numel() / t}
+        also["soft_rank_1024x8192"] = sr
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -337,3 +337,39 @@ def test_bad_rows_flagged():
     z, _, st = oracle.pava(y, w)
     assert list(st) == [0, oracle.BAD_Y, oracle.BAD_W]
     assert np.isnan(z[1]).all() and np.isnan(z[2]).all() and np.isfinite(z[0]).all()
+
+
+# ---- the soft rank composition (Section 7.9) on the oracle ----
+def test_soft_rank_composition_finite_differences():
+    """d/dx of the host soft rank is (g_s - A g_s) back through the sort, / eps
+    (A: block averaging over the fit's blocks), by fp64 finite differences on a
+    small row whose fit has no near-ties."""
+    from soft_rank_ref import ref_soft_rank
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 12)) * 3
+    eps = 0.7
+    g = rng.standard_normal(12)
+
+    def f(v):
+        r, _, _ = ref_soft_rank(v, eps)
+        return float((r[0] * g).sum())
+    _, blocks, perms = ref_soft_rank(x, eps)
+    gs = g[perms[0]]
+    gs = gs - oracle.backward(gs[None, :].astype(np.float32), blocks)[0]
+    an = np.empty(12)
+    an[perms[0]] = gs / eps
+    h = 1e-3
+    for i in range(12):
+        d = np.zeros((1, 12))
+        d[0, i] = h
+        fd = (f(x + d) - f(x - d)) / (2 * h)
+        assert abs(fd - an[i]) <= 2e-2 * (1 + abs(an[i]))
+
+
+def test_soft_rank_composition_small_eps_is_hard_rank():
+    from soft_rank_ref import ref_soft_rank
+    x = np.random.default_rng(4).standard_normal((3, 50))
+    r, _, _ = ref_soft_rank(x, 1e-6)
+    hard = np.argsort(np.argsort(x, axis=1), axis=1) + 1
+    assert np.abs(r - hard).max() <= 1e-3
+
