@@ -395,6 +395,34 @@ __device__ __forceinline__ Move merge_plan(const MView<WEIGHTED, SMEM>& V, int j
     return Move{a.k + 1, b.k, len};
 }
 
+// Exclusive block-wide scan of one int per thread (blockDim.x <= 1024, a
+// multiple of 32); total: the block's sum.
+__device__ __forceinline__ int block_excl_scan_int(int v, int* tmp, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(kFull, x, d);
+        if (lane >= d) x += o;
+    }
+    if (lane == 31) tmp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(kFull, t, d);
+            if (lane >= d) t += o;
+        }
+        if (lane < nw) tmp[lane] = t;
+    }
+    __syncthreads();
+    const int base = warp ? tmp[warp - 1] : 0;
+    total = tmp[nw - 1];
+    __syncthreads();
+    return base + x - v;
+}
+
 // Exclusive block-wide scan of (S, W, H) per thread (blockDim.x <= 1024, a
 // multiple of 32); also returns the block totals.
 struct Acc3 { i128 s, w; int64_t h; };
@@ -786,18 +814,30 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
     }
     merge_levels<WEIGHTED, SMEM>(V, 0, m, kGroup);
 
-    // ---- ends: each chunk's root segment, and the root vertices around it ----
+    // ---- ends: each chunk's root segment, and the root vertices around it.
+    // With c(j) the number of root segments of chunks <= j (a scan of "chunk j
+    // holds one"), the first after chunk j is c(j) and the last before it is
+    // c(j) - [j holds one] - 1. ----
     const int4* seg = V.seg;
     const int nroot = V.cnt[0];
     for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
     __syncthreads();
-    for (int k = tid; k < nroot; k += nth) {
-        const int cj = seg[k].x;
-        segOf[cj] = k;
-        const int cprev = k > 0 ? seg[k - 1].x : -1;
-        const int cnext = k + 1 < nroot ? seg[k + 1].x : (int)m;
-        for (int q = max(cprev, 0); q < cj; ++q) nextSeg[q] = k;   // chunks in [cprev, cj)
-        for (int q = cj + 1; q <= min(cnext, (int)m - 1); ++q) prevSeg[q] = k;
+    for (int k = tid; k < nroot; k += nth) segOf[seg[k].x] = k;
+    __syncthreads();
+    {
+        __shared__ int s_tmp2[32];
+        const int64_t per2 = (m + nth - 1) / nth;
+        const int64_t jb2 = imin64(m, tid * per2), je2 = imin64(m, jb2 + per2);
+        int c = 0;
+        for (int64_t j = jb2; j < je2; ++j) c += segOf[j] >= 0 ? 1 : 0;
+        int tot2;
+        c = block_excl_scan_int(c, s_tmp2, tot2);
+        for (int64_t j = jb2; j < je2; ++j) {
+            const int has = segOf[j] >= 0 ? 1 : 0;
+            c += has;
+            nextSeg[j] = c;                 // first root segment of a chunk > j
+            prevSeg[j] = c - has - 1;       // last root segment of a chunk < j
+        }
     }
     __syncthreads();
     for (int64_t j = tid; j < m; j += nth) {
@@ -846,18 +886,21 @@ merge_top_kernel(int64_t m, LongWs ws) {
         }
     }
     __syncthreads();
-    Acc3 carry{0, 0, 0};
-    for (int64_t q0 = 0; q0 < m; q0 += nth) {
-        const int64_t j = q0 + tid;
-        Acc3 v{0, 0, j < m ? (int64_t)len[j] : 0};
-        Acc3 tot;
-        const Acc3 e = block_excl_scan3(v, s_scan, tot);
-        __syncthreads();
-        if (j < m) len[j] = (int32_t)(carry.h + e.h);     // now the base of chunk j
-        carry.h += tot.h;
+    // bases: each thread scans a contiguous range of chunks
+    __shared__ int s_tmp[32];
+    const int64_t per = (m + nth - 1) / nth;
+    const int64_t jb = imin64(m, tid * per), je = imin64(m, jb + per);
+    int sum = 0;
+    for (int64_t j = jb; j < je; ++j) sum += len[j];
+    int total;
+    int base = block_excl_scan_int(sum, s_tmp, total);
+    for (int64_t j = jb; j < je; ++j) {
+        const int l = len[j];
+        len[j] = base;                                     // now the base of chunk j
+        base += l;
     }
     __syncthreads();
-    const int64_t Hs = carry.h;
+    const int64_t Hs = total;
     if (MergeLayout(m, Hs, WEIGHTED, true).bytes <= (size_t)kMergeSmem)
         merge_top<WEIGHTED, true>(m, ws, c0, Hs, len, lo0);
     else
