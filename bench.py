@@ -376,6 +376,34 @@ def run_gpu(args):
             t = float(np.median(ts)) * 1e-3
             sr[tag] = {"ms_fwd_bwd": t * 1e3, "elements_per_s": xs.numel() / t}
         also["soft_rank_1024x8192"] = sr
+        # a ragged batch of calibration curves: 65,536 segments of 1 to 8,192
+        # points (log-uniform) and 8 of about 2^20, weighted, end to end
+        lens = wl.ragged_lengths(65_536, 8192, seed=0, long_segments=8, long_len=1 << 20)
+        yr_h, wr_h, off_h = wl.ragged_calibration(lens, seed=0)
+        yr = torch.from_numpy(yr_h).to(dev)
+        wr = torch.from_numpy(wr_h).to(dev)
+        offr = torch.from_numpy(off_h).to(dev)
+        orr = torch.empty_like(yr)
+        br = torch.empty(yr.shape, dtype=torch.uint8, device=dev)
+        wsr = torch.empty(chp.iso_fit_ragged_workspace_bytes(lens.size, yr.numel(), int(lens.max()), True),
+                          dtype=torch.uint8, device=dev)
+        ts = []
+        for i in range(13):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            chp.iso_fit_ragged(yr, offr, wr, True, max_len=int(lens.max()), out=orr, blocks=br,
+                               workspace=wsr, stream=stream)
+            b.record(stream); b.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        t = float(np.median(ts)) * 1e-3
+        by = yr.numel() * 13 + off_h.nbytes
+        also["ragged_calibration_65544"] = {
+            "segments": int(lens.size), "elements": int(yr.numel()),
+            "elements_per_s": yr.numel() / t, "ms": t * 1e3, "gbs": by / t / 1e9,
+            "frac": by / t / 1e9 / hbm_peak, "bytes": by}
+        del yr, wr, offr, orr, br, wsr
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -10,9 +10,13 @@ Entry points (same names as the C ABI):
 
 * :func:`iso_fit` -- forward fit of ``[rows, n]`` float32 CUDA tensors.
 * :func:`iso_backward` -- block-averaging backward.
-* :func:`iso_fit_workspace_bytes`, :func:`iso_backward_workspace_bytes`.
+* :func:`iso_fit_ragged` -- forward fit of segments of unequal lengths laid
+  end to end (int64 offsets on the device).
+* :func:`iso_fit_workspace_bytes`, :func:`iso_backward_workspace_bytes`,
+  :func:`iso_fit_ragged_workspace_bytes`.
 * :func:`isotonic` -- differentiable convenience op (autograd), which also
-  accepts host tensors (copied to the GPU and back).
+  accepts host tensors (copied to the GPU and back); :func:`isotonic_ragged`,
+  its counterpart for a ragged batch.
 """
 from __future__ import annotations
 
@@ -30,10 +34,12 @@ ISO_ERR_CUDA = -3
 ISO_ERR_TIMEOUT = -4
 ISO_ROW_BAD_Y = 1
 ISO_ROW_BAD_W = 2
+ISO_ROW_BAD_SHAPE = 4
 
 EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
            "iso_backward_workspace_bytes", "iso_backward", "iso_backward_w",
-           "iso_backward_noalloc", "iso_profile_enable", "iso_profile_read")
+           "iso_backward_noalloc", "iso_fit_ragged_workspace_bytes", "iso_fit_ragged",
+           "iso_profile_enable", "iso_profile_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -73,6 +79,10 @@ def load_library(path: str | None = None):
         lib.iso_backward_w.restype = ci
         lib.iso_backward_noalloc.argtypes = [vp, vp, vp, i64, i64, vp, vp]
         lib.iso_backward_noalloc.restype = ci
+        lib.iso_fit_ragged_workspace_bytes.argtypes = [i64, i64, i64, ci]
+        lib.iso_fit_ragged_workspace_bytes.restype = sz
+        lib.iso_fit_ragged.argtypes = [vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, sz, vp, vp]
+        lib.iso_fit_ragged.restype = ci
         lib.iso_profile_enable.argtypes = [ci]
         lib.iso_profile_enable.restype = ci
         lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
@@ -92,6 +102,11 @@ def iso_fit_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
 
 def iso_backward_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
     return int(load_library().iso_backward_workspace_bytes(int(rows), int(n), int(bool(weighted))))
+
+
+def iso_fit_ragged_workspace_bytes(segments: int, total: int, max_len: int, weighted: bool) -> int:
+    return int(load_library().iso_fit_ragged_workspace_bytes(int(segments), int(total),
+                                                             int(max_len), int(bool(weighted))))
 
 
 def profile_enable(on: bool = True) -> None:
@@ -178,6 +193,43 @@ def iso_fit(y, w=None, increasing: bool = True, *, out=None, blocks=None, want_b
         None if ws is None else ws.data_ptr(), ws_bytes, row_status.data_ptr(), _stream_ptr(stream))
     if st != ISO_OK:
         raise IsoError(st, "iso_fit")
+    return out, blocks, row_status
+
+
+def iso_fit_ragged(y, offsets, w=None, increasing: bool = True, *, max_len: int = 0, out=None,
+                   blocks=None, want_blocks: bool = True, row_status=None, workspace=None,
+                   stream=None):
+    """Fit each segment ``y[offsets[s]:offsets[s+1]]`` of a 1-D float32 CUDA
+    tensor as its own row.  ``offsets``: int64 CUDA tensor of ``segments + 1``
+    entries (not read by the host).  ``max_len``: an upper bound on the
+    segments' lengths, or 0 for none; a longer segment is rejected
+    (``ISO_ROW_BAD_SHAPE`` in its status word).  Returns ``(out, blocks,
+    row_status)``, ``row_status`` one word per segment."""
+    torch = _torch()
+    _check_dev(y, "y", torch.float32)
+    _check_dev(offsets, "offsets", torch.int64)
+    if y.dim() != 1 or offsets.dim() != 1 or offsets.numel() < 2:
+        raise ValueError("expected a 1-D y and at least two offsets")
+    total, segments = y.numel(), offsets.numel() - 1
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+        if w.shape != y.shape:
+            raise ValueError("w must have the shape of y")
+    if out is None:
+        out = torch.empty_like(y)
+    if blocks is None and want_blocks:
+        blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+    if row_status is None:
+        row_status = torch.empty(segments, dtype=torch.int32, device=y.device)
+    nbytes = iso_fit_ragged_workspace_bytes(segments, total, max_len, w is not None)
+    ws, ws_bytes = _workspace(nbytes, workspace, y.device)
+    st = load_library().iso_fit_ragged(
+        y.data_ptr(), None if w is None else w.data_ptr(), offsets.data_ptr(), segments, total,
+        int(max_len), int(bool(increasing)), out.data_ptr(),
+        None if blocks is None else blocks.data_ptr(), None if ws is None else ws.data_ptr(),
+        ws_bytes, row_status.data_ptr(), _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_fit_ragged")
     return out, blocks, row_status
 
 
@@ -271,20 +323,41 @@ def _make_function():
                 return gy, gw, None
             return iso_backward(g, blocks, w), None, None
 
-    return _Isotonic
+    class _IsotonicRagged(torch.autograd.Function):
+        # Every segment's first element starts a block, so the backward of the
+        # whole array as one row is each segment's own backward.
+        @staticmethod
+        def forward(ctx, y, offsets, w, increasing, max_len):
+            y = y.contiguous()
+            w = None if w is None else w.contiguous()
+            out, blocks, _ = iso_fit_ragged(y, offsets, w, increasing, max_len=max_len)
+            ctx.save_for_backward(blocks, w, y, out)
+            return out
+
+        @staticmethod
+        def backward(ctx, g):
+            blocks, w, y, out = ctx.saved_tensors
+            g = g.contiguous()
+            if w is not None and ctx.needs_input_grad[2]:
+                gy, gw = iso_backward_w(g, blocks, w, y, out, want_dy=ctx.needs_input_grad[0])
+                return gy, None, gw, None, None
+            return iso_backward(g, blocks, w), None, None, None, None
+
+    return _Isotonic, _IsotonicRagged
 
 
 _Fn = None
+_FnRagged = None
 
 
 def isotonic(y, w=None, increasing: bool = True):
     """Differentiable isotonic regression of each row of ``y`` (gradients with
     respect to ``y`` and, when it requires one, to ``w``).  Host tensors are
     copied to the current CUDA device and the result is copied back."""
-    global _Fn
+    global _Fn, _FnRagged
     torch = _torch()
     if _Fn is None:
-        _Fn = _make_function()
+        _Fn, _FnRagged = _make_function()
     host = not y.is_cuda
     if host:
         dev = torch.device("cuda", torch.cuda.current_device())
@@ -294,3 +367,14 @@ def isotonic(y, w=None, increasing: bool = True):
     if host:
         z = z.to("cpu")
     return z
+
+
+def isotonic_ragged(y, offsets, w=None, increasing: bool = True, max_len: int = 0):
+    """Differentiable fit of each segment ``y[offsets[s]:offsets[s+1]]`` of a
+    1-D CUDA tensor (gradients with respect to ``y`` and, when it requires one,
+    to ``w``).  The backward assumes the segments cover ``y`` end to end
+    (``offsets[0] == 0``, ``offsets[-1] == len(y)``, non-decreasing)."""
+    global _Fn, _FnRagged
+    if _FnRagged is None:
+        _Fn, _FnRagged = _make_function()
+    return _FnRagged.apply(y, offsets, w, bool(increasing), int(max_len))

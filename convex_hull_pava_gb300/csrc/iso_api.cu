@@ -83,6 +83,40 @@ iso_status iso_fit(const float* y, const float* w, int64_t rows, int64_t n, int 
                                       workspace_bytes, row_status, st));
 }
 
+namespace {
+bool ragged_ok(int64_t segments, int64_t total, int64_t max_len) {
+    return segments >= 1 && segments <= kMaxN && total >= 1 && total <= kMaxElems &&
+           max_len <= kMaxN;
+}
+int64_t ragged_max_len(int64_t total, int64_t max_len) {
+    return max_len <= 0 || max_len > total ? total : max_len;
+}
+}  // namespace
+
+size_t iso_fit_ragged_workspace_bytes(int64_t segments, int64_t total, int64_t max_len,
+                                      int weighted) {
+    if (!ragged_ok(segments, total, max_len)) return 0;
+    return isodev::ragged_workspace(segments, total, ragged_max_len(total, max_len), weighted != 0);
+}
+
+iso_status iso_fit_ragged(const float* y, const float* w, const int64_t* offsets,
+                          int64_t segments, int64_t total, int64_t max_len, int increasing,
+                          float* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
+                          uint32_t* row_status, void* stream) {
+    if (!y || !offsets || !out || !ragged_ok(segments, total, max_len) ||
+        (increasing != 0 && increasing != 1))
+        return ISO_ERR_INVALID_ARG;
+    const int64_t ml = ragged_max_len(total, max_len);
+    if (ml > kMaxN) return ISO_ERR_INVALID_ARG;
+    const size_t need = isodev::ragged_workspace(segments, total, ml, w != nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ISO_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    return from_cuda(isodev::ragged_fit(y, w, offsets, segments, total, ml, increasing, out, blocks,
+                                        workspace, row_status, st));
+}
+
 size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted) {
     if (!shape_ok(rows, n)) return 0;
     if (n <= isodev::kRowMax) return 0;

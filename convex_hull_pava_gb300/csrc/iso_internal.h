@@ -30,6 +30,25 @@ cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, in
                      float* out, uint8_t* blocks, void* ws, size_t ws_bytes, uint32_t* row_status,
                      cudaStream_t stream);
 
+// Ragged batches (iso_ragged.cu): segments laid end to end, offsets on the
+// device.  The segments of each lane class L (n <= 32 L) and the long ones
+// are listed on the device; `count` is the list's length (device), `cap` its
+// capacity.  A grid of at most kRaggedCtas CTAs walks a class's list.
+constexpr int64_t kRaggedCtas = 152 * 16;
+size_t ragged_workspace(int64_t segments, int64_t total, int64_t max_len, bool weighted);
+cudaError_t ragged_fit(const float* y, const float* w, const int64_t* off, int64_t segments,
+                       int64_t total, int64_t max_len, int increasing, float* out,
+                       uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream);
+cudaError_t rows_fit_ragged(const float* y, const float* w, const int64_t* off,
+                            const int32_t* list, const unsigned long long* count, int64_t cap,
+                            int L, int increasing, float* out, uint8_t* blocks,
+                            uint32_t* row_status, cudaStream_t stream);
+size_t long_ragged_workspace(int64_t rows_max, int64_t total, bool weighted);
+cudaError_t long_fit_ragged(const float* y, const float* w, const int64_t* off,
+                            const int32_t* long_id, const unsigned long long* nlong,
+                            int64_t rows_max, int64_t total, int increasing, float* out,
+                            uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream);
+
 size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted);
 cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
                           int64_t n, float* out, const float* y, const float* fit, float* dw,

@@ -9,7 +9,7 @@
 //     bridge by moving its two ends to their tangent points in turn, a few
 //     steps by walking and then by bisection over the list, cuts two segments
 //     and moves the right list's descriptors down.  No vertex is ever copied
-//     between levels.  The first levels run in one CTA per group of 32 chunks,
+//     between levels.  The first levels run in one CTA per group of 64 chunks,
 //     all groups at once; the rest in one CTA per row.  A CTA reads the hull
 //     vertices it needs into shared memory when they fit (noisy rows keep few
 //     vertices), else it reads them from the slots in global memory.  The top
@@ -17,14 +17,21 @@
 //     vertices before and after it (Section 3.4, Corollary 4.5).
 //  3. expand_kernel: one CTA per chunk writes every element's slope and its
 //     block-start byte (Section 3.4).
+//
+// The rows are either a dense [rows, n] batch or the long segments of a ragged
+// batch (LongGeo): the kernels find their row's place from the geometry.
+#include "../../include/iso.h"
 #include "iso_internal.h"
 #include "iso_tile.cuh"
+
+#include <algorithm>
 
 namespace isodev {
 
 namespace {
 
 constexpr int kMergeThreads = 512;
+constexpr int64_t kRaggedTopCtas = 152;  // one top-merge CTA per SM
 constexpr int kMergeSmem = 210 * 1024;    // shared memory of the merge kernel
 
 template <bool WEIGHTED> struct LongCfg;
@@ -74,11 +81,10 @@ struct LongWs {
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Workspace of `rows` long rows holding M chunks in all.
 template <bool WEIGHTED>
-__host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t n, LongWs* ws) {
+__host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t M, LongWs* ws) {
     constexpr int C = LongCfg<WEIGHTED>::C;
-    const int64_t m = (n + C - 1) / C;
-    const int64_t M = rows * m;
     const size_t cap = (size_t)C + 1;
     size_t off = 0;
     char* b = static_cast<char*>(base);
@@ -107,6 +113,32 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t n, Lon
     return off;
 }
 
+// Where the long rows of a call lie.  A dense batch: row r holds elements
+// r*n .. r*n+n-1 and chunks r*m .. r*m+m-1.  A ragged batch (segments of their
+// own lengths laid end to end, see iso_ragged.cu): per-row tables that a plan
+// kernel writes on the device, and the counts of rows, chunks and groups that
+// the grids, sized for the largest possible counts, are checked against.
+struct LongGeo {
+    int64_t n = 0, m = 0;                 // dense: row length, chunks per row
+    const int64_t* e0 = nullptr;          // ragged [rows]: the row's first element (null: dense)
+    const int64_t* len = nullptr;         // [rows]: its length (> kRowMax)
+    const int64_t* c0 = nullptr;          // [rows]: its first chunk
+    const int64_t* g0 = nullptr;          // [rows]: its first group of kGroup chunks
+    const int32_t* id = nullptr;          // [rows]: its segment index
+    const int32_t* chunk_row = nullptr;   // [chunks]: row of each chunk
+    const int32_t* group_row = nullptr;   // [groups]: row of each group
+    const int64_t* count = nullptr;       // [3]: rows, chunks, groups
+};
+
+struct RowRef { int64_t id, e0, n, m, c0; };
+
+template <int C>
+__device__ __forceinline__ RowRef geo_row(const LongGeo& g, int64_t r) {
+    if (!g.e0) return RowRef{r, r * g.n, g.n, g.m, r * g.m};
+    const int64_t n = g.len[r];
+    return RowRef{g.id[r], g.e0[r], n, (n + C - 1) / C, g.c0[r]};
+}
+
 __device__ __forceinline__ bool fits64(i128 x) { return (i128)(int64_t)x == x; }
 
 // A double within 3 ulp of a 128-bit integer (exact below 2^53).
@@ -129,20 +161,18 @@ __device__ __forceinline__ int64_t conv(int64_t x, int d) {
 // 1. chunk hulls
 // ---------------------------------------------------------------------------
 template <bool WEIGHTED>
-__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
-chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t n, int64_t m,
-                  int increasing, LongWs ws) {
+__device__ __forceinline__ void chunk_hull_one(const float* __restrict__ y,
+                                               const float* __restrict__ w, const LongGeo& geo,
+                                               int increasing, const LongWs& ws, int64_t c) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
     extern __shared__ __align__(128) unsigned char smem[];
     using SM = TileSmem<NT, WEIGHTED, false, 1>;
-    const int64_t c = blockIdx.x;
-    const int64_t row = c / m;
-    const int64_t j = c - row * m;
-    const int64_t e0 = j * C;
-    const int nt = (int)imin64(C, n - e0);
-    const float* yr = y + row * n + e0;
-    const float* wr = WEIGHTED ? w + row * n + e0 : nullptr;
+    const RowRef R = geo_row<C>(geo, geo.e0 ? (int64_t)geo.chunk_row[c] : c / geo.m);
+    const int64_t e0 = (c - R.c0) * C;
+    const int nt = (int)imin64(C, R.n - e0);
+    const float* yr = y + R.e0 + e0;
+    const float* wr = WEIGHTED ? w + R.e0 + e0 : nullptr;
 
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, false, 1>(yr, wr, nt, true, !increasing, NT, smem, H);
@@ -173,6 +203,23 @@ chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, int6
         mt.totS = H.T.LS[NT];
         mt.totW = WEIGHTED ? H.T.LW[NT] : (int64_t)nt;
         ws.meta[c] = mt;
+    }
+}
+
+// One CTA per chunk; a ragged batch's grid is bounded and its CTAs take the
+// chunks in turn.
+template <bool WEIGHTED, bool RAGGED>
+__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
+chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, LongGeo geo,
+                  int increasing, LongWs ws) {
+    if (!RAGGED) {
+        chunk_hull_one<WEIGHTED>(y, w, geo, increasing, ws, blockIdx.x);
+        return;
+    }
+    const int64_t M = geo.count[1];
+    for (int64_t c = blockIdx.x; c < M; c += gridDim.x) {
+        chunk_hull_one<WEIGHTED>(y, w, geo, increasing, ws, c);
+        __syncthreads();   // shared memory is reused by the next chunk
     }
 }
 
@@ -682,23 +729,26 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
 }
 
 template <bool WEIGHTED>
-__global__ void __launch_bounds__(kGroupThreads)
-merge_groups_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
+__device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, const LongWs& ws,
+                                                uint32_t* __restrict__ row_status, int64_t g) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
     __shared__ Acc3 s_scan[32];
     __shared__ int s_red[3];
     __shared__ i128 s_part[2][kGroupThreads / 32];
     __shared__ i128 s_gS[kGroup], s_gW[kGroup];
     __shared__ int32_t s_gH[kGroup];
     __shared__ long long s_Hg;
-    const int64_t row = blockIdx.x;
-    const int64_t c0 = row * m;
-    const int jb = blockIdx.y * kGroup;
+    const int64_t row = geo.e0 ? (int64_t)geo.group_row[g] : g / ng;
+    const RowRef R = geo_row<C>(geo, row);
+    const int64_t m = R.m, c0 = R.c0;
+    const int64_t gi = g - (geo.e0 ? geo.g0[row] : row * ng);
+    const int jb = (int)gi * kGroup;
     const int je = (int)imin64(jb + kGroup, m);
     const int tid = threadIdx.x, nth = blockDim.x;
     const RowQ q = row_quanta(m, ws, c0, s_red);
-    if (blockIdx.y == 0 && tid == 0) {
+    if (gi == 0 && tid == 0) {
         ws.rowq[row * 4 + 0] = q.qs; ws.rowq[row * 4 + 1] = q.qw; ws.rowq[row * 4 + 2] = q.bad;
-        if (row_status) row_status[row] = (uint32_t)q.bad;
+        if (row_status) row_status[R.id] = (uint32_t)q.bad;
     }
     if (q.bad) {
         for (int j = jb + tid; j < je; j += nth) {
@@ -757,6 +807,20 @@ merge_groups_kernel(int64_t m, LongWs ws, uint32_t* __restrict__ row_status) {
         merge_group<WEIGHTED, true>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
     else
         merge_group<WEIGHTED, false>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
+}
+
+template <bool WEIGHTED, bool RAGGED>
+__global__ void __launch_bounds__(kGroupThreads)
+merge_groups_kernel(LongGeo geo, int64_t ng, LongWs ws, uint32_t* __restrict__ row_status) {
+    if (!RAGGED) {
+        merge_group_one<WEIGHTED>(geo, ng, ws, row_status, blockIdx.x);
+        return;
+    }
+    const int64_t G = geo.count[2];
+    for (int64_t g = blockIdx.x; g < G; g += gridDim.x) {
+        merge_group_one<WEIGHTED>(geo, ng, ws, row_status, g);
+        __syncthreads();
+    }
 }
 
 template <bool WEIGHTED, bool SMEM>
@@ -864,11 +928,10 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
 }
 
 template <bool WEIGHTED>
-__global__ void __launch_bounds__(kMergeThreads, 1)
-merge_top_kernel(int64_t m, LongWs ws) {
-    __shared__ Acc3 s_scan[32];
-    const int64_t row = blockIdx.x;
-    const int64_t c0 = row * m;
+__device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& ws, int64_t row) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const RowRef R = geo_row<C>(geo, row);
+    const int64_t m = R.m, c0 = R.c0;
     const int tid = threadIdx.x, nth = blockDim.x;
     if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
     // the chunks' surviving segments (each chunk in at most one): lengths into
@@ -907,6 +970,20 @@ merge_top_kernel(int64_t m, LongWs ws) {
         merge_top<WEIGHTED, false>(m, ws, c0, Hs, len, lo0);
 }
 
+template <bool WEIGHTED, bool RAGGED>
+__global__ void __launch_bounds__(kMergeThreads, 1)
+merge_top_kernel(LongGeo geo, LongWs ws) {
+    if (!RAGGED) {
+        merge_top_row<WEIGHTED>(geo, ws, blockIdx.x);
+        return;
+    }
+    const int64_t rows = geo.count[0];
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        merge_top_row<WEIGHTED>(geo, ws, row);
+        __syncthreads();
+    }
+}
+
 // ---------------------------------------------------------------------------
 // 3. expansion: each element gets the slope of the root-hull edge above it
 // ---------------------------------------------------------------------------
@@ -921,9 +998,10 @@ struct ExpandSmem {
 };
 
 template <bool WEIGHTED>
-__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
-expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing, LongWs ws,
-              float* __restrict__ out, uint8_t* __restrict__ blocks) {
+__device__ __forceinline__ void expand_one(const float* __restrict__ y, const LongGeo& geo,
+                                           int increasing, const LongWs& ws,
+                                           float* __restrict__ out, uint8_t* __restrict__ blocks,
+                                           int64_t c) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
     using XS = ExpandSmem<WEIGHTED>;
@@ -932,22 +1010,24 @@ expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing,
     int64_t* s_tmp = reinterpret_cast<int64_t*>(smem + XS::oTmp);
     float* slope = reinterpret_cast<float*>(smem + XS::oSlope);   // per point, swizzled rows
 
-    const int64_t c = blockIdx.x;
-    const int64_t row = c / m;
-    const int64_t j = c - row * m;
-    const int64_t e0 = j * C;
-    const int nt = (int)imin64(C, n - e0);
+    const int64_t row = geo.e0 ? (int64_t)geo.chunk_row[c] : c / geo.m;
+    const RowRef R = geo_row<C>(geo, row);
+    const int64_t e0 = (c - R.c0) * C;
+    const int nt = (int)imin64(C, R.n - e0);
     const int tid = threadIdx.x;
     const ChunkEnds ce = ws.ends[c];
-    float* orow = out + row * n + e0;
-    uint8_t* brow = blocks ? blocks + row * n + e0 : nullptr;
+    float* orow = out + R.e0 + e0;
+    uint8_t* brow = blocks ? blocks + R.e0 + e0 : nullptr;
     const bool neg = !increasing;
 
     if (ce.bad) {
+        // a rejected row: NaN fit; its block flags are 0, but a ragged
+        // segment keeps its first element a block start
         const float qnan = __int_as_float(0x7fffffff);
+        const bool mark0 = geo.e0 && e0 == 0;
         for (int i = tid; i < nt; i += NT) {
             orow[i] = qnan;
-            if (brow) brow[i] = 0;
+            if (brow) brow[i] = (mark0 && i == 0) ? 1 : 0;
         }
         return;
     }
@@ -960,7 +1040,7 @@ expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing,
     // element's mean; for a decreasing fit the negations cancel).
     if (ce.lo <= ce.hi && ce.hi - ce.lo + sp[ce.lo] == nt && sp[ce.hi] == nt &&
         (sp[ce.lo] == 0 || (sp[ce.lo] == 1 && ce.pt0_vertex))) {
-        const float* yrow = y + row * n + e0;
+        const float* yrow = y + R.e0 + e0;
         if ((reinterpret_cast<uintptr_t>(yrow) & 15u) == 0 &&
             (reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
             const int n4 = nt >> 2;
@@ -1031,7 +1111,7 @@ expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing,
         // the edge entering the chunk: from the previous root vertex to the first
         // root vertex of the chunk, or to the next root vertex if the chunk has none
         float in_sl = 0.0f;
-        if (j > 0) {
+        if (e0 > 0) {
             i128 Wb, Sb;
             if (has) vrow(ce.lo, Wb, Sb);
             else { Wb = ce.nextW; Sb = ce.nextS; }
@@ -1105,51 +1185,187 @@ expand_kernel(const float* __restrict__ y, int64_t n, int64_t m, int increasing,
     }
 }
 
+template <bool WEIGHTED, bool RAGGED>
+__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
+expand_kernel(const float* __restrict__ y, LongGeo geo, int increasing, LongWs ws,
+              float* __restrict__ out, uint8_t* __restrict__ blocks) {
+    if (!RAGGED) {
+        expand_one<WEIGHTED>(y, geo, increasing, ws, out, blocks, blockIdx.x);
+        return;
+    }
+    const int64_t M = geo.count[1];
+    for (int64_t c = blockIdx.x; c < M; c += gridDim.x) {
+        expand_one<WEIGHTED>(y, geo, increasing, ws, out, blocks, c);
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 4. ragged batches: the long segments' tables
+// ---------------------------------------------------------------------------
+// Per-row tables of the long segments of a ragged batch, then the chunk and
+// group maps.  One CTA: the long segments are listed (in any order) by the
+// classification kernel, at most total / (kRowMax + 1) of them, and their
+// chunks and groups fit the bounds the grids were sized for.  (Only
+// overlapping segments, which the offsets' checks let through when a rejected
+// segment lies between them, could exceed the bounds: the rows past the
+// bounds are then rejected with ISO_ROW_BAD_SHAPE.)
+template <int C>
+__global__ void __launch_bounds__(1024)
+long_plan_kernel(const int64_t* __restrict__ off, const int32_t* __restrict__ long_id,
+                 const unsigned long long* __restrict__ nlong, int64_t rows_cap,
+                 int64_t chunks_cap, int64_t groups_cap, LongGeo geo,
+                 uint32_t* __restrict__ row_status) {
+    __shared__ Acc3 s_scan[32];
+    __shared__ unsigned long long s_keep;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    int64_t nL = (int64_t)min((unsigned long long)rows_cap, *nlong);
+    if (tid == 0) s_keep = (unsigned long long)nL;
+    int64_t* e0 = const_cast<int64_t*>(geo.e0);
+    int64_t* len = const_cast<int64_t*>(geo.len);
+    int64_t* c0 = const_cast<int64_t*>(geo.c0);
+    int64_t* g0 = const_cast<int64_t*>(geo.g0);
+    int32_t* id = const_cast<int32_t*>(geo.id);
+    int64_t carryC = 0, carryG = 0;
+    for (int64_t b = 0; b < nL; b += nth) {
+        const int64_t r = b + tid;
+        Acc3 v{0, 0, 0};
+        if (r < nL) {
+            const int32_t s = long_id[r];
+            const int64_t a = off[s], n = off[s + 1] - a;
+            const int64_t m = (n + C - 1) / C;
+            e0[r] = a; len[r] = n; id[r] = s;
+            v.s = m; v.w = (m + kGroup - 1) / kGroup;
+        }
+        Acc3 tot;
+        const Acc3 e = block_excl_scan3(v, s_scan, tot);
+        if (r < nL) {
+            c0[r] = carryC + (int64_t)e.s;
+            g0[r] = carryG + (int64_t)e.w;
+            if (c0[r] + (int64_t)v.s > chunks_cap || g0[r] + (int64_t)v.w > groups_cap)
+                atomicMin(&s_keep, (unsigned long long)r);
+        }
+        carryC += (int64_t)tot.s;
+        carryG += (int64_t)tot.w;
+    }
+    __syncthreads();   // the tables are written
+    const int64_t keep = (int64_t)s_keep;
+    for (int64_t r = keep + tid; r < nL; r += nth)
+        if (row_status) row_status[id[r]] = ISO_ROW_BAD_SHAPE;
+    nL = keep;
+    if (tid == 0) {
+        int64_t* cnt = const_cast<int64_t*>(geo.count);
+        cnt[0] = nL;
+        cnt[1] = nL > 0 ? c0[nL - 1] + (len[nL - 1] + C - 1) / C : 0;
+        cnt[2] = nL > 0 ? g0[nL - 1] + ((len[nL - 1] + C - 1) / C + kGroup - 1) / kGroup : 0;
+    }
+    // fill the maps, one warp per row
+    int32_t* crow = const_cast<int32_t*>(geo.chunk_row);
+    int32_t* grow = const_cast<int32_t*>(geo.group_row);
+    for (int64_t r = tid >> 5; r < nL; r += nth >> 5) {
+        const int64_t m = (len[r] + C - 1) / C, gm = (m + kGroup - 1) / kGroup;
+        for (int64_t k = tid & 31; k < m; k += 32) crow[c0[r] + k] = (int32_t)r;
+        for (int64_t k = tid & 31; k < gm; k += 32) grow[g0[r] + k] = (int32_t)r;
+    }
+}
+
+// Launch sizes: exact counts for a dense batch, bounds for a ragged one.
+struct LongGrid { int64_t rows, chunks, groups, ng; };
+
+template <bool WEIGHTED, bool RAGGED>
+static cudaError_t long_launch(const float* y, const float* w, const LongGeo& geo,
+                               const LongGrid& gr, int increasing, float* out, uint8_t* blocks,
+                               const LongWs& ws, uint32_t* row_status, cudaStream_t stream) {
+    constexpr int NT = LongCfg<WEIGHTED>::NT;
+    using SM = TileSmem<NT, WEIGHTED, false, 1>;
+    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, RAGGED>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+    if (err != cudaSuccess) return err;
+    chunk_hull_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.chunks, NT, SM::kBytes, stream>>>(y, w, geo,
+                                                                                increasing, ws);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "chunk_hull");
+    err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, RAGGED>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
+    if (err != cudaSuccess) return err;
+    merge_groups_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.groups, kGroupThreads, kGroupSmem, stream>>>(
+        geo, gr.ng, ws, row_status);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "merge_groups");
+    err = cudaFuncSetAttribute(merge_top_kernel<WEIGHTED, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMergeSmem);
+    if (err != cudaSuccess) return err;
+    merge_top_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.rows, kMergeThreads, kMergeSmem, stream>>>(geo, ws);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "merge_top");
+    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ExpandSmem<WEIGHTED>::kBytes);
+    if (err != cudaSuccess) return err;
+    expand_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.chunks, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
+        y, geo, increasing, ws, out, blocks);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "expand");
+    return cudaSuccess;
+}
+
+// Bounds of a ragged batch's long part: at most `rows` long segments, whose
+// ceil(len / C) chunks number fewer than total / C + rows.
+struct RaggedBounds { int64_t rows, chunks, groups; };
+
+template <bool WEIGHTED>
+static RaggedBounds ragged_bounds(int64_t rows, int64_t total) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int64_t M = total / C + rows + 1;
+    return RaggedBounds{rows, M, M / kGroup + rows + 1};
+}
+
+// Tables of the ragged long part, then the workspace of the long path.
+template <bool WEIGHTED>
+static size_t carve_ragged(void* base, int64_t rows, int64_t total, LongGeo* geo, LongWs* ws) {
+    const RaggedBounds B = ragged_bounds<WEIGHTED>(rows, total);
+    size_t off = 0;
+    char* b = static_cast<char*>(base);
+    auto take = [&](size_t bytes) -> void* {
+        void* p = b ? (void*)(b + off) : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    LongGeo g;
+    g.e0 = (const int64_t*)take(8 * B.rows);
+    g.len = (const int64_t*)take(8 * B.rows);
+    g.c0 = (const int64_t*)take(8 * B.rows);
+    g.g0 = (const int64_t*)take(8 * B.rows);
+    g.id = (const int32_t*)take(4 * B.rows);
+    g.chunk_row = (const int32_t*)take(4 * B.chunks);
+    g.group_row = (const int32_t*)take(4 * B.groups);
+    g.count = (const int64_t*)take(8 * 4);
+    if (geo) *geo = g;
+    off += carve<WEIGHTED>(b ? (void*)(b + off) : nullptr, B.rows, B.chunks, ws);
+    return off;
+}
+
 }  // namespace
 
 size_t long_fit_workspace(int64_t rows, int64_t n, bool weighted) {
-    return weighted ? carve<true>(nullptr, rows, n, nullptr) : carve<false>(nullptr, rows, n, nullptr);
+    const int64_t C = weighted ? LongCfg<true>::C : LongCfg<false>::C;
+    const int64_t M = rows * ((n + C - 1) / C);
+    return weighted ? carve<true>(nullptr, rows, M, nullptr) : carve<false>(nullptr, rows, M, nullptr);
 }
 
 template <bool WEIGHTED>
 static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int64_t n,
                               int increasing, float* out, uint8_t* blocks, void* wsp,
                               uint32_t* row_status, cudaStream_t stream) {
-    constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
-    using SM = TileSmem<NT, WEIGHTED, false, 1>;
-    LongWs ws;
-    carve<WEIGHTED>(wsp, rows, n, &ws);
     const int64_t m = (n + C - 1) / C;
-    const int64_t M = rows * m;
-    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
-    if (err != cudaSuccess) return err;
-    chunk_hull_kernel<WEIGHTED><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, n, m, increasing, ws);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    prof_mark(stream, "chunk_hull");
-    err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
-    if (err != cudaSuccess) return err;
+    LongWs ws;
+    carve<WEIGHTED>(wsp, rows, rows * m, &ws);
+    LongGeo geo;
+    geo.n = n;
+    geo.m = m;
     const int64_t ng = (m + kGroup - 1) / kGroup;
-    merge_groups_kernel<WEIGHTED><<<dim3((unsigned)rows, (unsigned)ng), kGroupThreads, kGroupSmem,
-                                    stream>>>(m, ws, row_status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    prof_mark(stream, "merge_groups");
-    err = cudaFuncSetAttribute(merge_top_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMergeSmem);
-    if (err != cudaSuccess) return err;
-    merge_top_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, kMergeSmem, stream>>>(m, ws);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    prof_mark(stream, "merge_top");
-    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               ExpandSmem<WEIGHTED>::kBytes);
-    if (err != cudaSuccess) return err;
-    expand_kernel<WEIGHTED><<<(unsigned)M, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
-        y, n, m, increasing, ws, out, blocks);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    prof_mark(stream, "expand");
-    return cudaSuccess;
+    return long_launch<WEIGHTED, false>(y, w, geo, LongGrid{rows, rows * m, rows * ng, ng}, increasing,
+                                 out, blocks, ws, row_status, stream);
 }
 
 cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, int increasing,
@@ -1158,6 +1374,43 @@ cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, in
     (void)ws_bytes;
     return w ? long_fit_t<true>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream)
              : long_fit_t<false>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream);
+}
+
+size_t long_ragged_workspace(int64_t rows_max, int64_t total, bool weighted) {
+    return weighted ? carve_ragged<true>(nullptr, rows_max, total, nullptr, nullptr)
+                    : carve_ragged<false>(nullptr, rows_max, total, nullptr, nullptr);
+}
+
+template <bool WEIGHTED>
+static cudaError_t long_fit_ragged_t(const float* y, const float* w, const int64_t* off,
+                                     const int32_t* long_id, const unsigned long long* nlong,
+                                     int64_t rows_max, int64_t total, int increasing, float* out,
+                                     uint8_t* blocks, void* wsp, uint32_t* row_status,
+                                     cudaStream_t stream) {
+    LongGeo geo;
+    LongWs ws;
+    carve_ragged<WEIGHTED>(wsp, rows_max, total, &geo, &ws);
+    const RaggedBounds B = ragged_bounds<WEIGHTED>(rows_max, total);
+    long_plan_kernel<LongCfg<WEIGHTED>::C><<<1, 1024, 0, stream>>>(
+        off, long_id, nlong, B.rows, B.chunks, B.groups, geo, row_status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    prof_mark(stream, "long_plan");
+    // bounded grids: the CTAs take the chunks (rows) in turn
+    const LongGrid gr{std::min<int64_t>(B.rows, kRaggedTopCtas),
+                      std::min<int64_t>(B.chunks, kRaggedCtas),
+                      std::min<int64_t>(B.groups, kRaggedCtas), 0};
+    return long_launch<WEIGHTED, true>(y, w, geo, gr, increasing, out, blocks, ws, row_status, stream);
+}
+
+cudaError_t long_fit_ragged(const float* y, const float* w, const int64_t* off,
+                            const int32_t* long_id, const unsigned long long* nlong,
+                            int64_t rows_max, int64_t total, int increasing, float* out,
+                            uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream) {
+    return w ? long_fit_ragged_t<true>(y, w, off, long_id, nlong, rows_max, total, increasing, out,
+                                       blocks, ws, row_status, stream)
+             : long_fit_ragged_t<false>(y, w, off, long_id, nlong, rows_max, total, increasing,
+                                        out, blocks, ws, row_status, stream);
 }
 
 }  // namespace isodev

@@ -6,24 +6,24 @@
 #include "iso_internal.h"
 #include "iso_tile.cuh"
 
+#include <algorithm>
+
 namespace isodev {
 
-// Fit of whole rows: CTA of NT threads, R = NT / L rows of L lanes each.
+// Fit of the rows of one CTA of NT threads: R = NT / L tiles of L lanes, each
+// thread's tile a row of n <= 32 L elements at yr (wr), its fit written to
+// orow and its block flags to brow (may be null), its status to *status (may
+// be null).  A tile that is not live reads and writes nothing.  `mark0`: a
+// rejected row still flags its first element as a block start (ragged
+// batches, where each segment's first element must start a block).  Every
+// thread of the CTA calls it.
 template <int NT, bool WEIGHTED>
-__global__ void __launch_bounds__(NT)
-rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t rows, int n,
-                int L, int increasing, float* __restrict__ out, uint8_t* __restrict__ blocks,
-                uint32_t* __restrict__ row_status) {
-    extern __shared__ __align__(128) unsigned char smem[];
+__device__ __forceinline__ void fit_row_tiles(const float* __restrict__ yr,
+                                              const float* __restrict__ wr, int n, bool live,
+                                              int L, bool neg, float* __restrict__ orow,
+                                              uint8_t* __restrict__ brow, uint32_t* status,
+                                              bool mark0, unsigned char* smem) {
     using SM = TileSmem<NT, WEIGHTED, true>;
-    const int R = NT / L;
-    const int tile = threadIdx.x / L;
-    const int64_t row = (int64_t)blockIdx.x * R + tile;
-    const bool live = row < rows;
-    const float* yr = y + (live ? row : 0) * (int64_t)n;
-    const float* wr = WEIGHTED ? w + (live ? row : 0) * (int64_t)n : nullptr;
-    const bool neg = !increasing;
-
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, true>(yr, wr, n, live, neg, L, smem, H);
 
@@ -78,7 +78,6 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
 
     // ---- coalesced write-out of the fit and of the block-start bytes ----
     if (live) {
-        float* orow = out + row * (int64_t)n;
         const float* ost = reinterpret_cast<const float*>(ost4);
         const float qnan = __int_as_float(0x7fffffff);
         const int g0 = H.tile * L;
@@ -95,8 +94,7 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
         } else {
             for (int i = lane; i < n; i += L) orow[i] = work ? ost[spos(g0 + (i >> 5), i & 31)] : qnan;
         }
-        if (blocks) {
-            uint8_t* brow = blocks + row * (int64_t)n;
+        if (brow) {
             const uint32_t* ma = T.mask;
             if ((reinterpret_cast<uintptr_t>(brow) & 3u) == 0) {
                 const int n4 = n >> 2;
@@ -113,8 +111,56 @@ rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_
                 for (int i = lane; i < n; i += L)
                     brow[i] = work ? (uint8_t)((ma[i >> 5] >> (i & 31)) & 1u) : 0;
             }
+            if (mark0 && !work && lane == 0) brow[0] = 1;   // lane 0 wrote element 0 above
         }
-        if (row_status && lane == 0) row_status[row] = H.bad;
+        if (status && lane == 0) *status = H.bad;
+    }
+}
+
+// Fit of whole rows: CTA of NT threads, R = NT / L rows of L lanes each.
+template <int NT, bool WEIGHTED>
+__global__ void __launch_bounds__(NT)
+rows_fit_kernel(const float* __restrict__ y, const float* __restrict__ w, int64_t rows, int n,
+                int L, int increasing, float* __restrict__ out, uint8_t* __restrict__ blocks,
+                uint32_t* __restrict__ row_status) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int R = NT / L;
+    const int64_t row = (int64_t)blockIdx.x * R + threadIdx.x / L;
+    const bool live = row < rows;
+    const int64_t e0 = (live ? row : 0) * (int64_t)n;
+    fit_row_tiles<NT, WEIGHTED>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L, !increasing,
+                                out + e0, blocks ? blocks + e0 : nullptr,
+                                row_status ? row_status + (live ? row : 0) : nullptr, false, smem);
+}
+
+// Fit of the segments of one lane class of a ragged batch: list[0 .. count)
+// holds segment indices s, each of n = off[s+1] - off[s] <= 32 L elements at
+// element off[s].  Persistent: each CTA takes R segments at a time.
+template <int NT, bool WEIGHTED>
+__global__ void __launch_bounds__(NT)
+rows_fit_ragged_kernel(const float* __restrict__ y, const float* __restrict__ w,
+                       const int64_t* __restrict__ off, const int32_t* __restrict__ list,
+                       const unsigned long long* __restrict__ count, int64_t cap, int L,
+                       int increasing, float* __restrict__ out, uint8_t* __restrict__ blocks,
+                       uint32_t* __restrict__ row_status) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int R = NT / L;
+    const int tile = threadIdx.x / L;
+    const int64_t cnt = (int64_t)min((unsigned long long)cap, *count);
+    for (int64_t b = (int64_t)blockIdx.x * R; b < cnt; b += (int64_t)gridDim.x * R) {
+        const int64_t i = b + tile;
+        const bool live = i < cnt;
+        int64_t e0 = 0;
+        int n = 0, s = 0;
+        if (live) {
+            s = list[i];
+            e0 = off[s];
+            n = (int)(off[s + 1] - e0);
+        }
+        fit_row_tiles<NT, WEIGHTED>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L, !increasing,
+                                    out + e0, blocks ? blocks + e0 : nullptr,
+                                    row_status ? row_status + s : nullptr, true, smem);
+        __syncthreads();   // shared memory is reused by the next segments
     }
 }
 
@@ -151,6 +197,41 @@ cudaError_t rows_fit(const float* y, const float* w, int64_t rows, int n, int in
     if (L <= 128) { ISO_ROWS_LAUNCH(128); }
     ISO_ROWS_LAUNCH(256);
 #undef ISO_ROWS_LAUNCH
+}
+
+template <int NT, bool WEIGHTED>
+static cudaError_t launch_rows_ragged(const float* y, const float* w, const int64_t* off,
+                                      const int32_t* list, const unsigned long long* count,
+                                      int64_t cap, int L, int increasing, float* out,
+                                      uint8_t* blocks, uint32_t* row_status, cudaStream_t stream) {
+    using SM = TileSmem<NT, WEIGHTED, true>;
+    auto kern = rows_fit_ragged_kernel<NT, WEIGHTED>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           SM::kBytes);
+    if (err != cudaSuccess) return err;
+    const int R = NT / L;
+    const int64_t grid = std::min<int64_t>((cap + R - 1) / R, kRaggedCtas);
+    kern<<<(unsigned)grid, NT, SM::kBytes, stream>>>(y, w, off, list, count, cap, L, increasing,
+                                                    out, blocks, row_status);
+    prof_mark(stream, "rows_ragged");
+    return cudaGetLastError();
+}
+
+cudaError_t rows_fit_ragged(const float* y, const float* w, const int64_t* off,
+                            const int32_t* list, const unsigned long long* count, int64_t cap,
+                            int L, int increasing, float* out, uint8_t* blocks,
+                            uint32_t* row_status, cudaStream_t stream) {
+    const bool weighted = w != nullptr;
+#define ISO_RAGGED_LAUNCH(NT_)                                                                  \
+    return weighted ? launch_rows_ragged<NT_, true>(y, w, off, list, count, cap, L, increasing, \
+                                                    out, blocks, row_status, stream)            \
+                    : launch_rows_ragged<NT_, false>(y, w, off, list, count, cap, L,            \
+                                                     increasing, out, blocks, row_status, stream)
+    if (L <= 32) { ISO_RAGGED_LAUNCH(128); }
+    if (L <= 64) { ISO_RAGGED_LAUNCH(64); }
+    if (L <= 128) { ISO_RAGGED_LAUNCH(128); }
+    ISO_RAGGED_LAUNCH(256);
+#undef ISO_RAGGED_LAUNCH
 }
 
 }  // namespace isodev

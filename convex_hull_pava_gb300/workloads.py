@@ -64,6 +64,49 @@ def soft_rank_rows(rows: int, n: int, eps: float = 1.0, seed: int = 0) -> np.nda
     return (theta - (n - np.arange(n, dtype=np.float64))[None, :]).astype(np.float32)
 
 
+def ragged_lengths(segments: int, max_len: int, seed: int = 0, long_segments: int = 0,
+                   long_len: int = 0) -> np.ndarray:
+    """Segment lengths of a many-curve batch: log-uniform in [1, max_len] (many
+    short curves, few long ones), then ``long_segments`` lengths of
+    ``long_len`` +- 25% placed at seeded positions."""
+    rng = np.random.default_rng(seed)
+    lens = np.exp(rng.uniform(0.0, np.log(max_len + 1.0), segments)).astype(np.int64)
+    lens = np.clip(lens, 1, max_len)
+    if long_segments:
+        pos = rng.choice(segments, size=min(long_segments, segments), replace=False)
+        lens[pos] = (long_len * rng.uniform(0.75, 1.25, pos.size)).astype(np.int64)
+    return lens
+
+
+def ragged_calibration(lengths, seed: int = 0):
+    """Per-segment calibration curves laid end to end (the paper's Section 7.7
+    fits one curve per segment of scored events): in a segment of n points,
+    scores u sorted from U(0, 1), each point a group of c = 1, 2 or 3 events
+    (probabilities 0.7, 0.22, 0.08) with floor(c u^g + U(0, 1)) positives (c
+    u^g on average), g ~ U(0.5, 2) per segment; the target is the group's
+    positive rate, its weight the count c.  Returns
+    ``(y, w, offsets)``: float32 [total] twice and int64 [segments + 1]."""
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, dtype=np.int64)
+    offsets = np.zeros(lengths.size + 1, dtype=np.int64)
+    np.cumsum(lengths, out=offsets[1:])
+    total = int(offsets[-1])
+    seg = np.repeat(np.arange(lengths.size), lengths)
+    g = rng.uniform(0.5, 2.0, lengths.size)[seg]
+    # sorted U(0, 1) scores per segment, without a sort: the k-th of n sorted
+    # uniforms is the k-th of n + 1 partial sums of Exp(1) draws over the last
+    e = rng.exponential(size=total)
+    cs = np.cumsum(e)
+    base = np.concatenate([[0.0], cs])[offsets[:-1]]
+    span = np.concatenate([[0.0], cs])[offsets[1:]] - base + rng.exponential(size=lengths.size)
+    u = (cs - base[seg]) / span[seg]
+    v = rng.random(total)
+    c = 1 + (v < 0.3) + (v < 0.08)
+    pos = np.floor(c * np.clip(u, 0.0, 1.0) ** g + rng.random(total))
+    y = (pos / c).astype(np.float32)
+    return y, c.astype(np.float32), offsets
+
+
 def normal(shape, seed: int) -> np.ndarray:
     return np.random.default_rng(seed).standard_normal(shape).astype(np.float32)
 

@@ -46,6 +46,8 @@ typedef enum {
 /* Bits of a row's status word. */
 #define ISO_ROW_BAD_Y 1u /* the row holds a NaN or infinite y                   */
 #define ISO_ROW_BAD_W 2u /* the row holds a weight that is not finite and > 0   */
+#define ISO_ROW_BAD_SHAPE 4u /* ragged batches: the segment's offsets are out of  */
+                             /* order or range, or it is longer than max_len      */
 
 /* Version of this ABI (major * 10000 + minor * 100 + patch). */
 int iso_version(void);
@@ -148,6 +150,59 @@ iso_status iso_backward_w(const float *grad, const uint8_t *blocks, const float 
                           const float *y, const float *fit, int64_t rows, int64_t n,
                           float *out_dy, float *out_dw, void *workspace, size_t workspace_bytes,
                           void *stream);
+
+/*
+ * Bytes of device workspace that iso_fit_ragged needs for `segments` segments
+ * covering `total` elements, none longer than max_len (max_len <= 0: total).
+ * Returns 0 for invalid arguments (iso_fit_ragged then reports the error).
+ */
+size_t iso_fit_ragged_workspace_bytes(int64_t segments, int64_t total, int64_t max_len,
+                                      int weighted);
+
+/*
+ * iso_fit_ragged -- forward fit of a ragged batch: segments of their own
+ * lengths laid end to end, each fitted as its own row (eq. (1)-(3), Section
+ * 2.1).  The paper fits such batches (many per-segment calibration curves,
+ * Section 7.7) by padding them to a rectangle or by laying them end to end in
+ * one row with each segment's targets lifted above the previous segment's;
+ * here the offsets are given to the library, and every segment gets exactly
+ * the fit iso_fit would give it as a row of its own.
+ *
+ *  y          [total] float32, device, read only: the segments end to end.
+ *  w          [total] float32, device, read only, or NULL for unit weights.
+ *  offsets    [segments + 1] int64, device, read only: segment s holds elements
+ *             offsets[s] .. offsets[s+1]-1.  The offsets are not read by the
+ *             host.  Non-decreasing offsets within [0, total] give disjoint
+ *             segments; elements outside every segment are not written.
+ *  segments   number of segments, 1 <= segments <= 2^31 - 1.
+ *  total      length of y (and w, out, blocks), 1 <= total <= 2^40.
+ *  max_len    an upper bound on the segments' lengths that the caller knows,
+ *             or <= 0 for none (total).  It only saves launches and workspace:
+ *             a segment longer than it is rejected (ISO_ROW_BAD_SHAPE).  At
+ *             most 2^31 - 1.
+ *  increasing as for iso_fit.
+ *  out        [total] float32, device, written: each segment's fit.
+ *  blocks     [total] uint8, device, written, or NULL: block starts as for
+ *             iso_fit.  The first element of every non-empty segment that was
+ *             not rejected for its shape is flagged 1, also in a segment
+ *             rejected for its values (whose other flags are 0), so that
+ *             iso_backward / iso_backward_w over the whole array as ONE row
+ *             (rows = 1, n = total) give each segment its own backward, when
+ *             the segments cover the array end to end.
+ *  workspace  device scratch of iso_fit_ragged_workspace_bytes(segments,
+ *             total, max_len, w != NULL) bytes, 256-byte aligned.
+ *  row_status [segments] uint32, device, written, or NULL: per segment, 0 or
+ *             ISO_ROW_BAD_* bits (an empty segment: 0).
+ *  stream     cudaStream_t.
+ *
+ * The segments are sorted on the device into lists by length: up to 8,192
+ * elements by the whole-row kernels (by lane class), longer ones by the
+ * long-row path; no host synchronisation.  Accuracy as for iso_fit.
+ */
+iso_status iso_fit_ragged(const float *y, const float *w, const int64_t *offsets,
+                          int64_t segments, int64_t total, int64_t max_len, int increasing,
+                          float *out, uint8_t *blocks, void *workspace, size_t workspace_bytes,
+                          uint32_t *row_status, void *stream);
 
 /*
  * iso_backward_noalloc -- iso_backward for callers that cannot allocate device

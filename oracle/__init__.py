@@ -13,6 +13,8 @@ The arithmetic lives in ``iso_oracle.c`` (plain C, compiled with gcc by
   eqs. (2)-(3); an independent route used only to cross-check :func:`pava`.
 * :func:`points` -- the cumulative-sum diagram itself, eq. (2).
 * :func:`backward` / :func:`backward_w` -- block averaging, Section 6, "Gradient".
+* :func:`pava_ragged` -- a ragged batch (segments of unequal lengths laid end
+  to end, Section 7.7): each segment fitted as its own row by :func:`pava`.
 """
 from __future__ import annotations
 
@@ -31,6 +33,7 @@ _lock = threading.Lock()
 
 BAD_Y = 1
 BAD_W = 2
+BAD_SHAPE = 4
 
 
 def build(force: bool = False) -> str:
@@ -150,3 +153,38 @@ def backward_w(grad, blocks, w, y, z):
     _load().oracle_backward_w(g.size, _ptr(g), _ptr(b), _ptr(w1), _ptr(y1), _ptr(z1),
                               _ptr(out))
     return out
+
+
+def pava_ragged(y, offsets, w=None, increasing=True, max_len=0):
+    """Fit of a ragged batch: segment s, elements ``offsets[s] .. offsets[s+1]-1``
+    of the 1-D ``y`` (and ``w``), fitted on its own by :func:`pava` (Section
+    7.7 fits such segments as separate curves).  Returns ``(z, blocks,
+    status)``: ``z`` float64 and ``blocks`` uint8 over ``y`` (NaN / 0 outside
+    every segment), ``status`` one word per segment.
+
+    Conventions of the library's ragged interface: a segment whose offsets
+    are out of order or out of ``[0, len(y)]``, or longer than ``max_len``
+    (when > 0), gets :data:`BAD_SHAPE` and no fit; an empty segment gets 0; a
+    segment rejected for its values keeps its first element flagged as a
+    block start."""
+    y = _f32(y).ravel()
+    off = np.asarray(offsets, dtype=np.int64).ravel()
+    w1 = None if w is None else _f32(w).ravel()
+    total, segments = y.size, off.size - 1
+    lim = total if max_len is None or max_len <= 0 else min(int(max_len), total)
+    z = np.full(total, np.nan)
+    blocks = np.zeros(total, dtype=np.uint8)
+    status = np.zeros(segments, dtype=np.uint32)
+    for s in range(segments):
+        a, b = int(off[s]), int(off[s + 1])
+        if a < 0 or b < a or b > total or b - a > lim:
+            status[s] = BAD_SHAPE
+            continue
+        if b == a:
+            continue
+        zs, bs, st = pava(y[a:b], None if w1 is None else w1[a:b], increasing)
+        z[a:b] = zs
+        blocks[a:b] = bs
+        blocks[a] = 1
+        status[s] = st
+    return z, blocks, status

@@ -72,3 +72,27 @@ def test_binding_rejects_host_tensors_without_fallback():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError):
         chp.iso_fit(torch.zeros(10))
+
+
+def test_ragged_host_checks():
+    lib = chp.load_library()
+    fake = ctypes.c_void_p(0x1000)
+    # workspace: always needed (the device lists), grows with the long part
+    short = chp.iso_fit_ragged_workspace_bytes(1000, 10**6, 8192, False)
+    full = chp.iso_fit_ragged_workspace_bytes(1000, 10**6, 0, False)
+    assert 0 < short < full
+    assert chp.iso_fit_ragged_workspace_bytes(1000, 10**6, 0, True) > full
+    assert chp.iso_fit_ragged_workspace_bytes(0, 10, 0, False) == 0
+    assert chp.iso_fit_ragged_workspace_bytes(1, 0, 0, False) == 0
+    args = lambda y, off, segs, total, ml, inc, out, ws, wsb: (
+        y, None, off, segs, total, ml, inc, out, None, ws, wsb, None, None)
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.iso_fit_ragged(*args(None, fake, 1, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(*args(fake, None, 1, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(*args(fake, fake, 0, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 3, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(*args(fake, fake, 1, 1 << 32, 1 << 31, 1, fake, ws, 1 << 40)) == chp.ISO_ERR_INVALID_ARG
+    need = chp.iso_fit_ragged_workspace_bytes(1, 10, 0, False)
+    assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, None, 0)) == chp.ISO_ERR_WORKSPACE
+    assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, ws, need - 1)) == chp.ISO_ERR_WORKSPACE
+    assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, ctypes.c_void_p(0x100010), need)) == chp.ISO_ERR_WORKSPACE

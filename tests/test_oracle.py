@@ -373,3 +373,61 @@ def test_soft_rank_composition_small_eps_is_hard_rank():
     hard = np.argsort(np.argsort(x, axis=1), axis=1) + 1
     assert np.abs(r - hard).max() <= 1e-3
 
+
+
+# ---- ragged batches (segments of unequal lengths end to end) ----
+def _quarter_rates(lengths, seed):
+    """Calibration-style targets on a grid of 1/4 (exact in float32 after a
+    lift by an even integer), with their weights and offsets."""
+    y, w, off = wl.ragged_calibration(lengths, seed)
+    return (np.floor(4.0 * y) / 4.0).astype(np.float32), w, off
+
+
+@pytest.mark.parametrize("increasing", [True, False])
+@pytest.mark.parametrize("weighted", [False, True])
+def test_ragged_oracle_equals_lifted_single_row(increasing, weighted):
+    """The paper's Section 7.7 fits per-segment curves as ONE row whose targets
+    in segment s are lifted by 2 s (they lie in [0, 1]), so that no block can
+    cross a segment boundary, and subtracts the lift from the fit.  With the
+    targets on a grid of 1/4 the lift is exact in float32, and the single-row
+    PAVA (minus the lift) must equal the per-segment fits."""
+    lengths = np.array([1, 7, 33, 2, 100, 64, 5, 250, 1, 17], dtype=np.int64)
+    y, w, off = _quarter_rates(lengths, 3)
+    w = w if weighted else None
+    seg = np.repeat(np.arange(lengths.size), lengths)
+    lift = (2.0 * seg) if increasing else (-2.0 * seg)
+    lifted = (y.astype(np.float64) + lift).astype(np.float32)
+    assert np.array_equal(lifted.astype(np.float64) - lift, y.astype(np.float64))
+    zl, bl, _ = oracle.pava(lifted, w, increasing)
+    z, b, st = oracle.pava_ragged(y, off, w, increasing)
+    assert not st.any()
+    np.testing.assert_allclose(zl - lift, z, rtol=0, atol=1e-12)
+    assert bl[off[:-1]].all()             # every segment start starts a lifted block
+    assert np.array_equal(bl, b)
+
+
+def test_ragged_oracle_equal_lengths_is_the_batch():
+    y = wl.noisy_ramp(6, 50, 4)
+    off = np.arange(0, 301, 50, dtype=np.int64)
+    z, b, st = oracle.pava_ragged(y.ravel(), off)
+    z2, b2, st2 = oracle.pava(y)
+    assert np.array_equal(z, z2.ravel()) and np.array_equal(b, b2.ravel())
+    assert np.array_equal(st, st2)
+
+
+def test_ragged_oracle_shapes_and_bad_values():
+    y = wl.noisy_ramp(1, 40, 5).ravel()
+    y[22] = np.nan
+    # segments: [0,5) ok, [5,5) empty, [5,3) out of order, [3,20) overlaps but is
+    # well formed, [20,30) holds the NaN, [30,41) ends past the array, [38,40) ok
+    off = np.array([0, 5, 5, 3, 20, 30, 41, 40], dtype=np.int64)
+    # the 7th segment runs from 41 down to 40: out of order as well
+    z, b, st = oracle.pava_ragged(y, off)
+    assert list(st) == [0, 0, oracle.BAD_SHAPE, 0, oracle.BAD_Y, oracle.BAD_SHAPE,
+                        oracle.BAD_SHAPE]
+    assert np.isnan(z[20:30]).all() and b[20] == 1 and not b[21:30].any()
+    z5, _, _ = oracle.pava(y[0:5])
+    z17, _, _ = oracle.pava(y[3:20])
+    assert np.array_equal(z[0:3], z5[0:3]) and np.array_equal(z[3:20], z17)
+    zl, _, st3 = oracle.pava_ragged(y, np.array([0, 10, 40], dtype=np.int64), max_len=12)
+    assert list(st3) == [0, oracle.BAD_SHAPE] and np.isnan(zl[10:]).all()
