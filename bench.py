@@ -207,6 +207,44 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+def copy_control(name, make, dev, flush, stream):
+    """Median per-stage times (CUDA events around each kernel) of iso_fit and of
+    the materialised-copy control on one workload."""
+    import torch
+    import convex_hull_pava_gb300 as chp
+    yh, wh, inc = make()
+    y = torch.from_numpy(np.atleast_2d(yh)).to(dev)
+    w = None if wh is None else torch.from_numpy(np.atleast_2d(wh)).to(dev)
+    rows, n = y.shape
+    o = torch.empty_like(y)
+    b = torch.empty(y.shape, dtype=torch.uint8, device=dev)
+    wa = torch.empty(max(chp.iso_fit_workspace_bytes(rows, n, w is not None), 1), dtype=torch.uint8, device=dev)
+    wc = torch.empty(max(chp.iso_fit_copy_control_workspace_bytes(rows, n, w is not None), 1),
+                     dtype=torch.uint8, device=dev)
+    out = {}
+    for tag, f in (("segment_lists", lambda: chp.iso_fit(y, w, inc, out=o, blocks=b, workspace=wa, stream=stream)),
+                   ("control", lambda: chp.iso_fit_copy_control(y, w, inc, out=o, blocks=b, workspace=wc,
+                                                                stream=stream))):
+        f()
+        chp.profile_enable(True)
+        stages, tot = {}, []
+        for _ in range(7):
+            flush.zero_()
+            f()
+            r = chp.profile_read()
+            for nm, ms in r:
+                stages.setdefault(nm, []).append(ms)
+            tot.append(sum(ms for _, ms in r))
+        chp.profile_enable(False)
+        st = {k: float(np.median(v)) for k, v in stages.items()}
+        merge = sum(v for k, v in st.items() if k.startswith(("merge_", "ctl_")))
+        out[tag] = {"ms": float(np.median(tot)), "merge_stage_ms": merge, "stages_ms": st}
+    out["whole_ratio"] = out["control"]["ms"] / out["segment_lists"]["ms"]
+    out["merge_stage_ratio"] = out["control"]["merge_stage_ms"] / out["segment_lists"]["merge_stage_ms"]
+    del y, w, o, b, wa, wc
+    return name, out
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -404,6 +442,17 @@ def run_gpu(args):
             "elements_per_s": yr.numel() / t, "ms": t * 1e3, "gbs": by / t / 1e9,
             "frac": by / t / 1e9 / hbm_peak, "bytes": by}
         del yr, wr, offr, orr, br, wsr
+        # the materialised-copy control against the segment lists: whole call and
+        # merge stage (segment lists: the two merge kernels; control: its setup,
+        # levels and root list)
+        ctl_cases = [("row1e7", lambda: (W.y, W.w, W.increasing))]
+        ctl_cases.append(("dense16x4m", lambda: (lambda V: (V.y, V.w, V.increasing))(wl.make("dense16x4m"))))
+        if args.control_table:
+            for fam, n in (("increasing", 10**7), ("increasing", 10**8), ("cliff", 10**8),
+                           ("noise", 10**7), ("noise", 10**8)):
+                ctl_cases.append((f"{fam}_{n:.0e}", lambda fam=fam, n=n: (wl.family(fam, 1, n, 0), None, True)))
+        also["copy_control"] = {k: v for k, v in (copy_control(name, mk, dev, flush, stream)
+                                                 for name, mk in ctl_cases)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -436,6 +485,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--control-table", action="store_true",
+                    help="also time the materialised-copy control on increasing, cliff and noise "
+                         "rows of 10^7 and 10^8 elements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -39,6 +39,7 @@ ISO_ROW_BAD_SHAPE = 4
 EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_fit",
            "iso_backward_workspace_bytes", "iso_backward", "iso_backward_w",
            "iso_backward_noalloc", "iso_fit_ragged_workspace_bytes", "iso_fit_ragged",
+           "iso_fit_copy_control_workspace_bytes", "iso_fit_copy_control",
            "iso_profile_enable", "iso_profile_read")
 
 _lib = None
@@ -83,6 +84,10 @@ def load_library(path: str | None = None):
         lib.iso_fit_ragged_workspace_bytes.restype = sz
         lib.iso_fit_ragged.argtypes = [vp, vp, vp, i64, i64, i64, ci, vp, vp, vp, sz, vp, vp]
         lib.iso_fit_ragged.restype = ci
+        lib.iso_fit_copy_control_workspace_bytes.argtypes = [i64, i64, ci]
+        lib.iso_fit_copy_control_workspace_bytes.restype = sz
+        lib.iso_fit_copy_control.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp, sz, vp, vp]
+        lib.iso_fit_copy_control.restype = ci
         lib.iso_profile_enable.argtypes = [ci]
         lib.iso_profile_enable.restype = ci
         lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
@@ -193,6 +198,40 @@ def iso_fit(y, w=None, increasing: bool = True, *, out=None, blocks=None, want_b
         None if ws is None else ws.data_ptr(), ws_bytes, row_status.data_ptr(), _stream_ptr(stream))
     if st != ISO_OK:
         raise IsoError(st, "iso_fit")
+    return out, blocks, row_status
+
+
+def iso_fit_copy_control_workspace_bytes(rows: int, n: int, weighted: bool) -> int:
+    return int(load_library().iso_fit_copy_control_workspace_bytes(int(rows), int(n),
+                                                                   int(bool(weighted))))
+
+
+def iso_fit_copy_control(y, w=None, increasing: bool = True, *, out=None, blocks=None,
+                         row_status=None, workspace=None, stream=None):
+    """The materialised-copy control (measurement only): :func:`iso_fit`'s
+    result, with every merge level's hulls copied into flat arrays instead of
+    kept as segment lists.  Returns ``(out, blocks, row_status)``."""
+    torch = _torch()
+    _check_dev(y, "y", torch.float32)
+    rows, n = _shape2(y)
+    if w is not None:
+        _check_dev(w, "w", torch.float32)
+        if w.shape != y.shape:
+            raise ValueError("w must have the shape of y")
+    if out is None:
+        out = torch.empty_like(y)
+    if blocks is None:
+        blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+    if row_status is None:
+        row_status = torch.empty(rows, dtype=torch.int32, device=y.device)
+    nbytes = iso_fit_copy_control_workspace_bytes(rows, n, w is not None)
+    ws, ws_bytes = _workspace(nbytes, workspace, y.device)
+    st = load_library().iso_fit_copy_control(
+        y.data_ptr(), None if w is None else w.data_ptr(), rows, n, int(bool(increasing)),
+        out.data_ptr(), blocks.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes,
+        row_status.data_ptr(), _stream_ptr(stream))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_fit_copy_control")
     return out, blocks, row_status
 
 

@@ -117,6 +117,29 @@ iso_status iso_fit_ragged(const float* y, const float* w, const int64_t* offsets
                                         workspace, row_status, st));
 }
 
+size_t iso_fit_copy_control_workspace_bytes(int64_t rows, int64_t n, int weighted) {
+    if (!shape_ok(rows, n) || n > (1LL << 30)) return 0;
+    if (n <= isodev::kRowMax) return 0;
+    return isodev::long_control_workspace(rows, n, weighted != 0);
+}
+
+iso_status iso_fit_copy_control(const float* y, const float* w, int64_t rows, int64_t n,
+                                int increasing, float* out, uint8_t* blocks, void* workspace,
+                                size_t workspace_bytes, uint32_t* row_status, void* stream) {
+    if (!y || !out || !shape_ok(rows, n) || n > (1LL << 30) || (increasing != 0 && increasing != 1))
+        return ISO_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    if (n <= isodev::kRowMax)
+        return from_cuda(isodev::rows_fit(y, w, rows, (int)n, increasing, out, blocks,
+                                          row_status, st));
+    const size_t need = isodev::long_control_workspace(rows, n, w != nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ISO_ERR_WORKSPACE;
+    return from_cuda(isodev::long_fit_control(y, w, rows, n, increasing, out, blocks, workspace,
+                                              row_status, st));
+}
+
 size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted) {
     if (!shape_ok(rows, n)) return 0;
     if (n <= isodev::kRowMax) return 0;

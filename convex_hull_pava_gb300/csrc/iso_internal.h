@@ -49,6 +49,13 @@ cudaError_t long_fit_ragged(const float* y, const float* w, const int64_t* off,
                             int64_t rows_max, int64_t total, int increasing, float* out,
                             uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream);
 
+// The materialised-copy control of the merge levels (measurement only): the
+// same fit as long_fit, with every merged hull copied into a flat array.
+size_t long_control_workspace(int64_t rows, int64_t n, bool weighted);
+cudaError_t long_fit_control(const float* y, const float* w, int64_t rows, int64_t n,
+                             int increasing, float* out, uint8_t* blocks, void* ws,
+                             uint32_t* row_status, cudaStream_t stream);
+
 size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted);
 cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
                           int64_t n, float* out, const float* y, const float* fit, float* dw,

@@ -318,9 +318,10 @@ constexpr int kLinearSteps = 12;   // walk steps before a tangent is found by bi
 // right end to its tangent from the left end, a few steps by walking and then
 // by bisection over the list (first over segments, then inside one).  The two
 // segments the bridge lands in are cut, the merged list's length is set, and
-// the move of the right list's tail is returned.
-template <bool WEIGHTED, bool SMEM>
-__device__ __forceinline__ Move merge_plan(const MView<WEIGHTED, SMEM>& V, int j0, int j1) {
+// the move of the right list's tail is returned.  View: MView, or the flat
+// arrays of the materialised-copy control (FlatView).
+template <bool WEIGHTED, class View>
+__device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
     int4* seg = V.seg;
     const int nL = V.cnt[j0], nR = V.cnt[j1];
     const int kLl = j0 + nL - 1, kR0 = j1, kRl = j1 + nR - 1;
@@ -598,7 +599,7 @@ __device__ __forceinline__ void merge_levels(const MView<WEIGHTED, SMEM>& V, int
             const int64_t j0 = jb + g * span, j1 = j0 + half;
             const bool act = g < merges && j1 < je;
             Move mv{0, 0, 0};
-            if (act && tl == 0) mv = merge_plan<WEIGHTED, SMEM>(V, (int)j0, (int)j1);
+            if (act && tl == 0) mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
             if (T == 1) {
                 for (int t = 0; t < mv.len; ++t) seg[mv.dst + t] = seg[mv.src + t];
             } else {
@@ -728,7 +729,9 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
     }
 }
 
-template <bool WEIGHTED>
+// One group of kGroup chunks: the row's quanta and status, the chunks' starts
+// in row coordinates and their grid shifts, then (MERGE) the group's merges.
+template <bool WEIGHTED, bool MERGE = true>
 __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, const LongWs& ws,
                                                 uint32_t* __restrict__ row_status, int64_t g) {
     constexpr int C = LongCfg<WEIGHTED>::C;
@@ -802,6 +805,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
         if (tid == 0) s_Hg = tot.h;
         __syncthreads();
     }
+    if (!MERGE) return;
     const int64_t Hg = s_Hg;
     if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
         merge_group<WEIGHTED, true>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
@@ -809,17 +813,73 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
         merge_group<WEIGHTED, false>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
 }
 
-template <bool WEIGHTED, bool RAGGED>
+template <bool WEIGHTED, bool RAGGED, bool MERGE = true>
 __global__ void __launch_bounds__(kGroupThreads)
 merge_groups_kernel(LongGeo geo, int64_t ng, LongWs ws, uint32_t* __restrict__ row_status) {
     if (!RAGGED) {
-        merge_group_one<WEIGHTED>(geo, ng, ws, row_status, blockIdx.x);
+        merge_group_one<WEIGHTED, MERGE>(geo, ng, ws, row_status, blockIdx.x);
         return;
     }
     const int64_t G = geo.count[2];
     for (int64_t g = blockIdx.x; g < G; g += gridDim.x) {
         merge_group_one<WEIGHTED>(geo, ng, ws, row_status, g);
         __syncthreads();
+    }
+}
+
+// Ends: each chunk's root segment, and the root vertices around it, from the
+// root list V.seg[0 .. V.cnt[0]) (at most one segment per chunk, in chunk
+// order).  Every thread of the CTA calls it; segOf, nextSeg and prevSeg are
+// scratch of m entries.
+template <bool WEIGHTED, class View>
+__device__ __forceinline__ void root_ends(const View& V, int64_t m, const LongWs& ws, int64_t c0,
+                                          int32_t* segOf, int32_t* nextSeg, int32_t* prevSeg) {
+    const int tid = threadIdx.x, nth = blockDim.x;
+    // With c(j) the number of root segments of chunks <= j (a scan of "chunk j
+    // holds one"), the first after chunk j is c(j) and the last before it is
+    // c(j) - [j holds one] - 1.
+    const int4* seg = V.seg;
+    const int nroot = V.cnt[0];
+    for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
+    __syncthreads();
+    for (int k = tid; k < nroot; k += nth) segOf[seg[k].x] = k;
+    __syncthreads();
+    {
+        __shared__ int s_tmp2[32];
+        const int64_t per2 = (m + nth - 1) / nth;
+        const int64_t jb2 = imin64(m, tid * per2), je2 = imin64(m, jb2 + per2);
+        int c = 0;
+        for (int64_t j = jb2; j < je2; ++j) c += segOf[j] >= 0 ? 1 : 0;
+        int tot2;
+        c = block_excl_scan_int(c, s_tmp2, tot2);
+        for (int64_t j = jb2; j < je2; ++j) {
+            const int has = segOf[j] >= 0 ? 1 : 0;
+            c += has;
+            nextSeg[j] = c;                 // first root segment of a chunk > j
+            prevSeg[j] = c - has - 1;       // last root segment of a chunk < j
+        }
+    }
+    __syncthreads();
+    for (int64_t j = tid; j < m; j += nth) {
+        ChunkEnds ce;
+        ce.bad = 0;
+        const int sk = segOf[j];
+        if (sk >= 0) { const int4 s = seg[sk]; ce.lo = s.y; ce.hi = s.z; }
+        else { ce.lo = 1; ce.hi = 0; }
+        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
+        ce.pt0_vertex = 0;
+        if (j > 0) {
+            const int pk = prevSeg[j];
+            const Seg gp = V.load(pk);
+            V.at(gp, gp.hi, ce.prevW, ce.prevS);
+            // the previous root vertex is this chunk's first point when it closes chunk j-1
+            ce.pt0_vertex = (gp.jc == j - 1 && gp.hi == ws.meta[c0 + gp.jc].h - 1) ? 1 : 0;
+        }
+        if (j + 1 < m) {
+            const Seg gn = V.load(nextSeg[j]);
+            V.at(gn, gn.lo, ce.nextW, ce.nextS);
+        }
+        ws.ends[c0 + j] = ce;
     }
 }
 
@@ -878,53 +938,7 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
     }
     merge_levels<WEIGHTED, SMEM>(V, 0, m, kGroup);
 
-    // ---- ends: each chunk's root segment, and the root vertices around it.
-    // With c(j) the number of root segments of chunks <= j (a scan of "chunk j
-    // holds one"), the first after chunk j is c(j) and the last before it is
-    // c(j) - [j holds one] - 1. ----
-    const int4* seg = V.seg;
-    const int nroot = V.cnt[0];
-    for (int64_t j = tid; j < m; j += nth) segOf[j] = -1;
-    __syncthreads();
-    for (int k = tid; k < nroot; k += nth) segOf[seg[k].x] = k;
-    __syncthreads();
-    {
-        __shared__ int s_tmp2[32];
-        const int64_t per2 = (m + nth - 1) / nth;
-        const int64_t jb2 = imin64(m, tid * per2), je2 = imin64(m, jb2 + per2);
-        int c = 0;
-        for (int64_t j = jb2; j < je2; ++j) c += segOf[j] >= 0 ? 1 : 0;
-        int tot2;
-        c = block_excl_scan_int(c, s_tmp2, tot2);
-        for (int64_t j = jb2; j < je2; ++j) {
-            const int has = segOf[j] >= 0 ? 1 : 0;
-            c += has;
-            nextSeg[j] = c;                 // first root segment of a chunk > j
-            prevSeg[j] = c - has - 1;       // last root segment of a chunk < j
-        }
-    }
-    __syncthreads();
-    for (int64_t j = tid; j < m; j += nth) {
-        ChunkEnds ce;
-        ce.bad = 0;
-        const int sk = segOf[j];
-        if (sk >= 0) { const int4 s = seg[sk]; ce.lo = s.y; ce.hi = s.z; }
-        else { ce.lo = 1; ce.hi = 0; }
-        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
-        ce.pt0_vertex = 0;
-        if (j > 0) {
-            const int pk = prevSeg[j];
-            const Seg gp = V.load(pk);
-            V.at(gp, gp.hi, ce.prevW, ce.prevS);
-            // the previous root vertex is this chunk's first point when it closes chunk j-1
-            ce.pt0_vertex = (gp.jc == j - 1 && gp.hi == ws.meta[c0 + gp.jc].h - 1) ? 1 : 0;
-        }
-        if (j + 1 < m) {
-            const Seg gn = V.load(nextSeg[j]);
-            V.at(gn, gn.lo, ce.nextW, ce.nextS);
-        }
-        ws.ends[c0 + j] = ce;
-    }
+    root_ends<WEIGHTED>(V, m, ws, c0, segOf, nextSeg, prevSeg);
 }
 
 template <bool WEIGHTED>
@@ -1269,6 +1283,290 @@ long_plan_kernel(const int64_t* __restrict__ off, const int32_t* __restrict__ lo
     }
 }
 
+// ---------------------------------------------------------------------------
+// 5. materialised-copy control (the paper's Section 7.3, "grid copying")
+// ---------------------------------------------------------------------------
+// The same chunk hulls, bridge search (merge_plan) and merge schedule as the
+// segment lists, but every node of the tree is one contiguous array of
+// vertices: after each level's bridges are found, a grid-wide kernel copies
+// every merged hull's surviving vertices into the other buffer.  A vertex
+// record holds S (and W) on its chunk's grid and a tag, chunk << 32 | rank in
+// the chunk's hull << 16 | point index, since a copied vertex leaves its
+// chunk's slot.  The root array is turned back into the root list of chunk
+// segments, so the ends and the expansion are those of the segment lists and
+// the results are identical; only the cost of the merge levels differs.
+struct CtlWs {
+    int64_t* fS[2];      // [M][C+1] per buffer; a row's region starts at its c0 * (C+1)
+    int64_t* fW[2];      // weighted
+    uint64_t* tag[2];
+    int32_t* base[2];    // [M] node base within the row's region, by the node's first chunk
+    int32_t* size[2];    // [M] node vertices
+    int4* desc;          // [M] a merged node's sources: (left start, count, right start, count)
+    int32_t* runLo;      // [M] first root rank of each chunk, -1 if none
+    int32_t* runHi;      // [M]
+    int32_t* rowH;       // [rows] vertices of the row at the current level
+};
+
+template <bool WEIGHTED>
+__host__ __device__ inline size_t carve_ctl(void* base, int64_t rows, int64_t M, CtlWs* cw) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const size_t V = (size_t)M * ((size_t)C + 1);
+    size_t off = 0;
+    char* b = static_cast<char*>(base);
+    auto take = [&](size_t bytes) -> void* {
+        void* p = b ? (void*)(b + off) : nullptr;
+        off += align256(bytes);
+        return p;
+    };
+    CtlWs w;
+    for (int k = 0; k < 2; ++k) {
+        w.fS[k] = (int64_t*)take(8 * V);
+        w.fW[k] = WEIGHTED ? (int64_t*)take(8 * V) : nullptr;
+        w.tag[k] = (uint64_t*)take(8 * V);
+        w.base[k] = (int32_t*)take(4 * M);
+        w.size[k] = (int32_t*)take(4 * M);
+    }
+    w.desc = (int4*)take(16 * M);
+    w.runLo = (int32_t*)take(4 * M);
+    w.runHi = (int32_t*)take(4 * M);
+    w.rowH = (int32_t*)take(4 * rows);
+    if (cw) *cw = w;
+    return off;
+}
+
+// merge_plan's view of one level's flat arrays: node j (its first chunk) is
+// the single segment (j, lo, hi) of seg[j], over ranks of its array.
+template <bool WEIGHTED>
+struct FlatView {
+    int4* seg;
+    int32_t* cnt;
+    const int32_t* base;
+    const int64_t* S;
+    const int64_t* W;
+    const uint64_t* tag;
+    const i128* offS;
+    const i128* offW;
+    const int32_t* dS;
+    const int32_t* dW;
+    int C;
+
+    __device__ __forceinline__ Seg load(int k) const {
+        const int4 s = seg[k];
+        Seg g;
+        g.jc = s.x; g.lo = s.y; g.hi = s.z;
+        g.vb = base[s.x];
+        g.dS = 0; g.dW = 0;
+        g.oS = 0; g.oW = 0;
+        return g;
+    }
+    __device__ __forceinline__ void at(const Seg& g, int r, i128& Wv, i128& Sv) const {
+        const int64_t i = (int64_t)g.vb + r;
+        const uint64_t t = tag[i];
+        const int ch = (int)(t >> 32);
+        Sv = offS[ch] + conv(S[i], dS[ch]);
+        if constexpr (WEIGHTED) Wv = offW[ch] + conv(W[i], dW[ch]);
+        else Wv = (i128)((int64_t)ch * C + (int)(t & 0xffffu));
+    }
+};
+
+__device__ __forceinline__ bool ctl_bad(const LongWs& ws, int64_t row) { return ws.rowq[row * 4 + 2] != 0; }
+
+// Level 0: every chunk hull is a node; bases by a scan of the hull sizes.
+// One CTA per row.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(kMergeThreads)
+ctl_base_kernel(int64_t m, LongWs ws, CtlWs cw) {
+    __shared__ int s_tmp[32];
+    const int64_t row = blockIdx.x, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int64_t per = (m + nth - 1) / nth;
+    const int64_t jb = imin64(m, tid * per), je = imin64(m, jb + per);
+    int sum = 0;
+    for (int64_t j = jb; j < je; ++j) sum += ws.meta[c0 + j].h;
+    int total;
+    int b = block_excl_scan_int(sum, s_tmp, total);
+    for (int64_t j = jb; j < je; ++j) {
+        const int h = ws.meta[c0 + j].h;
+        cw.base[0][c0 + j] = b;
+        cw.size[0][c0 + j] = h;
+        ws.seg[c0 + j] = make_int4((int)j, 0, h - 1, 0);
+        ws.cnt[c0 + j] = 1;
+        cw.runLo[c0 + j] = -1;
+        b += h;
+    }
+    if (tid == 0) cw.rowH[row] = total;
+}
+
+// Level 0: each chunk's slot copied into the flat array, every vertex tagged.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(128)
+ctl_flatten_kernel(int64_t m, LongWs ws, CtlWs cw) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int64_t c = blockIdx.x, row = c / m, j = c - row * m, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int h = ws.meta[c].h;
+    const size_t cap = (size_t)C + 1;
+    const size_t d = (size_t)c0 * cap + (size_t)cw.base[0][c];
+    for (int r = threadIdx.x; r < h; r += blockDim.x) {
+        const size_t s = (size_t)c * cap + r;
+        cw.fS[0][d + r] = ws.slot_S[s];
+        if constexpr (WEIGHTED) cw.fW[0][d + r] = ws.slot_W[s];
+        cw.tag[0][d + r] = ((uint64_t)j << 32) | ((uint64_t)r << 16) | ws.slot_p[s];
+    }
+}
+
+// One level's bridges: one thread per merge of nodes j0 = 2 k half and
+// j1 = j0 + half (the paper's first control kernel).
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(128)
+ctl_bridge_kernel(int64_t m, int64_t half, int64_t nmerge, LongWs ws, CtlWs cw, int cur) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int64_t row = blockIdx.y, c0 = row * m;
+    const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= nmerge || ctl_bad(ws, row)) return;
+    const size_t R = (size_t)c0 * ((size_t)C + 1);
+    FlatView<WEIGHTED> V;
+    V.seg = ws.seg + c0;
+    V.cnt = ws.cnt + c0;
+    V.base = cw.base[cur] + c0;
+    V.S = cw.fS[cur] + R;
+    V.W = WEIGHTED ? cw.fW[cur] + R : nullptr;
+    V.tag = cw.tag[cur] + R;
+    V.offS = ws.offS + c0;
+    V.offW = ws.offW + c0;
+    V.dS = ws.dS + c0;
+    V.dW = ws.dW + c0;
+    V.C = C;
+    const int64_t j0 = 2 * k * half;
+    merge_plan<WEIGHTED>(V, (int)j0, (int)(j0 + half));
+}
+
+// One level's layout: each merged node's sources and size, bases by a scan,
+// and the nodes' single segments for the next level.  One CTA per row.
+__global__ void __launch_bounds__(kMergeThreads)
+ctl_scan_kernel(int64_t m, int64_t half, LongWs ws, CtlWs cw, int cur) {
+    __shared__ int s_tmp[32];
+    const int64_t row = blockIdx.x, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int nxt = cur ^ 1;
+    const int64_t step = 2 * half, nodes = (m + step - 1) / step;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int64_t per = (nodes + nth - 1) / nth;
+    const int64_t kb = imin64(nodes, tid * per), ke = imin64(nodes, kb + per);
+    int sum = 0;
+    for (int64_t k = kb; k < ke; ++k) {
+        const int64_t j = k * step, j1 = j + half;
+        int4 d;
+        if (j1 < m) {
+            const int4 sl = ws.seg[c0 + j], sr = ws.seg[c0 + j1];
+            d = make_int4(cw.base[cur][c0 + j] + sl.y, sl.z - sl.y + 1,
+                          cw.base[cur][c0 + j1] + sr.y, sr.z - sr.y + 1);
+        } else {
+            d = make_int4(cw.base[cur][c0 + j], cw.size[cur][c0 + j], 0, 0);
+        }
+        cw.desc[c0 + j] = d;
+        sum += d.y + d.w;
+    }
+    int total;
+    int b = block_excl_scan_int(sum, s_tmp, total);
+    for (int64_t k = kb; k < ke; ++k) {
+        const int64_t j = k * step;
+        const int4 d = cw.desc[c0 + j];
+        const int sz = d.y + d.w;
+        cw.base[nxt][c0 + j] = b;
+        cw.size[nxt][c0 + j] = sz;
+        ws.seg[c0 + j] = make_int4((int)j, 0, sz - 1, 0);
+        ws.cnt[c0 + j] = 1;
+        b += sz;
+    }
+    if (tid == 0) cw.rowH[row] = total;
+}
+
+// One level's copy: every surviving vertex of the row moves to its place in
+// the other buffer, the whole grid over the row's vertices (the paper's
+// second control kernel).  Each output position finds its node by bisection
+// over the level's node bases.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(256)
+ctl_copy_kernel(int64_t m, int64_t step, LongWs ws, CtlWs cw, int cur) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int64_t row = blockIdx.y, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int nxt = cur ^ 1;
+    const int64_t H = cw.rowH[row], nodes = (m + step - 1) / step;
+    const size_t R = (size_t)c0 * ((size_t)C + 1);
+    const int32_t* nb = cw.base[nxt] + c0;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < H;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        int64_t lo = 0, hi = nodes - 1;
+        while (lo < hi) {
+            const int64_t mid = (lo + hi + 1) >> 1;
+            if (nb[mid * step] <= p) lo = mid; else hi = mid - 1;
+        }
+        const int64_t j = lo * step;
+        const int64_t q = p - nb[j];
+        const int4 d = cw.desc[c0 + j];
+        const int64_t src = q < d.y ? d.x + q : d.z + (q - d.y);
+        cw.fS[nxt][R + p] = cw.fS[cur][R + src];
+        if constexpr (WEIGHTED) cw.fW[nxt][R + p] = cw.fW[cur][R + src];
+        cw.tag[nxt][R + p] = cw.tag[cur][R + src];
+    }
+}
+
+// The root array's runs of equal chunk: each chunk's first and last root rank.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(256)
+ctl_runs_kernel(int64_t m, LongWs ws, CtlWs cw, int cur) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int64_t row = blockIdx.y, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int64_t H = cw.rowH[row];
+    const uint64_t* tg = cw.tag[cur] + (size_t)c0 * ((size_t)C + 1);
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < H;
+         p += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t t = tg[p];
+        const int64_t ch = (int64_t)(t >> 32);
+        const int rank = (int)((t >> 16) & 0xffffu);
+        if (p == 0 || (int64_t)(tg[p - 1] >> 32) != ch) cw.runLo[c0 + ch] = rank;
+        if (p + 1 == H || (int64_t)(tg[p + 1] >> 32) != ch) cw.runHi[c0 + ch] = rank;
+    }
+}
+
+// The root list from the runs (at most one per chunk, in chunk order), then
+// the ends exactly as the segment lists compute them.  One CTA per row.
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(kMergeThreads)
+ctl_root_kernel(int64_t m, LongWs ws, CtlWs cw) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    __shared__ int s_tmp[32];
+    const int64_t row = blockIdx.x, c0 = row * m;
+    if (ctl_bad(ws, row)) return;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const int64_t per = (m + nth - 1) / nth;
+    const int64_t jb = imin64(m, tid * per), je = imin64(m, jb + per);
+    int sum = 0;
+    for (int64_t j = jb; j < je; ++j) sum += cw.runLo[c0 + j] >= 0 ? 1 : 0;
+    int total;
+    int k = block_excl_scan_int(sum, s_tmp, total);
+    for (int64_t j = jb; j < je; ++j)
+        if (cw.runLo[c0 + j] >= 0)
+            ws.seg[c0 + k++] = make_int4((int)j, cw.runLo[c0 + j], cw.runHi[c0 + j], 0);
+    if (tid == 0) ws.cnt[c0] = total;
+    __syncthreads();
+    MView<WEIGHTED, false> V;
+    V.c0 = c0;
+    V.C = C;
+    V.seg = ws.seg + c0;
+    V.cnt = ws.cnt + c0;
+    V.offS = ws.offS + c0;
+    V.offW = ws.offW + c0;
+    V.vb = nullptr;
+    V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
+    V.dS = ws.dS + c0; V.dW = ws.dW + c0;
+    root_ends<WEIGHTED>(V, m, ws, c0, ws.segOf + c0, ws.nextSeg + c0, ws.prevSeg + c0);
+}
+
 // Launch sizes: exact counts for a dense batch, bounds for a ragged one.
 struct LongGrid { int64_t rows, chunks, groups, ng; };
 
@@ -1411,6 +1709,81 @@ cudaError_t long_fit_ragged(const float* y, const float* w, const int64_t* off,
                                        blocks, ws, row_status, stream)
              : long_fit_ragged_t<false>(y, w, off, long_id, nlong, rows_max, total, increasing,
                                         out, blocks, ws, row_status, stream);
+}
+
+size_t long_control_workspace(int64_t rows, int64_t n, bool weighted) {
+    const int64_t C = weighted ? LongCfg<true>::C : LongCfg<false>::C;
+    const int64_t M = rows * ((n + C - 1) / C);
+    return weighted ? carve<true>(nullptr, rows, M, nullptr) + carve_ctl<true>(nullptr, rows, M, nullptr)
+                    : carve<false>(nullptr, rows, M, nullptr) + carve_ctl<false>(nullptr, rows, M, nullptr);
+}
+
+template <bool WEIGHTED>
+static cudaError_t long_control_t(const float* y, const float* w, int64_t rows, int64_t n,
+                                  int increasing, float* out, uint8_t* blocks, void* wsp,
+                                  uint32_t* row_status, cudaStream_t stream) {
+    constexpr int NT = LongCfg<WEIGHTED>::NT;
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    using SM = TileSmem<NT, WEIGHTED, false, 1>;
+    const int64_t m = (n + C - 1) / C, M = rows * m;
+    LongWs ws;
+    const size_t off = carve<WEIGHTED>(wsp, rows, M, &ws);
+    CtlWs cw;
+    carve_ctl<WEIGHTED>(static_cast<char*>(wsp) + off, rows, M, &cw);
+    LongGeo geo;
+    geo.n = n;
+    geo.m = m;
+    const int64_t ng = (m + kGroup - 1) / kGroup;
+    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, false>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
+    if (err != cudaSuccess) return err;
+    chunk_hull_kernel<WEIGHTED, false><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, geo,
+                                                                               increasing, ws);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "chunk_hull");
+    // the rows' grids and the chunks' starts, without merging
+    err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
+    if (err != cudaSuccess) return err;
+    merge_groups_kernel<WEIGHTED, false, false><<<(unsigned)(rows * ng), kGroupThreads, kGroupSmem,
+                                                  stream>>>(geo, ng, ws, row_status);
+    ctl_base_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, 0, stream>>>(m, ws, cw);
+    ctl_flatten_kernel<WEIGHTED><<<(unsigned)M, 128, 0, stream>>>(m, ws, cw);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "ctl_setup");
+    const unsigned xg = (unsigned)std::max<int64_t>(1, (152 * 8) / rows);
+    int cur = 0;
+    for (int64_t half = 1; half < m; half *= 2) {
+        const int64_t nmerge = ((m + half - 1) / half) / 2;
+        ctl_bridge_kernel<WEIGHTED><<<dim3((unsigned)((nmerge + 127) / 128), (unsigned)rows), 128, 0,
+                                      stream>>>(m, half, nmerge, ws, cw, cur);
+        ctl_scan_kernel<<<(unsigned)rows, kMergeThreads, 0, stream>>>(m, half, ws, cw, cur);
+        ctl_copy_kernel<WEIGHTED><<<dim3(xg, (unsigned)rows), 256, 0, stream>>>(m, 2 * half, ws, cw,
+                                                                                cur);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        cur ^= 1;
+    }
+    prof_mark(stream, "ctl_merge_levels");
+    ctl_runs_kernel<WEIGHTED><<<dim3(xg, (unsigned)rows), 256, 0, stream>>>(m, ws, cw, cur);
+    ctl_root_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, 0, stream>>>(m, ws, cw);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "ctl_root");
+    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ExpandSmem<WEIGHTED>::kBytes);
+    if (err != cudaSuccess) return err;
+    expand_kernel<WEIGHTED, false><<<(unsigned)M, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
+        y, geo, increasing, ws, out, blocks);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    prof_mark(stream, "expand");
+    return cudaSuccess;
+}
+
+cudaError_t long_fit_control(const float* y, const float* w, int64_t rows, int64_t n,
+                             int increasing, float* out, uint8_t* blocks, void* ws,
+                             uint32_t* row_status, cudaStream_t stream) {
+    return w ? long_control_t<true>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream)
+             : long_control_t<false>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream);
 }
 
 }  // namespace isodev

@@ -205,6 +205,26 @@ iso_status iso_fit_ragged(const float *y, const float *w, const int64_t *offsets
                           uint32_t *row_status, void *stream);
 
 /*
+ * iso_fit_copy_control -- a measurement control, not a faster fit: the same
+ * fit as iso_fit (bit for bit), with the merge levels of rows longer than
+ * 8,192 elements run on materialised hulls instead of segment lists -- the
+ * paper's "grid copying" control of Section 7.3: after every level's bridges
+ * are found (the same search), every merged hull's surviving vertices are
+ * copied into a second flat array by the whole grid.  It measures what the
+ * segment lists save; rows of up to 8,192 elements (no merge tree) take the
+ * whole-row kernels as in iso_fit.
+ *
+ * Arguments, results and errors as iso_fit, with a workspace of
+ * iso_fit_copy_control_workspace_bytes(rows, n, weighted) bytes (about four
+ * times iso_fit's: two flat buffers of C + 1 vertex records per chunk);
+ * n <= 2^30.
+ */
+size_t iso_fit_copy_control_workspace_bytes(int64_t rows, int64_t n, int weighted);
+iso_status iso_fit_copy_control(const float *y, const float *w, int64_t rows, int64_t n,
+                                int increasing, float *out, uint8_t *blocks, void *workspace,
+                                size_t workspace_bytes, uint32_t *row_status, void *stream);
+
+/*
  * iso_backward_noalloc -- iso_backward for callers that cannot allocate device
  * memory (no counterpart in the paper: it is an interface addition).
  *

@@ -96,3 +96,15 @@ def test_ragged_host_checks():
     assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, None, 0)) == chp.ISO_ERR_WORKSPACE
     assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, ws, need - 1)) == chp.ISO_ERR_WORKSPACE
     assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 1, fake, ctypes.c_void_p(0x100010), need)) == chp.ISO_ERR_WORKSPACE
+
+
+def test_copy_control_host_checks():
+    lib = chp.load_library()
+    fake = ctypes.c_void_p(0x1000)
+    assert chp.iso_fit_copy_control_workspace_bytes(4096, 1024, False) == 0
+    big = chp.iso_fit_copy_control_workspace_bytes(1, 10_000_000, False)
+    assert big > chp.iso_fit_workspace_bytes(1, 10_000_000, False)
+    assert chp.iso_fit_copy_control_workspace_bytes(1, (1 << 30) + 1, False) == 0
+    assert lib.iso_fit_copy_control(None, None, 1, 100000, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_copy_control(fake, None, 1, (1 << 30) + 1, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_copy_control(fake, None, 1, 100000, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_WORKSPACE
