@@ -210,6 +210,7 @@ def run_reference(args):
 def copy_control(name, make, dev, flush, stream):
     """Median per-stage times (CUDA events around each kernel) of iso_fit and of
     the materialised-copy control on one workload."""
+    import numpy as np
     import torch
     import convex_hull_pava_gb300 as chp
     yh, wh, inc = make()
@@ -437,7 +438,7 @@ def run_gpu(args):
                 ts.append(a.elapsed_time(b))
         t = float(np.median(ts)) * 1e-3
         by = yr.numel() * 13 + off_h.nbytes
-        also["ragged_calibration_65544"] = {
+        also["ragged_calibration_65536"] = {
             "segments": int(lens.size), "elements": int(yr.numel()),
             "elements_per_s": yr.numel() / t, "ms": t * 1e3, "gbs": by / t / 1e9,
             "frac": by / t / 1e9 / hbm_peak, "bytes": by}
