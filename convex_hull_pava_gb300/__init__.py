@@ -8,7 +8,8 @@ library or a CUDA device the calls raise.
 
 Entry points (same names as the C ABI):
 
-* :func:`iso_fit` -- forward fit of ``[rows, n]`` float32 CUDA tensors.
+* :func:`iso_fit` -- forward fit of ``[rows, n]`` float32 or float64 CUDA
+  tensors (float64 calls go to the ABI's ``_f64`` twins).
 * :func:`iso_backward` -- block-averaging backward.
 * :func:`iso_fit_ragged` -- forward fit of segments of unequal lengths laid
   end to end (int64 offsets on the device).
@@ -40,6 +41,7 @@ EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_f
            "iso_backward_workspace_bytes", "iso_backward", "iso_backward_w",
            "iso_backward_noalloc", "iso_fit_ragged_workspace_bytes", "iso_fit_ragged",
            "iso_fit_copy_control_workspace_bytes", "iso_fit_copy_control",
+           "iso_fit_f64", "iso_backward_f64", "iso_backward_w_f64", "iso_fit_ragged_f64",
            "iso_profile_enable", "iso_profile_read")
 
 _lib = None
@@ -88,6 +90,10 @@ def load_library(path: str | None = None):
         lib.iso_fit_copy_control_workspace_bytes.restype = sz
         lib.iso_fit_copy_control.argtypes = [vp, vp, i64, i64, ci, vp, vp, vp, sz, vp, vp]
         lib.iso_fit_copy_control.restype = ci
+        for name in ("iso_fit", "iso_backward", "iso_backward_w", "iso_fit_ragged"):
+            f64 = getattr(lib, name + "_f64")
+            f64.argtypes = getattr(lib, name).argtypes
+            f64.restype = ci
         lib.iso_profile_enable.argtypes = [ci]
         lib.iso_profile_enable.restype = ci
         lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
@@ -146,6 +152,20 @@ def _check_dev(t, name, dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _io_dtype(t, name):
+    """The I/O type of a call: float32 or float64, taken from its first array."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.dtype not in (torch.float32, torch.float64):
+        raise ValueError(f"{name} must be a float32 or float64 tensor")
+    return t.dtype
+
+
+def _entry(name, dtype):
+    """The ABI function for the I/O type: name, or name + '_f64' for float64."""
+    torch = _torch()
+    return getattr(load_library(), name + ("_f64" if dtype == torch.float64 else ""))
+
+
 def _shape2(t):
     if t.dim() == 1:
         return 1, t.shape[0]
@@ -178,21 +198,23 @@ def iso_fit(y, w=None, increasing: bool = True, *, out=None, blocks=None, want_b
     CUDA tensor of at least :func:`iso_fit_workspace_bytes` bytes (allocated
     here otherwise)."""
     torch = _torch()
-    _check_dev(y, "y", torch.float32)
+    dt = _io_dtype(y, "y")
+    _check_dev(y, "y", dt)
     rows, n = _shape2(y)
     if w is not None:
-        _check_dev(w, "w", torch.float32)
+        _check_dev(w, "w", dt)
         if w.shape != y.shape:
             raise ValueError("w must have the shape of y")
     if out is None:
         out = torch.empty_like(y)
+    _check_dev(out, "out", dt)
     if blocks is None and want_blocks:
         blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
     if row_status is None:
         row_status = torch.empty(rows, dtype=torch.int32, device=y.device)
     nbytes = iso_fit_workspace_bytes(rows, n, w is not None)
     ws, ws_bytes = _workspace(nbytes, workspace, y.device)
-    st = load_library().iso_fit(
+    st = _entry("iso_fit", dt)(
         y.data_ptr(), None if w is None else w.data_ptr(), rows, n, int(bool(increasing)),
         out.data_ptr(), None if blocks is None else blocks.data_ptr(),
         None if ws is None else ws.data_ptr(), ws_bytes, row_status.data_ptr(), _stream_ptr(stream))
@@ -245,13 +267,14 @@ def iso_fit_ragged(y, offsets, w=None, increasing: bool = True, *, max_len: int 
     (``ISO_ROW_BAD_SHAPE`` in its status word).  Returns ``(out, blocks,
     row_status)``, ``row_status`` one word per segment."""
     torch = _torch()
-    _check_dev(y, "y", torch.float32)
+    dt = _io_dtype(y, "y")
+    _check_dev(y, "y", dt)
     _check_dev(offsets, "offsets", torch.int64)
     if y.dim() != 1 or offsets.dim() != 1 or offsets.numel() < 2:
         raise ValueError("expected a 1-D y and at least two offsets")
     total, segments = y.numel(), offsets.numel() - 1
     if w is not None:
-        _check_dev(w, "w", torch.float32)
+        _check_dev(w, "w", dt)
         if w.shape != y.shape:
             raise ValueError("w must have the shape of y")
     if out is None:
@@ -262,7 +285,9 @@ def iso_fit_ragged(y, offsets, w=None, increasing: bool = True, *, max_len: int 
         row_status = torch.empty(segments, dtype=torch.int32, device=y.device)
     nbytes = iso_fit_ragged_workspace_bytes(segments, total, max_len, w is not None)
     ws, ws_bytes = _workspace(nbytes, workspace, y.device)
-    st = load_library().iso_fit_ragged(
+    if out is not None:
+        _check_dev(out, "out", dt)
+    st = _entry("iso_fit_ragged", dt)(
         y.data_ptr(), None if w is None else w.data_ptr(), offsets.data_ptr(), segments, total,
         int(max_len), int(bool(increasing)), out.data_ptr(),
         None if blocks is None else blocks.data_ptr(), None if ws is None else ws.data_ptr(),
@@ -275,16 +300,18 @@ def iso_fit_ragged(y, offsets, w=None, increasing: bool = True, *, max_len: int 
 def iso_backward(grad, blocks, w=None, *, out=None, workspace=None, stream=None):
     """Block-averaging backward: ``out_i = w_i * G / W`` over the blocks of ``blocks``."""
     torch = _torch()
-    _check_dev(grad, "grad", torch.float32)
+    dt = _io_dtype(grad, "grad")
+    _check_dev(grad, "grad", dt)
     _check_dev(blocks, "blocks", torch.uint8)
     rows, n = _shape2(grad)
     if w is not None:
-        _check_dev(w, "w", torch.float32)
+        _check_dev(w, "w", dt)
     if out is None:
         out = torch.empty_like(grad)
+    _check_dev(out, "out", dt)
     nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
     ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
-    st = load_library().iso_backward(
+    st = _entry("iso_backward", dt)(
         grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), rows, n,
         out.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))
     if st != ISO_OK:
@@ -298,20 +325,21 @@ def iso_backward_w(grad, blocks, w, y, fit, *, out_dy=None, out_dw=None, want_dy
     ``d/dw_i = (y_i - z_i) * G / W`` over the blocks of ``blocks`` (``w`` may be
     None: unit weights).  Returns ``(dy or None, dw)``."""
     torch = _torch()
-    _check_dev(grad, "grad", torch.float32)
+    dt = _io_dtype(grad, "grad")
+    _check_dev(grad, "grad", dt)
     _check_dev(blocks, "blocks", torch.uint8)
-    _check_dev(y, "y", torch.float32)
-    _check_dev(fit, "fit", torch.float32)
+    _check_dev(y, "y", dt)
+    _check_dev(fit, "fit", dt)
     rows, n = _shape2(grad)
     if w is not None:
-        _check_dev(w, "w", torch.float32)
+        _check_dev(w, "w", dt)
     if want_dy and out_dy is None:
         out_dy = torch.empty_like(grad)
     if out_dw is None:
         out_dw = torch.empty_like(grad)
     nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
     ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
-    st = load_library().iso_backward_w(
+    st = _entry("iso_backward_w", dt)(
         grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), y.data_ptr(),
         fit.data_ptr(), rows, n, None if out_dy is None else out_dy.data_ptr(),
         out_dw.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))

@@ -42,6 +42,90 @@ bool shape_ok(int64_t rows, int64_t n) {
 
 iso_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ISO_OK : ISO_ERR_CUDA; }
 
+// Typed implementations of the entry points: IO is the I/O type (float or
+// double); the arithmetic inside is the same fixed point for both.
+template <class IO>
+iso_status fit_impl(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing, IO* out,
+                    uint8_t* blocks, void* workspace, size_t workspace_bytes,
+                    uint32_t* row_status, void* stream) {
+    if (!y || !out || !shape_ok(rows, n) || (increasing != 0 && increasing != 1))
+        return ISO_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    if (n <= isodev::kRowMax)
+        return from_cuda(isodev::rows_fit<IO>(y, w, rows, (int)n, increasing, out, blocks,
+                                              row_status, st));
+    const size_t need = isodev::long_fit_workspace(rows, n, w != nullptr);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return ISO_ERR_WORKSPACE;
+    return from_cuda(isodev::long_fit<IO>(y, w, rows, n, increasing, out, blocks, workspace,
+                                          workspace_bytes, row_status, st));
+}
+
+bool ragged_ok(int64_t segments, int64_t total, int64_t max_len) {
+    return segments >= 1 && segments <= kMaxN && total >= 1 && total <= kMaxElems &&
+           max_len <= kMaxN;
+}
+int64_t ragged_max_len(int64_t total, int64_t max_len) {
+    return max_len <= 0 || max_len > total ? total : max_len;
+}
+
+template <class IO>
+iso_status ragged_impl(const IO* y, const IO* w, const int64_t* offsets, int64_t segments,
+                       int64_t total, int64_t max_len, int increasing, IO* out, uint8_t* blocks,
+                       void* workspace, size_t workspace_bytes, uint32_t* row_status,
+                       void* stream) {
+    if (!y || !offsets || !out || !ragged_ok(segments, total, max_len) ||
+        (increasing != 0 && increasing != 1))
+        return ISO_ERR_INVALID_ARG;
+    const int64_t ml = ragged_max_len(total, max_len);
+    if (ml > kMaxN) return ISO_ERR_INVALID_ARG;
+    const size_t need = isodev::ragged_workspace(segments, total, ml, w != nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ISO_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    return from_cuda(isodev::ragged_fit<IO>(y, w, offsets, segments, total, ml, increasing, out,
+                                            blocks, workspace, row_status, st));
+}
+
+template <class IO>
+iso_status control_impl(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing,
+                        IO* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
+                        uint32_t* row_status, void* stream) {
+    if (!y || !out || !shape_ok(rows, n) || n > (1LL << 30) || (increasing != 0 && increasing != 1))
+        return ISO_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    if (n <= isodev::kRowMax)
+        return from_cuda(isodev::rows_fit<IO>(y, w, rows, (int)n, increasing, out, blocks,
+                                              row_status, st));
+    const size_t need = isodev::long_control_workspace(rows, n, w != nullptr);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ISO_ERR_WORKSPACE;
+    return from_cuda(isodev::long_fit_control<IO>(y, w, rows, n, increasing, out, blocks,
+                                                  workspace, row_status, st));
+}
+
+// Both gradients (out_dy and/or out_dw; y and fit needed only for out_dw).
+template <class IO>
+iso_status backward_impl(const IO* grad, const uint8_t* blocks, const IO* w, const IO* y,
+                         const IO* fit, int64_t rows, int64_t n, IO* out_dy, IO* out_dw,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    isodev::prof_start(st);
+    if (n <= isodev::kRowMax)
+        return from_cuda(isodev::rows_backward<IO>(grad, blocks, w, rows, (int)n, out_dy, y, fit,
+                                                   out_dw, st));
+    const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
+    if (need > 0 && (!workspace || workspace_bytes < need ||
+                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
+        return ISO_ERR_WORKSPACE;
+    return from_cuda(isodev::long_backward<IO>(grad, blocks, w, rows, n, out_dy, y, fit, out_dw,
+                                               workspace, workspace_bytes, st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -68,30 +152,16 @@ size_t iso_fit_workspace_bytes(int64_t rows, int64_t n, int weighted) {
 iso_status iso_fit(const float* y, const float* w, int64_t rows, int64_t n, int increasing,
                    float* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
                    uint32_t* row_status, void* stream) {
-    if (!y || !out || !shape_ok(rows, n) || (increasing != 0 && increasing != 1))
-        return ISO_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    isodev::prof_start(st);
-    if (n <= isodev::kRowMax)
-        return from_cuda(isodev::rows_fit(y, w, rows, (int)n, increasing, out, blocks,
-                                          row_status, st));
-    const size_t need = isodev::long_fit_workspace(rows, n, w != nullptr);
-    if (need > 0 && (!workspace || workspace_bytes < need ||
-                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
-        return ISO_ERR_WORKSPACE;
-    return from_cuda(isodev::long_fit(y, w, rows, n, increasing, out, blocks, workspace,
-                                      workspace_bytes, row_status, st));
+    return fit_impl<float>(y, w, rows, n, increasing, out, blocks, workspace, workspace_bytes,
+                           row_status, stream);
 }
 
-namespace {
-bool ragged_ok(int64_t segments, int64_t total, int64_t max_len) {
-    return segments >= 1 && segments <= kMaxN && total >= 1 && total <= kMaxElems &&
-           max_len <= kMaxN;
+iso_status iso_fit_f64(const double* y, const double* w, int64_t rows, int64_t n, int increasing,
+                       double* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
+                       uint32_t* row_status, void* stream) {
+    return fit_impl<double>(y, w, rows, n, increasing, out, blocks, workspace, workspace_bytes,
+                            row_status, stream);
 }
-int64_t ragged_max_len(int64_t total, int64_t max_len) {
-    return max_len <= 0 || max_len > total ? total : max_len;
-}
-}  // namespace
 
 size_t iso_fit_ragged_workspace_bytes(int64_t segments, int64_t total, int64_t max_len,
                                       int weighted) {
@@ -103,18 +173,16 @@ iso_status iso_fit_ragged(const float* y, const float* w, const int64_t* offsets
                           int64_t segments, int64_t total, int64_t max_len, int increasing,
                           float* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
                           uint32_t* row_status, void* stream) {
-    if (!y || !offsets || !out || !ragged_ok(segments, total, max_len) ||
-        (increasing != 0 && increasing != 1))
-        return ISO_ERR_INVALID_ARG;
-    const int64_t ml = ragged_max_len(total, max_len);
-    if (ml > kMaxN) return ISO_ERR_INVALID_ARG;
-    const size_t need = isodev::ragged_workspace(segments, total, ml, w != nullptr);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return ISO_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    isodev::prof_start(st);
-    return from_cuda(isodev::ragged_fit(y, w, offsets, segments, total, ml, increasing, out, blocks,
-                                        workspace, row_status, st));
+    return ragged_impl<float>(y, w, offsets, segments, total, max_len, increasing, out, blocks,
+                              workspace, workspace_bytes, row_status, stream);
+}
+
+iso_status iso_fit_ragged_f64(const double* y, const double* w, const int64_t* offsets,
+                              int64_t segments, int64_t total, int64_t max_len, int increasing,
+                              double* out, uint8_t* blocks, void* workspace,
+                              size_t workspace_bytes, uint32_t* row_status, void* stream) {
+    return ragged_impl<double>(y, w, offsets, segments, total, max_len, increasing, out, blocks,
+                               workspace, workspace_bytes, row_status, stream);
 }
 
 size_t iso_fit_copy_control_workspace_bytes(int64_t rows, int64_t n, int weighted) {
@@ -126,18 +194,8 @@ size_t iso_fit_copy_control_workspace_bytes(int64_t rows, int64_t n, int weighte
 iso_status iso_fit_copy_control(const float* y, const float* w, int64_t rows, int64_t n,
                                 int increasing, float* out, uint8_t* blocks, void* workspace,
                                 size_t workspace_bytes, uint32_t* row_status, void* stream) {
-    if (!y || !out || !shape_ok(rows, n) || n > (1LL << 30) || (increasing != 0 && increasing != 1))
-        return ISO_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    isodev::prof_start(st);
-    if (n <= isodev::kRowMax)
-        return from_cuda(isodev::rows_fit(y, w, rows, (int)n, increasing, out, blocks,
-                                          row_status, st));
-    const size_t need = isodev::long_control_workspace(rows, n, w != nullptr);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return ISO_ERR_WORKSPACE;
-    return from_cuda(isodev::long_fit_control(y, w, rows, n, increasing, out, blocks, workspace,
-                                              row_status, st));
+    return control_impl<float>(y, w, rows, n, increasing, out, blocks, workspace,
+                               workspace_bytes, row_status, stream);
 }
 
 size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted) {
@@ -150,34 +208,33 @@ iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w
                         int64_t n, float* out, void* workspace, size_t workspace_bytes,
                         void* stream) {
     if (!grad || !blocks || !out || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    isodev::prof_start(st);
-    if (n <= isodev::kRowMax)
-        return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out, nullptr, nullptr,
-                                               nullptr, st));
-    const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
-    if (need > 0 && (!workspace || workspace_bytes < need ||
-                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
-        return ISO_ERR_WORKSPACE;
-    return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out, nullptr, nullptr, nullptr,
-                                           workspace, workspace_bytes, st));
+    return backward_impl<float>(grad, blocks, w, nullptr, nullptr, rows, n, out, nullptr,
+                                workspace, workspace_bytes, stream);
+}
+
+iso_status iso_backward_f64(const double* grad, const uint8_t* blocks, const double* w,
+                            int64_t rows, int64_t n, double* out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (!grad || !blocks || !out || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
+    return backward_impl<double>(grad, blocks, w, nullptr, nullptr, rows, n, out, nullptr,
+                                 workspace, workspace_bytes, stream);
 }
 
 iso_status iso_backward_w(const float* grad, const uint8_t* blocks, const float* w, const float* y,
                           const float* fit, int64_t rows, int64_t n, float* out_dy, float* out_dw,
                           void* workspace, size_t workspace_bytes, void* stream) {
     if (!grad || !blocks || !y || !fit || !out_dw || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    isodev::prof_start(st);
-    if (n <= isodev::kRowMax)
-        return from_cuda(isodev::rows_backward(grad, blocks, w, rows, (int)n, out_dy, y, fit, out_dw,
-                                               st));
-    const size_t need = isodev::long_backward_workspace(rows, n, w != nullptr);
-    if (need > 0 && (!workspace || workspace_bytes < need ||
-                     (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0))
-        return ISO_ERR_WORKSPACE;
-    return from_cuda(isodev::long_backward(grad, blocks, w, rows, n, out_dy, y, fit, out_dw,
-                                           workspace, workspace_bytes, st));
+    return backward_impl<float>(grad, blocks, w, y, fit, rows, n, out_dy, out_dw, workspace,
+                                workspace_bytes, stream);
+}
+
+iso_status iso_backward_w_f64(const double* grad, const uint8_t* blocks, const double* w,
+                              const double* y, const double* fit, int64_t rows, int64_t n,
+                              double* out_dy, double* out_dw, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    if (!grad || !blocks || !y || !fit || !out_dw || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
+    return backward_impl<double>(grad, blocks, w, y, fit, rows, n, out_dy, out_dw, workspace,
+                                 workspace_bytes, stream);
 }
 
 int iso_profile_enable(int on) {

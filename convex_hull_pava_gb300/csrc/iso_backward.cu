@@ -3,9 +3,9 @@
 // d/dy_i = w_i * G / W with G, W the sums of grad and w over element i's block.
 // Blocks are given by the block-start bytes of the forward pass.
 //
-// Sums are exact: grad and w are rounded to a fixed-point grid of 2^-31 of the
+// Sums are exact: grad and w are rounded to a fixed-point grid of 2^-50 of the
 // tile's largest magnitude and summed as integers, so the result does not
-// depend on the order of the additions.  A row that is one tile is finished in
+// depend on the order of the additions.  The I/O type IO is float or double.  A row that is one tile is finished in
 // one kernel; a longer row takes three steps (tile sums, a pass over the
 // tiles' boundary sums, and the fill of blocks that cross tiles), as in the
 // paper, without atomics.
@@ -19,11 +19,12 @@ namespace {
 // Shared memory of a backward CTA of NT lanes: grad (and w) staging, which
 // later holds each run's ratio and then the output, and the lanes' carries of
 // the two segmented scans.
-template <int NT, bool WEIGHTED>
+template <int NT, bool WEIGHTED, class IO = float>
 struct BwdSmem {
+    static constexpr int kRowB = 32 * (int)sizeof(IO);                // one lane's 32 values
     static constexpr int oStage = 0;                                  // grad, ratios, output
-    static constexpr int oStageW = oStage + NT * 128;                 // w
-    static constexpr int oCarry = oStageW + (WEIGHTED ? NT * 128 : 0);   // [4][NT] int64
+    static constexpr int oStageW = oStage + NT * kRowB;               // w
+    static constexpr int oCarry = oStageW + (WEIGHTED ? NT * kRowB : 0);   // [4][NT] int64
     static constexpr int oWarp = oCarry + 4 * NT * 8;                 // [4][NT/32] int64 + flags
     static constexpr int oWarpF = oWarp + 4 * (NT / 32) * 8;          // [2][NT/32] int
     static constexpr int oInfo = oWarpF + 2 * (NT / 32) * 4;          // per tile: 8 int64
@@ -48,11 +49,18 @@ enum { kSlotTW = 4, kSlotHG = 5, kSlotHW = 6, kSlotTG = 7 };
 
 // Optional weight gradient: d/dw_i = (y_i - z_i) G / W (the paper's Section 6,
 // "Gradient"), from the fit z of the forward pass.
+template <class IO>
 struct WGrad {
-    const float* y;      // the forward pass's input, [rows, n]
-    const float* fit;    // its output z, [rows, n]
-    float* dw;           // nullptr: not wanted
+    const IO* y;      // the forward pass's input, [rows, n]
+    const IO* fit;    // its output z, [rows, n]
+    IO* dw;           // nullptr: not wanted
 };
+
+// Component j of a 16-byte vector of the I/O type.
+__device__ __forceinline__ float vcomp(const float4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ double vcomp(const double2& v, int j) { return j == 0 ? v.x : v.y; }
 
 // One tile of L lanes (32 elements each): every element gets w_i G / W of its
 // block, where the block's sums come from the lane's own run sums and, for
@@ -63,15 +71,15 @@ struct WGrad {
 // tile's part; the long-row path completes them.  All threads of the CTA call
 // it.  On return, stage holds the output of the tile's elements and, for
 // weighted tiles, the w staging holds each element's ratio G / W.
-template <int NT, bool WEIGHTED>
-__device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
+template <int NT, bool WEIGHTED, class IO>
+__device__ __forceinline__ void bwd_tile_phase(const IO* __restrict__ gr,
                                                const uint8_t* __restrict__ br,
-                                               const float* __restrict__ wr, int nt, bool live,
+                                               const IO* __restrict__ wr, int nt, bool live,
                                                bool first_is_start, int L, unsigned char* smem,
                                                BwdTile& B) {
-    using SM = BwdSmem<NT, WEIGHTED>;
-    float* stage = reinterpret_cast<float*>(smem + SM::oStage);
-    float* stagew = reinterpret_cast<float*>(smem + SM::oStageW);
+    using SM = BwdSmem<NT, WEIGHTED, IO>;
+    IO* stage = reinterpret_cast<IO*>(smem + SM::oStage);
+    IO* stagew = reinterpret_cast<IO*>(smem + SM::oStageW);
     int64_t* carry = reinterpret_cast<int64_t*>(smem + SM::oCarry);
     int64_t* wsum = reinterpret_cast<int64_t*>(smem + SM::oWarp);
     int* wflag = reinterpret_cast<int*>(smem + SM::oWarpF);
@@ -98,8 +106,9 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     uint32_t starts = 0;
     const int e = live ? min(max(nt - (lane << 5), 0), 32) : 0;
     if (live) {
-        stage_tile<false>(gr, nt, lane, L, tile * L, false, stage, gmax, bad);
-        if constexpr (WEIGHTED) stage_tile<true>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
+        stage_tile<false, IO>(gr, nt, lane, L, tile * L, false, stage, gmax, bad);
+        if constexpr (WEIGHTED)
+            stage_tile<true, IO>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
         // the lane's 32 block-start bytes, as a bit mask
         const uint8_t* bl = br + (lane << 5);
         if (e == 32 && (reinterpret_cast<uintptr_t>(bl) & 15u) == 0) {
@@ -138,28 +147,30 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     gmax = max(info[kBInfoG], 1);
     ewmax = max(info[kBInfoW], 1);
     B.nan = info[kBInfoBad] != 0;
-    B.qg = qexp_unit(gmax);
-    B.qw = WEIGHTED ? qexp_unit(ewmax) : 0;
+    B.qg = qexp_unit_t<IO>(gmax);
+    B.qw = WEIGHTED ? qexp_unit_t<IO>(ewmax) : 0;
     B.first_start = info[kBInfoFs] == 0x7fffffff ? -1 : info[kBInfoFs];
     B.last_start = info[kBInfoLs];
-    const Quant qg(gmax), qwt(ewmax);
+    const QuantT<IO> qg(gmax), qwt(ewmax);
 
-    const float4* st4 = reinterpret_cast<const float4*>(stage);
-    const float4* sw4 = reinterpret_cast<const float4*>(stagew);
-    auto lane_values = [&](int q, float (&vv)[4], float (&ww)[4]) {
-        const int unit = (gl << 3) | ((q ^ gl) & 7);
-        const float4 v = st4[unit];
-        vv[0] = v.x; vv[1] = v.y; vv[2] = v.z; vv[3] = v.w;
-        ww[0] = ww[1] = ww[2] = ww[3] = 1.0f;
+    using V = typename IoT<IO>::V;
+    constexpr int P = IoT<IO>::kPerV;
+    const V* stv = reinterpret_cast<const V*>(stage);
+    const V* swv = reinterpret_cast<const V*>(stagew);
+    auto lane_values = [&](int q, IO (&vv)[P], IO (&ww)[P]) {
+        const int unit = sunit_t<IO>(gl, q);
+        const V v = stv[unit];
+#pragma unroll
+        for (int j = 0; j < P; ++j) { vv[j] = vcomp(v, j); ww[j] = IO(1); }
         if constexpr (WEIGHTED) {
-            const float4 t = sw4[unit];
-            ww[0] = t.x; ww[1] = t.y; ww[2] = t.z; ww[3] = t.w;
+            const V t = swv[unit];
+#pragma unroll
+            for (int j = 0; j < P; ++j) ww[j] = vcomp(t, j);
         }
     };
-    const Pow2 scale(B.qg - B.qw);
-    const float qnan = __int_as_float(0x7fffffff);
-    auto ratio = [&](int64_t G, int64_t Wt) {
-        return B.nan ? qnan : scale(i64_to_f32(G) / i64_to_f32(Wt));
+    const IO qnan = qnan_t<IO>();
+    auto ratio = [&](int64_t G, int64_t Wt) -> IO {
+        return B.nan ? qnan : ratio_t<IO>(G, Wt, B.qg - B.qw);
     };
     // pass 1: the lane's head (before its first start) and tail (from its
     // last start) sums, a lane without a start having head = tail = its total;
@@ -169,14 +180,14 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     {
         bool seen = false;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float vv[4], ww[4];
+        for (int q = 0; q < 32 / P; ++q) {
+            IO vv[P], ww[P];
             lane_values(q, vv, ww);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int k = 4 * q + j;
+            for (int j = 0; j < P; ++j) {
+                const int k = P * q + j;
                 if ((starts >> k) & 1u) {
-                    if (seen) stage[spos(gl, k - 1)] = ratio(tg, tw);
+                    if (seen) stage[spos_t<IO>(gl, k - 1)] = ratio(tg, tw);
                     else { hg = tg; hw = tw; seen = true; }
                     tg = 0; tw = 0;
                 }
@@ -268,20 +279,20 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     if (e > 0) {
         if (starts) {
             const int f = __ffs(starts) - 1;
-            if (f > 0) stage[spos(gl, f - 1)] = ratio(cing + hg, cinw + hw);
-            stage[spos(gl, e - 1)] = ratio(tg + coutg, tw + coutw);
+            if (f > 0) stage[spos_t<IO>(gl, f - 1)] = ratio(cing + hg, cinw + hw);
+            stage[spos_t<IO>(gl, e - 1)] = ratio(tg + coutg, tw + coutw);
         } else {
-            stage[spos(gl, e - 1)] = ratio(cing + tg + coutg, cinw + tw + coutw);
+            stage[spos_t<IO>(gl, e - 1)] = ratio(cing + tg + coutg, cinw + tw + coutw);
         }
     }
     // pass 2, backwards: each element takes the ratio of its run (times w)
     {
-        float r = 0.0f;
+        IO r = IO(0);
 #pragma unroll
         for (int k = 31; k >= 0; --k) {
             if (k < e) {
                 const bool last = k == e - 1 || ((starts >> (k + 1)) & 1u);
-                const int p = spos(gl, k);
+                const int p = spos_t<IO>(gl, k);
                 if (last) r = stage[p];
                 if constexpr (WEIGHTED) {
                     stage[p] = stagew[p] * r;
@@ -299,13 +310,13 @@ __device__ __forceinline__ void bwd_tile_phase(const float* __restrict__ gr,
     B.tW = info64[tile * 8 + kSlotTW];
 }
 
-template <int NT, bool WEIGHTED>
+template <int NT, bool WEIGHTED, class IO>
 __global__ void __launch_bounds__(NT)
-rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__ blocks,
-                     const float* __restrict__ w, int64_t rows, int n, int L,
-                     float* __restrict__ out, WGrad wg) {
+rows_backward_kernel(const IO* __restrict__ grad, const uint8_t* __restrict__ blocks,
+                     const IO* __restrict__ w, int64_t rows, int n, int L,
+                     IO* __restrict__ out, WGrad<IO> wg) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = BwdSmem<NT, WEIGHTED>;
+    using SM = BwdSmem<NT, WEIGHTED, IO>;
     const int R = NT / L;
     const int tile = threadIdx.x / L;
     const int lane = threadIdx.x - tile * L;
@@ -313,21 +324,22 @@ rows_backward_kernel(const float* __restrict__ grad, const uint8_t* __restrict__
     const bool live = row < rows;
     const int64_t off = (live ? row : 0) * (int64_t)n;
     BwdTile B;
-    bwd_tile_phase<NT, WEIGHTED>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, n, live,
-                                 true, L, smem, B);
-    const float* stage = reinterpret_cast<const float*>(smem + SM::oStage);
-    const float* ratio = reinterpret_cast<const float*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
+    bwd_tile_phase<NT, WEIGHTED, IO>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, n,
+                                     live, true, L, smem, B);
+    const IO* stage = reinterpret_cast<const IO*>(smem + SM::oStage);
+    const IO* ratio = reinterpret_cast<const IO*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
     if (live) {
         if (out) {
-            float* orow = out + off;
-            for (int i = lane; i < n; i += L) orow[i] = stage[spos(tile * L + (i >> 5), i & 31)];
+            IO* orow = out + off;
+            for (int i = lane; i < n; i += L) orow[i] = stage[spos_t<IO>(tile * L + (i >> 5), i & 31)];
         }
         if (wg.dw) {
-            const float* yrow = wg.y + off;
-            const float* zrow = wg.fit + off;
-            float* drow = wg.dw + off;
+            const IO* yrow = wg.y + off;
+            const IO* zrow = wg.fit + off;
+            IO* drow = wg.dw + off;
             for (int i = lane; i < n; i += L)
-                drow[i] = (__ldg(yrow + i) - __ldg(zrow + i)) * ratio[spos(tile * L + (i >> 5), i & 31)];
+                drow[i] = (__ldg(yrow + i) - __ldg(zrow + i)) *
+                          ratio[spos_t<IO>(tile * L + (i >> 5), i & 31)];
         }
     }
 }
@@ -349,14 +361,13 @@ struct BwdTot {
     int32_t nan, pad0, pad1, pad2;
 };
 
-template <bool WEIGHTED>
+template <bool WEIGHTED, class IO>
 __global__ void __launch_bounds__(kBNT)
-long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict__ blocks,
-                      const float* __restrict__ w, int64_t n, int64_t m, float* __restrict__ out,
-                      WGrad wg,
-                      BwdRec* __restrict__ rec) {
+long_bwd_tiles_kernel(const IO* __restrict__ grad, const uint8_t* __restrict__ blocks,
+                      const IO* __restrict__ w, int64_t n, int64_t m, IO* __restrict__ out,
+                      WGrad<IO> wg, BwdRec* __restrict__ rec) {
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = BwdSmem<kBNT, WEIGHTED>;
+    using SM = BwdSmem<kBNT, WEIGHTED, IO>;
     const int64_t c = blockIdx.x;
     const int64_t row = c / m;
     const int64_t j = c - row * m;
@@ -364,20 +375,21 @@ long_bwd_tiles_kernel(const float* __restrict__ grad, const uint8_t* __restrict_
     const int nt = (int)imin64(kBT, n - e0);
     const int64_t off = row * n + e0;
     BwdTile B;
-    bwd_tile_phase<kBNT, WEIGHTED>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, nt,
-                                   true, j == 0, kBNT, smem, B);
-    const float* stage = reinterpret_cast<const float*>(smem + SM::oStage);
+    bwd_tile_phase<kBNT, WEIGHTED, IO>(grad + off, blocks + off, WEIGHTED ? w + off : nullptr, nt,
+                                       true, j == 0, kBNT, smem, B);
+    const IO* stage = reinterpret_cast<const IO*>(smem + SM::oStage);
     // elements of complete blocks: from the first start to one before the last start
     const int lo = B.first_start < 0 ? nt : B.first_start;
     const int hi = B.last_start < 0 ? nt : B.last_start;
     if (out) {
-        float* o = out + off;
-        for (int i = lo + threadIdx.x; i < hi; i += kBNT) o[i] = stage[spos(i >> 5, i & 31)];
+        IO* o = out + off;
+        for (int i = lo + threadIdx.x; i < hi; i += kBNT) o[i] = stage[spos_t<IO>(i >> 5, i & 31)];
     }
     if (wg.dw) {
-        const float* ratio = reinterpret_cast<const float*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
+        const IO* ratio = reinterpret_cast<const IO*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
         for (int i = lo + threadIdx.x; i < hi; i += kBNT)
-            wg.dw[off + i] = (__ldg(wg.y + off + i) - __ldg(wg.fit + off + i)) * ratio[spos(i >> 5, i & 31)];
+            wg.dw[off + i] = (__ldg(wg.y + off + i) - __ldg(wg.fit + off + i)) *
+                             ratio[spos_t<IO>(i >> 5, i & 31)];
     }
     if (threadIdx.x == 0) {
         BwdRec r;
@@ -432,11 +444,11 @@ __global__ void long_bwd_totals_kernel(int64_t rows, int64_t m, const BwdRec* __
     }
 }
 
-template <bool WEIGHTED>
+template <bool WEIGHTED, class IO>
 __global__ void __launch_bounds__(kBNT)
-long_bwd_fill_kernel(const float* __restrict__ w, int64_t n, int64_t m,
+long_bwd_fill_kernel(const IO* __restrict__ w, int64_t n, int64_t m,
                      const BwdRec* __restrict__ rec, const BwdTot* __restrict__ tot,
-                     float* __restrict__ out, WGrad wg) {
+                     IO* __restrict__ out, WGrad<IO> wg) {
     const int64_t c = blockIdx.x;
     const int64_t row = c / m;
     const int64_t j = c - row * m;
@@ -445,16 +457,16 @@ long_bwd_fill_kernel(const float* __restrict__ w, int64_t n, int64_t m,
     const BwdRec r = rec[c];
     const BwdTot t = tot[c];
     const int64_t off = row * n + e0;
-    float* o = out ? out + off : nullptr;
-    const float* wr = WEIGHTED ? w + off : nullptr;
-    const float qnan = __int_as_float(0x7fffffff);
-    const float rh = t.nan ? qnan : (float)(t.headG / t.headW);
-    const float rt = t.nan ? qnan : (float)(t.tailG / t.tailW);
+    IO* o = out ? out + off : nullptr;
+    const IO* wr = WEIGHTED ? w + off : nullptr;
+    const IO qnan = qnan_t<IO>();
+    const IO rh = t.nan ? qnan : (IO)(t.headG / t.headW);
+    const IO rt = t.nan ? qnan : (IO)(t.tailG / t.tailW);
     const int hend = r.fs < 0 ? nt : r.fs;
     const int tbeg = r.ls >= 0 ? r.ls : nt;
     // the head (elements before the tile's first start) and the tail (from its
     // last start) belong to blocks that cross tiles; a bad row is NaN throughout
-    auto put = [&](int i, float rt) {
+    auto put = [&](int i, IO rt) {
         if (o) o[i] = WEIGHTED ? __ldg(wr + i) * rt : rt;
         if (wg.dw) wg.dw[off + i] = (__ldg(wg.y + off + i) - __ldg(wg.fit + off + i)) * rt;
     };
@@ -469,12 +481,11 @@ long_bwd_fill_kernel(const float* __restrict__ w, int64_t n, int64_t m,
 
 __host__ __device__ inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
-template <int NT, bool WEIGHTED>
-cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const float* w,
-                            int64_t rows, int n, int L, float* out, WGrad wg,
-                            cudaStream_t stream) {
-    using SM = BwdSmem<NT, WEIGHTED>;
-    auto kern = rows_backward_kernel<NT, WEIGHTED>;
+template <int NT, bool WEIGHTED, class IO>
+cudaError_t launch_rows_bwd(const IO* grad, const uint8_t* blocks, const IO* w, int64_t rows,
+                            int n, int L, IO* out, WGrad<IO> wg, cudaStream_t stream) {
+    using SM = BwdSmem<NT, WEIGHTED, IO>;
+    auto kern = rows_backward_kernel<NT, WEIGHTED, IO>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
     if (err != cudaSuccess) return err;
@@ -485,15 +496,15 @@ cudaError_t launch_rows_bwd(const float* grad, const uint8_t* blocks, const floa
     return cudaGetLastError();
 }
 
-template <bool WEIGHTED>
-cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                       int64_t n, float* out, WGrad wg, void* ws, cudaStream_t stream) {
-    using SM = BwdSmem<kBNT, WEIGHTED>;
+template <bool WEIGHTED, class IO>
+cudaError_t long_bwd_t(const IO* grad, const uint8_t* blocks, const IO* w, int64_t rows,
+                       int64_t n, IO* out, WGrad<IO> wg, void* ws, cudaStream_t stream) {
+    using SM = BwdSmem<kBNT, WEIGHTED, IO>;
     const int64_t m = (n + kBT - 1) / kBT;
     const int64_t M = rows * m;
     BwdRec* rec = static_cast<BwdRec*>(ws);
     BwdTot* tot = reinterpret_cast<BwdTot*>(static_cast<char*>(ws) + a256(sizeof(BwdRec) * M));
-    auto k1 = long_bwd_tiles_kernel<WEIGHTED>;
+    auto k1 = long_bwd_tiles_kernel<WEIGHTED, IO>;
     cudaError_t err = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
     if (err != cudaSuccess) return err;
@@ -503,23 +514,24 @@ cudaError_t long_bwd_t(const float* grad, const uint8_t* blocks, const float* w,
     long_bwd_totals_kernel<<<(unsigned)((rows + 63) / 64), 64, 0, stream>>>(rows, m, rec, tot);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "bwd_totals");
-    long_bwd_fill_kernel<WEIGHTED><<<(unsigned)M, kBNT, 0, stream>>>(w, n, m, rec, tot, out, wg);
+    long_bwd_fill_kernel<WEIGHTED, IO><<<(unsigned)M, kBNT, 0, stream>>>(w, n, m, rec, tot, out, wg);
     prof_mark(stream, "bwd_fill");
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t rows_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int n, float* out, const float* y, const float* fit, float* dw,
-                          cudaStream_t stream) {
+template <class IO>
+cudaError_t rows_backward(const IO* grad, const uint8_t* blocks, const IO* w, int64_t rows, int n,
+                          IO* out, const IO* y, const IO* fit, IO* dw, cudaStream_t stream) {
     int L = 1;
     while (32 * L < n) L <<= 1;
-    const WGrad wg{y, fit, dw};
+    const WGrad<IO> wg{y, fit, dw};
     const bool weighted = w != nullptr;
 #define ISO_BWD_LAUNCH(NT_)                                                                     \
-    return weighted ? launch_rows_bwd<NT_, true>(grad, blocks, w, rows, n, L, out, wg, stream)  \
-                    : launch_rows_bwd<NT_, false>(grad, blocks, w, rows, n, L, out, wg, stream)
+    return weighted                                                                             \
+               ? launch_rows_bwd<NT_, true, IO>(grad, blocks, w, rows, n, L, out, wg, stream)  \
+               : launch_rows_bwd<NT_, false, IO>(grad, blocks, w, rows, n, L, out, wg, stream)
     if (L <= 32) { ISO_BWD_LAUNCH(128); }
     if (L <= 64) { ISO_BWD_LAUNCH(64); }
     if (L <= 128) { ISO_BWD_LAUNCH(128); }
@@ -533,13 +545,24 @@ size_t long_backward_workspace(int64_t rows, int64_t n, bool weighted) {
     return a256(sizeof(BwdRec) * M) + a256(sizeof(BwdTot) * M);
 }
 
-cudaError_t long_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
-                          int64_t n, float* out, const float* y, const float* fit, float* dw,
-                          void* ws, size_t ws_bytes, cudaStream_t stream) {
+template <class IO>
+cudaError_t long_backward(const IO* grad, const uint8_t* blocks, const IO* w, int64_t rows,
+                          int64_t n, IO* out, const IO* y, const IO* fit, IO* dw, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
     (void)ws_bytes;
-    const WGrad wg{y, fit, dw};
-    return w ? long_bwd_t<true>(grad, blocks, w, rows, n, out, wg, ws, stream)
-             : long_bwd_t<false>(grad, blocks, w, rows, n, out, wg, ws, stream);
+    const WGrad<IO> wg{y, fit, dw};
+    return w ? long_bwd_t<true, IO>(grad, blocks, w, rows, n, out, wg, ws, stream)
+             : long_bwd_t<false, IO>(grad, blocks, w, rows, n, out, wg, ws, stream);
 }
+
+#define ISO_BWD_INSTANTIATE(IO)                                                                  \
+    template cudaError_t rows_backward<IO>(const IO*, const uint8_t*, const IO*, int64_t, int,   \
+                                           IO*, const IO*, const IO*, IO*, cudaStream_t);        \
+    template cudaError_t long_backward<IO>(const IO*, const uint8_t*, const IO*, int64_t,        \
+                                           int64_t, IO*, const IO*, const IO*, IO*, void*,       \
+                                           size_t, cudaStream_t);
+ISO_BWD_INSTANTIATE(float)
+ISO_BWD_INSTANTIATE(double)
+#undef ISO_BWD_INSTANTIATE
 
 }  // namespace isodev

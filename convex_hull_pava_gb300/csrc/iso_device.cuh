@@ -34,15 +34,47 @@ __device__ __forceinline__ int bexp(float v) {
     return e == 0 ? 1 : e;
 }
 
+// Biased float64 exponent, with zero and subnormals mapped to 1.
+__device__ __forceinline__ int bexp(double v) {
+    const int e = (int)(((unsigned long long)__double_as_longlong(v) >> 52) & 0x7ff);
+    return e == 0 ? 1 : e;
+}
+
+// Inf or NaN.
+__device__ __forceinline__ bool nonfinite(float v) { return ((__float_as_uint(v) >> 23) & 0xff) == 0xff; }
+__device__ __forceinline__ bool nonfinite(double v) {
+    return (((unsigned long long)__double_as_longlong(v) >> 52) & 0x7ff) == 0x7ff;
+}
+
+// I/O types.  The grid is the same for float32 and float64 inputs: 2^-50 of the
+// power of two above the tile's largest magnitude, i.e. the quantum exponent
+// of a tile whose largest biased exponent is e is e - kUnitK (values) or
+// pe - kProdK for products w*y whose exponents sum to at most pe.  V: the
+// 16-byte vector of staged loads, kPerV elements.
+template <class T> struct IoT;
+template <> struct IoT<float> {
+    static constexpr int kUnitK = 176;    // 127 + 49
+    static constexpr int kProdK = 302;    // 2 * 150 + 48 - 46
+    using V = float4;
+    static constexpr int kPerV = 4;
+};
+template <> struct IoT<double> {
+    static constexpr int kUnitK = 1072;   // 1023 + 49
+    static constexpr int kProdK = 2094;   // 2 * 1075 + 48 - 104
+    using V = double2;
+    static constexpr int kPerV = 2;
+};
+
 // round(v / 2^(emax - 176)): |result| < 2^50 when bexp(v) <= emax.  The
 // scaling by a power of two is exact in float32 wherever the result is at
 // least 1/2 (it only moves the exponent), so one conversion rounds it to the
 // nearest integer (ties to even).  Scales above 2^127 (tiles whose values are
 // all below 2^-78) take two factors.  A non-finite v gives an arbitrary value
 // (the row is flagged and its output discarded).
-struct Quant {
+template <class T> struct QuantT;
+template <> struct QuantT<float> {
     float s1, s2;
-    __device__ __forceinline__ explicit Quant(int emax) {
+    __device__ __forceinline__ explicit QuantT(int emax) {
         const int sh = 176 - emax;                 // -78 .. 175
         const int a = sh < 127 ? sh : 127;
         s1 = __int_as_float((a + 127) << 23);
@@ -50,6 +82,24 @@ struct Quant {
     }
     __device__ __forceinline__ int64_t operator()(float v) const {
         return __float2ll_rn((v * s1) * s2);
+    }
+};
+using Quant = QuantT<float>;
+
+// The same for float64: round(v / 2^(emax - 1072)), |result| < 2^50 when
+// bexp(v) <= emax; the scale 2^(1072 - emax) (2^-974 .. 2^1071) as two
+// factors.  A product that falls below the normal range is below 2^-1022 of
+// a quantum and rounds to 0 either way.
+template <> struct QuantT<double> {
+    double s1, s2;
+    __device__ __forceinline__ explicit QuantT(int emax) {
+        const int sh = 1072 - emax;
+        const int a = sh < 1023 ? sh : 1023;
+        s1 = __longlong_as_double((long long)(a + 1023) << 52);
+        s2 = __longlong_as_double((long long)(sh - a + 1023) << 52);
+    }
+    __device__ __forceinline__ int64_t operator()(double v) const {
+        return __double2ll_rn((v * s1) * s2);
     }
 };
 
@@ -98,9 +148,44 @@ __device__ __forceinline__ int64_t quant_prod(float w, float y, int pemax) {
     return ((bw ^ by) >> 31) ? -v64 : v64;
 }
 
+// round(w*y / 2^(pemax - 2094)) for float64 from the exact 106-bit product of
+// the mantissas: |result| < 2^50 when bexp(w) + bexp(y) <= pemax.
+__device__ __forceinline__ int64_t quant_prod(double w, double y, int pemax) {
+    const uint64_t bw = (uint64_t)__double_as_longlong(w), by = (uint64_t)__double_as_longlong(y);
+    int ew = (int)((bw >> 52) & 0x7ff), ey = (int)((by >> 52) & 0x7ff);
+    uint64_t mw = bw & 0xfffffffffffffull, my = by & 0xfffffffffffffull;
+    if (ew) mw |= 1ull << 52; else ew = 1;
+    if (ey) my |= 1ull << 52; else ey = 1;
+    const unsigned __int128 prod = (unsigned __int128)mw * my;
+    const int t = pemax - (ew + ey) + 56;                    // >= 56
+    const uint64_t mag = t >= 128 ? 0ull : (uint64_t)(((prod >> (t - 1)) + 1u) >> 1);
+    const int64_t v64 = (int64_t)mag;
+    return ((bw ^ by) >> 63) ? -v64 : v64;
+}
+
 // Quantum exponents: value = integer * 2^q.
 __device__ __forceinline__ int qexp_unit(int emax) { return emax - 176; }
 __device__ __forceinline__ int qexp_prod(int pemax) { return pemax - 302; }
+template <class T> __device__ __forceinline__ int qexp_unit_t(int emax) { return emax - IoT<T>::kUnitK; }
+template <class T> __device__ __forceinline__ int qexp_prod_t(int pemax) { return pemax - IoT<T>::kProdK; }
+
+// A slope (or a ratio) dS / dW * 2^k in the I/O type: float32 from two
+// rounded conversions and one division, scaled exactly; float64 likewise in
+// double (exact conversions below 2^53).
+template <class T> __device__ __forceinline__ T ratio_t(int64_t dS, int64_t dW, int k);
+template <> __device__ __forceinline__ float ratio_t<float>(int64_t dS, int64_t dW, int k) {
+    return Pow2(k)(i64_to_f32(dS) / i64_to_f32(dW));
+}
+template <> __device__ __forceinline__ double ratio_t<double>(int64_t dS, int64_t dW, int k) {
+    return ldexp((double)dS / (double)dW, k);
+}
+
+// Quiet NaN of the I/O type.
+template <class T> __device__ __forceinline__ T qnan_t();
+template <> __device__ __forceinline__ float qnan_t<float>() { return __int_as_float(0x7fffffff); }
+template <> __device__ __forceinline__ double qnan_t<double>() {
+    return __longlong_as_double(0x7fffffffffffffffll);
+}
 
 // ---------------------------------------------------------------------------
 // Turn predicate.  For points O, A, B with A - O = (w1, s1), B - O = (w2, s2),

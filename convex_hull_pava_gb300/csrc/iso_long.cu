@@ -160,22 +160,22 @@ __device__ __forceinline__ int64_t conv(int64_t x, int d) {
 // ---------------------------------------------------------------------------
 // 1. chunk hulls
 // ---------------------------------------------------------------------------
-template <bool WEIGHTED>
-__device__ __forceinline__ void chunk_hull_one(const float* __restrict__ y,
-                                               const float* __restrict__ w, const LongGeo& geo,
+template <bool WEIGHTED, class IO>
+__device__ __forceinline__ void chunk_hull_one(const IO* __restrict__ y,
+                                               const IO* __restrict__ w, const LongGeo& geo,
                                                int increasing, const LongWs& ws, int64_t c) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
     extern __shared__ __align__(128) unsigned char smem[];
-    using SM = TileSmem<NT, WEIGHTED, false, 1>;
+    using SM = TileSmem<NT, WEIGHTED, false, 1, IO>;
     const RowRef R = geo_row<C>(geo, geo.e0 ? (int64_t)geo.chunk_row[c] : c / geo.m);
     const int64_t e0 = (c - R.c0) * C;
     const int nt = (int)imin64(C, R.n - e0);
-    const float* yr = y + R.e0 + e0;
-    const float* wr = WEIGHTED ? w + R.e0 + e0 : nullptr;
+    const IO* yr = y + R.e0 + e0;
+    const IO* wr = WEIGHTED ? w + R.e0 + e0 : nullptr;
 
     TileHull H;
-    tile_hull_phase<NT, WEIGHTED, false, 1>(yr, wr, nt, true, !increasing, NT, smem, H);
+    tile_hull_phase<NT, WEIGHTED, false, 1, IO>(yr, wr, nt, true, !increasing, NT, smem, H);
 
     // the chunk hull is the compact list of lane 0's row and the chunk's end
     // point: copy them to the slot
@@ -208,17 +208,17 @@ __device__ __forceinline__ void chunk_hull_one(const float* __restrict__ y,
 
 // One CTA per chunk; a ragged batch's grid is bounded and its CTAs take the
 // chunks in turn.
-template <bool WEIGHTED, bool RAGGED>
+template <bool WEIGHTED, bool RAGGED, class IO>
 __global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
-chunk_hull_kernel(const float* __restrict__ y, const float* __restrict__ w, LongGeo geo,
+chunk_hull_kernel(const IO* __restrict__ y, const IO* __restrict__ w, LongGeo geo,
                   int increasing, LongWs ws) {
     if (!RAGGED) {
-        chunk_hull_one<WEIGHTED>(y, w, geo, increasing, ws, blockIdx.x);
+        chunk_hull_one<WEIGHTED, IO>(y, w, geo, increasing, ws, blockIdx.x);
         return;
     }
     const int64_t M = geo.count[1];
     for (int64_t c = blockIdx.x; c < M; c += gridDim.x) {
-        chunk_hull_one<WEIGHTED>(y, w, geo, increasing, ws, c);
+        chunk_hull_one<WEIGHTED, IO>(y, w, geo, increasing, ws, c);
         __syncthreads();   // shared memory is reused by the next chunk
     }
 }
@@ -1001,28 +1001,29 @@ merge_top_kernel(LongGeo geo, LongWs ws) {
 // ---------------------------------------------------------------------------
 // 3. expansion: each element gets the slope of the root-hull edge above it
 // ---------------------------------------------------------------------------
-template <bool WEIGHTED>
+template <bool WEIGHTED, class IO = float>
 struct ExpandSmem {
     static constexpr int NT = LongCfg<WEIGHTED>::NT;
     static constexpr int C = LongCfg<WEIGHTED>::C;
     static constexpr int oMask = 0;
     static constexpr int oTmp = oMask + NT * 4;
-    static constexpr int oSlope = ((oTmp + (NT / 32 + 2) * 8 + 15) / 16) * 16;   // float4 rows
-    static constexpr int kBytes = oSlope + C * 4;
+    static constexpr int oSlope = ((oTmp + (NT / 32 + 2) * 8 + 15) / 16) * 16;   // 16-byte rows
+    static constexpr int kBytes = oSlope + C * (int)sizeof(IO);
 };
 
-template <bool WEIGHTED>
-__device__ __forceinline__ void expand_one(const float* __restrict__ y, const LongGeo& geo,
+template <bool WEIGHTED, class IO>
+__device__ __forceinline__ void expand_one(const IO* __restrict__ y, const LongGeo& geo,
                                            int increasing, const LongWs& ws,
-                                           float* __restrict__ out, uint8_t* __restrict__ blocks,
+                                           IO* __restrict__ out, uint8_t* __restrict__ blocks,
                                            int64_t c) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
-    using XS = ExpandSmem<WEIGHTED>;
+    using XS = ExpandSmem<WEIGHTED, IO>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + XS::oMask);
     int64_t* s_tmp = reinterpret_cast<int64_t*>(smem + XS::oTmp);
-    float* slope = reinterpret_cast<float*>(smem + XS::oSlope);   // per point, swizzled rows
+    __shared__ IO s_in_sl;                                         // slope of the entering edge
+    IO* slope = reinterpret_cast<IO*>(smem + XS::oSlope);   // per point, swizzled rows
 
     const int64_t row = geo.e0 ? (int64_t)geo.chunk_row[c] : c / geo.m;
     const RowRef R = geo_row<C>(geo, row);
@@ -1030,14 +1031,14 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
     const int nt = (int)imin64(C, R.n - e0);
     const int tid = threadIdx.x;
     const ChunkEnds ce = ws.ends[c];
-    float* orow = out + R.e0 + e0;
+    IO* orow = out + R.e0 + e0;
     uint8_t* brow = blocks ? blocks + R.e0 + e0 : nullptr;
     const bool neg = !increasing;
 
     if (ce.bad) {
         // a rejected row: NaN fit; its block flags are 0, but a ragged
         // segment keeps its first element a block start
-        const float qnan = __int_as_float(0x7fffffff);
+        const IO qnan = qnan_t<IO>();
         const bool mark0 = geo.e0 && e0 == 0;
         for (int i = tid; i < nt; i += NT) {
             orow[i] = qnan;
@@ -1054,13 +1055,15 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
     // element's mean; for a decreasing fit the negations cancel).
     if (ce.lo <= ce.hi && ce.hi - ce.lo + sp[ce.lo] == nt && sp[ce.hi] == nt &&
         (sp[ce.lo] == 0 || (sp[ce.lo] == 1 && ce.pt0_vertex))) {
-        const float* yrow = y + R.e0 + e0;
+        const IO* yrow = y + R.e0 + e0;
         if ((reinterpret_cast<uintptr_t>(yrow) & 15u) == 0 &&
             (reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
-            const int n4 = nt >> 2;
-            for (int i = tid; i < n4; i += NT)
-                reinterpret_cast<float4*>(orow)[i] = __ldg(reinterpret_cast<const float4*>(yrow) + i);
-            for (int i = (n4 << 2) + tid; i < nt; i += NT) orow[i] = __ldg(yrow + i);
+            using V = typename IoT<IO>::V;
+            constexpr int P = IoT<IO>::kPerV;
+            const int nv = nt / P;
+            for (int i = tid; i < nv; i += NT)
+                reinterpret_cast<V*>(orow)[i] = __ldg(reinterpret_cast<const V*>(yrow) + i);
+            for (int i = nv * P + tid; i < nt; i += NT) orow[i] = __ldg(yrow + i);
         } else {
             for (int i = tid; i < nt; i += NT) orow[i] = __ldg(yrow + i);
         }
@@ -1082,12 +1085,12 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
     const i128 offW = WEIGHTED ? ws.offW[c] : (i128)0;
     const int ds = ws.dS[c], dw = WEIGHTED ? ws.dW[c] : 0;
 
-    const Pow2 cscale(mt.qs - (WEIGHTED ? mt.qw : 0));   // chunk quanta to values
+    const int cexp = mt.qs - (WEIGHTED ? mt.qw : 0);   // chunk quanta to values
     s_mask[tid] = 0u;
     __syncthreads();
-    auto row_slope = [&](i128 Wa, i128 Sa, i128 Wb, i128 Sb) -> float {
+    auto row_slope = [&](i128 Wa, i128 Sa, i128 Wb, i128 Sb) -> IO {
         const double f = i128_to_double(Sb - Sa) / i128_to_double(Wb - Wa);
-        return (float)ldexp(f, qs_row - qw_row);
+        return (IO)ldexp(f, qs_row - qw_row);
     };
     auto vrow = [&](int r, i128& Wv, i128& Sv) {
         Sv = offS + conv(sS[r], ds);
@@ -1107,24 +1110,24 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
             const unsigned bits = __reduce_or_sync(grp, p < nt ? 1u << (p & 31) : 0u);
             if (word >= 0 && (tid & 31) == __ffs(grp) - 1) atomicOr(&s_mask[word], bits);
             if (p >= nt) continue;
-            float sl;
+            IO sl;
             if (r < ce.hi) {
                 // both ends in the chunk: chunk-relative coordinates, chunk quanta
                 const int64_t dS_ = sS[r + 1] - sS[r];
                 const int64_t dW_ = WEIGHTED ? sW[r + 1] - sW[r] : (int64_t)(sp[r + 1] - p);
-                sl = cscale(i64_to_f32(dS_) / i64_to_f32(dW_));
+                sl = ratio_t<IO>(dS_, dW_, cexp);
             } else {
                 i128 Wa, Sa;
                 vrow(r, Wa, Sa);
                 sl = row_slope(Wa, Sa, ce.nextW, ce.nextS);
             }
-            slope[spos(p >> 5, p & 31)] = sl;
+            slope[spos_t<IO>(p >> 5, p & 31)] = sl;
         }
     }
     if (tid == 0) {
         // the edge entering the chunk: from the previous root vertex to the first
         // root vertex of the chunk, or to the next root vertex if the chunk has none
-        float in_sl = 0.0f;
+        IO in_sl = IO(0);
         if (e0 > 0) {
             i128 Wb, Sb;
             if (has) vrow(ce.lo, Wb, Sb);
@@ -1133,9 +1136,9 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
         }
         if (ce.pt0_vertex) {
             atomicOr(&s_mask[0], 1u);
-            slope[spos(0, 0)] = in_sl;
+            slope[spos_t<IO>(0, 0)] = in_sl;
         }
-        s_tmp[NT / 32 + 1] = (int64_t)__float_as_int(in_sl);
+        s_in_sl = in_sl;
     }
     __syncthreads();
     // the last vertex before each lane: exclusive max-scan of the lanes' last vertices
@@ -1157,31 +1160,19 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
         for (int q = 0; q < (tid >> 5); ++q) before = max(before, wmax[q]);
         lastv = before;
     }
-    const float in_sl = __int_as_float((int)s_tmp[NT / 32 + 1]);
-    const float carry = lastv >= 0 ? slope[spos(lastv >> 5, lastv & 31)] : in_sl;
-    float o[32];
+    const IO in_sl = s_in_sl;
+    const IO carry = lastv >= 0 ? slope[spos_t<IO>(lastv >> 5, lastv & 31)] : in_sl;
+    IO o[32];
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
         const uint32_t upto = k == 31 ? mk : (mk & ((2u << k) - 1u));
-        const float v = upto ? slope[spos(tid, 31 - __clz(upto))] : carry;
+        const IO v = upto ? slope[spos_t<IO>(tid, 31 - __clz(upto))] : carry;
         o[k] = neg ? -v : v;
     }
     __syncthreads();   // slopes read: stage the output in their place
-    float4* st4 = reinterpret_cast<float4*>(slope);
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-        st4[sunit(tid, q)] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    stage_out<IO>(slope, tid, o);
     __syncthreads();
-    if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
-        const int n4 = nt >> 2;
-        for (int i = tid; i < n4; i += NT) {
-            const int e4 = i << 2;
-            reinterpret_cast<float4*>(orow)[i] = st4[sunit(e4 >> 5, (e4 & 31) >> 2)];
-        }
-        for (int i = (n4 << 2) + tid; i < nt; i += NT) orow[i] = slope[spos(i >> 5, i & 31)];
-    } else {
-        for (int i = tid; i < nt; i += NT) orow[i] = slope[spos(i >> 5, i & 31)];
-    }
+    write_row<IO>(orow, slope, 0, nt, tid, NT, true);
     if (brow) {
         if ((reinterpret_cast<uintptr_t>(brow) & 3u) == 0) {
             const int n4 = nt >> 2;
@@ -1199,17 +1190,17 @@ __device__ __forceinline__ void expand_one(const float* __restrict__ y, const Lo
     }
 }
 
-template <bool WEIGHTED, bool RAGGED>
+template <bool WEIGHTED, bool RAGGED, class IO>
 __global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
-expand_kernel(const float* __restrict__ y, LongGeo geo, int increasing, LongWs ws,
-              float* __restrict__ out, uint8_t* __restrict__ blocks) {
+expand_kernel(const IO* __restrict__ y, LongGeo geo, int increasing, LongWs ws,
+              IO* __restrict__ out, uint8_t* __restrict__ blocks) {
     if (!RAGGED) {
-        expand_one<WEIGHTED>(y, geo, increasing, ws, out, blocks, blockIdx.x);
+        expand_one<WEIGHTED, IO>(y, geo, increasing, ws, out, blocks, blockIdx.x);
         return;
     }
     const int64_t M = geo.count[1];
     for (int64_t c = blockIdx.x; c < M; c += gridDim.x) {
-        expand_one<WEIGHTED>(y, geo, increasing, ws, out, blocks, c);
+        expand_one<WEIGHTED, IO>(y, geo, increasing, ws, out, blocks, c);
         __syncthreads();
     }
 }
@@ -1570,16 +1561,16 @@ ctl_root_kernel(int64_t m, LongWs ws, CtlWs cw) {
 // Launch sizes: exact counts for a dense batch, bounds for a ragged one.
 struct LongGrid { int64_t rows, chunks, groups, ng; };
 
-template <bool WEIGHTED, bool RAGGED>
-static cudaError_t long_launch(const float* y, const float* w, const LongGeo& geo,
-                               const LongGrid& gr, int increasing, float* out, uint8_t* blocks,
+template <bool WEIGHTED, bool RAGGED, class IO>
+static cudaError_t long_launch(const IO* y, const IO* w, const LongGeo& geo,
+                               const LongGrid& gr, int increasing, IO* out, uint8_t* blocks,
                                const LongWs& ws, uint32_t* row_status, cudaStream_t stream) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
-    using SM = TileSmem<NT, WEIGHTED, false, 1>;
-    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, RAGGED>,
+    using SM = TileSmem<NT, WEIGHTED, false, 1, IO>;
+    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, RAGGED, IO>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     if (err != cudaSuccess) return err;
-    chunk_hull_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.chunks, NT, SM::kBytes, stream>>>(y, w, geo,
+    chunk_hull_kernel<WEIGHTED, RAGGED, IO><<<(unsigned)gr.chunks, NT, SM::kBytes, stream>>>(y, w, geo,
                                                                                 increasing, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "chunk_hull");
@@ -1596,10 +1587,10 @@ static cudaError_t long_launch(const float* y, const float* w, const LongGeo& ge
     merge_top_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.rows, kMergeThreads, kMergeSmem, stream>>>(geo, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "merge_top");
-    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               ExpandSmem<WEIGHTED>::kBytes);
+    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, RAGGED, IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               ExpandSmem<WEIGHTED, IO>::kBytes);
     if (err != cudaSuccess) return err;
-    expand_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.chunks, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
+    expand_kernel<WEIGHTED, RAGGED, IO><<<(unsigned)gr.chunks, NT, ExpandSmem<WEIGHTED, IO>::kBytes, stream>>>(
         y, geo, increasing, ws, out, blocks);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "expand");
@@ -1650,9 +1641,9 @@ size_t long_fit_workspace(int64_t rows, int64_t n, bool weighted) {
     return weighted ? carve<true>(nullptr, rows, M, nullptr) : carve<false>(nullptr, rows, M, nullptr);
 }
 
-template <bool WEIGHTED>
-static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int64_t n,
-                              int increasing, float* out, uint8_t* blocks, void* wsp,
+template <bool WEIGHTED, class IO>
+static cudaError_t long_fit_t(const IO* y, const IO* w, int64_t rows, int64_t n,
+                              int increasing, IO* out, uint8_t* blocks, void* wsp,
                               uint32_t* row_status, cudaStream_t stream) {
     constexpr int C = LongCfg<WEIGHTED>::C;
     const int64_t m = (n + C - 1) / C;
@@ -1662,16 +1653,17 @@ static cudaError_t long_fit_t(const float* y, const float* w, int64_t rows, int6
     geo.n = n;
     geo.m = m;
     const int64_t ng = (m + kGroup - 1) / kGroup;
-    return long_launch<WEIGHTED, false>(y, w, geo, LongGrid{rows, rows * m, rows * ng, ng}, increasing,
+    return long_launch<WEIGHTED, false, IO>(y, w, geo, LongGrid{rows, rows * m, rows * ng, ng}, increasing,
                                  out, blocks, ws, row_status, stream);
 }
 
-cudaError_t long_fit(const float* y, const float* w, int64_t rows, int64_t n, int increasing,
-                     float* out, uint8_t* blocks, void* ws, size_t ws_bytes, uint32_t* row_status,
+template <class IO>
+cudaError_t long_fit(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing, IO* out,
+                     uint8_t* blocks, void* ws, size_t ws_bytes, uint32_t* row_status,
                      cudaStream_t stream) {
     (void)ws_bytes;
-    return w ? long_fit_t<true>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream)
-             : long_fit_t<false>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream);
+    return w ? long_fit_t<true, IO>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream)
+             : long_fit_t<false, IO>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream);
 }
 
 size_t long_ragged_workspace(int64_t rows_max, int64_t total, bool weighted) {
@@ -1679,10 +1671,10 @@ size_t long_ragged_workspace(int64_t rows_max, int64_t total, bool weighted) {
                     : carve_ragged<false>(nullptr, rows_max, total, nullptr, nullptr);
 }
 
-template <bool WEIGHTED>
-static cudaError_t long_fit_ragged_t(const float* y, const float* w, const int64_t* off,
+template <bool WEIGHTED, class IO>
+static cudaError_t long_fit_ragged_t(const IO* y, const IO* w, const int64_t* off,
                                      const int32_t* long_id, const unsigned long long* nlong,
-                                     int64_t rows_max, int64_t total, int increasing, float* out,
+                                     int64_t rows_max, int64_t total, int increasing, IO* out,
                                      uint8_t* blocks, void* wsp, uint32_t* row_status,
                                      cudaStream_t stream) {
     LongGeo geo;
@@ -1698,17 +1690,18 @@ static cudaError_t long_fit_ragged_t(const float* y, const float* w, const int64
     const LongGrid gr{std::min<int64_t>(B.rows, kRaggedTopCtas),
                       std::min<int64_t>(B.chunks, kRaggedCtas),
                       std::min<int64_t>(B.groups, kRaggedCtas), 0};
-    return long_launch<WEIGHTED, true>(y, w, geo, gr, increasing, out, blocks, ws, row_status, stream);
+    return long_launch<WEIGHTED, true, IO>(y, w, geo, gr, increasing, out, blocks, ws, row_status, stream);
 }
 
-cudaError_t long_fit_ragged(const float* y, const float* w, const int64_t* off,
+template <class IO>
+cudaError_t long_fit_ragged(const IO* y, const IO* w, const int64_t* off,
                             const int32_t* long_id, const unsigned long long* nlong,
-                            int64_t rows_max, int64_t total, int increasing, float* out,
+                            int64_t rows_max, int64_t total, int increasing, IO* out,
                             uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream) {
-    return w ? long_fit_ragged_t<true>(y, w, off, long_id, nlong, rows_max, total, increasing, out,
-                                       blocks, ws, row_status, stream)
-             : long_fit_ragged_t<false>(y, w, off, long_id, nlong, rows_max, total, increasing,
-                                        out, blocks, ws, row_status, stream);
+    return w ? long_fit_ragged_t<true, IO>(y, w, off, long_id, nlong, rows_max, total, increasing,
+                                           out, blocks, ws, row_status, stream)
+             : long_fit_ragged_t<false, IO>(y, w, off, long_id, nlong, rows_max, total, increasing,
+                                            out, blocks, ws, row_status, stream);
 }
 
 size_t long_control_workspace(int64_t rows, int64_t n, bool weighted) {
@@ -1718,13 +1711,13 @@ size_t long_control_workspace(int64_t rows, int64_t n, bool weighted) {
                     : carve<false>(nullptr, rows, M, nullptr) + carve_ctl<false>(nullptr, rows, M, nullptr);
 }
 
-template <bool WEIGHTED>
-static cudaError_t long_control_t(const float* y, const float* w, int64_t rows, int64_t n,
-                                  int increasing, float* out, uint8_t* blocks, void* wsp,
+template <bool WEIGHTED, class IO>
+static cudaError_t long_control_t(const IO* y, const IO* w, int64_t rows, int64_t n,
+                                  int increasing, IO* out, uint8_t* blocks, void* wsp,
                                   uint32_t* row_status, cudaStream_t stream) {
     constexpr int NT = LongCfg<WEIGHTED>::NT;
     constexpr int C = LongCfg<WEIGHTED>::C;
-    using SM = TileSmem<NT, WEIGHTED, false, 1>;
+    using SM = TileSmem<NT, WEIGHTED, false, 1, IO>;
     const int64_t m = (n + C - 1) / C, M = rows * m;
     LongWs ws;
     const size_t off = carve<WEIGHTED>(wsp, rows, M, &ws);
@@ -1734,10 +1727,10 @@ static cudaError_t long_control_t(const float* y, const float* w, int64_t rows, 
     geo.n = n;
     geo.m = m;
     const int64_t ng = (m + kGroup - 1) / kGroup;
-    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, false>,
+    cudaError_t err = cudaFuncSetAttribute(chunk_hull_kernel<WEIGHTED, false, IO>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytes);
     if (err != cudaSuccess) return err;
-    chunk_hull_kernel<WEIGHTED, false><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, geo,
+    chunk_hull_kernel<WEIGHTED, false, IO><<<(unsigned)M, NT, SM::kBytes, stream>>>(y, w, geo,
                                                                                increasing, ws);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "chunk_hull");
@@ -1768,22 +1761,38 @@ static cudaError_t long_control_t(const float* y, const float* w, int64_t rows, 
     ctl_root_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, 0, stream>>>(m, ws, cw);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "ctl_root");
-    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, false>,
+    err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, false, IO>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               ExpandSmem<WEIGHTED>::kBytes);
+                               ExpandSmem<WEIGHTED, IO>::kBytes);
     if (err != cudaSuccess) return err;
-    expand_kernel<WEIGHTED, false><<<(unsigned)M, NT, ExpandSmem<WEIGHTED>::kBytes, stream>>>(
+    expand_kernel<WEIGHTED, false, IO><<<(unsigned)M, NT, ExpandSmem<WEIGHTED, IO>::kBytes, stream>>>(
         y, geo, increasing, ws, out, blocks);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "expand");
     return cudaSuccess;
 }
 
-cudaError_t long_fit_control(const float* y, const float* w, int64_t rows, int64_t n,
-                             int increasing, float* out, uint8_t* blocks, void* ws,
-                             uint32_t* row_status, cudaStream_t stream) {
-    return w ? long_control_t<true>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream)
-             : long_control_t<false>(y, w, rows, n, increasing, out, blocks, ws, row_status, stream);
+template <class IO>
+cudaError_t long_fit_control(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing,
+                             IO* out, uint8_t* blocks, void* ws, uint32_t* row_status,
+                             cudaStream_t stream) {
+    return w ? long_control_t<true, IO>(y, w, rows, n, increasing, out, blocks, ws, row_status,
+                                        stream)
+             : long_control_t<false, IO>(y, w, rows, n, increasing, out, blocks, ws, row_status,
+                                         stream);
 }
+
+#define ISO_LONG_INSTANTIATE(IO)                                                                 \
+    template cudaError_t long_fit<IO>(const IO*, const IO*, int64_t, int64_t, int, IO*, uint8_t*, \
+                                      void*, size_t, uint32_t*, cudaStream_t);                   \
+    template cudaError_t long_fit_ragged<IO>(const IO*, const IO*, const int64_t*,               \
+                                             const int32_t*, const unsigned long long*, int64_t, \
+                                             int64_t, int, IO*, uint8_t*, void*, uint32_t*,      \
+                                             cudaStream_t);                                      \
+    template cudaError_t long_fit_control<IO>(const IO*, const IO*, int64_t, int64_t, int, IO*,  \
+                                              uint8_t*, void*, uint32_t*, cudaStream_t);
+ISO_LONG_INSTANTIATE(float)
+ISO_LONG_INSTANTIATE(double)
+#undef ISO_LONG_INSTANTIATE
 
 }  // namespace isodev

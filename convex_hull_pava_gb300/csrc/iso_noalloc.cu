@@ -57,7 +57,7 @@ extern "C" iso_status iso_backward_noalloc(const float* grad, const uint8_t* blo
     if (need > kScratchBytes) return ISO_ERR_WORKSPACE;
     void* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return ISO_ERR_CUDA;
-    return isodev::long_backward(grad, blocks, w, rows, n, out, nullptr, nullptr, nullptr, ws,
+    return isodev::long_backward<float>(grad, blocks, w, rows, n, out, nullptr, nullptr, nullptr, ws,
                                  kScratchBytes, st) == cudaSuccess
                ? ISO_OK
                : ISO_ERR_CUDA;

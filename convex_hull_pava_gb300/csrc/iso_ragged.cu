@@ -113,9 +113,10 @@ size_t ragged_workspace(int64_t segments, int64_t total, int64_t max_len, bool w
     return carve_ragged_ws(nullptr, segments, total, max_len, weighted).bytes;
 }
 
-cudaError_t ragged_fit(const float* y, const float* w, const int64_t* off, int64_t segments,
-                       int64_t total, int64_t max_len, int increasing, float* out,
-                       uint8_t* blocks, void* ws, uint32_t* row_status, cudaStream_t stream) {
+template <class IO>
+cudaError_t ragged_fit(const IO* y, const IO* w, const int64_t* off, int64_t segments,
+                       int64_t total, int64_t max_len, int increasing, IO* out, uint8_t* blocks,
+                       void* ws, uint32_t* row_status, cudaStream_t stream) {
     const RaggedWs r = carve_ragged_ws(ws, segments, total, max_len, w != nullptr);
     cudaError_t err = cudaMemsetAsync(r.ls.count, 0, sizeof(unsigned long long) * (kClasses + 1),
                                       stream);
@@ -127,15 +128,22 @@ cudaError_t ragged_fit(const float* y, const float* w, const int64_t* off, int64
     prof_mark(stream, "ragged_classify");
     for (int k = 0; k < kClasses; ++k) {
         if (r.ls.cap[k] == 0) continue;
-        err = rows_fit_ragged(y, w, off, r.ls.list[k], r.ls.count + k, r.ls.cap[k], 1 << k,
+        err = rows_fit_ragged<IO>(y, w, off, r.ls.list[k], r.ls.count + k, r.ls.cap[k], 1 << k,
                               increasing, out, blocks, row_status, stream);
         if (err != cudaSuccess) return err;
     }
     if (r.ls.cap[kLongList] > 0)
-        return long_fit_ragged(y, w, off, r.ls.list[kLongList], r.ls.count + kLongList,
-                               r.ls.cap[kLongList], total, increasing, out, blocks, r.long_ws,
-                               row_status, stream);
+        return long_fit_ragged<IO>(y, w, off, r.ls.list[kLongList], r.ls.count + kLongList,
+                                   r.ls.cap[kLongList], total, increasing, out, blocks, r.long_ws,
+                                   row_status, stream);
     return cudaSuccess;
 }
+
+template cudaError_t ragged_fit<float>(const float*, const float*, const int64_t*, int64_t,
+                                       int64_t, int64_t, int, float*, uint8_t*, void*, uint32_t*,
+                                       cudaStream_t);
+template cudaError_t ragged_fit<double>(const double*, const double*, const int64_t*, int64_t,
+                                        int64_t, int64_t, int, double*, uint8_t*, void*,
+                                        uint32_t*, cudaStream_t);
 
 }  // namespace isodev

@@ -17,6 +17,20 @@ __device__ __forceinline__ int spos(int gl, int k) {
 }
 __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ gl) & 7); }
 
+// The same for rows of 32 elements of the I/O type IO: 16-byte units of
+// IoT<IO>::kPerV elements (8 units of float4, or 16 of double2 per row),
+// XOR-swizzled by the row index (eight consecutive rows per phase).
+template <class IO> __device__ __forceinline__ int spos_t(int gl, int k);
+template <> __device__ __forceinline__ int spos_t<float>(int gl, int k) { return spos(gl, k); }
+template <> __device__ __forceinline__ int spos_t<double>(int gl, int k) {
+    return (gl << 5) | ((((k >> 1) ^ gl) & 15) << 1) | (k & 1);
+}
+template <class IO> __device__ __forceinline__ int sunit_t(int gl, int q);
+template <> __device__ __forceinline__ int sunit_t<float>(int gl, int q) { return sunit(gl, q); }
+template <> __device__ __forceinline__ int sunit_t<double>(int gl, int q) {
+    return (gl << 4) | ((q ^ gl) & 15);
+}
+
 // Layout of the dynamic shared memory of a CTA of NT threads holding R = NT/L
 // tiles of L lanes.  The input staging lives inside the lane-relative sums
 // array Sx (2 x 128 B per lane fit in its 264 B per lane): it is read into
@@ -25,7 +39,7 @@ __device__ __forceinline__ int sunit(int gl, int q) { return (gl << 3) | ((q ^ g
 // lane hulls by walking over vertex masks.  The others (chunks of long rows)
 // compact each lane hull into the front of its row, with the points' indices
 // in Px, and merge the compact lists.
-template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
+template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT, class IO = float>
 struct TileSmem {
     // 33 entries per lane row (an odd stride: the lanes' rows start in
     // different banks), points 0..32 of the lane.  Compact lists use the first
@@ -33,7 +47,7 @@ struct TileSmem {
     // lists of neighbouring lanes are contiguous in flat order.
     static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
-    static constexpr int kYB = EMIT ? NT * 128 : 0;             // slope per vertex (EMIT)
+    static constexpr int kYB = EMIT ? NT * 32 * (int)sizeof(IO) : 0;   // slope per vertex (EMIT)
     static constexpr int kPxB = EMIT ? 0 : ((NT * kRow * 2 + 15) / 16) * 16;   // point indices
     static constexpr int kCntB = EMIT ? 0 : NT * 4;             // entries of each compact list
     static constexpr int kLSB = (NT + RMAX) * 8;                // lane starts, L+1 per tile
@@ -56,9 +70,10 @@ struct TileSmem {
     static constexpr int oInfo = oBridge + kBridgeB;
     static constexpr int oScan = oInfo + kInfoB;
     static constexpr int kBytes = ((oScan + kScanB + 127) / 128) * 128;
-    // staging: y at the start of Sx, w after it (2 x 128 B per lane <= 256 B)
+    // staging: y at the start of Sx; w after it for float32 (2 x 128 B per lane
+    // <= 264 B), in Wx for float64 (256 B per lane each)
     static constexpr int oStageY = oSx;
-    static constexpr int oStageW = oSx + NT * 128;
+    static constexpr int oStageW = sizeof(IO) == 4 ? oSx + NT * 128 : oWx;
 };
 
 // Per-tile reduction slots in the info area.
@@ -111,62 +126,90 @@ __device__ __forceinline__ int tile_warp_or(int v, int L) {
 // rows of lanes [gl0, gl0 + L), by the tile's L threads.  All loads of a
 // thread are issued before any store.  Tracks the largest biased exponent and
 // flags non-finite values (and, for weights, values that are not > 0).
-template <bool IS_W>
-__device__ __forceinline__ void stage_tile(const float* __restrict__ src, int nt, int lane, int L,
-                                           int gl0, bool neg, float* stage, int& emax,
+template <bool IS_W, class IO>
+__device__ __forceinline__ void stage_tile(const IO* __restrict__ src, int nt, int lane, int L,
+                                           int gl0, bool neg, IO* stage, int& emax,
                                            uint32_t& bad) {
-    auto note = [&](float v) {
-        const int e = (__float_as_uint(v) >> 23) & 0xff;
+    auto note = [&](IO v) {
         if (IS_W) {
-            if (!(v > 0.0f) || e == 0xff) bad |= 2u;
-            else emax = max(emax, e == 0 ? 1 : e);
+            if (!(v > IO(0)) || nonfinite(v)) bad |= 2u;
+            else emax = max(emax, bexp(v));
         } else {
-            if (e == 0xff) bad |= 1u;
-            else emax = max(emax, e == 0 ? 1 : e);
+            if (nonfinite(v)) bad |= 1u;
+            else emax = max(emax, bexp(v));
         }
     };
     const bool aligned = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
     if (aligned) {
-        const int n4 = nt >> 2;
-        const float4* s4 = reinterpret_cast<const float4*>(src);
-        float4 v[8];
+        if constexpr (sizeof(IO) == 4) {
+            const int n4 = nt >> 2;
+            const float4* s4 = reinterpret_cast<const float4*>(src);
+            float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = lane + j * L;
-            v[j] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4* st4 = reinterpret_cast<float4*>(stage);
+            for (int j = 0; j < 8; ++j) {
+                const int i = lane + j * L;
+                v[j] = i < n4 ? __ldg(s4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float4* st4 = reinterpret_cast<float4*>(stage);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int i = lane + j * L;
-            if (i < n4) {
-                float4 x = v[j];
-                if (neg) { x.x = -x.x; x.y = -x.y; x.z = -x.z; x.w = -x.w; }
-                note(x.x); note(x.y); note(x.z); note(x.w);
-                const int e = i << 2;
-                st4[sunit(gl0 + (e >> 5), (e & 31) >> 2)] = x;
+            for (int j = 0; j < 8; ++j) {
+                const int i = lane + j * L;
+                if (i < n4) {
+                    float4 x = v[j];
+                    if (neg) { x.x = -x.x; x.y = -x.y; x.z = -x.z; x.w = -x.w; }
+                    note(x.x); note(x.y); note(x.z); note(x.w);
+                    const int e = i << 2;
+                    st4[sunit(gl0 + (e >> 5), (e & 31) >> 2)] = x;
+                }
+            }
+            for (int e = (n4 << 2) + lane; e < nt; e += L) {
+                float x = __ldg(src + e);
+                if (neg) x = -x;
+                note(x);
+                stage[spos(gl0 + (e >> 5), e & 31)] = x;
+            }
+        } else {
+            const int n2 = nt >> 1;
+            const double2* s2 = reinterpret_cast<const double2*>(src);
+            double2 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = lane + j * L;
+                v[j] = i < n2 ? __ldg(s2 + i) : make_double2(0.0, 0.0);
+            }
+            double2* st2 = reinterpret_cast<double2*>(stage);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int i = lane + j * L;
+                if (i < n2) {
+                    double2 x = v[j];
+                    if (neg) { x.x = -x.x; x.y = -x.y; }
+                    note(x.x); note(x.y);
+                    const int e = i << 1;
+                    st2[sunit_t<double>(gl0 + (e >> 5), (e & 31) >> 1)] = x;
+                }
+            }
+            for (int e = (n2 << 1) + lane; e < nt; e += L) {
+                double x = __ldg(src + e);
+                if (neg) x = -x;
+                note(x);
+                stage[spos_t<double>(gl0 + (e >> 5), e & 31)] = x;
             }
         }
-        for (int e = (n4 << 2) + lane; e < nt; e += L) {
-            float x = __ldg(src + e);
-            if (neg) x = -x;
-            note(x);
-            stage[spos(gl0 + (e >> 5), e & 31)] = x;
-        }
     } else {
-        float v[32];
+        IO v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int e = lane + j * L;
-            v[j] = e < nt ? __ldg(src + e) : 0.f;
+            v[j] = e < nt ? __ldg(src + e) : IO(0);
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int e = lane + j * L;
             if (e < nt) {
-                const float x = neg ? -v[j] : v[j];
+                const IO x = neg ? -v[j] : v[j];
                 note(x);
-                stage[spos(gl0 + (e >> 5), e & 31)] = x;
+                stage[spos_t<IO>(gl0 + (e >> 5), e & 31)] = x;
             }
         }
     }
@@ -191,16 +234,16 @@ struct TileHull {
 // 3.2), up to the hull of the whole tile.  `yr`/`wr` point at the tile's first
 // element; `neg` negates y on load (the decreasing fit, Section 2.1).
 // All threads of the CTA must call it (it synchronises the CTA).
-template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT>
-__device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
-                                                const float* __restrict__ wr, int nt, bool live,
+template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT, class IO = float>
+__device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
+                                                const IO* __restrict__ wr, int nt, bool live,
                                                 bool neg, int L, unsigned char* smem,
                                                 TileHull& H) {
-    using SM = TileSmem<NT, WEIGHTED, EMIT, RMAX>;
+    using SM = TileSmem<NT, WEIGHTED, EMIT, RMAX, IO>;
     int64_t* Sx = reinterpret_cast<int64_t*>(smem + SM::oSx);
     int64_t* Wx = reinterpret_cast<int64_t*>(smem + SM::oWx);
-    float* stagey = reinterpret_cast<float*>(smem + SM::oStageY);
-    float* stagew = reinterpret_cast<float*>(smem + SM::oStageW);
+    IO* stagey = reinterpret_cast<IO*>(smem + SM::oStageY);
+    IO* stagew = reinterpret_cast<IO*>(smem + SM::oStageW);
     int64_t* LSa = reinterpret_cast<int64_t*>(smem + SM::oLS);
     int64_t* LWa = reinterpret_cast<int64_t*>(smem + SM::oLW);
     uint32_t* maska = reinterpret_cast<uint32_t*>(smem + SM::oMask);
@@ -224,8 +267,9 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     int emax = 0, ewmax = 0;
     uint32_t bad = 0;
     if (live) {
-        stage_tile<false>(yr, nt, lane, L, tile * L, neg, stagey, emax, bad);
-        if constexpr (WEIGHTED) stage_tile<true>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
+        stage_tile<false, IO>(yr, nt, lane, L, tile * L, neg, stagey, emax, bad);
+        if constexpr (WEIGHTED)
+            stage_tile<true, IO>(wr, nt, lane, L, tile * L, false, stagew, ewmax, bad);
     }
     emax = tile_warp_max(emax, L);
     const int bad_or = tile_warp_or((int)bad, L);
@@ -242,8 +286,8 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     H.e = e;
 
     // ---- the lane's values into registers ----
-    float yv[32], wv[WEIGHTED ? 32 : 1];
-    {
+    IO yv[32], wv[WEIGHTED ? 32 : 1];
+    if constexpr (sizeof(IO) == 4) {
         const float4* sy4 = reinterpret_cast<const float4*>(stagey);
         const float4* sw4 = reinterpret_cast<const float4*>(stagew);
 #pragma unroll
@@ -253,6 +297,18 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
             if constexpr (WEIGHTED) {
                 const float4 x = sw4[sunit(gl, q)];
                 wv[4 * q] = x.x; wv[4 * q + 1] = x.y; wv[4 * q + 2] = x.z; wv[4 * q + 3] = x.w;
+            }
+        }
+    } else {
+        const double2* sy2 = reinterpret_cast<const double2*>(stagey);
+        const double2* sw2 = reinterpret_cast<const double2*>(stagew);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const double2 v = sy2[sunit_t<double>(gl, q)];
+            yv[2 * q] = v.x; yv[2 * q + 1] = v.y;
+            if constexpr (WEIGHTED) {
+                const double2 x = sw2[sunit_t<double>(gl, q)];
+                wv[2 * q] = x.x; wv[2 * q + 1] = x.y;
             }
         }
     }
@@ -270,8 +326,8 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     emax = max(info[tile * 4 + kInfoEmax], 1);
     pemax = max(info[tile * 4 + kInfoPemax], 2);
     ewmax = max(info[tile * 4 + kInfoEwmax], 1);
-    H.qs = WEIGHTED ? qexp_prod(pemax) : qexp_unit(emax);
-    H.qw = WEIGHTED ? qexp_unit(ewmax) : 0;
+    H.qs = WEIGHTED ? qexp_prod_t<IO>(pemax) : qexp_unit_t<IO>(emax);
+    H.qw = WEIGHTED ? qexp_unit_t<IO>(ewmax) : 0;
 
     // ---- candidates and lane-relative cumulative sums ----
     int64_t* myS = Sx + gl * kRow;
@@ -279,7 +335,7 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     int64_t s = 0, wsum = 0;
     uint32_t cand = 0;
     {
-        const Quant qy(emax), qw(ewmax);
+        const QuantT<IO> qy(emax), qw(ewmax);
         int64_t up = 0, op = 1;   // previous element's value and weight
         myS[0] = 0;
         if constexpr (WEIGHTED) myW[0] = 0;
@@ -458,14 +514,57 @@ __device__ __forceinline__ void tile_hull_phase(const float* __restrict__ yr,
     }
 }
 
-// Slope of the edge between tile points a < b, rounded to float32 from the
-// exact integer differences (up to the rounding of the two conversions).
-template <bool WEIGHTED>
-__device__ __forceinline__ float tile_slope(const Tile& T, int a, int b, int qs, int qw) {
+// Slope of the edge between tile points a < b, rounded to the I/O type from
+// the exact integer differences (up to the rounding of the two conversions).
+template <bool WEIGHTED, class IO = float>
+__device__ __forceinline__ IO tile_slope(const Tile& T, int a, int b, int qs, int qw) {
     const int64_t dS = tile_S<WEIGHTED>(T, b) - tile_S<WEIGHTED>(T, a);
     const int64_t dW = tile_W<WEIGHTED>(T, b) - tile_W<WEIGHTED>(T, a);
-    const float f = i64_to_f32(dS) / i64_to_f32(dW);
-    return Pow2(qs - qw)(f);
+    return ratio_t<IO>(dS, dW, qs - qw);
+}
+
+// A lane's 32 outputs into its swizzled staging row (16-byte stores).
+template <class IO>
+__device__ __forceinline__ void stage_out(IO* ost, int gl, const IO (&o)[32]) {
+    if constexpr (sizeof(IO) == 4) {
+        float4* o4 = reinterpret_cast<float4*>(ost);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            o4[sunit(gl, q)] = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    } else {
+        double2* o2 = reinterpret_cast<double2*>(ost);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) o2[sunit_t<double>(gl, q)] = make_double2(o[2 * q], o[2 * q + 1]);
+    }
+}
+
+// Coalesced write of a tile's n staged outputs (rows g0.. of ost) to orow by
+// its L lanes, with 16-byte stores where orow is 16-byte aligned; NaN for a
+// rejected row.
+template <class IO>
+__device__ __forceinline__ void write_row(IO* __restrict__ orow, const IO* ost, int g0, int n,
+                                          int lane, int L, bool work) {
+    const IO qnan = qnan_t<IO>();
+    constexpr int P = IoT<IO>::kPerV;
+    using V = typename IoT<IO>::V;
+    if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
+        const int nv = n / P;
+        const V* sv = reinterpret_cast<const V*>(ost);
+        for (int i = lane; i < nv; i += L) {
+            const int ev = i * P;
+            V v = sv[sunit_t<IO>(g0 + (ev >> 5), (ev & 31) / P)];
+            if (!work) {
+                if constexpr (sizeof(IO) == 4) v = make_float4(qnan, qnan, qnan, qnan);
+                else v = make_double2(qnan, qnan);
+            }
+            reinterpret_cast<V*>(orow)[i] = v;
+        }
+        for (int i = nv * P + lane; i < n; i += L)
+            orow[i] = work ? ost[spos_t<IO>(g0 + (i >> 5), i & 31)] : qnan;
+    } else {
+        for (int i = lane; i < n; i += L)
+            orow[i] = work ? ost[spos_t<IO>(g0 + (i >> 5), i & 31)] : qnan;
+    }
 }
 
 }  // namespace isodev

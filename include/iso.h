@@ -24,6 +24,10 @@
  *    flags are 0, and its bit in `row_status` is set (the paper's per-row NaN
  *    flags, Section 6 "Blocks and memory", without its host synchronisation).
  *  - Limits: 1 <= n <= 2^31 - 1, 1 <= rows, rows * n <= 2^40.
+ *  - float64 I/O: every entry point that takes float32 arrays has an _f64
+ *    twin taking float64 arrays (the paper supports both working types,
+ *    Section 6 "Implementation"), with the same arguments, layout, workspace
+ *    sizes, errors and status bits; only the element type differs.
  */
 #ifndef ISO_H
 #define ISO_H
@@ -91,13 +95,26 @@ size_t iso_fit_workspace_bytes(int64_t rows, int64_t n, int weighted);
  *  stream     cudaStream_t to enqueue on.
  *
  * Accuracy: cumulative sums are exact integer sums of values rounded to a
- * fixed-point grid of 2^-31 of the largest |w*y| (and |w|) of each chunk; the
+ * fixed-point grid of 2^-50 of the largest |w*y| (and |w|) of each chunk; the
  * fit deviates from the exact one by about that amount plus one float32
  * rounding of each slope.
  */
 iso_status iso_fit(const float *y, const float *w, int64_t rows, int64_t n, int increasing,
                    float *out, uint8_t *blocks, void *workspace, size_t workspace_bytes,
                    uint32_t *row_status, void *stream);
+
+/*
+ * iso_fit_f64 -- iso_fit on float64 arrays.  The same fixed-point arithmetic:
+ * values are rounded to 2^-50 of their tile's largest magnitude (a float64
+ * value keeps 50 of its 53 bits at the tile's top exponent), sums and turns
+ * are exact, and each slope is one float64 quotient of two integers, so the
+ * fit deviates from the exact fit of the input by about 2^-49 of the row's
+ * largest |y| (times the weights' dynamic range for weighted rows) plus one
+ * float64 rounding.
+ */
+iso_status iso_fit_f64(const double *y, const double *w, int64_t rows, int64_t n, int increasing,
+                       double *out, uint8_t *blocks, void *workspace, size_t workspace_bytes,
+                       uint32_t *row_status, void *stream);
 
 /* Bytes of device workspace that iso_backward needs (0 = none). */
 size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted);
@@ -121,6 +138,11 @@ size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted);
 iso_status iso_backward(const float *grad, const uint8_t *blocks, const float *w, int64_t rows,
                         int64_t n, float *out, void *workspace, size_t workspace_bytes,
                         void *stream);
+
+/* iso_backward on float64 arrays (grad, w, out); the blocks are iso_fit_f64's. */
+iso_status iso_backward_f64(const double *grad, const uint8_t *blocks, const double *w,
+                            int64_t rows, int64_t n, double *out, void *workspace,
+                            size_t workspace_bytes, void *stream);
 
 /*
  * iso_backward_w -- the vector-Jacobian products of the fit with respect to y
@@ -204,6 +226,12 @@ iso_status iso_fit_ragged(const float *y, const float *w, const int64_t *offsets
                           float *out, uint8_t *blocks, void *workspace, size_t workspace_bytes,
                           uint32_t *row_status, void *stream);
 
+/* iso_fit_ragged on float64 arrays (y, w, out); offsets and statuses as iso_fit_ragged. */
+iso_status iso_fit_ragged_f64(const double *y, const double *w, const int64_t *offsets,
+                              int64_t segments, int64_t total, int64_t max_len, int increasing,
+                              double *out, uint8_t *blocks, void *workspace,
+                              size_t workspace_bytes, uint32_t *row_status, void *stream);
+
 /*
  * iso_fit_copy_control -- a measurement control, not a faster fit: the same
  * fit as iso_fit (bit for bit), with the merge levels of rows longer than
@@ -223,6 +251,12 @@ size_t iso_fit_copy_control_workspace_bytes(int64_t rows, int64_t n, int weighte
 iso_status iso_fit_copy_control(const float *y, const float *w, int64_t rows, int64_t n,
                                 int increasing, float *out, uint8_t *blocks, void *workspace,
                                 size_t workspace_bytes, uint32_t *row_status, void *stream);
+
+/* iso_backward_w on float64 arrays. */
+iso_status iso_backward_w_f64(const double *grad, const uint8_t *blocks, const double *w,
+                              const double *y, const double *fit, int64_t rows, int64_t n,
+                              double *out_dy, double *out_dw, void *workspace,
+                              size_t workspace_bytes, void *stream);
 
 /*
  * iso_backward_noalloc -- iso_backward for callers that cannot allocate device

@@ -13,6 +13,9 @@ The arithmetic lives in ``iso_oracle.c`` (plain C, compiled with gcc by
   eqs. (2)-(3); an independent route used only to cross-check :func:`pava`.
 * :func:`points` -- the cumulative-sum diagram itself, eq. (2).
 * :func:`backward` / :func:`backward_w` -- block averaging, Section 6, "Gradient".
+* :func:`pava_f64`, :func:`backward_f64`, :func:`backward_w_f64` -- the same
+  definitions for float64 inputs, with sums in double-double (about 106
+  bits), Section 6 "Implementation" (float32 and float64 working types).
 * :func:`pava_ragged` -- a ragged batch (segments of unequal lengths laid end
   to end, Section 7.7): each segment fitted as its own row by :func:`pava`.
 """
@@ -66,6 +69,12 @@ def _load():
             lib.oracle_backward_rows.restype = None
             lib.oracle_backward_w.argtypes = [i64, vp, vp, vp, vp, vp, vp]
             lib.oracle_backward_w.restype = None
+            lib.oracle_pava_rows_f64.argtypes = [i64, i64, vp, vp, ci, vp, vp, vp]
+            lib.oracle_pava_rows_f64.restype = None
+            lib.oracle_backward_rows_f64.argtypes = [i64, i64, vp, vp, vp, vp]
+            lib.oracle_backward_rows_f64.restype = None
+            lib.oracle_backward_w_f64.argtypes = [i64, vp, vp, vp, vp, vp, vp]
+            lib.oracle_backward_w_f64.restype = None
             _lib = lib
     return _lib
 
@@ -155,9 +164,58 @@ def backward_w(grad, blocks, w, y, z):
     return out
 
 
-def pava_ragged(y, offsets, w=None, increasing=True, max_len=0):
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def pava_f64(y, w=None, increasing=True):
+    """Fit by weighted PAVA of float64 inputs, block sums in double-double.
+    Same shapes and results as :func:`pava`."""
+    y2 = _f64(y)
+    squeeze = y2.ndim == 1
+    if squeeze:
+        y2 = y2.reshape(1, -1)
+    w2 = None if w is None else _f64(w).reshape(y2.shape)
+    rows, n = y2.shape
+    z = np.empty((rows, n), dtype=np.float64)
+    blocks = np.empty((rows, n), dtype=np.uint8)
+    status = np.empty(rows, dtype=np.uint32)
+    _load().oracle_pava_rows_f64(rows, n, _ptr(y2), _ptr(w2), int(bool(increasing)), _ptr(z),
+                                 _ptr(blocks), _ptr(status))
+    if squeeze:
+        return z[0], blocks[0], status[0]
+    return z, blocks, status
+
+
+def backward_f64(grad, blocks, w=None):
+    """Block averaging of float64 gradients (double-double block sums)."""
+    g2 = _f64(grad)
+    squeeze = g2.ndim == 1
+    if squeeze:
+        g2 = g2.reshape(1, -1)
+    b2 = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(g2.shape)
+    w2 = None if w is None else _f64(w).reshape(g2.shape)
+    out = np.empty(g2.shape, dtype=np.float64)
+    _load().oracle_backward_rows_f64(g2.shape[0], g2.shape[1], _ptr(g2), _ptr(b2), _ptr(w2),
+                                     _ptr(out))
+    return out[0] if squeeze else out
+
+
+def backward_w_f64(grad, blocks, w, y, z):
+    """Weight gradient of one float64 row: ``(y_i - z_i) * G_B / W_B``."""
+    g = _f64(grad).ravel()
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).ravel()
+    w1 = None if w is None else _f64(w).ravel()
+    out = np.empty(g.size, dtype=np.float64)
+    _load().oracle_backward_w_f64(g.size, _ptr(g), _ptr(b), _ptr(w1), _ptr(_f64(y).ravel()),
+                                  _ptr(_f64(z).ravel()), _ptr(out))
+    return out
+
+
+def pava_ragged(y, offsets, w=None, increasing=True, max_len=0, f64=False):
     """Fit of a ragged batch: segment s, elements ``offsets[s] .. offsets[s+1]-1``
-    of the 1-D ``y`` (and ``w``), fitted on its own by :func:`pava` (Section
+    of the 1-D ``y`` (and ``w``), fitted on its own by :func:`pava` (or
+    :func:`pava_f64` when ``f64``) (Section
     7.7 fits such segments as separate curves).  Returns ``(z, blocks,
     status)``: ``z`` float64 and ``blocks`` uint8 over ``y`` (NaN / 0 outside
     every segment), ``status`` one word per segment.
@@ -167,9 +225,11 @@ def pava_ragged(y, offsets, w=None, increasing=True, max_len=0):
     (when > 0), gets :data:`BAD_SHAPE` and no fit; an empty segment gets 0; a
     segment rejected for its values keeps its first element flagged as a
     block start."""
-    y = _f32(y).ravel()
+    cast = _f64 if f64 else _f32
+    fit = pava_f64 if f64 else pava
+    y = cast(y).ravel()
     off = np.asarray(offsets, dtype=np.int64).ravel()
-    w1 = None if w is None else _f32(w).ravel()
+    w1 = None if w is None else cast(w).ravel()
     total, segments = y.size, off.size - 1
     lim = total if max_len is None or max_len <= 0 else min(int(max_len), total)
     z = np.full(total, np.nan)
@@ -182,7 +242,7 @@ def pava_ragged(y, offsets, w=None, increasing=True, max_len=0):
             continue
         if b == a:
             continue
-        zs, bs, st = pava(y[a:b], None if w1 is None else w1[a:b], increasing)
+        zs, bs, st = fit(y[a:b], None if w1 is None else w1[a:b], increasing)
         z[a:b] = zs
         blocks[a:b] = bs
         blocks[a] = 1

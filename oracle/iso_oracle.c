@@ -30,6 +30,15 @@
  * oracle_backward_w -- the weight gradient of the same section,
  *                  d/dw_i = (y_i - z_i) * G / W.
  *
+ * float64 inputs (the paper supports float32 and float64 working types,
+ * Section 6 "Implementation"): oracle_pava_f64, oracle_backward_f64 and
+ * oracle_backward_w_f64 apply the same definitions to double y, w and g.
+ * w_i*y_i and the block sums are then no longer exact in double, so they are
+ * kept as unevaluated sums of two doubles (the error-free transformations of
+ * Dekker and Knuth: TwoSum for an addition, an FMA for the rounding error of a
+ * product), about 106 significant bits, and the pooling test compares the two
+ * cross products in the same arithmetic.
+ *
  * Error convention ("groupant" page on the Rust PAVA, "arithmetic_resource_
  * partition"): a row with a non-finite y, or a weight that is not finite and
  * positive, is rejected before any arithmetic; the row's status is returned
@@ -208,4 +217,164 @@ void oracle_backward_rows(int64_t rows, int64_t n, const float *grad, const uint
                           const float *w, double *out) {
     for (int64_t r = 0; r < rows; ++r)
         oracle_backward(n, grad + r * n, blocks + r * n, w ? w + r * n : NULL, out + r * n);
+}
+
+/* ---- float64 inputs ---------------------------------------------------- */
+
+typedef struct { double hi, lo; } dd;   /* the value hi + lo, |lo| <= ulp(hi) / 2 */
+
+/* s + e = a + b exactly (Knuth's TwoSum, no precondition on a and b). */
+static dd two_sum(double a, double b) {
+    double s = a + b;
+    double bb = s - a;
+    double e = (a - (s - bb)) + (b - bb);
+    dd r = {s, e};
+    return r;
+}
+
+/* s + e = a + b exactly when |a| >= |b| (Dekker's FastTwoSum). */
+static dd fast_two_sum(double a, double b) {
+    double s = a + b;
+    double e = b - (s - a);
+    dd r = {s, e};
+    return r;
+}
+
+/* p + e = a * b exactly (the FMA gives the product's rounding error). */
+static dd two_prod(double a, double b) {
+    double p = a * b;
+    double e = fma(a, b, -p);
+    dd r = {p, e};
+    return r;
+}
+
+static dd dd_add(dd a, dd b) {
+    dd s = two_sum(a.hi, b.hi);
+    dd t = two_sum(a.lo, b.lo);
+    s.lo += t.hi;
+    s = fast_two_sum(s.hi, s.lo);
+    s.lo += t.lo;
+    return fast_two_sum(s.hi, s.lo);
+}
+
+static dd dd_neg(dd a) { dd r = {-a.hi, -a.lo}; return r; }
+
+static dd dd_mul(dd a, dd b) {
+    dd p = two_prod(a.hi, b.hi);
+    p.lo += a.hi * b.lo + a.lo * b.hi;
+    return fast_two_sum(p.hi, p.lo);
+}
+
+/* sign of a - b */
+static int dd_cmp(dd a, dd b) {
+    dd d = dd_add(a, dd_neg(b));
+    if (d.hi != 0.0) return d.hi > 0.0 ? 1 : -1;
+    return d.lo > 0.0 ? 1 : (d.lo < 0.0 ? -1 : 0);
+}
+
+/* a / b rounded to double (two quotient terms, then one rounding). */
+static double dd_div(dd a, dd b) {
+    double q1 = a.hi / b.hi;
+    dd r = dd_add(a, dd_neg(dd_mul(b, (dd){q1, 0.0})));
+    double q2 = r.hi / b.hi;
+    return q1 + q2;
+}
+
+static uint32_t check_row_f64(int64_t n, const double *y, const double *w) {
+    uint32_t st = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (!isfinite(y[i])) st |= ORACLE_BAD_Y;
+        if (w && (!isfinite(w[i]) || !(w[i] > 0.0))) st |= ORACLE_BAD_W;
+    }
+    return st;
+}
+
+/* One row of weighted PAVA on float64 inputs, sums in double-double. */
+uint32_t oracle_pava_f64(int64_t n, const double *y, const double *w, int increasing,
+                         double *z, uint8_t *blocks) {
+    uint32_t st = check_row_f64(n, y, w);
+    if (st) { fill_nan(n, z, blocks); return st; }
+    if (n <= 0) return 0;
+    dd *bs = (dd *)malloc(sizeof(dd) * n);
+    dd *bw = (dd *)malloc(sizeof(dd) * n);
+    int64_t *b0 = (int64_t *)malloc(sizeof(int64_t) * n);
+    int64_t top = 0;
+    const double sgn = increasing ? 1.0 : -1.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double wi = w ? w[i] : 1.0;
+        bs[top] = two_prod(wi, sgn * y[i]);
+        bw[top].hi = wi;
+        bw[top].lo = 0.0;
+        b0[top] = i;
+        ++top;
+        /* pool while mean(prev) >= mean(last) */
+        while (top >= 2 &&
+               dd_cmp(dd_mul(bs[top - 2], bw[top - 1]), dd_mul(bs[top - 1], bw[top - 2])) >= 0) {
+            bs[top - 2] = dd_add(bs[top - 2], bs[top - 1]);
+            bw[top - 2] = dd_add(bw[top - 2], bw[top - 1]);
+            --top;
+        }
+    }
+    for (int64_t k = 0; k < top; ++k) {
+        int64_t end = (k + 1 < top) ? b0[k + 1] : n;
+        double mean = sgn * dd_div(bs[k], bw[k]);
+        for (int64_t i = b0[k]; i < end; ++i) {
+            z[i] = mean;
+            if (blocks) blocks[i] = (uint8_t)(i == b0[k]);
+        }
+    }
+    free(bs); free(bw); free(b0);
+    return 0;
+}
+
+void oracle_pava_rows_f64(int64_t rows, int64_t n, const double *y, const double *w,
+                          int increasing, double *z, uint8_t *blocks, uint32_t *status) {
+    for (int64_t r = 0; r < rows; ++r) {
+        uint32_t st = oracle_pava_f64(n, y + r * n, w ? w + r * n : NULL, increasing, z + r * n,
+                                      blocks ? blocks + r * n : NULL);
+        if (status) status[r] = st;
+    }
+}
+
+/* Block averaging on float64 inputs: out_i = w_i * G / W, G and W summed in
+ * double-double over the block that the start flags delimit. */
+void oracle_backward_rows_f64(int64_t rows, int64_t n, const double *grad,
+                              const uint8_t *blocks, const double *w, double *out) {
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *g = grad + r * n;
+        const uint8_t *b = blocks + r * n;
+        const double *wr = w ? w + r * n : NULL;
+        double *o = out + r * n;
+        int64_t i = 0;
+        while (i < n) {
+            int64_t j = i + 1;
+            while (j < n && !b[j]) ++j;
+            dd G = {0.0, 0.0}, W = {0.0, 0.0};
+            for (int64_t k = i; k < j; ++k) {
+                G = dd_add(G, (dd){g[k], 0.0});
+                W = dd_add(W, (dd){wr ? wr[k] : 1.0, 0.0});
+            }
+            double ratio = dd_div(G, W);
+            for (int64_t k = i; k < j; ++k) o[k] = (wr ? wr[k] : 1.0) * ratio;
+            i = j;
+        }
+    }
+}
+
+/* The weight gradient on float64 inputs: (y_i - z_i) * G / W. */
+void oracle_backward_w_f64(int64_t n, const double *grad, const uint8_t *blocks, const double *w,
+                           const double *y, const double *z, double *out) {
+    int64_t i = 0;
+    while (i < n) {
+        int64_t j = i + 1;
+        while (j < n && !blocks[j]) ++j;
+        dd G = {0.0, 0.0}, W = {0.0, 0.0};
+        for (int64_t k = i; k < j; ++k) {
+            G = dd_add(G, (dd){grad[k], 0.0});
+            W = dd_add(W, (dd){w ? w[k] : 1.0, 0.0});
+        }
+        double ratio = dd_div(G, W);
+        for (int64_t k = i; k < j; ++k) out[k] = (y[k] - z[k]) * ratio;
+        i = j;
+    }
 }

@@ -9,6 +9,14 @@
   so such a pair is a tie) must be a boundary of the CUDA path; a CUDA boundary that the oracle does not have must
   split a tie (|out_i - out_{i-1}| within the fit tolerance); inside one CUDA
   block the output is constant; element 0 starts a block.
+
+float64 I/O: the fit is within 1e-13 * (1 + max|y|) * max(1, max w / min w).
+The CUDA path rounds each value to 2^-50 of its tile's largest magnitude and
+vertex coordinates to the row's grid, so its fit moves by about 2^-48 of max|y|
+(3.6e-15); for weighted rows the grid of the weights is coarser, relative to a
+small weight, by the weights' dynamic range.  The bar leaves a margin of about
+30.  Required boundaries: means that differ by more than 1e-12 relative and by
+more than 2^-44 * max|y| times the same weight ratio.
 """
 import numpy as np
 
@@ -16,18 +24,29 @@ FIT_TOL = 1e-5
 GAP_REL = 1e-6
 GAP_FLOOR = 2.0 ** -44
 
+FIT_TOL_F64 = 1e-13
+GAP_REL_F64 = 1e-12
+GAP_FLOOR_F64 = 2.0 ** -44
+
+
+def f64_params(w):
+    """(tol, gap_rel, gap_floor) of float64 parity for a row's weights."""
+    ratio = 1.0 if w is None else float(np.max(w) / np.min(w))
+    return FIT_TOL_F64 * max(1.0, ratio), GAP_REL_F64, GAP_FLOOR_F64 * max(1.0, ratio)
+
 
 def fit_tol(y):
     y = np.asarray(y, dtype=np.float64)
     return FIT_TOL * (1.0 + np.abs(y).max(axis=-1))
 
 
-def check_row(y, out, blocks, z, zb, label=""):
+def check_row(y, out, blocks, z, zb, label="", fit_tol=FIT_TOL, gap_rel=GAP_REL,
+              gap_floor=GAP_FLOOR):
     """y: float32 [n]; out: float32 [n] (CUDA); blocks: uint8 [n] (CUDA);
     z: float64 [n] (oracle); zb: uint8 [n] (oracle block starts)."""
     y = np.asarray(y, np.float64)
     out = np.asarray(out, np.float64)
-    tol = FIT_TOL * (1.0 + np.abs(y).max())
+    tol = fit_tol * (1.0 + np.abs(y).max())
     err = np.abs(out - z)
     imax = int(err.argmax())
     assert err[imax] <= tol, f"{label}: fit error {err[imax]:.3e} > {tol:.3e} at {imax} (out {out[imax]!r}, oracle {z[imax]!r})"
@@ -43,7 +62,7 @@ def check_row(y, out, blocks, z, zb, label=""):
         assert bad.size == 0, f"{label}: output not constant inside a block at {bad[:5] + 1}"
         gap = np.abs(z[1:] - z[:-1])
         scale = np.maximum(np.abs(z[1:]), np.abs(z[:-1]))
-        required = zb[1:] & (gap > GAP_REL * scale) & (gap > GAP_FLOOR * np.abs(y).max())
+        required = zb[1:] & (gap > gap_rel * scale) & (gap > gap_floor * np.abs(y).max())
         missing = np.nonzero(required & ~blocks[1:])[0]
         assert missing.size == 0, f"{label}: oracle boundaries missing at {missing[:5] + 1} (gaps {gap[missing[:5]]})"
         extra = np.nonzero(blocks[1:] & ~zb[1:])[0]

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "iso.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    names = re.findall(r"\b(iso_[a-z_]+)\s*\(", src)
+    names = re.findall(r"\b(iso_[a-z0-9_]+)\s*\(", src)
     return sorted(set(names))
 
 

@@ -431,3 +431,117 @@ def test_ragged_oracle_shapes_and_bad_values():
     assert np.array_equal(z[0:3], z5[0:3]) and np.array_equal(z[3:20], z17)
     zl, _, st3 = oracle.pava_ragged(y, np.array([0, 10, 40], dtype=np.int64), max_len=12)
     assert list(st3) == [0, oracle.BAD_SHAPE] and np.isnan(zl[10:]).all()
+
+
+# ---- float64 inputs (double-double sums) ----
+def _f64_row(rng, n, kind):
+    if kind == "ties":
+        return rng.integers(-3, 4, size=n).astype(np.float64)
+    if kind == "near_ties":        # gaps far below float32 resolution
+        return 1.0 + 1e-13 * rng.integers(-3, 4, size=n)
+    if kind == "cancel":           # magnitudes 1e-8 .. 1e8: plain double sums lose the small terms
+        return rng.standard_normal(n) * 10.0 ** rng.integers(-8, 9, size=n)
+    return rng.standard_normal(n) + 1e-9 * rng.standard_normal(n)
+
+
+def _plain_double_pava(y, w):
+    """PAVA with plain double sums (what a float64 oracle without the
+    double-double arithmetic would compute)."""
+    bs, bw, b0 = [], [], []
+    for i, (yi, wi) in enumerate(zip(y, w)):
+        bs.append(wi * yi); bw.append(wi); b0.append(i)
+        while len(bs) >= 2 and bs[-2] * bw[-1] >= bs[-1] * bw[-2]:
+            s, ww = bs.pop(), bw.pop(); b0.pop()
+            bs[-1] += s; bw[-1] += ww
+    z = np.empty(len(y))
+    for k, a in enumerate(b0):
+        b = b0[k + 1] if k + 1 < len(b0) else len(y)
+        z[a:b] = bs[k] / bw[k]
+    return z
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_f64_brute_force(seed):
+    """float64 inputs against the exact rational optimum over every contiguous
+    partition: the fit is the optimum rounded to double (within 2 ulp)."""
+    rng = np.random.default_rng(500 + seed)
+    n = int(rng.integers(1, 10))
+    kind = ("ties", "near_ties", "cancel", "normal")[seed % 4]
+    y = _f64_row(rng, n, kind)
+    w = np.ones(n) if seed % 2 == 0 else rng.uniform(0.1, 3.0, n) * (1 + 1e-9 * rng.standard_normal(n))
+    obj, zb, _ = brute_force(y, w)
+    z, _, st = oracle.pava_f64(y, None if seed % 2 == 0 else w)
+    assert st == 0
+    exact = np.array([float(v) for v in zb])
+    assert np.all(np.abs(z - exact) <= 4.5e-16 * np.maximum(np.abs(exact), 1e-300)), (z, exact)
+
+
+def test_f64_cancellation_needs_double_double():
+    """A row on which plain double block sums give a wrong fit while the
+    double-double oracle matches the rational optimum: the pin above would
+    catch an oracle that dropped the error terms."""
+    y = np.array([1e16, 1.0, -1e16, 3.0, 2.0])
+    w = np.ones(5)
+    exact = np.array([float(v) for v in brute_force(y, w)[1]])
+    z, _, _ = oracle.pava_f64(y)
+    assert np.array_equal(z, exact)
+    assert not np.allclose(_plain_double_pava(y, w), exact, rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("fam", ["noise", "random_walk", "sawtooth", "cliff", "offset", "gaussian"])
+@pytest.mark.parametrize("weighting", wl.WEIGHTINGS)
+def test_f64_kkt_and_float32_agreement(fam, weighting):
+    """KKT conditions of the float64 fit (prefix residuals >= 0, zero at the end
+    and at every strict rise), and agreement with the float32 oracle on
+    float32-representable inputs (the same definition computed with plain
+    double sums, exact there)."""
+    n = 2000
+    y32 = wl.family(fam, 1, n, seed=9)[0]
+    w32 = wl.weights(weighting, 1, n, seed=9)
+    w32 = None if w32 is None else w32[0]
+    z, b, st = oracle.pava_f64(y32.astype(np.float64), None if w32 is None else w32.astype(np.float64))
+    z32, b32, _ = oracle.pava(y32, w32)
+    assert st == 0
+    scale = 1.0 + np.abs(y32).max()
+    np.testing.assert_allclose(z, z32, rtol=0, atol=1e-13 * scale)
+    yd = y32.astype(np.float64) + 1e-10 * np.random.default_rng(3).standard_normal(n)
+    wd = None if w32 is None else w32.astype(np.float64)
+    z, b, _ = oracle.pava_f64(yd, wd)
+    r = kkt_residuals(yd, wd, z)
+    tot = np.sum((np.ones(n) if wd is None else wd) * np.abs(yd))
+    assert r.min() >= -1e-13 * tot and abs(r[-1]) <= 1e-13 * tot
+    rises = np.nonzero(z[1:] > z[:-1] + 1e-12 * scale)[0]
+    assert np.all(np.abs(r[rises]) <= 1e-13 * tot)
+
+
+def test_f64_against_scipy():
+    sp = pytest.importorskip("scipy.optimize")
+    rng = np.random.default_rng(8)
+    y = rng.standard_normal(5000) + np.linspace(0, 2, 5000) + 1e-11 * rng.standard_normal(5000)
+    w = rng.uniform(0.5, 2.0, 5000)
+    ref = sp.isotonic_regression(y, weights=w).x
+    z, _, _ = oracle.pava_f64(y, w)
+    np.testing.assert_allclose(z, ref, rtol=0, atol=1e-13)
+
+
+def test_f64_backward():
+    """Block averaging of float64 gradients: exact rational block means on a
+    small case, and the float32 oracle on float32-representable inputs."""
+    rng = np.random.default_rng(12)
+    g = rng.standard_normal(9) * 10.0 ** rng.integers(-6, 7, 9)
+    w = rng.uniform(0.1, 2.0, 9)
+    blocks = np.array([1, 0, 0, 1, 0, 1, 1, 0, 0], np.uint8)
+    out = oracle.backward_f64(g, blocks, w)
+    starts = [0, 3, 5, 6, 9]
+    for a, b in zip(starts[:-1], starts[1:]):
+        G = sum(Fraction(float(v)) for v in g[a:b])
+        W = sum(Fraction(float(v)) for v in w[a:b])
+        for i in range(a, b):
+            assert abs(out[i] - float(Fraction(float(w[i])) * G / W)) <= 4.5e-16 * abs(out[i]) + 1e-300
+    g32 = g.astype(np.float32)
+    np.testing.assert_allclose(oracle.backward_f64(g32.astype(np.float64), blocks),
+                               oracle.backward(g32, blocks), rtol=1e-14, atol=0)
+    y = rng.standard_normal(9)
+    z = oracle.pava_f64(y, w)[0]
+    dw = oracle.backward_w_f64(g, blocks, w, y, z)
+    np.testing.assert_allclose(dw, (y - z) * out / w, rtol=1e-14, atol=1e-300)
