@@ -443,6 +443,29 @@ def run_gpu(args):
             "elements_per_s": yr.numel() / t, "ms": t * 1e3, "gbs": by / t / 1e9,
             "frac": by / t / 1e9 / hbm_peak, "bytes": by}
         del yr, wr, offr, orr, br, wsr
+        # the paper's Table 1 shapes (decreasing unweighted fits of noisy ramps),
+        # with the paper's H100 time beside ours (other hardware: context only)
+        t1 = {}
+        for rows, n, h100 in ((100, 10**3, 0.07), (10**6, 16, 0.28), (10**4, 10**3, 0.35),
+                              (10**3, 10**4, 0.37), (1, 10**6, 0.21), (1, 10**7, 0.56),
+                              (1, 10**8, 2.74)):
+            yv = torch.from_numpy(wl.noisy_ramp(rows, n, 0)).to(dev)
+            ov = torch.empty_like(yv)
+            wsv = torch.empty(max(chp.iso_fit_workspace_bytes(rows, n, False), 1), dtype=torch.uint8,
+                              device=dev)
+            ts = []
+            for i in range(13):
+                flush.zero_()
+                a = torch.cuda.Event(enable_timing=True); b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                chp.iso_fit(yv, None, False, out=ov, want_blocks=False, workspace=wsv, stream=stream)
+                b.record(stream); b.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(b))
+            t = float(np.median(ts))
+            t1[f"{rows}x{n}"] = {"ms": t, "paper_h100_ms": h100, "elements_per_s": rows * n / t * 1e3}
+            del yv, ov, wsv
+        also["paper_table1_decreasing"] = t1
         # the materialised-copy control against the segment lists: whole call and
         # merge stage (segment lists: the two merge kernels; control: its setup,
         # levels and root list)
