@@ -332,24 +332,41 @@ def run_gpu(args):
     fit_bytes = W.elements * (12 if W.weighted else 8)
     whole = fit_bytes / (ms_step * 1e-3) / 1e9
 
-    # ---- end to end through the public API with pinned host buffers ----
+    # ---- end to end through the public API with pinned host buffers: the
+    # input y is in pinned host memory and the fit goes to pinned host memory.
+    # Two ways through the same call: (1) the host buffers passed straight to
+    # iso_fit, whose kernels read y and write the fit over the host link
+    # (NVLink-C2C), and (2) explicit copies to and from device buffers around
+    # the call.  e2e reports the faster; both are in the line. ----
     yh = torch.from_numpy(W.y).pin_memory()
     oh = torch.empty(W.y.shape, dtype=torch.float32).pin_memory()
-    e2e_ms = []
-    for i in range(max(3, args.steps // 4) + 2):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
+
+    def e2e_time(one):
+        ts = []
+        for i in range(max(3, args.steps // 4) + 2):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            one()
+            b.record(stream)
+            b.synchronize()
+            if i >= 2:
+                ts.append(a.elapsed_time(b))
+        return float(np.mean(ts))
+
+    def in_place():
+        chp.iso_fit(yh, None, W.increasing, out=oh, want_blocks=False, workspace=ws, stream=stream)
+
+    def with_copies():
         yd = yh.to(dev, non_blocking=True)
-        z, _, _ = chp.iso_fit(yd, None, W.increasing, want_blocks=False, workspace=ws,
-                              stream=stream)
+        z, _, _ = chp.iso_fit(yd, None, W.increasing, want_blocks=False, workspace=ws, stream=stream)
         oh.copy_(z, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        if i >= 2:
-            e2e_ms.append(a.elapsed_time(b))
-    e2e_val = job_value(W.elements, world, cross_rank_max(float(np.mean(e2e_ms)), dev))
+
+    e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies)}
+    e2e_mode = min(e2e_modes, key=e2e_modes.get)
+    e2e_val = job_value(W.elements, world, cross_rank_max(e2e_modes[e2e_mode], dev))
+    e2e_all = {k: job_value(W.elements, world, cross_rank_max(v, dev)) for k, v in e2e_modes.items()}
 
     # ---- the other named workloads (parity-test configurations), for context ----
     also = {}
@@ -491,7 +508,7 @@ def run_gpu(args):
             "hbm_gbs_whole_call": whole, "hbm_frac_whole_call": whole / hbm_peak,
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": W.elements * 4,
-                    "d2h_bytes_per_step": W.elements * 4},
+                    "d2h_bytes_per_step": W.elements * 4, "mode": e2e_mode, "modes": e2e_all},
             "gpu_launches": launches, "clocks": clocks, "also": also,
         }
         print(json.dumps(line))

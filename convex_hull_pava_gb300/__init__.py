@@ -152,6 +152,33 @@ def _check_dev(t, name, dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_io(t, name, dtype):
+    """A CUDA tensor, or a pinned (page-locked) host tensor: with unified
+    addressing a pinned allocation is device-accessible at the same address,
+    so the kernels read and write it in place over the host link."""
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or a pinned host tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _gpu(t):
+    """The device a call on t runs on (the current device for host tensors)."""
+    torch = _torch()
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
+
+
+def _empty_io(shape, dtype, like):
+    """An output next to `like`: on its device, or pinned host memory."""
+    torch = _torch()
+    if like.is_cuda:
+        return torch.empty(shape, dtype=dtype, device=like.device)
+    return torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
 def _io_dtype(t, name):
     """The I/O type of a call: float32 or float64, taken from its first array."""
     torch = _torch()
@@ -196,24 +223,28 @@ def iso_fit(y, w=None, increasing: bool = True, *, out=None, blocks=None, want_b
     Returns ``(out, blocks, row_status)``; ``blocks`` is None when
     ``want_blocks`` is False and none was given.  ``workspace`` may be a uint8
     CUDA tensor of at least :func:`iso_fit_workspace_bytes` bytes (allocated
-    here otherwise)."""
+    here otherwise).  y, w, out and blocks may also be pinned host tensors:
+    the kernels then read and write them in place over the host link (outputs
+    allocated here follow y)."""
     torch = _torch()
     dt = _io_dtype(y, "y")
-    _check_dev(y, "y", dt)
+    _check_io(y, "y", dt)
     rows, n = _shape2(y)
     if w is not None:
-        _check_dev(w, "w", dt)
+        _check_io(w, "w", dt)
         if w.shape != y.shape:
             raise ValueError("w must have the shape of y")
     if out is None:
-        out = torch.empty_like(y)
-    _check_dev(out, "out", dt)
+        out = _empty_io(y.shape, dt, y)
+    _check_io(out, "out", dt)
     if blocks is None and want_blocks:
-        blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+        blocks = _empty_io(y.shape, torch.uint8, y)
+    if blocks is not None:
+        _check_io(blocks, "blocks", torch.uint8)
     if row_status is None:
-        row_status = torch.empty(rows, dtype=torch.int32, device=y.device)
+        row_status = _empty_io((rows,), torch.int32, y)
     nbytes = iso_fit_workspace_bytes(rows, n, w is not None)
-    ws, ws_bytes = _workspace(nbytes, workspace, y.device)
+    ws, ws_bytes = _workspace(nbytes, workspace, _gpu(y))
     st = _entry("iso_fit", dt)(
         y.data_ptr(), None if w is None else w.data_ptr(), rows, n, int(bool(increasing)),
         out.data_ptr(), None if blocks is None else blocks.data_ptr(),
@@ -268,25 +299,26 @@ def iso_fit_ragged(y, offsets, w=None, increasing: bool = True, *, max_len: int 
     row_status)``, ``row_status`` one word per segment."""
     torch = _torch()
     dt = _io_dtype(y, "y")
-    _check_dev(y, "y", dt)
-    _check_dev(offsets, "offsets", torch.int64)
+    _check_io(y, "y", dt)
+    _check_io(offsets, "offsets", torch.int64)
     if y.dim() != 1 or offsets.dim() != 1 or offsets.numel() < 2:
         raise ValueError("expected a 1-D y and at least two offsets")
     total, segments = y.numel(), offsets.numel() - 1
     if w is not None:
-        _check_dev(w, "w", dt)
+        _check_io(w, "w", dt)
         if w.shape != y.shape:
             raise ValueError("w must have the shape of y")
     if out is None:
-        out = torch.empty_like(y)
+        out = _empty_io(y.shape, dt, y)
     if blocks is None and want_blocks:
-        blocks = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+        blocks = _empty_io(y.shape, torch.uint8, y)
+    if blocks is not None:
+        _check_io(blocks, "blocks", torch.uint8)
     if row_status is None:
-        row_status = torch.empty(segments, dtype=torch.int32, device=y.device)
+        row_status = _empty_io((segments,), torch.int32, y)
     nbytes = iso_fit_ragged_workspace_bytes(segments, total, max_len, w is not None)
-    ws, ws_bytes = _workspace(nbytes, workspace, y.device)
-    if out is not None:
-        _check_dev(out, "out", dt)
+    ws, ws_bytes = _workspace(nbytes, workspace, _gpu(y))
+    _check_io(out, "out", dt)
     st = _entry("iso_fit_ragged", dt)(
         y.data_ptr(), None if w is None else w.data_ptr(), offsets.data_ptr(), segments, total,
         int(max_len), int(bool(increasing)), out.data_ptr(),
@@ -301,16 +333,16 @@ def iso_backward(grad, blocks, w=None, *, out=None, workspace=None, stream=None)
     """Block-averaging backward: ``out_i = w_i * G / W`` over the blocks of ``blocks``."""
     torch = _torch()
     dt = _io_dtype(grad, "grad")
-    _check_dev(grad, "grad", dt)
-    _check_dev(blocks, "blocks", torch.uint8)
+    _check_io(grad, "grad", dt)
+    _check_io(blocks, "blocks", torch.uint8)
     rows, n = _shape2(grad)
     if w is not None:
-        _check_dev(w, "w", dt)
+        _check_io(w, "w", dt)
     if out is None:
-        out = torch.empty_like(grad)
-    _check_dev(out, "out", dt)
+        out = _empty_io(grad.shape, dt, grad)
+    _check_io(out, "out", dt)
     nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
-    ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
+    ws, ws_bytes = _workspace(nbytes, workspace, _gpu(grad))
     st = _entry("iso_backward", dt)(
         grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), rows, n,
         out.data_ptr(), None if ws is None else ws.data_ptr(), ws_bytes, _stream_ptr(stream))
@@ -326,19 +358,19 @@ def iso_backward_w(grad, blocks, w, y, fit, *, out_dy=None, out_dw=None, want_dy
     None: unit weights).  Returns ``(dy or None, dw)``."""
     torch = _torch()
     dt = _io_dtype(grad, "grad")
-    _check_dev(grad, "grad", dt)
-    _check_dev(blocks, "blocks", torch.uint8)
-    _check_dev(y, "y", dt)
-    _check_dev(fit, "fit", dt)
+    _check_io(grad, "grad", dt)
+    _check_io(blocks, "blocks", torch.uint8)
+    _check_io(y, "y", dt)
+    _check_io(fit, "fit", dt)
     rows, n = _shape2(grad)
     if w is not None:
-        _check_dev(w, "w", dt)
+        _check_io(w, "w", dt)
     if want_dy and out_dy is None:
-        out_dy = torch.empty_like(grad)
+        out_dy = _empty_io(grad.shape, dt, grad)
     if out_dw is None:
-        out_dw = torch.empty_like(grad)
+        out_dw = _empty_io(grad.shape, dt, grad)
     nbytes = iso_backward_workspace_bytes(rows, n, w is not None)
-    ws, ws_bytes = _workspace(nbytes, workspace, grad.device)
+    ws, ws_bytes = _workspace(nbytes, workspace, _gpu(grad))
     st = _entry("iso_backward_w", dt)(
         grad.data_ptr(), blocks.data_ptr(), None if w is None else w.data_ptr(), y.data_ptr(),
         fit.data_ptr(), rows, n, None if out_dy is None else out_dy.data_ptr(),

@@ -11,7 +11,13 @@
  *
  * Conventions shared by every entry point:
  *  - Layout: row-major, contiguous [rows, n] float32 arrays (row r starts at
- *    element r*n), on the device.  Any 4-byte alignment is accepted.
+ *    element r*n).  Any 4-byte alignment is accepted.
+ *  - Memory: every array argument ("device" below) must be accessible from
+ *    the device: device memory, or pinned (page-locked) host memory, which
+ *    under unified addressing is device-accessible at its host address -- the
+ *    kernels then read inputs and write outputs in place over the host link
+ *    (NVLink-C2C on GB300), with no separate copy.  The workspace is best
+ *    kept in device memory.
  *  - Ownership: the caller owns every buffer, the workspace and the stream.
  *    The library allocates no memory, keeps no state between calls, and never
  *    synchronises the stream: every call only enqueues kernels on `stream`

@@ -108,3 +108,13 @@ def test_copy_control_host_checks():
     assert lib.iso_fit_copy_control(None, None, 1, 100000, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_copy_control(fake, None, 1, (1 << 30) + 1, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_copy_control(fake, None, 1, 100000, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_WORKSPACE
+
+
+def test_plain_host_tensors_rejected():
+    """Host arrays must be pinned (device-accessible); pageable ones are refused
+    before any CUDA call."""
+    import torch
+    with pytest.raises(ValueError):
+        chp.iso_fit(torch.zeros(10))
+    with pytest.raises(ValueError):
+        chp.iso_backward(torch.zeros(10), torch.zeros(10, dtype=torch.uint8))
