@@ -63,10 +63,23 @@ def peaks():
         return 6800.0, "fallback"
 
 
+WORKLOAD_TEXT = {
+    "row1e7": "1 row x 10,000,000 fp32, y = linspace(0,3,n) + N(0,1) (seed 0), unit weights, "
+              "non-decreasing fit",
+    "row65k": "1 row x 65,536 fp32, y = linspace(0,3,n) + N(0,1) (seed 0), unit weights, "
+              "non-decreasing fit",
+    "batch4096x1024": "4,096 rows x 1,024 fp32, y = linspace(0,3,n) + N(0,1) (seed 0), unit "
+                      "weights, non-decreasing fit",
+    "dense16x4m": "16 rows x 4,194,304 fp32, y = sort(U(0,1)) + 1e-7 i (fp64, then fp32), "
+                  "w ~ U(0.5, 2), non-decreasing fit",
+    "softrank1024x8192": "1,024 rows x 8,192 fp32 soft-rank rows (theta ~ N(0,1) sorted "
+                         "decreasing, eps = 1), unit weights, non-increasing fit",
+}
+
+
 def workload_desc(W):
     return {
-        "workload": "1 row x 10,000,000 fp32, y = linspace(0,3,n) + N(0,1) (seed 0), unit weights, "
-                    "non-decreasing fit",
+        "workload": WORKLOAD_TEXT[W.name],
         "name": W.name, "rows": W.rows, "n": W.n, "weighted": W.weighted,
         "increasing": W.increasing,
         "l2": "flushed before every timed step (256 MB write outside the timed interval)",
@@ -143,12 +156,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel):
+def committed_traffic(workload, kernel):
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        e = d.get(kernel)
+        e = d.get(workload, {}).get(kernel)
         if e and e.get("source_hash") == kernel_source_hash():
             return float(e["bytes_per_launch"])
     except Exception:
@@ -181,7 +194,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from convex_hull_pava_gb300 import workloads as wl
-    W = wl.make(WORKLOAD)
+    W = wl.make(getattr(args, "workload", WORKLOAD))
     import oracle
     oracle.build()
     times = []
@@ -260,7 +273,7 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     hbm_peak, peak_kind = peaks()
 
-    W = wl.make(WORKLOAD)
+    W = wl.make(getattr(args, "workload", WORKLOAD))
     y = torch.from_numpy(W.y).to(dev)
     w = None if W.w is None else torch.from_numpy(W.w).to(dev)
     out = torch.empty_like(y)
@@ -326,7 +339,7 @@ def run_gpu(args):
     ab = alg_bytes.get(dom, W.elements * (12 if W.weighted else 8))
     achieved = ab / (kavg[dom] * 1e-3) / 1e9
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": committed_traffic(dom),
+            "frac": achieved / hbm_peak, "traffic": committed_traffic(W.name, dom),
             "peak_kind": peak_kind, "algorithmic_bytes_per_launch": ab,
             "kernel_ms": kavg}
     fit_bytes = W.elements * (12 if W.weighted else 8)
@@ -339,6 +352,7 @@ def run_gpu(args):
     # (NVLink-C2C), and (2) explicit copies to and from device buffers around
     # the call.  e2e reports the faster; both are in the line. ----
     yh = torch.from_numpy(W.y).pin_memory()
+    wh = None if W.w is None else torch.from_numpy(W.w).pin_memory()
     oh = torch.empty(W.y.shape, dtype=torch.float32).pin_memory()
 
     def e2e_time(one):
@@ -356,11 +370,12 @@ def run_gpu(args):
         return float(np.mean(ts))
 
     def in_place():
-        chp.iso_fit(yh, None, W.increasing, out=oh, want_blocks=False, workspace=ws, stream=stream)
+        chp.iso_fit(yh, wh, W.increasing, out=oh, want_blocks=False, workspace=ws, stream=stream)
 
     def with_copies():
         yd = yh.to(dev, non_blocking=True)
-        z, _, _ = chp.iso_fit(yd, None, W.increasing, want_blocks=False, workspace=ws, stream=stream)
+        wd = None if wh is None else wh.to(dev, non_blocking=True)
+        z, _, _ = chp.iso_fit(yd, wd, W.increasing, want_blocks=False, workspace=ws, stream=stream)
         oh.copy_(z, non_blocking=True)
 
     e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies)}
@@ -507,7 +522,8 @@ def run_gpu(args):
             "data": "synthetic", "config": workload_desc(W),
             "hbm_gbs_whole_call": whole, "hbm_frac_whole_call": whole / hbm_peak,
             "roofline": roof, "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": W.elements * 4,
+            "e2e": {"value": e2e_val, "unit": UNIT,
+                    "h2d_bytes_per_step": W.elements * (8 if W.weighted else 4),
                     "d2h_bytes_per_step": W.elements * 4, "mode": e2e_mode, "modes": e2e_all},
             "gpu_launches": launches, "clocks": clocks, "also": also,
         }
@@ -515,6 +531,12 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def wl_names():
+    sys.path.insert(0, ROOT)
+    from convex_hull_pava_gb300 import workloads as wl
+    return wl.CONFIG_NAMES
 
 
 def main():
@@ -526,6 +548,9 @@ def main():
     ap.add_argument("--quick", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--workload", default=WORKLOAD, choices=wl_names(),
+                    help="the workload of the timed steps, for profiling (the metric is quoted "
+                         "on the default)")
     ap.add_argument("--control-table", action="store_true",
                     help="also time the materialised-copy control on increasing, cliff and noise "
                          "rows of 10^7 and 10^8 elements")
