@@ -15,8 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libiso.so")
-SOURCES = ("iso_api.cu", "iso_rows.cu", "iso_long.cu", "iso_backward.cu", "iso_noalloc.cu",
-           "iso_ragged.cu")
+SOURCES = ("iso_api.cu", "iso_rows.cu", "iso_rows_f64.cu", "iso_long.cu", "iso_long_f64.cu",
+           "iso_backward.cu", "iso_noalloc.cu", "iso_ragged.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-Xptxas", "-warn-spills"]
