@@ -189,6 +189,88 @@ def time_oracle(W, budget_s=10.0, max_reps=200):
                       f"workload, one thread, {el:.1f} s"}
 
 
+def host_cpu():
+    """os.cpu_count() and the CPU's model as /proc/cpuinfo names it."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read().splitlines()
+        for key in ("model name", "Model", "Hardware"):
+            hit = [l.split(":", 1)[1].strip() for l in info if l.startswith(key)]
+            if hit:
+                model = hit[0]
+                break
+        else:
+            imp = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")]
+            part = [l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")]
+            if imp and part:
+                model = f"implementer {imp[0]}, part {part[0]}"
+    except OSError:
+        pass
+    return {"cpu_count": os.cpu_count(), "cpu_model": model}
+
+
+def _oracle_rows_worker(shm_y, shm_w, shape, increasing, a, b):
+    import numpy as np
+    from multiprocessing import shared_memory
+    import oracle
+    sy = shared_memory.SharedMemory(name=shm_y)
+    y = np.ndarray(shape, dtype=np.float32, buffer=sy.buf)
+    w = None
+    if shm_w:
+        sw = shared_memory.SharedMemory(name=shm_w)
+        w = np.ndarray(shape, dtype=np.float32, buffer=sw.buf)
+    t0 = time.perf_counter()
+    oracle.pava(y[a:b], None if w is None else w[a:b], increasing)
+    dt = time.perf_counter() - t0
+    sy.close()
+    if shm_w:
+        sw.close()
+    return dt
+
+
+def time_oracle_all_cores(W, pool, cores):
+    """The oracle over every row of a batched workload, one row per task across
+    the host's cores (rows read from shared memory), after one untimed pass."""
+    import numpy as np
+    from multiprocessing import shared_memory
+    need = W.y.nbytes + (0 if W.w is None else W.w.nbytes)
+    try:
+        st = os.statvfs("/dev/shm")
+        free = st.f_bavail * st.f_frsize
+    except OSError:
+        free = 0
+    if free < 2 * need:
+        return {"unavailable": f"/dev/shm has {free} bytes free, {need} needed"}
+    sy = shared_memory.SharedMemory(create=True, size=W.y.nbytes)
+    np.ndarray(W.y.shape, dtype=np.float32, buffer=sy.buf)[...] = W.y
+    sw = None
+    if W.w is not None:
+        sw = shared_memory.SharedMemory(create=True, size=W.w.nbytes)
+        np.ndarray(W.w.shape, dtype=np.float32, buffer=sw.buf)[...] = W.w
+    try:
+        per = max(1, W.rows // (4 * cores))
+        tasks = [(sy.name, sw.name if sw else "", W.y.shape, W.increasing, a, min(a + per, W.rows))
+                 for a in range(0, W.rows, per)]
+        pool.starmap(_oracle_rows_worker, tasks)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            pool.starmap(_oracle_rows_worker, tasks)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= 2.0 or reps >= 50:
+                break
+        el /= reps
+    finally:
+        sy.close(); sy.unlink()
+        if sw:
+            sw.close(); sw.unlink()
+    return {"value": W.elements / el, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"all {W.rows} rows of {W.n}, {len(tasks)} tasks of up to {per} rows over "
+                      f"{cores} processes, mean of {reps} passes after an untimed one "
+                      f"({el:.3f} s per pass)"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -385,6 +467,11 @@ def run_gpu(args):
 
     # ---- the other named workloads (parity-test configurations), for context ----
     also = {}
+    pool = None
+    if not args.quick and rank == 0 and world == 1 and not args.no_cpu:
+        import multiprocessing as mproc
+        cores = os.cpu_count() or 1
+        pool = mproc.get_context("spawn").Pool(cores)
     if not args.quick:
         for name in ("batch4096x1024", "dense16x4m", "softrank1024x8192", "row65k"):
             V = wl.make(name)
@@ -425,6 +512,8 @@ def run_gpu(args):
                 bb = V.elements * (9 if wv is None else 13)
                 rec["backward"] = {"elements_per_s": V.elements / tb, "ms": tb * 1e3,
                                    "gbs": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak}
+            if pool is not None and V.rows > 1:
+                rec["cpu_all_cores"] = time_oracle_all_cores(V, pool, os.cpu_count() or 1)
             also[name] = rec
             del yv, wv, ov, bv, wsv
         # the soft rank end to end (sort, non-increasing fit, gather; backward
@@ -510,9 +599,13 @@ def run_gpu(args):
         also["copy_control"] = {k: v for k, v in (copy_control(name, mk, dev, flush, stream)
                                                  for name, mk in ctl_cases)}
 
+    if pool is not None:
+        pool.close()
+        pool.join()
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = time_oracle(W, budget_s=args.cpu_seconds)
+        cpu["host"] = host_cpu()
 
     if rank == 0:
         line = {
