@@ -42,12 +42,17 @@ bool shape_ok(int64_t rows, int64_t n) {
 
 iso_status from_cuda(cudaError_t e) { return e == cudaSuccess ? ISO_OK : ISO_ERR_CUDA; }
 
+// An empty batch (no rows, or rows of no elements): nothing to do, whatever
+// the pointers.
+bool empty_call(int64_t rows, int64_t n) { return rows >= 0 && n >= 0 && (rows == 0 || n == 0); }
+
 // Typed implementations of the entry points: IO is the I/O type (float or
 // double); the arithmetic inside is the same fixed point for both.
 template <class IO>
 iso_status fit_impl(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing, IO* out,
                     uint8_t* blocks, void* workspace, size_t workspace_bytes,
                     uint32_t* row_status, void* stream) {
+    if (empty_call(rows, n) && (increasing == 0 || increasing == 1)) return ISO_OK;
     if (!y || !out || !shape_ok(rows, n) || (increasing != 0 && increasing != 1))
         return ISO_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -64,7 +69,7 @@ iso_status fit_impl(const IO* y, const IO* w, int64_t rows, int64_t n, int incre
 }
 
 bool ragged_ok(int64_t segments, int64_t total, int64_t max_len) {
-    return segments >= 1 && segments <= kMaxN && total >= 1 && total <= kMaxElems &&
+    return segments >= 1 && segments <= kMaxN && total >= 0 && total <= kMaxElems &&
            max_len <= kMaxN;
 }
 int64_t ragged_max_len(int64_t total, int64_t max_len) {
@@ -76,7 +81,9 @@ iso_status ragged_impl(const IO* y, const IO* w, const int64_t* offsets, int64_t
                        int64_t total, int64_t max_len, int increasing, IO* out, uint8_t* blocks,
                        void* workspace, size_t workspace_bytes, uint32_t* row_status,
                        void* stream) {
-    if (!y || !offsets || !out || !ragged_ok(segments, total, max_len) ||
+    if (segments == 0 && total >= 0 && (increasing == 0 || increasing == 1)) return ISO_OK;
+    // with no elements every segment is empty (or rejected): y and out are not read
+    if ((total > 0 && (!y || !out)) || !offsets || !ragged_ok(segments, total, max_len) ||
         (increasing != 0 && increasing != 1))
         return ISO_ERR_INVALID_ARG;
     const int64_t ml = ragged_max_len(total, max_len);
@@ -94,6 +101,7 @@ template <class IO>
 iso_status control_impl(const IO* y, const IO* w, int64_t rows, int64_t n, int increasing,
                         IO* out, uint8_t* blocks, void* workspace, size_t workspace_bytes,
                         uint32_t* row_status, void* stream) {
+    if (empty_call(rows, n) && (increasing == 0 || increasing == 1)) return ISO_OK;
     if (!y || !out || !shape_ok(rows, n) || n > (1LL << 30) || (increasing != 0 && increasing != 1))
         return ISO_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -207,6 +215,7 @@ size_t iso_backward_workspace_bytes(int64_t rows, int64_t n, int weighted) {
 iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w, int64_t rows,
                         int64_t n, float* out, void* workspace, size_t workspace_bytes,
                         void* stream) {
+    if (empty_call(rows, n)) return ISO_OK;
     if (!grad || !blocks || !out || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
     return backward_impl<float>(grad, blocks, w, nullptr, nullptr, rows, n, out, nullptr,
                                 workspace, workspace_bytes, stream);
@@ -215,6 +224,7 @@ iso_status iso_backward(const float* grad, const uint8_t* blocks, const float* w
 iso_status iso_backward_f64(const double* grad, const uint8_t* blocks, const double* w,
                             int64_t rows, int64_t n, double* out, void* workspace,
                             size_t workspace_bytes, void* stream) {
+    if (empty_call(rows, n)) return ISO_OK;
     if (!grad || !blocks || !out || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
     return backward_impl<double>(grad, blocks, w, nullptr, nullptr, rows, n, out, nullptr,
                                  workspace, workspace_bytes, stream);
@@ -223,6 +233,7 @@ iso_status iso_backward_f64(const double* grad, const uint8_t* blocks, const dou
 iso_status iso_backward_w(const float* grad, const uint8_t* blocks, const float* w, const float* y,
                           const float* fit, int64_t rows, int64_t n, float* out_dy, float* out_dw,
                           void* workspace, size_t workspace_bytes, void* stream) {
+    if (empty_call(rows, n)) return ISO_OK;
     if (!grad || !blocks || !y || !fit || !out_dw || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
     return backward_impl<float>(grad, blocks, w, y, fit, rows, n, out_dy, out_dw, workspace,
                                 workspace_bytes, stream);
@@ -232,6 +243,7 @@ iso_status iso_backward_w_f64(const double* grad, const uint8_t* blocks, const d
                               const double* y, const double* fit, int64_t rows, int64_t n,
                               double* out_dy, double* out_dw, void* workspace,
                               size_t workspace_bytes, void* stream) {
+    if (empty_call(rows, n)) return ISO_OK;
     if (!grad || !blocks || !y || !fit || !out_dw || !shape_ok(rows, n)) return ISO_ERR_INVALID_ARG;
     return backward_impl<double>(grad, blocks, w, y, fit, rows, n, out_dy, out_dw, workspace,
                                  workspace_bytes, stream);

@@ -47,6 +47,7 @@ cudaError_t scratch_address(void** out) {
 extern "C" iso_status iso_backward_noalloc(const float* grad, const uint8_t* blocks,
                                            const float* w, int64_t rows, int64_t n, float* out,
                                            void* stream) {
+    if (rows >= 0 && n >= 0 && (rows == 0 || n == 0)) return ISO_OK;   // empty: nothing to do
     if (!grad || !blocks || !out || rows < 1 || n < 1 || n > 2147483647LL ||
         rows > (int64_t(1) << 40) / n)
         return ISO_ERR_INVALID_ARG;

@@ -29,7 +29,10 @@
  *    positive) never fail the call: that row's outputs are NaN, its block
  *    flags are 0, and its bit in `row_status` is set (the paper's per-row NaN
  *    flags, Section 6 "Blocks and memory", without its host synchronisation).
- *  - Limits: 1 <= n <= 2^31 - 1, 1 <= rows, rows * n <= 2^40.
+ *  - Limits: 1 <= n <= 2^31 - 1, 1 <= rows, rows * n <= 2^40.  An empty call
+ *    (rows == 0 or n == 0, neither negative; for ragged batches segments == 0)
+ *    does nothing and returns ISO_OK whatever the pointers; a ragged batch
+ *    with total == 0 only writes the segments' statuses.
  *  - float64 I/O: every entry point that takes float32 arrays has an _f64
  *    twin taking float64 arrays (the paper supports both working types,
  *    Section 6 "Implementation"), with the same arguments, layout, workspace
@@ -202,8 +205,9 @@ size_t iso_fit_ragged_workspace_bytes(int64_t segments, int64_t total, int64_t m
  *             offsets[s] .. offsets[s+1]-1.  The offsets are not read by the
  *             host.  Non-decreasing offsets within [0, total] give disjoint
  *             segments; elements outside every segment are not written.
- *  segments   number of segments, 1 <= segments <= 2^31 - 1.
- *  total      length of y (and w, out, blocks), 1 <= total <= 2^40.
+ *  segments   number of segments, 0 <= segments <= 2^31 - 1 (0: nothing to do).
+ *  total      length of y (and w, out, blocks), 0 <= total <= 2^40 (with 0, y and
+ *             out may be NULL and every segment is empty or rejected).
  *  max_len    an upper bound on the segments' lengths that the caller knows,
  *             or <= 0 for none (total).  It only saves launches and workspace:
  *             a segment longer than it is rejected (ISO_ROW_BAD_SHAPE).  At

@@ -47,7 +47,7 @@ def test_invalid_arguments_rejected_on_host():
     # NULL y / out, bad shapes, bad flag: rejected before any CUDA call
     assert lib.iso_fit(None, None, 1, 10, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit(fake, None, 1, 10, 1, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
-    assert lib.iso_fit(fake, None, 0, 10, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(fake, None, -1, 10, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit(fake, None, 1, -3, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit(fake, None, 1, 10, 2, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit(fake, None, 1 << 30, 1 << 30, 1, fake, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
@@ -83,13 +83,13 @@ def test_ragged_host_checks():
     assert 0 < short < full
     assert chp.iso_fit_ragged_workspace_bytes(1000, 10**6, 0, True) > full
     assert chp.iso_fit_ragged_workspace_bytes(0, 10, 0, False) == 0
-    assert chp.iso_fit_ragged_workspace_bytes(1, 0, 0, False) == 0
+    assert chp.iso_fit_ragged_workspace_bytes(1, 0, 0, False) == 256   # the list counters only
     args = lambda y, off, segs, total, ml, inc, out, ws, wsb: (
         y, None, off, segs, total, ml, inc, out, None, ws, wsb, None, None)
     ws = ctypes.c_void_p(0x100000)
     assert lib.iso_fit_ragged(*args(None, fake, 1, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_ragged(*args(fake, None, 1, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
-    assert lib.iso_fit_ragged(*args(fake, fake, 0, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(*args(fake, fake, -1, 10, 0, 1, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_ragged(*args(fake, fake, 1, 10, 0, 3, fake, ws, 1 << 30)) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_ragged(*args(fake, fake, 1, 1 << 32, 1 << 31, 1, fake, ws, 1 << 40)) == chp.ISO_ERR_INVALID_ARG
     need = chp.iso_fit_ragged_workspace_bytes(1, 10, 0, False)
@@ -118,3 +118,22 @@ def test_plain_host_tensors_rejected():
         chp.iso_fit(torch.zeros(10))
     with pytest.raises(ValueError):
         chp.iso_backward(torch.zeros(10), torch.zeros(10, dtype=torch.uint8))
+
+
+def test_empty_calls_do_nothing():
+    """No rows, or rows of no elements (ragged: no segments): ISO_OK before any
+    CUDA call, whatever the pointers; negative sizes are still errors."""
+    lib = chp.load_library()
+    for rows, n in [(0, 10), (5, 0), (0, 0)]:
+        assert lib.iso_fit(None, None, rows, n, 1, None, None, None, 0, None, None) == chp.ISO_OK
+        assert lib.iso_fit_f64(None, None, rows, n, 0, None, None, None, 0, None, None) == chp.ISO_OK
+        assert lib.iso_backward(None, None, None, rows, n, None, None, 0, None) == chp.ISO_OK
+        assert lib.iso_backward_w(None, None, None, None, None, rows, n, None, None, None, 0,
+                                  None) == chp.ISO_OK
+        assert lib.iso_backward_noalloc(None, None, None, rows, n, None, None) == chp.ISO_OK
+        assert lib.iso_fit_copy_control(None, None, rows, n, 1, None, None, None, 0, None,
+                                        None) == chp.ISO_OK
+        assert chp.iso_fit_workspace_bytes(rows, n, False) == 0
+    assert lib.iso_fit(None, None, 0, -1, 1, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit(None, None, 0, 10, 2, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
+    assert lib.iso_fit_ragged(None, None, None, 0, 0, 0, 1, None, None, None, 0, None, None) == chp.ISO_OK
