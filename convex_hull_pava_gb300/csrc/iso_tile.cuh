@@ -6,6 +6,8 @@
 
 #include "iso_device.cuh"
 
+#include <type_traits>
+
 namespace isodev {
 
 // Shared-memory position of element k (0..31) of lane row gl in a staging buffer
@@ -125,19 +127,28 @@ __device__ __forceinline__ int tile_warp_or(int v, int L) {
 // Coalesced load of a tile's nt floats from `src` into the swizzled staging
 // rows of lanes [gl0, gl0 + L), by the tile's L threads.  All loads of a
 // thread are issued before any store.  Tracks the largest biased exponent and
-// flags non-finite values (and, for weights, values that are not > 0).
+// flags non-finite values (and, for weights, values that are not > 0): the
+// bit patterns of non-negative floats order like their values, so the largest
+// |bits| gives both the exponent and whether an Inf or NaN occurred, and for
+// weights the smallest signed bits is > 0 exactly when every weight is.
 template <bool IS_W, class IO>
 __device__ __forceinline__ void stage_tile(const IO* __restrict__ src, int nt, int lane, int L,
                                            int gl0, bool neg, IO* stage, int& emax,
                                            uint32_t& bad) {
+    using UB = typename std::conditional<sizeof(IO) == 4, int32_t, long long>::type;
+    constexpr UB kMag = sizeof(IO) == 4 ? (UB)0x7fffffff : (UB)0x7fffffffffffffffll;
+    constexpr UB kInf = sizeof(IO) == 4 ? (UB)0x7f800000 : (UB)0x7ff0000000000000ll;
+    UB bhi = 0, blo = kMag;
     auto note = [&](IO v) {
-        if (IS_W) {
-            if (!(v > IO(0)) || nonfinite(v)) bad |= 2u;
-            else emax = max(emax, bexp(v));
-        } else {
-            if (nonfinite(v)) bad |= 1u;
-            else emax = max(emax, bexp(v));
-        }
+        UB b;
+        if constexpr (sizeof(IO) == 4) b = __float_as_int(v); else b = __double_as_longlong(v);
+        if (IS_W) { bhi = max(bhi, b); blo = min(blo, b); }
+        else bhi = max(bhi, b & kMag);
+    };
+    auto finish = [&]() {
+        const int e = sizeof(IO) == 4 ? (int)((bhi >> 23) & 0xff) : (int)((bhi >> 52) & 0x7ff);
+        if (IS_W ? (blo <= 0 || bhi >= kInf) : bhi >= kInf) bad |= IS_W ? 2u : 1u;
+        else emax = max(emax, e == 0 ? 1 : e);
     };
     const bool aligned = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0);
     if (aligned) {
@@ -213,6 +224,7 @@ __device__ __forceinline__ void stage_tile(const IO* __restrict__ src, int nt, i
             }
         }
     }
+    finish();
 }
 
 // Result of the common hull phase, per thread (one lane of one tile).
