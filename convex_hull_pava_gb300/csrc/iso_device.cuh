@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <type_traits>
 
 namespace isodev {
 
@@ -271,14 +272,18 @@ template <bool WEIGHTED>
 __device__ __forceinline__ uint32_t lane_hull(const int64_t* Sx, const int64_t* Wx, uint32_t cand,
                                               int e) {
     if (e <= 0) return 0u;
+    // W of a unit-weight lane is a point index (at most 32): 32-bit, and its
+    // turn products are 32 x 64-bit (below 2^61, exact in 64 bits)
+    using WT = typename std::conditional<WEIGHTED, int64_t, int>::type;
     uint32_t mask = 1u;          // stack membership
     int t = 0, b = -1;           // top and the entry below it
-    int64_t St = 0, Wt = 0, Sb = 0, Wb = 0;
+    int64_t St = 0, Sb = 0;
+    WT Wt = 0, Wb = 0;
     uint32_t rem = cand & ~1u & (e >= 32 ? 0xffffffffu : ((1u << e) - 1u));
     int k = rem ? (__ffs(rem) - 1) : e;
     rem &= rem - 1u;
     int64_t Sk = Sx[k];
-    int64_t Wk = WEIGHTED ? Wx[k] : (int64_t)k;
+    WT Wk = WEIGHTED ? (WT)Wx[k] : (WT)k;
     // Every iteration pushes or pops; both loads it may need next are issued
     // before the turn is known, so a lane never waits on a dependent load.
     for (int it = 0; it < 2 * kPts + 2; ++it) {
@@ -287,10 +292,13 @@ __device__ __forceinline__ uint32_t lane_hull(const int64_t* Sx, const int64_t* 
         const int b2 = below ? (31 - __clz(below)) : -1;           // new below-top after a pop
         const int bl = b2 < 0 ? 0 : b2;
         const int64_t Sk2 = Sx[k2];
-        const int64_t Wk2 = WEIGHTED ? Wx[k2] : (int64_t)k2;
+        const WT Wk2 = WEIGHTED ? (WT)Wx[k2] : (WT)k2;
         const int64_t Sb2 = Sx[bl];
-        const int64_t Wb2 = WEIGHTED ? Wx[bl] : (int64_t)bl;
-        const bool push = (b < 0) || left_turn<WEIGHTED>(Wt - Wb, St - Sb, Wk - Wb, Sk - Sb);
+        const WT Wb2 = WEIGHTED ? (WT)Wx[bl] : (WT)bl;
+        bool lt;
+        if constexpr (WEIGHTED) lt = left_turn<true>(Wt - Wb, St - Sb, Wk - Wb, Sk - Sb);
+        else lt = (int64_t)(Wt - Wb) * (Sk - Sb) > (St - Sb) * (int64_t)(Wk - Wb);
+        const bool push = (b < 0) || lt;
         if (push) {
             if (k >= e) break;
             mask |= 1u << k;
