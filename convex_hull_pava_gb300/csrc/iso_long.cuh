@@ -287,13 +287,24 @@ struct MView {
 
 // The turn o -> a -> b is strictly left, exactly.  Unit weights: every W
 // difference is below 2^31 and every S difference below 2^82, so 128-bit
-// products are exact.  Weighted rows: a double-precision determinant decides
-// when it is clear of its rounding bound, the 256-bit products otherwise.
+// products are exact (formed from 32 x 32-bit wide products).  Weighted
+// rows: a double-precision determinant decides when it is clear of its
+// rounding bound, the 256-bit products otherwise.
 template <bool WEIGHTED>
 __device__ __forceinline__ bool row_turn(i128 Wo, i128 So, i128 Wa, i128 Sa, i128 Wb, i128 Sb) {
     const i128 w1 = Wa - Wo, s1 = Sa - So, w2 = Wb - Wo, s2 = Sb - So;
     if constexpr (!WEIGHTED) {
-        return (i128)(int64_t)w1 * s2 > s1 * (i128)(int64_t)w2;
+        // w * s exactly from 32 x 32-bit wide products: |w| < 2^31 (differences
+        // of point indices) and |s| < 2^95, so every partial product fits
+        auto mul = [](i128 w, i128 s) -> i128 {
+            const int64_t wv = (int64_t)(int32_t)(int64_t)w;
+            const uint64_t lo = (uint64_t)s;
+            const int64_t hi = (int64_t)(s >> 64);
+            const int64_t a = wv * (int64_t)(uint32_t)lo;
+            const int64_t b = wv * (int64_t)(uint32_t)(lo >> 32);
+            return (i128)a + ((i128)b << 32) + ((i128)(wv * hi) << 64);
+        };
+        return mul(w1, s2) > mul(w2, s1);
     } else {
         if (fits64(w1) && fits64(s1) && fits64(w2) && fits64(s2))
             return left_turn<true>((int64_t)w1, (int64_t)s1, (int64_t)w2, (int64_t)s2);
