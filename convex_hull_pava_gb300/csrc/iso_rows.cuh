@@ -20,39 +20,55 @@ namespace isodev {
 // rejected row still flags its first element as a block start (ragged
 // batches, where each segment's first element must start a block).  Every
 // thread of the CTA calls it.
-template <int NT, bool WEIGHTED, class IO>
+template <int NT, int RMAX, bool WEIGHTED, class IO>
 __device__ __forceinline__ void fit_row_tiles(const IO* __restrict__ yr,
                                               const IO* __restrict__ wr, int n, bool live,
                                               int L, bool neg, IO* __restrict__ orow,
                                               uint8_t* __restrict__ brow, uint32_t* status,
                                               bool mark0, unsigned char* smem) {
-    using SM = TileSmem<NT, WEIGHTED, true, NT, IO>;
+    using SM = TileSmem<NT, WEIGHTED, true, RMAX, IO>;
     TileHull H;
-    tile_hull_phase<NT, WEIGHTED, true, NT, IO>(yr, wr, n, live, neg, L, smem, H);
+    tile_hull_phase<NT, WEIGHTED, true, RMAX, IO>(yr, wr, n, live, neg, L, smem, H);
 
-    IO* slope = reinterpret_cast<IO*>(smem + SM::oY);   // slope of each vertex's edge
     const Tile& T = H.T;
     const int lane = H.lane, gl = H.gl, e = H.e;
     const bool work = live && H.bad == 0;
     const uint32_t mask = work ? T.mask[lane] : 0u;
+    int64_t* Sx = reinterpret_cast<int64_t*>(smem + SM::oSx);
+    const int64_t* myS = Sx + gl * kRow;            // tile-relative sums at the lane's points
+    const int64_t* myW = reinterpret_cast<const int64_t*>(smem + SM::oWx) + gl * kRow;
+    IO* mySlope = reinterpret_cast<IO*>(Sx + gl * kRow);
 
     // ---- 1. every vertex: the slope of the hull edge leaving it (eq. (3)).  A
-    // one-element block is fitted by its own value, read again from y. ----
+    // one-element block is fitted by its own value, read again from y.  A lane
+    // writes its vertices' slopes over its own row of sums (slot k for the
+    // vertex at bit k, which covers only sums at or before point k, not read
+    // again once that vertex's slope is known); the sums at the vertex after
+    // its last one, in a later lane's row or at the tile's end, are read
+    // before any lane writes. ----
+    const int bl = mask ? tile_succ(T, (lane << 5) + 31 - __clz(mask), L, n) : 0;
+    const int64_t Sbl = mask ? tile_S<WEIGHTED>(T, bl) : 0;
+    const int64_t Wbl = mask ? tile_W<WEIGHTED>(T, bl) : 0;
+    __syncthreads();
     {
         uint32_t m = mask;
         while (m) {
             const int k = __ffs(m) - 1;
             m &= m - 1u;
+            const int k2 = m ? __ffs(m) - 1 : -1;         // this lane's next vertex
             const int v = (lane << 5) + k;
-            const int b = m ? (lane << 5) + __ffs(m) - 1 : tile_succ(T, v, L, n);
+            const int b = k2 >= 0 ? (lane << 5) + k2 : bl;
             IO sl;
             if (b == v + 1) {
-                const IO yv = __ldg(yr + v);               // a one-element block keeps its value
+                const IO yv = __ldg(yr + v);
                 sl = neg ? -yv : yv;
             } else {
-                sl = tile_slope<WEIGHTED, IO>(T, v, b, H.qs, H.qw);
+                const int64_t Sb = k2 >= 0 ? myS[k2] : Sbl;
+                const int64_t Wb = k2 >= 0 ? (WEIGHTED ? myW[k2] : (int64_t)b) : Wbl;
+                const int64_t Wv = WEIGHTED ? myW[k] : (int64_t)v;
+                sl = ratio_t<IO>(Sb - myS[k], Wb - Wv, H.qs - H.qw);
             }
-            slope[spos_t<IO>(gl, k)] = sl;
+            mySlope[k] = sl;
         }
     }
     __syncthreads();
@@ -63,16 +79,16 @@ __device__ __forceinline__ void fit_row_tiles(const IO* __restrict__ yr,
         IO carry = IO(0);
         if (work && e > 0 && !(mask & 1u)) {
             const int cv = tile_pred(T, lane << 5, 0);
-            carry = slope[spos_t<IO>(H.tile * L + (cv >> 5), cv & 31)];
+            carry = reinterpret_cast<const IO*>(Sx + (H.tile * L + (cv >> 5)) * kRow)[cv & 31];
         }
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             const uint32_t upto = k == 31 ? mask : (mask & ((2u << k) - 1u));
-            const IO v = upto ? slope[spos_t<IO>(gl, 31 - __clz(upto))] : carry;
+            const IO v = upto ? mySlope[31 - __clz(upto)] : carry;
             o[k] = neg ? -v : v;
         }
     }
-    __syncthreads();   // Sx and the slopes are dead: stage the output in Sx
+    __syncthreads();   // Sx is dead: stage the output in Sx
     IO* ost = reinterpret_cast<IO*>(smem + SM::oSx);
     stage_out<IO>(ost, gl, o);
     __syncthreads();
@@ -105,7 +121,7 @@ __device__ __forceinline__ void fit_row_tiles(const IO* __restrict__ yr,
 }
 
 // Fit of whole rows: CTA of NT threads, R = NT / L rows of L lanes each.
-template <int NT, bool WEIGHTED, class IO>
+template <int NT, int RMAX, bool WEIGHTED, class IO>
 __global__ void __launch_bounds__(NT)
 rows_fit_kernel(const IO* __restrict__ y, const IO* __restrict__ w, int64_t rows, int n,
                 int L, int increasing, IO* __restrict__ out, uint8_t* __restrict__ blocks,
@@ -115,16 +131,16 @@ rows_fit_kernel(const IO* __restrict__ y, const IO* __restrict__ w, int64_t rows
     const int64_t row = (int64_t)blockIdx.x * R + threadIdx.x / L;
     const bool live = row < rows;
     const int64_t e0 = (live ? row : 0) * (int64_t)n;
-    fit_row_tiles<NT, WEIGHTED, IO>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L, !increasing,
-                                    out + e0, blocks ? blocks + e0 : nullptr,
-                                    row_status ? row_status + (live ? row : 0) : nullptr, false,
-                                    smem);
+    fit_row_tiles<NT, RMAX, WEIGHTED, IO>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L,
+                                          !increasing, out + e0, blocks ? blocks + e0 : nullptr,
+                                          row_status ? row_status + (live ? row : 0) : nullptr,
+                                          false, smem);
 }
 
 // Fit of the segments of one lane class of a ragged batch: list[0 .. count)
 // holds segment indices s, each of n = off[s+1] - off[s] <= 32 L elements at
 // element off[s].  Persistent: each CTA takes R segments at a time.
-template <int NT, bool WEIGHTED, class IO>
+template <int NT, int RMAX, bool WEIGHTED, class IO>
 __global__ void __launch_bounds__(NT)
 rows_fit_ragged_kernel(const IO* __restrict__ y, const IO* __restrict__ w,
                        const int64_t* __restrict__ off, const int32_t* __restrict__ list,
@@ -145,19 +161,20 @@ rows_fit_ragged_kernel(const IO* __restrict__ y, const IO* __restrict__ w,
             e0 = off[s];
             n = (int)(off[s + 1] - e0);
         }
-        fit_row_tiles<NT, WEIGHTED, IO>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L,
-                                        !increasing, out + e0, blocks ? blocks + e0 : nullptr,
-                                        row_status ? row_status + s : nullptr, true, smem);
+        fit_row_tiles<NT, RMAX, WEIGHTED, IO>(y + e0, WEIGHTED ? w + e0 : nullptr, n, live, L,
+                                              !increasing, out + e0,
+                                              blocks ? blocks + e0 : nullptr,
+                                              row_status ? row_status + s : nullptr, true, smem);
         __syncthreads();   // shared memory is reused by the next segments
     }
 }
 
-template <int NT, bool WEIGHTED, class IO>
+template <int NT, int RMAX, bool WEIGHTED, class IO>
 static cudaError_t launch_rows_fit(const IO* y, const IO* w, int64_t rows, int n, int L,
                                    int increasing, IO* out, uint8_t* blocks,
                                    uint32_t* row_status, cudaStream_t stream) {
-    using SM = TileSmem<NT, WEIGHTED, true, NT, IO>;
-    auto kern = rows_fit_kernel<NT, WEIGHTED, IO>;
+    using SM = TileSmem<NT, WEIGHTED, true, RMAX, IO>;
+    auto kern = rows_fit_kernel<NT, RMAX, WEIGHTED, IO>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
     if (err != cudaSuccess) return err;
@@ -170,31 +187,34 @@ static cudaError_t launch_rows_fit(const IO* y, const IO* w, int64_t rows, int n
 }
 
 // n <= 8192.  Lanes per row: the smallest power of two L with 32 L >= n.
+// RMAX bounds the rows of a CTA (its per-row arrays in shared memory): 128
+// for L <= 16, 4 for L = 32, 1 for rows of a CTA of their own.
 template <class IO>
 cudaError_t rows_fit(const IO* y, const IO* w, int64_t rows, int n, int increasing, IO* out,
                      uint8_t* blocks, uint32_t* row_status, cudaStream_t stream) {
     int L = 1;
     while (32 * L < n) L <<= 1;
     const bool weighted = w != nullptr;
-#define ISO_ROWS_LAUNCH(NT_)                                                                    \
-    return weighted ? launch_rows_fit<NT_, true, IO>(y, w, rows, n, L, increasing, out, blocks, \
-                                                     row_status, stream)                       \
-                    : launch_rows_fit<NT_, false, IO>(y, w, rows, n, L, increasing, out,       \
-                                                      blocks, row_status, stream)
-    if (L <= 32) { ISO_ROWS_LAUNCH(128); }   // several rows per CTA of 128 threads
-    if (L <= 64) { ISO_ROWS_LAUNCH(64); }
-    if (L <= 128) { ISO_ROWS_LAUNCH(128); }
-    ISO_ROWS_LAUNCH(256);
+#define ISO_ROWS_LAUNCH(NT_, RMAX_)                                                             \
+    return weighted ? launch_rows_fit<NT_, RMAX_, true, IO>(y, w, rows, n, L, increasing, out,  \
+                                                            blocks, row_status, stream)         \
+                    : launch_rows_fit<NT_, RMAX_, false, IO>(y, w, rows, n, L, increasing, out, \
+                                                             blocks, row_status, stream)
+    if (L <= 16) { ISO_ROWS_LAUNCH(128, 128); }   // several rows per CTA of 128 threads
+    if (L <= 32) { ISO_ROWS_LAUNCH(128, 4); }
+    if (L <= 64) { ISO_ROWS_LAUNCH(64, 1); }      // one row per CTA
+    if (L <= 128) { ISO_ROWS_LAUNCH(128, 1); }
+    ISO_ROWS_LAUNCH(256, 1);
 #undef ISO_ROWS_LAUNCH
 }
 
-template <int NT, bool WEIGHTED, class IO>
+template <int NT, int RMAX, bool WEIGHTED, class IO>
 static cudaError_t launch_rows_ragged(const IO* y, const IO* w, const int64_t* off,
                                       const int32_t* list, const unsigned long long* count,
                                       int64_t cap, int L, int increasing, IO* out,
                                       uint8_t* blocks, uint32_t* row_status, cudaStream_t stream) {
-    using SM = TileSmem<NT, WEIGHTED, true, NT, IO>;
-    auto kern = rows_fit_ragged_kernel<NT, WEIGHTED, IO>;
+    using SM = TileSmem<NT, WEIGHTED, true, RMAX, IO>;
+    auto kern = rows_fit_ragged_kernel<NT, RMAX, WEIGHTED, IO>;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            SM::kBytes);
     if (err != cudaSuccess) return err;
@@ -211,17 +231,18 @@ cudaError_t rows_fit_ragged(const IO* y, const IO* w, const int64_t* off, const 
                             const unsigned long long* count, int64_t cap, int L, int increasing,
                             IO* out, uint8_t* blocks, uint32_t* row_status, cudaStream_t stream) {
     const bool weighted = w != nullptr;
-#define ISO_RAGGED_LAUNCH(NT_)                                                                  \
-    return weighted ? launch_rows_ragged<NT_, true, IO>(y, w, off, list, count, cap, L,         \
-                                                        increasing, out, blocks, row_status,    \
-                                                        stream)                                 \
-                    : launch_rows_ragged<NT_, false, IO>(y, w, off, list, count, cap, L,        \
-                                                         increasing, out, blocks, row_status,   \
-                                                         stream)
-    if (L <= 32) { ISO_RAGGED_LAUNCH(128); }
-    if (L <= 64) { ISO_RAGGED_LAUNCH(64); }
-    if (L <= 128) { ISO_RAGGED_LAUNCH(128); }
-    ISO_RAGGED_LAUNCH(256);
+#define ISO_RAGGED_LAUNCH(NT_, RMAX_)                                                           \
+    return weighted ? launch_rows_ragged<NT_, RMAX_, true, IO>(y, w, off, list, count, cap, L,  \
+                                                               increasing, out, blocks,         \
+                                                               row_status, stream)              \
+                    : launch_rows_ragged<NT_, RMAX_, false, IO>(y, w, off, list, count, cap, L, \
+                                                                increasing, out, blocks,        \
+                                                                row_status, stream)
+    if (L <= 16) { ISO_RAGGED_LAUNCH(128, 128); }
+    if (L <= 32) { ISO_RAGGED_LAUNCH(128, 4); }
+    if (L <= 64) { ISO_RAGGED_LAUNCH(64, 1); }
+    if (L <= 128) { ISO_RAGGED_LAUNCH(128, 1); }
+    ISO_RAGGED_LAUNCH(256, 1);
 #undef ISO_RAGGED_LAUNCH
 }
 

@@ -36,11 +36,11 @@ template <> __device__ __forceinline__ int sunit_t<double>(int gl, int q) {
 // Layout of the dynamic shared memory of a CTA of NT threads holding R = NT/L
 // tiles of L lanes.  The input staging lives inside the lane-relative sums
 // array Sx (2 x 128 B per lane fit in its 264 B per lane): it is read into
-// registers before Sx is written.  Kernels that write the fit (EMIT) keep y in
-// a separate area, which later holds each vertex's edge slope, and merge the
-// lane hulls by walking over vertex masks.  The others (chunks of long rows)
-// compact each lane hull into the front of its row, with the points' indices
-// in Px, and merge the compact lists.
+// registers before Sx is written.  Kernels that write the fit (EMIT) merge the
+// lane hulls by walking over vertex masks and later write each vertex's edge
+// slope over the lane's row of Sx.  The others (chunks of long rows) compact
+// each lane hull into the front of its row, with the points' indices in Px,
+// and merge the compact lists.
 template <int NT, bool WEIGHTED, bool EMIT, int RMAX = NT, class IO = float>
 struct TileSmem {
     // 33 entries per lane row (an odd stride: the lanes' rows start in
@@ -49,7 +49,6 @@ struct TileSmem {
     // lists of neighbouring lanes are contiguous in flat order.
     static constexpr int kSxB = NT * kRow * 8;                  // lane-relative S (+ staging)
     static constexpr int kWxB = WEIGHTED ? NT * kRow * 8 : 0;   // lane-relative W
-    static constexpr int kYB = EMIT ? NT * 32 * (int)sizeof(IO) : 0;   // slope per vertex (EMIT)
     static constexpr int kPxB = EMIT ? 0 : ((NT * kRow * 2 + 15) / 16) * 16;   // point indices
     static constexpr int kCntB = EMIT ? 0 : NT * 4;             // entries of each compact list
     static constexpr int kLSB = (NT + RMAX) * 8;                // lane starts, L+1 per tile
@@ -61,8 +60,7 @@ struct TileSmem {
     static constexpr int kScanB = (NT / 16 + 2) * 8;            // cross-warp scan partials
     static constexpr int oSx = 0;
     static constexpr int oWx = oSx + kSxB;
-    static constexpr int oY = oWx + kWxB;
-    static constexpr int oPx = oY + kYB;
+    static constexpr int oPx = oWx + kWxB;
     static constexpr int oCnt = oPx + kPxB;
     static constexpr int oLS = oCnt + kCntB;
     static constexpr int oLW = oLS + kLSB;
