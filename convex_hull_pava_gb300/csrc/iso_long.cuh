@@ -333,8 +333,11 @@ constexpr int kLinearSteps = 12;   // walk steps before a tangent is found by bi
 // by bisection over the list (first over segments, then inside one).  The two
 // segments the bridge lands in are cut, the merged list's length is set, and
 // the move of the right list's tail is returned.  View: MView, or the flat
-// arrays of the materialised-copy control (FlatView).
-template <bool WEIGHTED, class View>
+// arrays of the materialised-copy control (FlatView).  LOOK > 1: inside a
+// segment a walk step tests LOOK vertices as independent chains (the group
+// merges, whose lists are whole chunk hulls; measured faster there, slower at
+// the top levels, where segments hold one or two vertices).
+template <bool WEIGHTED, int LOOK = 1, class View>
 __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
     int4* seg = V.seg;
     const int nL = V.cnt[j0], nR = V.cnt[j1];
@@ -422,10 +425,34 @@ __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
     for (;;) {
         bool moved = false;
         // the left end moves to its tangent point from b
-        for (int steps = 0;; ++steps) {
+        for (int steps = 0;;) {
             const bool hasPrev = a.r > a.g.lo || a.k > j0;
             if (!hasPrev) break;
-            if (steps == kLinearSteps) { tanL(a, b); break; }
+            if (steps >= kLinearSteps) { tanL(a, b); break; }
+            if (LOOK > 1 && a.r - a.g.lo >= LOOK) {
+                // LOOK vertices of this segment at once, as independent tests:
+                // x_0 = a, x_u = a - u; the walk stops at the first x_u with
+                // turn(x_{u+1}, x_u, b)
+                i128 Wc[LOOK + 1], Sc[LOOK + 1];
+                Wc[0] = a.W; Sc[0] = a.S;
+#pragma unroll
+                for (int u = 1; u <= LOOK; ++u) V.at(a.g, a.r - u, Wc[u], Sc[u]);
+                int u = LOOK;
+#pragma unroll
+                for (int q = LOOK - 1; q >= 0; --q)
+                    if (turn(Wc[q + 1], Sc[q + 1], Wc[q], Sc[q], b.W, b.S)) u = q;
+                steps += LOOK;
+                if (u > 0) {
+                    a.r -= u;
+#pragma unroll
+                    for (int q = 1; q <= LOOK; ++q)
+                        if (q == u) { a.W = Wc[q]; a.S = Sc[q]; }     // no indexed array
+                    moved = true;
+                }
+                if (u < LOOK) break;
+                continue;
+            }
+            ++steps;
             Walker p = a;
             if (a.r > a.g.lo) p.r = a.r - 1;
             else { p.k = a.k - 1; p.g = V.load(p.k); p.r = p.g.hi; }
@@ -435,10 +462,31 @@ __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
             moved = true;
         }
         // the right end moves to its tangent point from a
-        for (int steps = 0;; ++steps) {
+        for (int steps = 0;;) {
             const bool hasNext = b.r < b.g.hi || b.k < kRl;
             if (!hasNext) break;
-            if (steps == kLinearSteps) { tanR(a, b); break; }
+            if (steps >= kLinearSteps) { tanR(a, b); break; }
+            if (LOOK > 1 && b.g.hi - b.r >= LOOK) {
+                i128 Wc[LOOK + 1], Sc[LOOK + 1];
+                Wc[0] = b.W; Sc[0] = b.S;
+#pragma unroll
+                for (int u = 1; u <= LOOK; ++u) V.at(b.g, b.r + u, Wc[u], Sc[u]);
+                int u = LOOK;
+#pragma unroll
+                for (int q = LOOK - 1; q >= 0; --q)
+                    if (turn(a.W, a.S, Wc[q], Sc[q], Wc[q + 1], Sc[q + 1])) u = q;
+                steps += LOOK;
+                if (u > 0) {
+                    b.r += u;
+#pragma unroll
+                    for (int q = 1; q <= LOOK; ++q)
+                        if (q == u) { b.W = Wc[q]; b.S = Sc[q]; }
+                    moved = true;
+                }
+                if (u < LOOK) break;
+                continue;
+            }
+            ++steps;
             Walker q = b;
             if (b.r < b.g.hi) q.r = b.r + 1;
             else { q.k = b.k + 1; q.g = V.load(q.k); q.r = q.g.lo; }
@@ -597,7 +645,7 @@ __device__ __forceinline__ RowQ row_quanta(int64_t m, const LongWs& ws, int64_t 
 // of T threads per merge (T = 1 when merges are many): its first thread finds
 // the bridge and cuts the lists, then the team moves the right list's
 // descriptors in rounds of T.
-template <bool WEIGHTED, bool SMEM>
+template <bool WEIGHTED, bool SMEM, int LOOK = 1>
 __device__ __forceinline__ void merge_levels(const MView<WEIGHTED, SMEM>& V, int64_t jb, int64_t je,
                                              int64_t span0) {
     const int tid = threadIdx.x, nth = blockDim.x;
@@ -613,7 +661,7 @@ __device__ __forceinline__ void merge_levels(const MView<WEIGHTED, SMEM>& V, int
             const int64_t j0 = jb + g * span, j1 = j0 + half;
             const bool act = g < merges && j1 < je;
             Move mv{0, 0, 0};
-            if (act && tl == 0) mv = merge_plan<WEIGHTED>(V, (int)j0, (int)j1);
+            if (act && tl == 0) mv = merge_plan<WEIGHTED, LOOK>(V, (int)j0, (int)j1);
             if (T == 1) {
                 for (int t = 0; t < mv.len; ++t) seg[mv.dst + t] = seg[mv.src + t];
             } else {
@@ -734,7 +782,7 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
                                 const_cast<uint16_t*>(V.P));
         __syncthreads();
     }
-    merge_levels<WEIGHTED, SMEM>(V, jb, je, 1);
+    merge_levels<WEIGHTED, SMEM, 2>(V, jb, je, 1);
     if constexpr (SMEM) {
         // the group's list back to the workspace
         const int n = V.cnt[jb];
