@@ -58,6 +58,7 @@ extern "C" iso_status iso_backward_noalloc(const float* grad, const uint8_t* blo
     if (need > kScratchBytes) return ISO_ERR_WORKSPACE;
     void* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return ISO_ERR_CUDA;
+    isodev::prof_start(st);
     return isodev::long_backward<float>(grad, blocks, w, rows, n, out, nullptr, nullptr, nullptr, ws,
                                  kScratchBytes, st) == cudaSuccess
                ? ISO_OK

@@ -79,3 +79,33 @@ def check_rows(y, out, blocks, z, zb, label=""):
     blocks = None if blocks is None else np.atleast_2d(blocks)
     for r in range(y.shape[0]):
         check_row(y[r], out[r], None if blocks is None else blocks[r], z[r], zb[r], f"{label} row {r}")
+
+
+def check_batch(y, out, blocks, z, zb, label=""):
+    """check_row's criteria (float32 I/O) over every row of a [rows, n] batch at
+    once, vectorised for batches of many short rows."""
+    y = np.atleast_2d(np.asarray(y, np.float64))
+    out = np.atleast_2d(np.asarray(out, np.float64))
+    z = np.atleast_2d(np.asarray(z, np.float64))
+    blocks = np.atleast_2d(np.asarray(blocks)).astype(bool)
+    zb = np.atleast_2d(np.asarray(zb)).astype(bool)
+    ymax = np.abs(y).max(axis=1, keepdims=True)
+    tol = FIT_TOL * (1.0 + ymax)
+    err = np.abs(out - z)
+    bad = np.nonzero((err > tol).any(axis=1))[0]
+    assert bad.size == 0, f"{label}: fit error above tolerance in rows {bad[:5]}"
+    assert blocks[:, 0].all(), f"{label}: element 0 does not start a block in rows {np.nonzero(~blocks[:, 0])[0][:5]}"
+    if y.shape[1] < 2:
+        return
+    inner = ~blocks[:, 1:]
+    r, c = np.nonzero(inner & (out[:, 1:] != out[:, :-1]))
+    assert r.size == 0, f"{label}: output not constant inside a block at rows {r[:5]}, elements {c[:5] + 1}"
+    gap = np.abs(z[:, 1:] - z[:, :-1])
+    scale = np.maximum(np.abs(z[:, 1:]), np.abs(z[:, :-1]))
+    required = zb[:, 1:] & (gap > GAP_REL * scale) & (gap > GAP_FLOOR * ymax)
+    r, c = np.nonzero(required & ~blocks[:, 1:])
+    assert r.size == 0, f"{label}: oracle boundaries missing at rows {r[:5]}, elements {c[:5] + 1}"
+    r, c = np.nonzero(blocks[:, 1:] & ~zb[:, 1:])
+    if r.size:
+        d = np.abs(out[r, c + 1] - out[r, c])
+        assert (d <= tol[r, 0]).all(), f"{label}: extra boundaries that are not ties at rows {r[:5]}"

@@ -52,7 +52,7 @@ def test_fit_and_backward(cuda_ok, case):
     # the backward over the GPU's own blocks
     ref = (oracle.backward_f64 if f64 else oracle.backward)(g, blocks, w)
     scale = np.abs(g).max() * (1.0 if w is None else float(np.max(w) / np.min(w)))
-    assert np.abs(dy - ref).max() <= (1e-12 if f64 else 2e-5) * scale, label
+    assert np.abs(dy - ref).max() <= (1e-12 if f64 else 1e-5) * scale, label
 
 
 @pytest.mark.parametrize("case", range(20))

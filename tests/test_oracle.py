@@ -545,3 +545,53 @@ def test_f64_backward():
     z = oracle.pava_f64(y, w)[0]
     dw = oracle.backward_w_f64(g, blocks, w, y, z)
     np.testing.assert_allclose(dw, (y - z) * out / w, rtol=1e-14, atol=1e-300)
+
+
+def test_f64_backward_w_exact_rationals():
+    """The float64 weight gradient against its definition in exact rationals:
+    d/dw_i = (y_i - z_i) * G_B / W_B with G_B, W_B the block sums of g and w
+    (the paper's Section 6 "Gradient"), on magnitudes from 1e-6 to 1e6 where
+    plain double block sums lose digits."""
+    rng = np.random.default_rng(41)
+    for trial in range(20):
+        n = int(rng.integers(2, 40))
+        g = rng.standard_normal(n) * 10.0 ** rng.integers(-6, 7, n)
+        w = rng.uniform(0.05, 3.0, n) * 10.0 ** rng.integers(-3, 4, n)
+        y = rng.standard_normal(n) * 10.0 ** rng.integers(-2, 3, n)
+        z, blocks, st = oracle.pava_f64(y, w)
+        assert st == 0
+        dw = oracle.backward_w_f64(g, blocks, w, y, z)
+        starts = list(np.nonzero(blocks)[0]) + [n]
+        for a, b in zip(starts[:-1], starts[1:]):
+            G = sum(Fraction(float(v)) for v in g[a:b])
+            W = sum(Fraction(float(v)) for v in w[a:b])
+            for i in range(a, b):
+                exact = (Fraction(float(y[i])) - Fraction(float(z[i]))) * G / W
+                # one rounding of y - z, of G / W and of the product
+                assert abs(dw[i] - float(exact)) <= 8e-16 * abs(float(exact)) + 1e-300, (trial, i)
+
+
+def test_f64_backward_w_finite_differences():
+    """The float64 weight gradient is the derivative of <g, fit(y, w)> in w:
+    central differences in float64 on data without near-ties, wherever the
+    perturbation keeps the block partition (Section 6 "Gradient", App. C)."""
+    rng = np.random.default_rng(42)
+    n = 50
+    y = np.cumsum(rng.uniform(-1.0, 1.0, n)) + 0.3 * rng.standard_normal(n)
+    w = rng.uniform(0.5, 2.0, n)
+    g = rng.standard_normal(n)
+    z0, b0, _ = oracle.pava_f64(y, w)
+    dw = oracle.backward_w_f64(g, b0, w, y, z0)
+    checked = 0
+    for j in range(n):
+        h = 1e-6 * w[j]
+        wp = w.copy(); wp[j] += h
+        wm = w.copy(); wm[j] -= h
+        zp, bp, _ = oracle.pava_f64(y, wp)
+        zm, bm, _ = oracle.pava_f64(y, wm)
+        if not (np.array_equal(bp, b0) and np.array_equal(bm, b0)):
+            continue
+        fd = float(np.dot(g, zp - zm)) / (wp[j] - wm[j])
+        assert abs(fd - dw[j]) <= 1e-7 * (1.0 + abs(dw[j])), (j, fd, dw[j])
+        checked += 1
+    assert checked >= n // 2
