@@ -180,16 +180,16 @@ __device__ __forceinline__ void chunk_hull_one(const IO* __restrict__ y,
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, false, 1, IO>(yr, wr, nt, true, !increasing, NT, smem, H);
 
-    // the chunk hull is the compact list of lane 0's row and the chunk's end
-    // point: copy them to the slot
     const int64_t* Sx = reinterpret_cast<const int64_t*>(smem + SM::oSx);
     const int64_t* Wx = reinterpret_cast<const int64_t*>(smem + SM::oWx);
-    const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
-    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] + 1 : 0;
     const size_t cap = (size_t)C + 1;
     uint16_t* sp = ws.slot_p + c * cap;
     int64_t* sS = ws.slot_S + c * cap;
     int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
+    // the chunk hull is the compact list of lane 0's row and the chunk's end
+    // point: copy them to the slot
+    const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
+    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] + 1 : 0;
     for (int j = threadIdx.x; j < h; j += NT) {
         const bool endp = j == h - 1;
         const int f = j + (j >> 5);                    // flat entry j
@@ -791,6 +791,219 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
     }
 }
 
+// ---------------------------------------------------------------------------
+// Merge levels over flat vertex arrays in shared memory
+// ---------------------------------------------------------------------------
+// When a group's hull vertices fit in shared memory, each chunk hull becomes a
+// contiguous array of its vertices there, with row coordinates formed once (S,
+// and W for weights; unit weights: W is the point's index in the row) and a tag
+// (chunk in the row << 13 | rank in the chunk's hull).  Neighbouring nodes
+// share a point: the left node's last vertex is the right node's first (a
+// chunk hull holds both its ends).  A merge keeps the left node's head and
+// moves the right node's kept tail down behind it, which in shared memory is a
+// few coalesced rounds of one warp; the segment lists of the paper's Section
+// 3.3 avoid that copy where the vertices live in global memory.  The bridge is
+// found by one warp in a few parallel steps instead of a walk (Lemma 4.2):
+//
+//   * if the chain is convex at the shared point s, s stays and nothing else
+//     changes;
+//   * otherwise the bridge joins L = the left node without s to R = the right
+//     node without s.  For a vertex x of L, t(x) is its tangent point on R:
+//     the first vertex of R that lies strictly below the segment from x to its
+//     successor (R's last vertex always does), found by bisection.  The vertex
+//     after x (s after L's last) lies strictly below the line from x to t(x)
+//     for every x before the bridge's left end and for none from it on, so the
+//     left end is the first x for which it does not; the lanes test 32 evenly
+//     spaced vertices of the remaining range at once and a ballot narrows it
+//     (one round for up to 32 candidates, two for up to 1,024).  The right end
+//     is t of the left end.  Ties resolve as in the walks: the left end is the
+//     leftmost and the right end the rightmost vertex on the bridge's line.
+template <bool WEIGHTED>
+struct FlatSm {
+    i128* S;          // row coordinates
+    i128* Wi;         // weighted rows: W
+    int64_t* Wu;      // unit weights: the point's index in the row
+    uint32_t* tag;    // chunk << 13 | rank
+    __device__ __forceinline__ void get(int i, i128& W, i128& Sv) const {
+        Sv = S[i];
+        if constexpr (WEIGHTED) W = Wi[i]; else W = (i128)Wu[i];
+    }
+    __device__ __forceinline__ bool turn(int o, int a, int b) const {
+        i128 Wo, So, Wa, Sa, Wb, Sb;
+        get(o, Wo, So); get(a, Wa, Sa); get(b, Wb, Sb);
+        return row_turn<WEIGHTED>(Wo, So, Wa, Sa, Wb, Sb);
+    }
+};
+
+constexpr int kFlatTagRank = 13;   // bits of the rank in a tag (C + 1 <= 2^13)
+
+// Merge of the nodes A = [a0, a0 + na) and B = [b0, b0 + nb), b0 >= a0 + na,
+// A's last vertex being B's first, by the 32 lanes of one warp.  The merged
+// node is left at a0; returns its size (on every lane).
+template <bool WEIGHTED>
+__device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int nb) {
+    const int lane = threadIdx.x & 31;
+    int keepA = na, fromB = 1;            // A[0 .. keepA) then B[fromB .. nb)
+    if (!F.turn(a0 + na - 2, b0, b0 + 1)) {
+        const int qR = nb - 1;            // R = B[1 .. nb)
+        auto tangent = [&](int x) -> int {
+            int jl = 0, jh = qR - 1;
+            while (jl < jh) {
+                const int mid = (jl + jh) >> 1;
+                if (F.turn(a0 + x, b0 + 1 + mid, b0 + 2 + mid)) jh = mid; else jl = mid + 1;
+            }
+            return jl;
+        };
+        // the bridge's left end is in [lo, hi] of L = A[0 .. na-1); P(hi) is false
+        int lo = 0, hi = na - 2;
+        for (;;) {
+            const int n = hi - lo + 1;
+            const int step = (n + 31) >> 5;
+            const int x = lo + lane * step;
+            bool nf = false;                    // "P(x) is false"
+            int t = 0;
+            if (x <= hi) {
+                t = tangent(x);
+                nf = !F.turn(a0 + x, a0 + x + 1, b0 + 1 + t);
+            }
+            const unsigned bal = __ballot_sync(kFull, nf);
+            if (step == 1) {
+                const int k = __ffs(bal) - 1;   // every x in [lo, hi] tested
+                keepA = lo + k + 1;
+                fromB = 1 + __shfl_sync(kFull, t, k);
+                break;
+            }
+            if (bal == 0u) {
+                const int kmax = (hi - lo) / step;        // last tested sample
+                lo = lo + kmax * step + 1;
+            } else {
+                const int k = __ffs(bal) - 1;
+                hi = lo + k * step;
+                lo = k == 0 ? hi : lo + (k - 1) * step + 1;
+            }
+        }
+    }
+    // the right node's kept tail moves down behind the left node's kept head
+    const int len = nb - fromB, dst = a0 + keepA, src = b0 + fromB;
+    for (int q = 0; q < len; q += 32) {
+        const int k = q + lane;
+        i128 sv = 0, wv = 0;
+        int64_t wu = 0;
+        uint32_t tg = 0;
+        if (k < len) {
+            sv = F.S[src + k];
+            if constexpr (WEIGHTED) wv = F.Wi[src + k]; else wu = F.Wu[src + k];
+            tg = F.tag[src + k];
+        }
+        __syncwarp();
+        if (k < len) {
+            F.S[dst + k] = sv;
+            if constexpr (WEIGHTED) F.Wi[dst + k] = wv; else F.Wu[dst + k] = wu;
+            F.tag[dst + k] = tg;
+        }
+        __syncwarp();
+    }
+    return keepA + len;
+}
+
+// Shared-memory layout of the flat group merge for mg chunks and H vertices.
+struct FlatLayout {
+    size_t oS, oW, oTag, oStart, oSize, bytes;
+    __host__ __device__ FlatLayout(int64_t mg, int64_t H, bool weighted) {
+        size_t o = 0;
+        auto take = [&](size_t b, size_t al) { o = (o + al - 1) & ~(al - 1); const size_t r = o; o += b; return r; };
+        oS = take(16 * H, 16);
+        oW = take((weighted ? 16 : 8) * H, 16);
+        oTag = take(4 * H, 4);
+        oStart = take(4 * mg, 4);
+        oSize = take(4 * mg, 4);
+        bytes = o;
+    }
+};
+constexpr int kFlatSmem = 96 * 1024;   // dynamic shared memory of the group kernel
+
+// The group's chunk hulls [jb, je) (Hg vertices; chunk starts gS/gW in row
+// coordinates, vertex bases gH) merged by levels of warp merges over flat
+// arrays; the group's root list is written to the workspace as segments, as
+// the segment-list merges leave it.  Every thread of the CTA calls it.
+template <bool WEIGHTED>
+__device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, int jb, int je,
+                                                 const i128* gS, const i128* gW,
+                                                 const int32_t* gH, int64_t Hg) {
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
+    const int mg = je - jb;
+    const FlatLayout Lo(mg, Hg, WEIGHTED);
+    unsigned char* sm = merge_smem;
+    FlatSm<WEIGHTED> F;
+    F.S = reinterpret_cast<i128*>(sm + Lo.oS);
+    F.Wi = reinterpret_cast<i128*>(sm + Lo.oW);
+    F.Wu = reinterpret_cast<int64_t*>(sm + Lo.oW);
+    F.tag = reinterpret_cast<uint32_t*>(sm + Lo.oTag);
+    int32_t* nstart = reinterpret_cast<int32_t*>(sm + Lo.oStart);
+    int32_t* nsize = reinterpret_cast<int32_t*>(sm + Lo.oSize);
+    for (int j = tid; j < mg; j += nth) {
+        nstart[j] = gH[j];
+        nsize[j] = (j + 1 < mg ? gH[j + 1] : (int32_t)Hg) - gH[j];
+    }
+    // every vertex in row coordinates: its chunk by bisection over the bases
+    for (int64_t i = tid; i < Hg; i += nth) {
+        int lo = 0, hi = mg - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gH[mid] <= i) lo = mid; else hi = mid - 1;
+        }
+        const int j = jb + lo;
+        const int r = (int)(i - gH[lo]);
+        const size_t g = (size_t)(c0 + j) * ((size_t)C + 1) + r;
+        F.S[i] = gS[lo] + conv(ws.slot_S[g], ws.dS[c0 + j]);
+        if constexpr (WEIGHTED) F.Wi[i] = gW[lo] + conv(ws.slot_W[g], ws.dW[c0 + j]);
+        else F.Wu[i] = (int64_t)j * C + ws.slot_p[g];
+        F.tag[i] = ((uint32_t)j << kFlatTagRank) | (uint32_t)r;
+    }
+    __syncthreads();
+    for (int half = 1; half < mg; half <<= 1) {
+        for (int j = 2 * half * warp; j + half < mg; j += 2 * half * nw) {
+            const int n = warp_merge<WEIGHTED>(F, nstart[j], nsize[j], nstart[j + half], nsize[j + half]);
+            if (lane == 0) nsize[j] = n;
+        }
+        __syncthreads();
+    }
+    // the root list of the group as segments (chunk, first rank, last rank):
+    // a segment starts at every vertex whose chunk differs from its predecessor's
+    if (warp == 0) {
+        const int n = nsize[0], v0 = nstart[0];
+        int nseg = 0;
+        for (int q = 0; q < n; q += 32) {
+            const int k = q + lane;
+            uint32_t tg = 0, tp = 0, tn = 0;
+            if (k < n) {
+                tg = F.tag[v0 + k];
+                tp = k > 0 ? F.tag[v0 + k - 1] : ~0u;
+                tn = k + 1 < n ? F.tag[v0 + k + 1] : ~0u;
+            }
+            const bool head = k < n && (tp >> kFlatTagRank) != (tg >> kFlatTagRank);
+            const bool tail = k < n && (tn >> kFlatTagRank) != (tg >> kFlatTagRank);
+            const unsigned hb = __ballot_sync(kFull, head);
+            if (head) {
+                // this segment's index; its last rank is found by the segment's tail lane
+                const int idx = nseg + __popc(hb & ((1u << lane) - 1u));
+                ws.seg[c0 + jb + idx].x = (int)(tg >> kFlatTagRank);
+                ws.seg[c0 + jb + idx].y = (int)(tg & ((1u << kFlatTagRank) - 1u));
+            }
+            // a tail lane belongs to the segment of the last head at or before it
+            const unsigned hb_upto = hb & (0xffffffffu >> (31 - lane));
+            if (tail) {
+                const int idx = nseg + __popc(hb_upto) - 1;
+                ws.seg[c0 + jb + idx].z = (int)(tg & ((1u << kFlatTagRank) - 1u));
+                ws.seg[c0 + jb + idx].w = 0;
+            }
+            nseg += __popc(hb);
+        }
+        if (lane == 0) ws.cnt[c0 + jb] = nseg;
+    }
+}
+
 // One group of kGroup chunks: the row's quanta and status, the chunks' starts
 // in row coordinates and their grid shifts, then (MERGE) the group's merges.
 template <bool WEIGHTED, bool MERGE = true>
@@ -869,7 +1082,9 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     }
     if (!MERGE) return;
     const int64_t Hg = s_Hg;
-    if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
+    if (FlatLayout(je - jb, Hg, WEIGHTED).bytes <= (size_t)kFlatSmem)
+        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
+    else if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
         merge_group<WEIGHTED, true>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
     else
         merge_group<WEIGHTED, false>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
@@ -1637,9 +1852,9 @@ static cudaError_t long_launch(const IO* y, const IO* w, const LongGeo& geo,
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "chunk_hull");
     err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, RAGGED>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kFlatSmem);
     if (err != cudaSuccess) return err;
-    merge_groups_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.groups, kGroupThreads, kGroupSmem, stream>>>(
+    merge_groups_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.groups, kGroupThreads, kFlatSmem, stream>>>(
         geo, gr.ng, ws, row_status);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     prof_mark(stream, "merge_groups");

@@ -5,6 +5,7 @@
 #pragma once
 
 #include "iso_device.cuh"
+#include "iso_qhull.cuh"
 
 #include <type_traits>
 
@@ -235,7 +236,22 @@ struct TileHull {
     int qs, qw;      // quantum exponents of S and W (W: 0 for unit weights)
     uint32_t bad;    // ISO_ROW_BAD_* bits of the tile (0 = valid)
     bool live;       // the tile exists (row index in range)
+    bool quick;      // the hull came from tile_quickhull (vertex masks only)
 };
+
+// Whole rows of kQuickMinLanes to 32 lanes (one warp) whose first half has a
+// larger mean than their second half (a trend against the fit's direction, so
+// few blocks) take the levels of farthest-point splits (iso_qhull.cuh) instead
+// of the lane hulls and merging rounds: a row of one block is finished by one
+// level, where the merging rounds walk long bridges.  Rows with the trend
+// along the fit keep the merging rounds, which measured faster there (each
+// level's lanes evaluate their points one by one, and the warp waits for its
+// busiest lane); so do longer rows (merging the warps' hulls by CTA-wide
+// levels measured slower) and the chunks of long rows.  A CTA in which more
+// than one lane in kQuickDense has over 24 of its 31 inner points locally
+// convex (a dense hull) also keeps them.
+constexpr int kQuickMinLanes = 4;
+constexpr int kQuickDense = 8;
 
 // Common phase of every tile kernel: stage the tile's nt elements (y, and w
 // when WEIGHTED) through shared memory, flag non-finite values, choose the
@@ -385,13 +401,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
         }
     }
 
-    // ---- lane hulls in bit masks, on lane-relative sums ----
-    // Each edge's slope is its element's mean, so a lane whose every interior
-    // point is locally convex (strictly increasing means) is a strictly convex
-    // chain: all its points are vertices and the monotone chain is not needed.
     const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
-    uint32_t mask = ((cand | 1u) & allp) == allp ? (e > 0 ? allp : 0u)
-                                                 : lane_hull<WEIGHTED>(myS, myW, cand, e);
     const int64_t ls = LSa[tile * (L + 1) + lane];
     const int64_t lw = WEIGHTED ? LWa[tile * (L + 1) + lane] : 0;
 
@@ -406,16 +416,57 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     T.L = L;
     T.nt = nt;
 
+    // ---- few vertices expected: the hull by levels of farthest-point splits,
+    // on tile-relative rows ----
+    bool rel = false;       // rows hold tile-relative sums
+    H.quick = false;
+    if (EMIT && L >= kQuickMinLanes && L <= 32) {
+        __syncthreads();   // lane starts written
+        // the tile's trend: mean of lanes [0, L/2) against the rest
+        bool down = false;
+        if (work && lane == 0) {
+            const int h = L >> 1;
+            const int64_t S1 = T.LS[h], S2 = T.LS[L] - S1;
+            const int64_t W1 = WEIGHTED ? T.LW[h] : (int64_t)min(h << 5, nt);
+            const int64_t W2 = (WEIGHTED ? T.LW[L] : (int64_t)nt) - W1;
+            down = W2 > 0 && (__int128)S1 * W2 > (__int128)S2 * W1;
+        }
+        const int tiles = __syncthreads_count(work && lane == 0);
+        const int downs = __syncthreads_count(down);
+        const int dense = __syncthreads_count(work && __popc(cand & allp) > 24);
+        const int filled = __syncthreads_count(e > 0);
+        if (tiles > 0 && downs == tiles && dense * kQuickDense <= filled) {
+#pragma unroll
+            for (int k = 0; k <= 32; ++k) myS[k] += ls;
+            if constexpr (WEIGHTED) {
+#pragma unroll
+                for (int k = 0; k <= 32; ++k) myW[k] += lw;
+            }
+            rel = true;
+            H.quick = tile_quickhull<WEIGHTED>(T, summ, lane, L, e, work, cand);
+        }
+    }
+    if (H.quick) return;
+
+    // ---- lane hulls in bit masks ----
+    // Each edge's slope is its element's mean, so a lane whose every interior
+    // point is locally convex (strictly increasing means) is a strictly convex
+    // chain: all its points are vertices and the monotone chain is not needed.
+    uint32_t mask = ((cand | 1u) & allp) == allp ? (e > 0 ? allp : 0u)
+                                                 : lane_hull<WEIGHTED>(myS, myW, cand, e);
+
     if constexpr (EMIT) {
         // ---- rows become tile-relative; the lane hulls are merged in rounds
         // by walking over the vertex masks: pairs of 2^r lanes, up to the
         // whole tile (Section 3.2).  Rounds whose groups lie inside one warp
         // synchronise the warp only. ----
+        if (!rel) {
 #pragma unroll
-        for (int k = 0; k <= 32; ++k) myS[k] += ls;
-        if constexpr (WEIGHTED) {
+            for (int k = 0; k <= 32; ++k) myS[k] += ls;
+            if constexpr (WEIGHTED) {
 #pragma unroll
-            for (int k = 0; k <= 32; ++k) myW[k] += lw;
+                for (int k = 0; k <= 32; ++k) myW[k] += lw;
+            }
         }
         maska[gl] = mask;
         {
@@ -460,11 +511,12 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
         uint16_t* myP = Px + gl * kRow;
         int c = 0;
         uint32_t mm = mask;
+        const int64_t ls2 = rel ? 0 : ls, lw2 = rel ? 0 : lw;
         while (mm) {
             const int k = __ffs(mm) - 1;
             mm &= mm - 1u;
-            myS[c] = myS[k] + ls;
-            if constexpr (WEIGHTED) myW[c] = myW[k] + lw;
+            myS[c] = myS[k] + ls2;
+            if constexpr (WEIGHTED) myW[c] = myW[k] + lw2;
             myP[c] = (uint16_t)((lane << 5) + k);
             ++c;
         }
