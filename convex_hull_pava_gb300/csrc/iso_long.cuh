@@ -49,6 +49,14 @@ template <> struct LongCfg<true> { static constexpr int NT = ISO_WEIGHTED_NT; st
 
 typedef __int128 i128;
 
+#ifndef ISO_GROUP
+#define ISO_GROUP 64
+#endif
+constexpr int kGroup = ISO_GROUP;
+// Vertices of a group's merged hull kept as a flat array in the workspace for
+// the top merge (groups with more take the segment-list route).
+constexpr int kGroupFlatCap = 1024;
+
 struct ChunkMeta {
     int32_t h;      // hull vertices (both ends included)
     int32_t bad;    // ISO_ROW_BAD_* bits
@@ -80,6 +88,10 @@ struct LongWs {
     int32_t* dW;       // [M]
     ChunkEnds* ends;   // [M]
     int32_t* rowq;     // [rows][4]: qs_row, qw_row, bad
+    i128* gfS;         // [G][kGroupFlatCap] each group's merged hull, row coordinates
+    void* gfW;         // i128 (weighted) or int64 (unit weights: point index) per vertex
+    uint32_t* gfTag;   // chunk << 13 | rank
+    int32_t* gfN;      // [G] its vertices, -1 when it is only a segment list
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -112,6 +124,11 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t M, Lon
     w.dW = (int32_t*)take(sizeof(int32_t) * M);
     w.ends = (ChunkEnds*)take(sizeof(ChunkEnds) * M);
     w.rowq = (int32_t*)take(sizeof(int32_t) * 4 * rows);
+    const size_t G = (size_t)(M / kGroup + rows + 1);      // groups of all rows, at most
+    w.gfS = (i128*)take(sizeof(i128) * kGroupFlatCap * G);
+    w.gfW = take((WEIGHTED ? sizeof(i128) : sizeof(int64_t)) * kGroupFlatCap * G);
+    w.gfTag = (uint32_t*)take(sizeof(uint32_t) * kGroupFlatCap * G);
+    w.gfN = (int32_t*)take(sizeof(int32_t) * G);
     if (ws) *ws = w;
     return off;
 }
@@ -581,10 +598,6 @@ __device__ __forceinline__ Acc3 block_excl_scan3(Acc3 v, Acc3* tmp, Acc3& total)
 // Each CTA reads its chunk hulls into shared memory when they fit (noisy rows
 // keep few vertices; the top kernel reads only the vertices still inside a
 // segment), else it reads them from the slots in global memory.
-#ifndef ISO_GROUP
-#define ISO_GROUP 64
-#endif
-constexpr int kGroup = ISO_GROUP;
 constexpr int kGroupThreads = 256;
 constexpr int kGroupSmem = 48 * 1024;
 
@@ -921,6 +934,7 @@ struct FlatLayout {
     }
 };
 constexpr int kFlatSmem = 96 * 1024;   // dynamic shared memory of the group kernel
+constexpr int kMaxFlatGroups = 2 * kMergeThreads;   // groups of a row whose flat arrays the top merge reads
 
 // The group's chunk hulls [jb, je) (Hg vertices; chunk starts gS/gW in row
 // coordinates, vertex bases gH) merged by levels of warp merges over flat
@@ -929,7 +943,7 @@ constexpr int kFlatSmem = 96 * 1024;   // dynamic shared memory of the group ker
 template <bool WEIGHTED>
 __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, int jb, int je,
                                                  const i128* gS, const i128* gW,
-                                                 const int32_t* gH, int64_t Hg) {
+                                                 const int32_t* gH, int64_t Hg, int64_t g) {
     constexpr int C = LongCfg<WEIGHTED>::C;
     const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
     const int mg = je - jb;
@@ -1001,6 +1015,19 @@ __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, i
             nseg += __popc(hb);
         }
         if (lane == 0) ws.cnt[c0 + jb] = nseg;
+    }
+    // the merged hull as a flat array for the top merge, when it fits
+    const int n = nsize[0], v0 = nstart[0];
+    const bool keep = n <= kGroupFlatCap;
+    if (tid == 0) ws.gfN[g] = keep ? n : -1;
+    if (keep) {
+        const size_t o = (size_t)g * kGroupFlatCap;
+        for (int k = tid; k < n; k += nth) {
+            ws.gfS[o + k] = F.S[v0 + k];
+            if constexpr (WEIGHTED) reinterpret_cast<i128*>(ws.gfW)[o + k] = F.Wi[v0 + k];
+            else reinterpret_cast<int64_t*>(ws.gfW)[o + k] = F.Wu[v0 + k];
+            ws.gfTag[o + k] = F.tag[v0 + k];
+        }
     }
 }
 
@@ -1082,9 +1109,12 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     }
     if (!MERGE) return;
     const int64_t Hg = s_Hg;
-    if (FlatLayout(je - jb, Hg, WEIGHTED).bytes <= (size_t)kFlatSmem)
-        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
-    else if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
+    if (FlatLayout(je - jb, Hg, WEIGHTED).bytes <= (size_t)kFlatSmem) {
+        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, Hg, g);
+        return;
+    }
+    if (tid == 0) ws.gfN[g] = -1;
+    if (MergeLayout(je - jb, Hg, WEIGHTED, false).bytes <= (size_t)kGroupSmem)
         merge_group<WEIGHTED, true>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
     else
         merge_group<WEIGHTED, false>(m, ws, c0, jb, je, s_gS, s_gW, s_gH, Hg);
@@ -1218,6 +1248,76 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
     root_ends<WEIGHTED>(V, m, ws, c0, segOf, nextSeg, prevSeg);
 }
 
+// The top of the tree over the groups' flat arrays (every group of the row
+// kept one, and they fit in shared memory together): the arrays are read as
+// the tree's nodes, merged by the warp merges of the group kernel, and each
+// chunk's root range and the root vertices around it are found by bisection
+// over the root array's tags (Section 3.4, Corollary 4.5).  A root vertex on
+// a chunk boundary is tagged with the chunk it ends, as in the segment lists.
+template <bool WEIGHTED>
+__device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int64_t m, int64_t gb,
+                                               int ng, int H, const int32_t* gbase) {
+    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
+    const FlatLayout Lo(ng, H, WEIGHTED);
+    unsigned char* sm = merge_smem;
+    FlatSm<WEIGHTED> F;
+    F.S = reinterpret_cast<i128*>(sm + Lo.oS);
+    F.Wi = reinterpret_cast<i128*>(sm + Lo.oW);
+    F.Wu = reinterpret_cast<int64_t*>(sm + Lo.oW);
+    F.tag = reinterpret_cast<uint32_t*>(sm + Lo.oTag);
+    int32_t* nstart = reinterpret_cast<int32_t*>(sm + Lo.oStart);
+    int32_t* nsize = reinterpret_cast<int32_t*>(sm + Lo.oSize);
+    for (int k = warp; k < ng; k += nw) {
+        const int n = ws.gfN[gb + k], b = gbase[k];
+        const size_t o = (size_t)(gb + k) * kGroupFlatCap;
+        if (lane == 0) { nstart[k] = b; nsize[k] = n; }
+        for (int i = lane; i < n; i += 32) {
+            F.S[b + i] = ws.gfS[o + i];
+            if constexpr (WEIGHTED) F.Wi[b + i] = reinterpret_cast<const i128*>(ws.gfW)[o + i];
+            else F.Wu[b + i] = reinterpret_cast<const int64_t*>(ws.gfW)[o + i];
+            F.tag[b + i] = ws.gfTag[o + i];
+        }
+    }
+    __syncthreads();
+    for (int half = 1; half < ng; half <<= 1) {
+        for (int k = 2 * half * warp; k + half < ng; k += 2 * half * nw) {
+            const int n = warp_merge<WEIGHTED>(F, nstart[k], nsize[k], nstart[k + half], nsize[k + half]);
+            if (lane == 0) nsize[k] = n;
+        }
+        __syncthreads();
+    }
+    // ends of every chunk from the root array R (tags in chunk order)
+    const int n = nsize[0], v0 = nstart[0];
+    const uint32_t* tg = F.tag + v0;
+    auto first_at_least = [&](int64_t j) -> int {       // first root vertex of a chunk >= j
+        int lo = 0, hi = n;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((int64_t)(tg[mid] >> kFlatTagRank) < j) lo = mid + 1; else hi = mid;
+        }
+        return lo;
+    };
+    constexpr uint32_t kRank = (1u << kFlatTagRank) - 1u;
+    for (int64_t j = tid; j < m; j += nth) {
+        const int lb = first_at_least(j), ub = first_at_least(j + 1);
+        ChunkEnds ce;
+        ce.bad = 0;
+        if (lb < ub) { ce.lo = (int)(tg[lb] & kRank); ce.hi = (int)(tg[ub - 1] & kRank); }
+        else { ce.lo = 1; ce.hi = 0; }
+        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
+        ce.pt0_vertex = 0;
+        if (j > 0) {
+            const int k = v0 + lb - 1;
+            F.get(k, ce.prevW, ce.prevS);
+            const uint32_t t = F.tag[k];
+            ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
+                             (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
+        }
+        if (j + 1 < m) F.get(v0 + ub, ce.nextW, ce.nextS);
+        ws.ends[c0 + j] = ce;
+    }
+}
+
 template <bool WEIGHTED>
 __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& ws, int64_t row) {
     constexpr int C = LongCfg<WEIGHTED>::C;
@@ -1225,6 +1325,28 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
     const int64_t m = R.m, c0 = R.c0;
     const int tid = threadIdx.x, nth = blockDim.x;
     if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
+    {
+        // every group of the row kept a flat array and they fit: the flat top
+        const int64_t ng = (m + kGroup - 1) / kGroup;
+        const int64_t gb = geo.e0 ? geo.g0[row] : row * ng;
+        __shared__ int32_t s_gbase[kMaxFlatGroups];
+        __shared__ int s_scan2[32];
+        if (ng <= kMaxFlatGroups) {
+            // the groups' sizes, bases by a block scan (ng <= blockDim.x * 2)
+            const int k0 = 2 * tid, k1 = 2 * tid + 1;
+            const int c0n = k0 < ng ? ws.gfN[gb + k0] : 0, c1n = k1 < ng ? ws.gfN[gb + k1] : 0;
+            const bool ok = __syncthreads_and(c0n >= 0 && c1n >= 0);
+            int tot;
+            const int b = block_excl_scan_int(c0n + c1n, s_scan2, tot);
+            if (k0 < ng) s_gbase[k0] = b;
+            if (k1 < ng) s_gbase[k1] = b + c0n;
+            __syncthreads();
+            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes <= (size_t)kMergeSmem) {
+                merge_top_flat<WEIGHTED>(ws, c0, m, gb, (int)ng, tot, s_gbase);
+                return;
+            }
+        }
+    }
     // the chunks' surviving segments (each chunk in at most one): lengths into
     // segOf, first ranks into prevSeg (scratch), then bases by a scan
     int32_t* len = ws.segOf + c0;

@@ -420,7 +420,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     // on tile-relative rows ----
     bool rel = false;       // rows hold tile-relative sums
     H.quick = false;
-    if (EMIT && L >= kQuickMinLanes && L <= 32) {
+    if constexpr (EMIT && RMAX > 1) if (L >= kQuickMinLanes && L <= 32) {
         __syncthreads();   // lane starts written
         // the tile's trend: mean of lanes [0, L/2) against the rest
         bool down = false;
