@@ -159,6 +159,16 @@ __device__ __forceinline__ RowRef geo_row(const LongGeo& g, int64_t r) {
     return RowRef{g.id[r], g.e0[r], n, (n + C - 1) / C, g.c0[r]};
 }
 
+// Programmatic dependent launch: a kernel launched with
+// cudaLaunchAttributeProgrammaticStreamSerialization may start before the
+// previous kernel of the stream has finished; it waits here, before touching
+// anything that kernel writes, until that kernel has completed and its memory
+// is visible.  A kernel launched without the attribute passes straight on.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the stream's next kernel (launched with the attribute) be scheduled now:
+// its CTAs become resident on idle SMs and wait in wait_prior_grid().
+__device__ __forceinline__ void launch_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool fits64(i128 x) { return (i128)(int64_t)x == x; }
 
 // A double within 3 ulp of a 128-bit integer (exact below 2^53).
@@ -1123,6 +1133,8 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
 template <bool WEIGHTED, bool RAGGED, bool MERGE = true>
 __global__ void __launch_bounds__(kGroupThreads)
 merge_groups_kernel(LongGeo geo, int64_t ng, LongWs ws, uint32_t* __restrict__ row_status) {
+    wait_prior_grid();
+    launch_next_grid();   // the top merge's CTAs may take idle SMs now
     if (!RAGGED) {
         merge_group_one<WEIGHTED, MERGE>(geo, ng, ws, row_status, blockIdx.x);
         return;
@@ -1286,20 +1298,24 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
         }
         __syncthreads();
     }
-    // ends of every chunk from the root array R (tags in chunk order)
+    // ends of every chunk from the root array R (tags in chunk order): first[j]
+    // = the first root vertex of a chunk >= j, filled by each root vertex for
+    // the chunks since its predecessor's (the nodes' arrays are dead now, so
+    // first[] lives in the vertex arrays' space after R)
     const int n = nsize[0], v0 = nstart[0];
     const uint32_t* tg = F.tag + v0;
-    auto first_at_least = [&](int64_t j) -> int {       // first root vertex of a chunk >= j
-        int lo = 0, hi = n;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((int64_t)(tg[mid] >> kFlatTagRank) < j) lo = mid + 1; else hi = mid;
-        }
-        return lo;
-    };
+    int32_t* first = reinterpret_cast<int32_t*>(F.tag + v0 + n);
+    __syncthreads();                       // nsize and nstart are read: first[] may cover them
     constexpr uint32_t kRank = (1u << kFlatTagRank) - 1u;
+    for (int k = tid; k <= n; k += nth) {
+        const int64_t jlo = k == 0 ? 0 : (int64_t)(tg[k - 1] >> kFlatTagRank) + 1;
+        const int64_t jhi = k == n ? m : (int64_t)(tg[k] >> kFlatTagRank);
+        for (int64_t j = jlo; j <= jhi && j <= m; ++j) first[j] = k;
+    }
+    __syncthreads();
+    constexpr int C = LongCfg<WEIGHTED>::C;
     for (int64_t j = tid; j < m; j += nth) {
-        const int lb = first_at_least(j), ub = first_at_least(j + 1);
+        const int lb = first[j], ub = first[j + 1];
         ChunkEnds ce;
         ce.bad = 0;
         if (lb < ub) { ce.lo = (int)(tg[lb] & kRank); ce.hi = (int)(tg[ub - 1] & kRank); }
@@ -1309,9 +1325,14 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
         if (j > 0) {
             const int k = v0 + lb - 1;
             F.get(k, ce.prevW, ce.prevS);
-            const uint32_t t = F.tag[k];
-            ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
-                             (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
+            // the previous root vertex is this chunk's first point (it closes chunk j - 1)
+            if constexpr (WEIGHTED) {
+                const uint32_t t = F.tag[k];
+                ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
+                                 (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
+            } else {
+                ce.pt0_vertex = ce.prevW == (i128)(j * C) ? 1 : 0;
+            }
         }
         if (j + 1 < m) F.get(v0 + ub, ce.nextW, ce.nextS);
         ws.ends[c0 + j] = ce;
@@ -1341,7 +1362,7 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
             if (k0 < ng) s_gbase[k0] = b;
             if (k1 < ng) s_gbase[k1] = b + c0n;
             __syncthreads();
-            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes <= (size_t)kMergeSmem) {
+            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes + 4 * (size_t)(m + 1) <= (size_t)kMergeSmem) {
                 merge_top_flat<WEIGHTED>(ws, c0, m, gb, (int)ng, tot, s_gbase);
                 return;
             }
@@ -1386,6 +1407,8 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
 template <bool WEIGHTED, bool RAGGED>
 __global__ void __launch_bounds__(kMergeThreads, 1)
 merge_top_kernel(LongGeo geo, LongWs ws) {
+    wait_prior_grid();
+    launch_next_grid();   // the expansion's CTAs may take idle SMs now
     if (!RAGGED) {
         merge_top_row<WEIGHTED>(geo, ws, blockIdx.x);
         return;
@@ -1593,6 +1616,7 @@ template <bool WEIGHTED, bool RAGGED, class IO>
 __global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
 expand_kernel(const IO* __restrict__ y, LongGeo geo, int increasing, LongWs ws,
               IO* __restrict__ out, uint8_t* __restrict__ blocks) {
+    wait_prior_grid();
     if (!RAGGED) {
         expand_one<WEIGHTED, IO>(y, geo, increasing, ws, out, blocks, blockIdx.x);
         return;
@@ -1957,6 +1981,25 @@ ctl_root_kernel(int64_t m, LongWs ws, CtlWs cw) {
     root_ends<WEIGHTED>(V, m, ws, c0, ws.segOf + c0, ws.nextSeg + c0, ws.prevSeg + c0);
 }
 
+// Launch of a kernel that may start while the stream's previous kernel is
+// finishing (programmatic dependent launch); the kernel calls
+// wait_prior_grid() before reading what that kernel writes.
+template <typename... P, typename... A>
+static cudaError_t launch_after(void (*kern)(P...), unsigned grid, unsigned block, size_t smem,
+                                cudaStream_t stream, A... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Launch sizes: exact counts for a dense batch, bounds for a ragged one.
 struct LongGrid { int64_t rows, chunks, groups, ng; };
 
@@ -1976,22 +2019,23 @@ static cudaError_t long_launch(const IO* y, const IO* w, const LongGeo& geo,
     err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, RAGGED>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFlatSmem);
     if (err != cudaSuccess) return err;
-    merge_groups_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.groups, kGroupThreads, kFlatSmem, stream>>>(
-        geo, gr.ng, ws, row_status);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_after(merge_groups_kernel<WEIGHTED, RAGGED>, (unsigned)gr.groups, kGroupThreads, kFlatSmem,
+                       stream, geo, gr.ng, ws, row_status);
+    if (err != cudaSuccess) return err;
     prof_mark(stream, "merge_groups");
     err = cudaFuncSetAttribute(merge_top_kernel<WEIGHTED, RAGGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kMergeSmem);
     if (err != cudaSuccess) return err;
-    merge_top_kernel<WEIGHTED, RAGGED><<<(unsigned)gr.rows, kMergeThreads, kMergeSmem, stream>>>(geo, ws);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_after(merge_top_kernel<WEIGHTED, RAGGED>, (unsigned)gr.rows, kMergeThreads, kMergeSmem, stream,
+                       geo, ws);
+    if (err != cudaSuccess) return err;
     prof_mark(stream, "merge_top");
     err = cudaFuncSetAttribute(expand_kernel<WEIGHTED, RAGGED, IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                ExpandSmem<WEIGHTED, IO>::kBytes);
     if (err != cudaSuccess) return err;
-    expand_kernel<WEIGHTED, RAGGED, IO><<<(unsigned)gr.chunks, NT, ExpandSmem<WEIGHTED, IO>::kBytes, stream>>>(
-        y, geo, increasing, ws, out, blocks);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_after(expand_kernel<WEIGHTED, RAGGED, IO>, (unsigned)gr.chunks, NT,
+                       (size_t)ExpandSmem<WEIGHTED, IO>::kBytes, stream, y, geo, increasing, ws, out, blocks);
+    if (err != cudaSuccess) return err;
     prof_mark(stream, "expand");
     return cudaSuccess;
 }
