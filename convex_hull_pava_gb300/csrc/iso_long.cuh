@@ -213,16 +213,49 @@ __device__ __forceinline__ void chunk_hull_one(const IO* __restrict__ y,
     uint16_t* sp = ws.slot_p + c * cap;
     int64_t* sS = ws.slot_S + c * cap;
     int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
-    // the chunk hull is the compact list of lane 0's row and the chunk's end
-    // point: copy them to the slot
-    const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
-    const int h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] + 1 : 0;
-    for (int j = threadIdx.x; j < h; j += NT) {
-        const bool endp = j == h - 1;
-        const int f = j + (j >> 5);                    // flat entry j
-        sp[j] = endp ? (uint16_t)nt : Px[f];
-        sS[j] = endp ? H.T.LS[NT] : Sx[f];
-        if constexpr (WEIGHTED) sW[j] = endp ? H.T.LW[NT] : Wx[f];
+    int h;
+    if (H.list) {
+        // the hull of the candidates' list: its vertices (warp 0's bits, lane l
+        // holding entries [l K, l K + K)) and the list's last entry, the end point
+        __shared__ int s_h;
+        if (threadIdx.x < 32) {
+            const int wl = threadIdx.x, n = H.list, K = (n - 1 + 31) >> 5;
+            const uint16_t* LP = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
+            const int64_t* LSv = reinterpret_cast<const int64_t*>(smem + SM::oPx + 2 * kListCap);
+            const uint32_t vm = H.T.mask[wl];
+            const int cv = __popc(vm);
+            int x = cv;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(kFull, x, d);
+                if (wl >= d) x += o;
+            }
+            int j = x - cv;
+            uint32_t m = vm;
+            while (m) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1u;
+                sp[j] = LP[wl * K + k];
+                sS[j] = LSv[wl * K + k];
+                ++j;
+            }
+            const int total = __shfl_sync(kFull, x, 31);
+            if (wl == 0) { sp[total] = LP[n - 1]; sS[total] = LSv[n - 1]; s_h = total + 1; }
+        }
+        __syncthreads();
+        h = s_h;
+    } else {
+        // the chunk hull is the compact list of lane 0's row and the chunk's end
+        // point: copy them to the slot
+        const uint16_t* Px = reinterpret_cast<const uint16_t*>(smem + SM::oPx);
+        h = H.bad == 0 ? reinterpret_cast<const int*>(smem + SM::oCnt)[0] + 1 : 0;
+        for (int j = threadIdx.x; j < h; j += NT) {
+            const bool endp = j == h - 1;
+            const int f = j + (j >> 5);                    // flat entry j
+            sp[j] = endp ? (uint16_t)nt : Px[f];
+            sS[j] = endp ? H.T.LS[NT] : Sx[f];
+            if constexpr (WEIGHTED) sW[j] = endp ? H.T.LW[NT] : Wx[f];
+        }
     }
     if (threadIdx.x == 0) {
         ChunkMeta mt;
@@ -877,9 +910,11 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
             }
             return jl;
         };
-        // the bridge's left end is in [lo, hi] of L = A[0 .. na-1); P(hi) is false
+        // the bridge's left end is in [lo, hi] of L = A[0 .. na-1); P(hi) is
+        // false.  Each round narrows the range 32-fold, so 8 rounds cover any
+        // list; the range never empties.
         int lo = 0, hi = na - 2;
-        for (;;) {
+        for (int round = 0; round < 8; ++round) {
             const int n = hi - lo + 1;
             const int step = (n + 31) >> 5;
             const int x = lo + lane * step;
@@ -891,14 +926,16 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
             }
             const unsigned bal = __ballot_sync(kFull, nf);
             if (step == 1) {
-                const int k = __ffs(bal) - 1;   // every x in [lo, hi] tested
+                // every x in [lo, hi] tested; with exactly convex inputs some P is
+                // false, else (inputs convex only up to rounding) the last one
+                const int k = bal ? __ffs(bal) - 1 : hi - lo;
                 keepA = lo + k + 1;
                 fromB = 1 + __shfl_sync(kFull, t, k);
                 break;
             }
             if (bal == 0u) {
                 const int kmax = (hi - lo) / step;        // last tested sample
-                lo = lo + kmax * step + 1;
+                lo = min(lo + kmax * step + 1, hi);
             } else {
                 const int k = __ffs(bal) - 1;
                 hi = lo + k * step;

@@ -6,6 +6,7 @@
 
 #include "iso_device.cuh"
 #include "iso_qhull.cuh"
+#include "iso_filter.cuh"
 
 #include <type_traits>
 
@@ -237,6 +238,7 @@ struct TileHull {
     uint32_t bad;    // ISO_ROW_BAD_* bits of the tile (0 = valid)
     bool live;       // the tile exists (row index in range)
     bool quick;      // the hull came from tile_quickhull (vertex masks only)
+    int list;        // chunks: entries of the list whose hull was found (0: none)
 };
 
 // Whole rows of kQuickMinLanes to 32 lanes (one warp) whose first half has a
@@ -401,7 +403,6 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
         }
     }
 
-    const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
     const int64_t ls = LSa[tile * (L + 1) + lane];
     const int64_t lw = WEIGHTED ? LWa[tile * (L + 1) + lane] : 0;
 
@@ -415,6 +416,49 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     T.sbase = tile * L;
     T.L = L;
     T.nt = nt;
+
+    // ---- chunks of long rows (unit weights, float32 input; the tile is the
+    // CTA): the candidates filter (iso_filter.cuh); when few survive, their
+    // list, whose hull one warp finds by farthest-point levels ----
+    H.list = 0;
+    if constexpr (!EMIT && !WEIGHTED && sizeof(IO) == 4) {
+        static_assert((3 * NT + 3 * (NT / 32)) * 4 <= SM::kPxB && kListCap * 10 <= SM::kPxB, "list area");
+        unsigned char* area = smem + SM::oPx;
+        __syncthreads();                                     // lane starts written
+        cand = chunk_filter<NT>(yv, e, lane, nt, H.qs, LSa, work ? cand : 0u,
+                                reinterpret_cast<float*>(area));
+        const int cnt_l = __popc(cand);
+        const int64_t inc = tile_scan_incl<NT>(cnt_l, lane, L, scan);
+        __shared__ int s_total;
+        if (lane == L - 1) s_total = (int)inc;
+        __syncthreads();                                     // scratch read, total known
+        const int n_list = s_total + 2;
+        if (work && n_list <= kListCap) {
+            uint16_t* LP = reinterpret_cast<uint16_t*>(area);
+            int64_t* LSv = reinterpret_cast<int64_t*>(area + 2 * kListCap);
+            int j = 1 + (int)inc - cnt_l;
+            uint32_t m = cand;
+            while (m) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1u;
+                LP[j] = (uint16_t)((lane << 5) + k);
+                LSv[j] = ls + myS[k];
+                ++j;
+            }
+            if (lane == 0) { LP[0] = 0; LSv[0] = 0; LP[n_list - 1] = (uint16_t)nt; LSv[n_list - 1] = LSa[L]; }
+            __syncthreads();
+            __shared__ int s_ok;
+            if (tid < 32) {
+                const bool ok = warp_list_hull(LP, LSv, n_list, maska);
+                if (tid == 0) s_ok = ok;
+            }
+            __syncthreads();
+            if (s_ok) { H.list = n_list; return; }
+        }
+    }
+
+    const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
+
 
     // ---- few vertices expected: the hull by levels of farthest-point splits,
     // on tile-relative rows ----
