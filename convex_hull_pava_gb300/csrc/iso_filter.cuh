@@ -45,44 +45,34 @@ constexpr int kListCap = 512;   // list entries (survivors + the two ends) for t
 // sum_j (s/2 + 2^-24 |d_j| + 2^-24 |f_{j+1}|) with d_j = fl(y_j - c).  The
 // lane's bound doubles that total (covering the rounding of the bound itself).
 //
-// A test "p strictly above the segment from x to z" computes
-//     t = (f_p - f_x)(z - x) - (f_z - f_x)(p - x)
-// in float32 and drops p only when t exceeds
-//     m = (d_p + d_x)(z - x) + (d_z + d_x)(p - x) + 2^-21 (|f_p - f_x| (z - x) + |f_z - f_x| (p - x)),
-// d the bounds of the three points: the first two terms bound the effect of the
-// values' errors, the last the rounding of t's own operations (at most four
-// roundings of 2^-24 of terms of those sizes).  With point indices exact in
-// float (below 2^24), t and m are formed for each side of the lane's lowest
-// point from per-lane constants: t = (z - x) f_p - (f_z - f_x) p - k0 and m =
-// m0 + m1 p + 2^-21 (z - x) |f_p - f_x|.
-struct FSide {
-    float w, a, k0, fx, m0, m1;   // segment from x to z: w = z - x, a = f_z - f_x
-    float kabs;                   // |w f_x| + |a x|: the size of k0's terms
+// A test "p strictly above the segment from x to z" (x < p < z) uses the
+// segment's float slope sigma = fl(fl(f_z - f_x) / (z - x)) and intercept
+// beta = fl(f_x - sigma x) (one fused multiply-add), the line's value at p
+// l = fl(sigma p + beta) (another) and t = fl(f_p - l).  With F the exact
+// sheared values, Sigma = (F_z - F_x) / (z - x) and Lambda = F_x + Sigma (p - x):
+//   |sigma - Sigma| <= (d_x + d_z + 2^-23 |f_z - f_x|) / (z - x),
+//   |l - Lambda|    <= 2 d_x + d_z + 2^-23 |f_z - f_x| + 2^-24 (|beta| + |l|),
+//   |t - T|         <= d_p + |l - Lambda| + 2^-24 |t|,   T = F_p - Lambda,
+// d the bounds of the three points (p - x <= z - x).  With |l| <= F and
+// |t| <= 2 F, F the largest |f| of the lane and of the two ends, p is dropped
+// when t exceeds the per-segment constant
+//   M = (d_p + 2 d_x + d_z + 2^-23 |f_z - f_x| + 2^-24 |beta| + 2^-22 F)(1 + 2^-20):
+// then T >= t - |t - T| > 0, p lies strictly above the exact segment.
+struct FSeg {
+    float sigma, beta, M;
 };
 
-__device__ __forceinline__ FSide side(int x, float fx, float dx, int z, float fz, float dz, float dp) {
-    FSide r;
-    r.w = (float)(z - x);
-    r.a = fz - fx;
-    r.fx = fx;
-    // t = w (f_p - f_x) - a (p - x) = w f_p - a p - (w f_x - a x)
-    r.k0 = fmaf(r.w, fx, -r.a * (float)x);
-    r.kabs = fabsf(r.w * fx) + fabsf(r.a * (float)x);
-    // m = (dp + dx) w + (dz + dx)(p - x) + 2^-21 (w |f_p - f_x| + |a| (p - x))
-    const float g = dz + dx + 0x1p-21f * fabsf(r.a);
-    r.m1 = g;
-    r.m0 = (dp + dx) * r.w - g * (float)x;
+__device__ __forceinline__ FSeg fseg(int x, float fx, float dx, int z, float fz, float dz, float dp,
+                                     float F) {
+    FSeg r;
+    const float num = fz - fx;
+    r.sigma = num / (float)(z - x);
+    r.beta = fmaf(-r.sigma, (float)x, fx);
+    const float Fm = fmaxf(F, fmaxf(fabsf(fx), fabsf(fz)));
+    r.M = (dp + 2.0f * dx + dz + 0x1p-23f * fabsf(num) + 0x1p-24f * fabsf(r.beta) + 0x1p-22f * Fm) *
+          (1.0f + 0x1p-20f);
+    if (!(r.M < 1.0e37f)) r.M = __int_as_float(0x7f800000);   // inf or nan: nothing is dropped
     return r;
-}
-
-// p (index pf as a float, sheared value fp) is strictly above the side's segment
-// beyond the rounding bound (the bound is inflated by 2^-20 of itself and of the
-// sizes of t's terms, for the rounding of t, k0 and m's own arithmetic).
-__device__ __forceinline__ bool fabove(float w, float a, float k0, float fx, float m0, float m1,
-                                       float kabs, float pf, float fp) {
-    const float t = fmaf(w, fp, -fmaf(a, pf, k0));
-    const float m = fmaf(m1, pf, m0) + 0x1p-21f * w * fabsf(fp - fx);
-    return t > m * (1.0f + 0x1p-20f) + 0x1p-20f * (fabsf(w * fp) + fabsf(a * pf) + kabs);
 }
 
 // Filter of the candidates of every lane of a chunk tile (one tile of L = NT
@@ -111,7 +101,7 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
     }
     const float fend = tot - c * (float)nt;
     const float dend = 2.0f * (0x1p-22f * fabsf(tot) + 0x1p-24f * (fabsf(c * (float)nt) + fabsf(fend)));
-    float f = G, fmin = G;
+    float f = G, fmin = G, fabsmax = fabsf(G);
     int kmin = 0;
     const float half_q = 0.5f * sc;
 #pragma unroll
@@ -120,6 +110,7 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
             const float d = yv[k] - c;
             f = f + d;
             err += half_q + 0x1p-24f * (fabsf(d) + fabsf(f));
+            fabsmax = fmaxf(fabsmax, fabsf(f));
             if (k + 1 < e && f < fmin) { fmin = f; kmin = k + 1; }
         }
     }
@@ -173,11 +164,11 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
     float fb = fend, db = dend;
     if (lane + 1 < L && xp[lane + 1] >= 0) { pb = xp[lane + 1]; fb = xf[lane + 1]; db = xd[lane + 1]; }
     const int pm = (lane << 5) + kmin;
-    const FSide left = side(pa, fa, da, pm, fmin, delta, delta);    // points before the lowest
-    const FSide right = side(pm, fmin, delta, pb, fb, db, delta);   // points after it
-    const FSide mid = side(pa, fa, da, pb, fb, db, delta);          // the lowest point itself
-    const FSide gl = side(0, 0.0f, 0.0f, g, fg, dg, delta);         // chord from point 0 to g
-    const FSide gr = side(g, fg, dg, nt, fend, dend, delta);        // chord from g to the end
+    const FSeg left = fseg(pa, fa, da, pm, fmin, delta, delta, fabsmax);    // points before the lowest
+    const FSeg right = fseg(pm, fmin, delta, pb, fb, db, delta, fabsmax);   // points after it
+    const FSeg mid = fseg(pa, fa, da, pb, fb, db, delta, fabsmax);          // the lowest point itself
+    const FSeg gl = fseg(0, 0.0f, 0.0f, g, fg, dg, delta, fabsmax);         // chord from point 0 to g
+    const FSeg gr = fseg(g, fg, dg, nt, fend, dend, delta, fabsmax);        // chord from g to the end
     uint32_t drop = 0u;
     f = G;
     float pf = (float)(lane << 5);
@@ -185,22 +176,89 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
     for (int k = 0; k < 32; ++k) {
         if (k < e && ((keep >> k) & 1u)) {
             const int p = (lane << 5) + k;
-            const bool lt = p < pm, gt = p > pm;
-            // the side of the lane's lowest point that p lies on, field by field
-#define ISO_SEL(F) (lt ? left.F : (gt ? right.F : mid.F))
-#define ISO_SELG(F) (p < g ? gl.F : gr.F)
-            const bool out = (p != g && fabove(ISO_SELG(w), ISO_SELG(a), ISO_SELG(k0), ISO_SELG(fx), ISO_SELG(m0),
-                                               ISO_SELG(m1), ISO_SELG(kabs), pf, f)) ||
-                             fabove(ISO_SEL(w), ISO_SEL(a), ISO_SEL(k0), ISO_SEL(fx), ISO_SEL(m0), ISO_SEL(m1),
-                                    ISO_SEL(kabs), pf, f);
-#undef ISO_SELG
-#undef ISO_SEL
-            if (out) drop |= 1u << k;
+            const bool lt = p < pm, gt = p > pm, lg = p < g;
+            const float s1 = lt ? left.sigma : (gt ? right.sigma : mid.sigma);
+            const float b1 = lt ? left.beta : (gt ? right.beta : mid.beta);
+            const float m1 = lt ? left.M : (gt ? right.M : mid.M);
+            const float s2 = lg ? gl.sigma : gr.sigma;
+            const float b2 = lg ? gl.beta : gr.beta;
+            const float m2 = p == g ? __int_as_float(0x7f800000) : (lg ? gl.M : gr.M);
+            const float t1 = f - fmaf(s1, pf, b1);
+            const float t2 = f - fmaf(s2, pf, b2);
+            if (t1 > m1 || t2 > m2) drop |= 1u << k;
         }
         if (k < e) f = f + (yv[k] - c);
         pf += 1.0f;
     }
     return keep & ~drop;
+}
+
+// Hull of a short list (n <= the CTA's threads) in one pass: entry t is a
+// strict vertex of the lower hull iff the steepest slope into it from an
+// earlier entry is below the shallowest slope out of it to a later one.  With
+// w = |P_j - P_t| and s = S_t - S_j for every other entry j, the steepest slope
+// in is the largest s / w over j < t and the shallowest slope out the smallest
+// -s / w over j > t, i.e. again the largest s / w: one running best per side,
+// compared exactly by cross products (w below 2^13, |s| below 2^63).  R
+// threads (R = the CTA's threads / n, a power of two up to 32, neighbours in
+// one warp) share an entry, each scanning a share of the other entries, and
+// their bests are combined by shuffles.  The test is then the exact turn from
+// the best entry before t, over t, to the best entry after it.  Entries 0 and
+// n - 1 are vertices.  The vertices' bits go to vm in warp_list_hull's layout
+// (lane l, bit k for entry l K + k, K = ceil((n - 1) / 32); the last entry
+// implied).  Every thread of the CTA calls it.
+template <int NT>
+__device__ __forceinline__ void cta_list_hull(const uint16_t* P, const int64_t* S, int n, uint32_t* vm) {
+    const int tid = threadIdx.x;
+    if (tid < 32) vm[tid] = 0u;
+    int R = 1;
+    while (R < 32 && 2 * R * n <= NT) R <<= 1;
+    const int t = tid / R, sub = tid % R;
+    __syncthreads();
+    // the running bests (entry, w, s) of this thread's share
+    int bl = 0, br = n - 1, wl = 1, wr = 1;
+    int64_t sl = 0, sr = 0;
+    const bool mine = t > 0 && t < n - 1;
+    int Pt = 0;
+    int64_t St = 0;
+    if (mine) {
+        Pt = P[t];
+        St = S[t];
+        wl = Pt - P[0]; sl = St - S[0];
+        wr = P[n - 1] - Pt; sr = St - S[n - 1];
+        const int span = (n - 2 + R - 1) / R;
+        const int j0 = 1 + sub * span, j1 = min(n - 1, j0 + span);
+        for (int j = j0; j < j1; ++j) {
+            const int w0 = P[j] - Pt;
+            const int64_t sv = St - S[j];
+            const bool left = j < t;
+            const int w = left ? -w0 : w0;
+            const int wb = left ? wl : wr;
+            const int64_t sb = left ? sl : sr;
+            // sv / w > sb / wb  <=>  wb sv - w sb > 0 (w, wb > 0)
+            const bool better = j != t && left_turn_w32(wb, sb, w, sv);
+            if (better && left) { bl = j; wl = w; sl = sv; }
+            if (better && !left) { br = j; wr = w; sr = sv; }
+        }
+    }
+    // the shares' bests combined (lanes of one entry are neighbours in a warp)
+    for (int d = 1; d < R; d <<= 1) {
+        const int obl = __shfl_xor_sync(kFull, bl, d), owl = __shfl_xor_sync(kFull, wl, d);
+        const int64_t osl = __shfl_xor_sync(kFull, sl, d);
+        const int obr = __shfl_xor_sync(kFull, br, d), owr = __shfl_xor_sync(kFull, wr, d);
+        const int64_t osr = __shfl_xor_sync(kFull, sr, d);
+        if (left_turn_w32(wl, sl, owl, osl)) { bl = obl; wl = owl; sl = osl; }
+        if (left_turn_w32(wr, sr, owr, osr)) { br = obr; wr = owr; sr = osr; }
+    }
+    if (sub == 0 && t < n - 1) {
+        const bool vertex = t == 0 ||
+                            (mine && left_turn_w32(Pt - P[bl], St - S[bl], P[br] - P[bl], S[br] - S[bl]));
+        if (vertex) {
+            const int K = (n - 1 + 31) >> 5;
+            atomicOr(&vm[t / K], 1u << (t % K));
+        }
+    }
+    __syncthreads();
 }
 
 // Lower hull of the entries of a list by one warp: entry i is the point with

@@ -447,6 +447,12 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
             }
             if (lane == 0) { LP[0] = 0; LSv[0] = 0; LP[n_list - 1] = (uint16_t)nt; LSv[n_list - 1] = LSa[L]; }
             __syncthreads();
+            if (n_list <= NT) {
+                // a short list: one pass, one thread per entry
+                cta_list_hull<NT>(LP, LSv, n_list, maska);
+                H.list = n_list;
+                return;
+            }
             __shared__ int s_ok;
             if (tid < 32) {
                 const bool ok = warp_list_hull(LP, LSv, n_list, maska);
