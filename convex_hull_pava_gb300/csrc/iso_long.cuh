@@ -674,9 +674,18 @@ __device__ __forceinline__ RowQ row_quanta(int64_t m, const LongWs& ws, int64_t 
     if (tid == 0) { red[0] = -100000; red[1] = -100000; red[2] = 0; }
     __syncthreads();
     int qs = -100000, qw = -100000, bad = 0;
-    for (int64_t j = tid; j < m; j += nth) {
-        const ChunkMeta mt = ws.meta[c0 + j];
-        qs = max(qs, mt.qs); qw = max(qw, mt.qw); bad |= mt.bad;
+    // four chunks in flight per thread (the loads are independent)
+    for (int64_t j0 = tid; j0 < m; j0 += 4 * (int64_t)nth) {
+        int4 q4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t j = j0 + (int64_t)u * nth;
+            q4[u] = j < m ? *reinterpret_cast<const int4*>(&ws.meta[c0 + j]) : make_int4(0, 0, -100000, -100000);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {   // (h, bad, qs, qw)
+            bad |= q4[u].y; qs = max(qs, q4[u].z); qw = max(qw, q4[u].w);
+        }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
@@ -902,19 +911,53 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
     int keepA = na, fromB = 1;            // A[0 .. keepA) then B[fromB .. nb)
     if (!F.turn(a0 + na - 2, b0, b0 + 1)) {
         const int qR = nb - 1;            // R = B[1 .. nb)
+        // the tangent point by bisection; on long right hulls first by
+        // galloping from R's first vertex (bridges lie near the shared point
+        // as a rule)
         auto tangent = [&](int x) -> int {
+            auto h = [&](int j) { return j >= qR - 1 || F.turn(a0 + x, b0 + 1 + j, b0 + 2 + j); };
             int jl = 0, jh = qR - 1;
+            if (qR > 32) {
+                if (h(0)) return 0;
+                int step = 1;
+                jl = 1;
+                while (!h(jl + step - 1)) { jl += step; step <<= 1; }
+                jh = min(jl + step - 1, qR - 1);
+            }
             while (jl < jh) {
                 const int mid = (jl + jh) >> 1;
-                if (F.turn(a0 + x, b0 + 1 + mid, b0 + 2 + mid)) jh = mid; else jl = mid + 1;
+                if (h(mid)) jh = mid; else jl = mid + 1;
             }
             return jl;
         };
         // the bridge's left end is in [lo, hi] of L = A[0 .. na-1); P(hi) is
-        // false.  Each round narrows the range 32-fold, so 8 rounds cover any
-        // list; the range never empties.
+        // false.  The first round tests the 32 vertices nearest the shared
+        // point; when the first of them already fails, the left end lies at or
+        // before it and 32-fold narrowing follows (8 rounds cover any list; the
+        // range never empties).
         int lo = 0, hi = na - 2;
-        for (int round = 0; round < 8; ++round) {
+        {
+            const int w0 = max(0, hi - 31);
+            const int x = w0 + lane;
+            bool nf = false;
+            int t = 0;
+            if (x <= hi) {
+                t = tangent(x);
+                nf = !F.turn(a0 + x, a0 + x + 1, b0 + 1 + t);
+            }
+            const unsigned bal = __ballot_sync(kFull, nf);
+            if (!(bal & 1u) || w0 == 0) {
+                // the window's first vertex passes (or the window is all of L):
+                // the left end is the window's first failing vertex
+                const int k = bal ? __ffs(bal) - 1 : hi - w0;
+                keepA = w0 + k + 1;
+                fromB = 1 + __shfl_sync(kFull, t, k);
+                lo = hi + 1;                    // done
+            } else {
+                hi = w0;
+            }
+        }
+        for (int round = 0; round < 8 && lo <= hi; ++round) {
             const int n = hi - lo + 1;
             const int step = (n + 31) >> 5;
             const int x = lo + lane * step;
@@ -1113,10 +1156,20 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     // the group's start in row coordinates: the converted totals of the chunks before it
     {
         i128 aS = 0, aW = 0;
-        for (int64_t j = tid; j < jb; j += nth) {
-            const ChunkMeta mt = ws.meta[c0 + j];
-            aS += conv(mt.totS, q.qs - mt.qs);
-            aW += WEIGHTED ? (i128)conv(mt.totW, q.qw - mt.qw) : (i128)mt.totW;
+        // four chunks in flight per thread (the loads are independent)
+        for (int64_t j0 = tid; j0 < jb; j0 += 4 * (int64_t)nth) {
+            ChunkMeta m4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t j = j0 + (int64_t)u * nth;
+                if (j < jb) m4[u] = ws.meta[c0 + j];
+                else { m4[u].qs = q.qs; m4[u].qw = q.qw; m4[u].totS = 0; m4[u].totW = 0; }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                aS += conv(m4[u].totS, q.qs - m4[u].qs);
+                aW += WEIGHTED ? (i128)conv(m4[u].totW, q.qw - m4[u].qw) : (i128)m4[u].totW;
+            }
         }
 #pragma unroll
         for (int d = 16; d > 0; d >>= 1) {
