@@ -120,9 +120,21 @@ __device__ __forceinline__ void fit_row_tiles(const IO* __restrict__ yr,
     }
 }
 
+// CTAs per SM that a kernel's shared memory allows (228 KB per SM, 1 KB of it
+// reserved per CTA, at most 2,048 threads): the float32 kernels' registers are
+// held to that occupancy, so they never limit it further; the float64 ones,
+// whose 32 staged values take twice the registers, get 128 per thread.
+template <int NT, int RMAX, bool WEIGHTED, class IO>
+constexpr int rows_min_blocks() {
+    constexpr int by_smem = (228 * 1024) / (TileSmem<NT, WEIGHTED, true, RMAX, IO>::kBytes + 1024);
+    constexpr int by_threads = sizeof(IO) == 4 ? 2048 / NT : 512 / NT;
+    constexpr int b = by_smem < by_threads ? by_smem : by_threads;
+    return b < 1 ? 1 : b;
+}
+
 // Fit of whole rows: CTA of NT threads, R = NT / L rows of L lanes each.
 template <int NT, int RMAX, bool WEIGHTED, class IO>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, rows_min_blocks<NT, RMAX, WEIGHTED, IO>())
 rows_fit_kernel(const IO* __restrict__ y, const IO* __restrict__ w, int64_t rows, int n,
                 int L, int increasing, IO* __restrict__ out, uint8_t* __restrict__ blocks,
                 uint32_t* __restrict__ row_status) {

@@ -405,6 +405,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
 
     const int64_t ls = LSa[tile * (L + 1) + lane];
     const int64_t lw = WEIGHTED ? LWa[tile * (L + 1) + lane] : 0;
+    const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
 
     Tile& T = H.T;
     T.Sx = Sx + tile * L * kRow;
@@ -463,14 +464,41 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
         }
     }
 
-    const uint32_t allp = e >= 32 ? 0xffffffffu : ((1u << e) - 1u);
 
 
+    bool rel = false;       // rows hold tile-relative sums
+    bool oneblock = false;  // every tile of the CTA is one block
+    H.quick = false;
+    // ---- whole rows of more than one warp: a tile none of whose points (the
+    // locally convex ones, and each lane's first) lies strictly below the
+    // chord from its first point to its end is one block, its hull that chord;
+    // the lane hulls and merging rounds are then skipped (a soft-rank row,
+    // whose merging rounds would each walk the whole merged hull).  Rows of
+    // one warp or less have the farthest-point levels for that. ----
+    if constexpr (EMIT && RMAX == 1) {
+        __syncthreads();                                     // lane starts written
+        bool below = false;
+        uint32_t m = work ? (cand | (lane > 0 ? 1u : 0u)) & allp : 0u;
+        if (m) {
+            const int64_t Sn = T.LS[L];
+            while (m && !below) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1u;
+                const int64_t Sp = ls + myS[k];
+                if constexpr (WEIGHTED) {
+                    QBest<true> d;
+                    below = qdist(lw + myW[k], Sp, T.LW[L], Sn, d);
+                } else {
+                    QBest<false> d;
+                    below = qdist((lane << 5) + k, Sp, nt, Sn, d);
+                }
+            }
+        }
+        oneblock = !__syncthreads_or(below);
+    }
     // ---- few vertices expected: the hull by levels of farthest-point splits,
     // on tile-relative rows ----
-    bool rel = false;       // rows hold tile-relative sums
-    H.quick = false;
-    if constexpr (EMIT && RMAX > 1) if (L >= kQuickMinLanes && L <= 32) {
+    if constexpr (EMIT && RMAX > 1) if (!oneblock && L >= kQuickMinLanes && L <= 32) {
         __syncthreads();   // lane starts written
         // the tile's trend: mean of lanes [0, L/2) against the rest
         bool down = false;
@@ -502,8 +530,9 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     // Each edge's slope is its element's mean, so a lane whose every interior
     // point is locally convex (strictly increasing means) is a strictly convex
     // chain: all its points are vertices and the monotone chain is not needed.
-    uint32_t mask = ((cand | 1u) & allp) == allp ? (e > 0 ? allp : 0u)
-                                                 : lane_hull<WEIGHTED>(myS, myW, cand, e);
+    uint32_t mask = oneblock ? ((work && lane == 0 && nt > 0) ? 1u : 0u)
+                             : ((cand | 1u) & allp) == allp ? (e > 0 ? allp : 0u)
+                                                            : lane_hull<WEIGHTED>(myS, myW, cand, e);
 
     if constexpr (EMIT) {
         // ---- rows become tile-relative; the lane hulls are merged in rounds
@@ -524,7 +553,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
             if ((tid & 31) == 0) summ[tid >> 5] = bal;
         }
         __syncthreads();
-        for (int r = 0; (1 << r) < L; ++r) {
+        for (int r = 0; !oneblock && (1 << r) < L; ++r) {
             const int grp = lane >> (r + 1);
             const int A0 = grp << (r + 1);
             const int B0 = A0 + (1 << r);
