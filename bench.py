@@ -444,10 +444,16 @@ def run_gpu(args):
 
     # ---- end to end through the public API with pinned host buffers: the
     # input y is in pinned host memory and the fit goes to pinned host memory.
-    # Two ways through the same call: (1) the host buffers passed straight to
+    # Three ways through the same call: (1) the host buffers passed straight to
     # iso_fit, whose kernels read y and write the fit over the host link
-    # (NVLink-C2C), and (2) explicit copies to and from device buffers around
-    # the call.  e2e reports the faster; both are in the line. ----
+    # (NVLink-C2C); (2) explicit copies to and from device buffers around each
+    # call, one call at a time; (3) the same copies for a stream of independent
+    # problems, the next problem's input copied in while this one is fitted and
+    # copied out (two device slots, copies on their own streams).  One call
+    # cannot start writing its fit before all of y has arrived (every output
+    # depends on every input), so (1) and (2) pay the link's read and write
+    # times in turn; (3) overlaps the two directions.  e2e reports the fastest;
+    # all are in the line, with the link's own copy rates. ----
     yh = torch.from_numpy(W.y).pin_memory()
     wh = None if W.w is None else torch.from_numpy(W.w).pin_memory()
     oh = torch.empty(W.y.shape, dtype=torch.float32).pin_memory()
@@ -475,7 +481,92 @@ def run_gpu(args):
         z, _, _ = chp.iso_fit(yd, wd, W.increasing, want_blocks=False, workspace=ws, stream=stream)
         oh.copy_(z, non_blocking=True)
 
-    e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies)}
+    # (3): host buffers rotate over four sets (more bytes than L2 holds), so
+    # no problem's input can still be cached from an earlier one
+    nrot = 4
+    yhs = [yh] + [torch.from_numpy(W.y).pin_memory() for _ in range(nrot - 1)]
+    whs = None if wh is None else [wh] + [torch.from_numpy(W.w).pin_memory() for _ in range(nrot - 1)]
+    ohs = [oh] + [torch.empty(W.y.shape, dtype=torch.float32).pin_memory() for _ in range(nrot - 1)]
+    yds = [torch.empty(W.y.shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    wds = None if wh is None else [torch.empty(W.w.shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    ods = [torch.empty(W.y.shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_fit = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def pipelined(nsteps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        s_in.wait_event(a)
+        s_out.wait_event(a)
+        for i in range(nsteps):
+            k, h = i % 2, i % nrot
+            if i >= 2:
+                s_in.wait_event(ev_fit[k])        # slot k's input read by its last fit
+            with torch.cuda.stream(s_in):
+                yds[k].copy_(yhs[h], non_blocking=True)
+                if wds is not None:
+                    wds[k].copy_(whs[h], non_blocking=True)
+                ev_in[k].record(s_in)
+            stream.wait_event(ev_in[k])
+            if i >= 2:
+                stream.wait_event(ev_out[k])      # slot k's fit copied out
+            chp.iso_fit(yds[k], None if wds is None else wds[k], W.increasing, out=ods[k],
+                        want_blocks=False, workspace=ws, stream=stream)
+            ev_fit[k].record(stream)
+            s_out.wait_event(ev_fit[k])
+            with torch.cuda.stream(s_out):
+                ohs[h].copy_(ods[k], non_blocking=True)
+                ev_out[k].record(s_out)
+        stream.wait_event(ev_out[0])
+        if nsteps > 1:
+            stream.wait_event(ev_out[1])
+        b.record(stream)
+        b.synchronize()
+        return a.elapsed_time(b) / nsteps
+
+    npipe = max(10, args.steps // 4)
+    pipelined(npipe)
+    e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies),
+                 "pipelined_copies": pipelined(npipe)}
+
+    # the host link's own rates on the same bytes: one direction at a time and
+    # both at once (copy engines, pinned memory)
+    def link_rates():
+        def t(fn, reps=10):
+            fn()
+            torch.cuda.synchronize(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            b.synchronize()
+            return a.elapsed_time(b) / reps
+
+        def both():
+            s_in.wait_stream(stream)
+            s_out.wait_stream(stream)
+            with torch.cuda.stream(s_in):
+                yds[0].copy_(yhs[1], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                ohs[1].copy_(ods[0], non_blocking=True)
+            stream.wait_stream(s_in)
+            stream.wait_stream(s_out)
+
+        nb = W.elements * 4
+        h2d = t(lambda: yds[0].copy_(yhs[1], non_blocking=True))
+        d2h = t(lambda: ohs[1].copy_(ods[0], non_blocking=True))
+        bi = t(both)
+        return {"bytes": nb, "h2d_gbs": nb / h2d / 1e6, "d2h_gbs": nb / d2h / 1e6,
+                "both_directions_gbs": 2 * nb / bi / 1e6,
+                "one_call_floor_ms": h2d + d2h, "overlapped_floor_ms": bi}
+
+    link = link_rates()
     e2e_mode = min(e2e_modes, key=e2e_modes.get)
     e2e_val = job_value(W.elements, world, cross_rank_max(e2e_modes[e2e_mode], dev))
     e2e_all = {k: job_value(W.elements, world, cross_rank_max(v, dev)) for k, v in e2e_modes.items()}
@@ -632,7 +723,11 @@ def run_gpu(args):
             "roofline": roof, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": UNIT,
                     "h2d_bytes_per_step": W.elements * (8 if W.weighted else 4),
-                    "d2h_bytes_per_step": W.elements * 4, "mode": e2e_mode, "modes": e2e_all},
+                    "d2h_bytes_per_step": W.elements * 4, "mode": e2e_mode, "modes": e2e_all,
+                    "pipelined_problems": npipe,
+                    "l2": "single calls flush L2 before each; the pipelined problems rotate over "
+                          f"{nrot} host input buffers ({nrot * W.elements * 4 >> 20} MiB)",
+                    "host_link": link},
             "gpu_launches": launches, "clocks": clocks, "also": also,
         }
         print(json.dumps(line))
