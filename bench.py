@@ -530,8 +530,9 @@ def run_gpu(args):
 
     npipe = max(10, args.steps // 4)
     pipelined(npipe)
-    e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies),
-                 "pipelined_copies": pipelined(npipe)}
+    e2e_modes = {"host_buffers_in_place": e2e_time(in_place), "explicit_copies": e2e_time(with_copies)}
+    pipe_runs = [pipelined(npipe) for _ in range(3)]     # three runs of npipe problems: the median
+    e2e_modes["pipelined_copies"] = float(np.median(pipe_runs))
 
     # the host link's own rates on the same bytes: one direction at a time and
     # both at once (copy engines, pinned memory)
@@ -567,6 +568,17 @@ def run_gpu(args):
                 "one_call_floor_ms": h2d + d2h, "overlapped_floor_ms": bi}
 
     link = link_rates()
+
+    # bridge-search depth of one call (untimed; the library's debugging counters)
+    def bridge_counts(call):
+        chp.bridge_stats_mode(1)
+        try:
+            call()
+            return chp.bridge_stats_read()
+        finally:
+            chp.bridge_stats_mode(0)
+
+    bridge = bridge_counts(step) if W.n > 8192 else None
     e2e_mode = min(e2e_modes, key=e2e_modes.get)
     e2e_val = job_value(W.elements, world, cross_rank_max(e2e_modes[e2e_mode], dev))
     e2e_all = {k: job_value(W.elements, world, cross_rank_max(v, dev)) for k, v in e2e_modes.items()}
@@ -620,6 +632,8 @@ def run_gpu(args):
                                    "gbs": bb / tb / 1e9, "frac": bb / tb / 1e9 / hbm_peak}
             if pool is not None and V.rows > 1:
                 rec["cpu_all_cores"] = time_oracle_all_cores(V, pool, os.cpu_count() or 1)
+            if V.n > 8192:
+                rec["bridge_search"] = bridge_counts(fv)
             also[name] = rec
             del yv, wv, ov, bv, wsv
         # the soft rank end to end (sort, non-increasing fit, gather; backward
@@ -720,11 +734,12 @@ def run_gpu(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
             "data": "synthetic", "config": workload_desc(W),
             "hbm_gbs_whole_call": whole, "hbm_frac_whole_call": whole / hbm_peak,
-            "roofline": roof, "cpu_baseline": cpu,
+            "roofline": roof, "cpu_baseline": cpu, "bridge_search": bridge,
             "e2e": {"value": e2e_val, "unit": UNIT,
                     "h2d_bytes_per_step": W.elements * (8 if W.weighted else 4),
                     "d2h_bytes_per_step": W.elements * 4, "mode": e2e_mode, "modes": e2e_all,
                     "pipelined_problems": npipe,
+                    "pipelined_ms_per_problem_runs": pipe_runs,
                     "l2": "single calls flush L2 before each; the pipelined problems rotate over "
                           f"{nrot} host input buffers ({nrot * W.elements * 4 >> 20} MiB)",
                     "host_link": link},

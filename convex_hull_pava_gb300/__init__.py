@@ -42,7 +42,8 @@ EXPORTS = ("iso_version", "iso_status_string", "iso_fit_workspace_bytes", "iso_f
            "iso_backward_noalloc", "iso_fit_ragged_workspace_bytes", "iso_fit_ragged",
            "iso_fit_copy_control_workspace_bytes", "iso_fit_copy_control",
            "iso_fit_f64", "iso_backward_f64", "iso_backward_w_f64", "iso_fit_ragged_f64",
-           "iso_profile_enable", "iso_profile_read")
+           "iso_profile_enable", "iso_profile_read", "iso_bridge_stats_mode",
+           "iso_bridge_stats_read")
 
 _lib = None
 _lock = threading.Lock()
@@ -99,6 +100,10 @@ def load_library(path: str | None = None):
         lib.iso_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_char_p), ci]
         lib.iso_profile_read.restype = ci
+        lib.iso_bridge_stats_mode.argtypes = [ci]
+        lib.iso_bridge_stats_mode.restype = ci
+        lib.iso_bridge_stats_read.argtypes = [ctypes.POINTER(ctypes.c_uint64)]
+        lib.iso_bridge_stats_read.restype = ci
         _lib = lib
         return lib
 
@@ -135,6 +140,30 @@ def profile_read(max_kernels: int = 16):
     if k < 0:
         raise IsoError(k, "iso_profile_read")
     return [(names[i].decode(), float(ms[i])) for i in range(k)]
+
+
+BRIDGE_MAX_PASSES = 6   # ISO_BRIDGE_MAX_PASSES
+BRIDGE_MAX_ROUNDS = 8   # ISO_BRIDGE_MAX_ROUNDS
+BRIDGE_STATS = ("list_merges", "list_searches", "passes", "max_passes", "nested",
+                "flat_searches", "max_rounds", "flat_unfinished")
+
+
+def bridge_stats_mode(mode: int) -> None:
+    """Count the long-row merges' bridge searches on the current device
+    (0: off, 1: count, 2: count with every segment-list search taking the
+    nested bisection from its first pass).  A debugging aid."""
+    st = load_library().iso_bridge_stats_mode(int(mode))
+    if st != ISO_OK:
+        raise IsoError(st, "iso_bridge_stats_mode")
+
+
+def bridge_stats_read() -> dict:
+    """The current device's bridge-search counters (synchronises the device)."""
+    v = (ctypes.c_uint64 * 8)()
+    st = load_library().iso_bridge_stats_read(v)
+    if st != ISO_OK:
+        raise IsoError(st, "iso_bridge_stats_read")
+    return {k: int(v[i]) for i, k in enumerate(BRIDGE_STATS)}
 
 
 def _torch():

@@ -29,6 +29,53 @@ void prof_mark(cudaStream_t stream, const char* name) {
         g_prof.name[g_prof.count++] = name;
 }
 
+namespace {
+constexpr int kStatDevices = 64;
+constexpr int kStatCount = 8;
+int g_bridge_mode = 0;
+unsigned long long* g_bridge_stats[kStatDevices];
+}  // namespace
+
+BridgeDebug bridge_debug() {
+    BridgeDebug d{nullptr, ISO_BRIDGE_MAX_PASSES};
+    if (g_bridge_mode == 0) return d;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStatDevices) return d;
+    d.stats = g_bridge_stats[dev];
+    if (d.stats && g_bridge_mode == 2) d.max_passes = 0;
+    return d;
+}
+
+iso_status bridge_stats_mode(int mode) {
+    if (mode < 0 || mode > 2) return ISO_ERR_INVALID_ARG;
+    if (mode == 0) { g_bridge_mode = 0; return ISO_OK; }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
+    if (dev < 0 || dev >= kStatDevices) return ISO_ERR_INVALID_ARG;
+    if (!g_bridge_stats[dev] &&
+        cudaMalloc(&g_bridge_stats[dev], kStatCount * sizeof(unsigned long long)) != cudaSuccess) {
+        g_bridge_stats[dev] = nullptr;
+        return ISO_ERR_CUDA;
+    }
+    if (cudaMemset(g_bridge_stats[dev], 0, kStatCount * sizeof(unsigned long long)) != cudaSuccess)
+        return ISO_ERR_CUDA;
+    g_bridge_mode = mode;
+    return ISO_OK;
+}
+
+iso_status bridge_stats_read(uint64_t* out) {
+    if (!out) return ISO_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ISO_ERR_CUDA;
+    if (dev < 0 || dev >= kStatDevices || !g_bridge_stats[dev]) return ISO_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ISO_ERR_CUDA;
+    unsigned long long v[kStatCount];
+    if (cudaMemcpy(v, g_bridge_stats[dev], sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ISO_ERR_CUDA;
+    for (int i = 0; i < kStatCount; ++i) out[i] = (uint64_t)v[i];
+    return ISO_OK;
+}
+
 }  // namespace isodev
 
 namespace {
@@ -275,5 +322,9 @@ int iso_profile_read(float* ms, const char** names, int max_kernels) {
     }
     return k;
 }
+
+iso_status iso_bridge_stats_mode(int mode) { return isodev::bridge_stats_mode(mode); }
+
+iso_status iso_bridge_stats_read(uint64_t* out) { return isodev::bridge_stats_read(out); }
 
 }  // extern "C"

@@ -5,12 +5,24 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/iso.h"
+
 namespace isodev {
 
 // Optional per-kernel timing (see iso_profile_enable): marks the start of an
 // API call, and the end of each kernel it launches.
 void prof_start(cudaStream_t stream);
 void prof_mark(cudaStream_t stream, const char* name);
+
+// The bridge-search counters of the current device (nullptr unless counting is
+// on) and the passes a segment-list search takes before its nested bisection.
+struct BridgeDebug {
+    unsigned long long* stats;
+    int max_passes;
+};
+BridgeDebug bridge_debug();
+iso_status bridge_stats_mode(int mode);
+iso_status bridge_stats_read(uint64_t* out);
 
 // Longest row handled by the whole-row kernels (one CTA of 256 lanes x 32).
 constexpr int kRowMax = 8192;

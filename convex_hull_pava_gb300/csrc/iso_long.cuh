@@ -92,6 +92,8 @@ struct LongWs {
     void* gfW;         // i128 (weighted) or int64 (unit weights: point index) per vertex
     uint32_t* gfTag;   // chunk << 13 | rank
     int32_t* gfN;      // [G] its vertices, -1 when it is only a segment list
+    unsigned long long* bst;   // bridge-search counters (nullptr: not counted)
+    int bmax;                  // passes of a segment-list search before its nested bisection
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -129,6 +131,16 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t M, Lon
     w.gfW = take((WEIGHTED ? sizeof(i128) : sizeof(int64_t)) * kGroupFlatCap * G);
     w.gfTag = (uint32_t*)take(sizeof(uint32_t) * kGroupFlatCap * G);
     w.gfN = (int32_t*)take(sizeof(int32_t) * G);
+#ifdef __CUDA_ARCH__
+    w.bst = nullptr;
+    w.bmax = ISO_BRIDGE_MAX_PASSES;
+#else
+    if (ws) {
+        const BridgeDebug bd = bridge_debug();
+        w.bst = bd.stats;
+        w.bmax = bd.max_passes;
+    }
+#endif
     if (ws) *ws = w;
     return off;
 }
@@ -319,6 +331,8 @@ struct MView {
     const uint16_t* P;
     int64_t c0;              // global index of the row's chunk 0
     int C;
+    unsigned long long* bst = nullptr;   // bridge-search counters
+    int bmax = ISO_BRIDGE_MAX_PASSES;
 
     __device__ __forceinline__ Seg load(int k) const {
         const int4 s = seg[k];
@@ -383,6 +397,91 @@ struct Walker {
     i128 W, S;
 };
 
+// h(x): x strictly below the segment from (AW, AS) to its successor (false
+// before the tangent point of A on the right list, true from it on).  B moves
+// to the first x in [B, the list's last vertex kRl] with h: bisection over
+// segments, then inside one.
+template <bool WEIGHTED, class View>
+__device__ __forceinline__ void list_tangent_right(const View& V, int kRl, i128 AW, i128 AS, Walker& B) {
+    int lo = B.k, hi = kRl;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const Seg gm = V.load(mid), gn = V.load(mid + 1);
+        i128 Wm, Sm, Wn, Sn;
+        V.at(gm, gm.hi, Wm, Sm);
+        V.at(gn, gn.lo, Wn, Sn);
+        if (row_turn<WEIGHTED>(AW, AS, Wm, Sm, Wn, Sn)) hi = mid; else lo = mid + 1;
+    }
+    const Seg g = lo == B.k ? B.g : V.load(lo);
+    int rlo = lo == B.k ? B.r : g.lo, rhi = g.hi;
+    while (rlo < rhi) {
+        const int mid = (rlo + rhi) >> 1;
+        i128 Wm, Sm, Wn, Sn;
+        V.at(g, mid, Wm, Sm);
+        V.at(g, mid + 1, Wn, Sn);
+        if (row_turn<WEIGHTED>(AW, AS, Wm, Sm, Wn, Sn)) rhi = mid; else rlo = mid + 1;
+    }
+    B.k = lo; B.g = g; B.r = rlo;
+    V.at(g, rlo, B.W, B.S);
+}
+
+// The end of a bridge search whose passes ran out, by nested bisection
+// (Theorem 5.2).  a is at or after the bridge's left end on the left list
+// (first segment j0) and b is the tangent point of a on the right list (last
+// segment kRl).  For x on the left list up to a, t(x) is its tangent point on
+// the right list (at or after b); the vertex after x lies strictly below the
+// line from x to t(x) for every x before the bridge's left end and for none
+// from it on.  The left end is the first x for which it does not: bisection
+// over the segments' first vertices, then inside one segment.  The right end
+// is t of the left end.
+template <bool WEIGHTED, class View>
+__device__ __forceinline__ void nested_bridge(const View& V, int j0, int kRl, Walker& a, Walker& b) {
+    // x = rank r of segment k (g); its successor is the next rank, else the
+    // next segment's first
+    auto below = [&](int k, const Seg& g, int r) -> bool {
+        i128 Wx, Sx, Wn, Sn;
+        V.at(g, r, Wx, Sx);
+        if (r < g.hi) {
+            V.at(g, r + 1, Wn, Sn);
+        } else {
+            const Seg h = V.load(k + 1);
+            V.at(h, h.lo, Wn, Sn);
+        }
+        Walker T = b;
+        list_tangent_right<WEIGHTED>(V, kRl, Wx, Sx, T);
+        return row_turn<WEIGHTED>(Wx, Sx, Wn, Sn, T.W, T.S);
+    };
+    // the last segment in [j0, a.k] whose first vertex passes (j0 - 1: none)
+    const int ak = a.k, ar = a.r;
+    int lo = j0 - 1, hi = ak;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const Seg g = V.load(mid);
+        if (below(mid, g, g.lo)) lo = mid; else hi = mid - 1;
+    }
+    int k, r;
+    if (lo < j0) {
+        k = j0;
+        r = V.load(j0).lo;
+    } else {
+        const Seg g = V.load(lo);
+        const int rmax = lo == ak ? ar : g.hi;
+        int rl = g.lo + 1, rh = rmax + 1;     // first failing rank; rmax + 1: none here
+        while (rl < rh) {
+            const int mid = (rl + rh) >> 1;
+            if (below(lo, g, mid)) rl = mid + 1; else rh = mid;
+        }
+        if (rl <= rmax) { k = lo; r = rl; }
+        else if (lo < ak) { k = lo + 1; r = V.load(lo + 1).lo; }
+        else { k = ak; r = ar; }   // every x up to a passes: ruled out by exact turns
+    }
+    a.k = k;
+    a.g = V.load(k);
+    a.r = r;
+    V.at(a.g, r, a.W, a.S);
+    list_tangent_right<WEIGHTED>(V, kRl, a.W, a.S, b);
+}
+
 constexpr int kLinearSteps = 12;   // walk steps before a tangent is found by bisection
 
 // Merge of the lists of the neighbouring nodes starting at j0 and j1
@@ -427,6 +526,7 @@ __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
         else seg[kR0].y = lo;
         const int len = kRl - first + 1;
         V.cnt[j0] = nL + len;
+        if (V.bst) atomicAdd(&V.bst[0], 1ull);
         return Move{j0 + nL, first, len};
     }
     // s is not a vertex of the merged hull: the bridge joins L without s to R
@@ -459,30 +559,17 @@ __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
     };
     // h(x): x strictly below the segment from a to its successor (false before
     // the tangent point of a on R', true from it on).  First x in [b, last] with h.
-    auto tanR = [&](const Walker& A, Walker& B) {
-        int lo = B.k, hi = kRl;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const Seg gm = V.load(mid), gn = V.load(mid + 1);
-            i128 Wm, Sm, Wn, Sn;
-            V.at(gm, gm.hi, Wm, Sm);
-            V.at(gn, gn.lo, Wn, Sn);
-            if (turn(A.W, A.S, Wm, Sm, Wn, Sn)) hi = mid; else lo = mid + 1;
-        }
-        const Seg g = lo == B.k ? B.g : V.load(lo);
-        int rlo = lo == B.k ? B.r : g.lo, rhi = g.hi;
-        while (rlo < rhi) {
-            const int mid = (rlo + rhi) >> 1;
-            i128 Wm, Sm, Wn, Sn;
-            V.at(g, mid, Wm, Sm);
-            V.at(g, mid + 1, Wn, Sn);
-            if (turn(A.W, A.S, Wm, Sm, Wn, Sn)) rhi = mid; else rlo = mid + 1;
-        }
-        B.k = lo; B.g = g; B.r = rlo;
-        V.at(g, rlo, B.W, B.S);
-    };
+    auto tanR = [&](const Walker& A, Walker& B) { list_tangent_right<WEIGHTED>(V, kRl, A.W, A.S, B); };
 
+    // Passes of V.bmax at most: a moves only left and b only right, and
+    // neither passes the bridge's ends (a tangent point moves right as its
+    // source moves left), so each pass leaves a at or after the left end and
+    // b at or before the right end; what remains goes to the nested bisection.
+    int passes = 0;
+    bool nested = false;
     for (;;) {
+        if (passes >= V.bmax) { nested = true; break; }
+        ++passes;
         bool moved = false;
         // the left end moves to its tangent point from b
         for (int steps = 0;;) {
@@ -556,6 +643,14 @@ __device__ __forceinline__ Move merge_plan(const View& V, int j0, int j1) {
             moved = true;
         }
         if (!moved) break;
+    }
+    if (nested) nested_bridge<WEIGHTED>(V, j0, kRl, a, b);
+    if (V.bst) {
+        atomicAdd(&V.bst[0], 1ull);
+        atomicAdd(&V.bst[1], 1ull);
+        atomicAdd(&V.bst[2], (unsigned long long)passes);
+        atomicMax(&V.bst[3], (unsigned long long)passes);
+        if (nested) atomicAdd(&V.bst[4], 1ull);
     }
     // cut L at a and R at b; R's tail moves down behind L's kept part
     seg[a.k].z = a.r;
@@ -808,6 +903,8 @@ __device__ __forceinline__ void merge_group(int64_t m, const LongWs& ws, int64_t
     MView<WEIGHTED, SMEM> V;
     V.c0 = c0;
     V.C = C;
+    V.bst = ws.bst;
+    V.bmax = ws.bmax;
     if constexpr (SMEM) {
         // arrays of the group's chunks, indexed by the chunk's index in the row
         V.seg = reinterpret_cast<int4*>(sm + L.oSeg) - jb;
@@ -889,6 +986,7 @@ struct FlatSm {
     i128* Wi;         // weighted rows: W
     int64_t* Wu;      // unit weights: the point's index in the row
     uint32_t* tag;    // chunk << 13 | rank
+    unsigned long long* bst = nullptr;   // bridge-search counters
     __device__ __forceinline__ void get(int i, i128& W, i128& Sv) const {
         Sv = S[i];
         if constexpr (WEIGHTED) W = Wi[i]; else W = (i128)Wu[i];
@@ -957,7 +1055,8 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
                 hi = w0;
             }
         }
-        for (int round = 0; round < 8 && lo <= hi; ++round) {
+        int round = 0;
+        for (; round < ISO_BRIDGE_MAX_ROUNDS && lo <= hi; ++round) {
             const int n = hi - lo + 1;
             const int step = (n + 31) >> 5;
             const int x = lo + lane * step;
@@ -974,6 +1073,8 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
                 const int k = bal ? __ffs(bal) - 1 : hi - lo;
                 keepA = lo + k + 1;
                 fromB = 1 + __shfl_sync(kFull, t, k);
+                lo = hi + 1;                    // done
+                ++round;
                 break;
             }
             if (bal == 0u) {
@@ -984,6 +1085,11 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
                 hi = lo + k * step;
                 lo = k == 0 ? hi : lo + (k - 1) * step + 1;
             }
+        }
+        if (F.bst && lane == 0) {
+            atomicAdd(&F.bst[5], 1ull);
+            atomicMax(&F.bst[6], (unsigned long long)round);
+            if (lo <= hi) atomicAdd(&F.bst[7], 1ull);
         }
     }
     // the right node's kept tail moves down behind the left node's kept head
@@ -1044,6 +1150,7 @@ __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, i
     F.Wi = reinterpret_cast<i128*>(sm + Lo.oW);
     F.Wu = reinterpret_cast<int64_t*>(sm + Lo.oW);
     F.tag = reinterpret_cast<uint32_t*>(sm + Lo.oTag);
+    F.bst = ws.bst;
     int32_t* nstart = reinterpret_cast<int32_t*>(sm + Lo.oStart);
     int32_t* nsize = reinterpret_cast<int32_t*>(sm + Lo.oSize);
     for (int j = tid; j < mg; j += nth) {
@@ -1302,6 +1409,8 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
     MView<WEIGHTED, SMEM> V;
     V.c0 = c0;
     V.C = C;
+    V.bst = ws.bst;
+    V.bmax = ws.bmax;
     int32_t *segOf, *nextSeg, *prevSeg;
     if constexpr (SMEM) {
         V.seg = reinterpret_cast<int4*>(sm + L.oSeg);
@@ -1367,6 +1476,7 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
     F.Wi = reinterpret_cast<i128*>(sm + Lo.oW);
     F.Wu = reinterpret_cast<int64_t*>(sm + Lo.oW);
     F.tag = reinterpret_cast<uint32_t*>(sm + Lo.oTag);
+    F.bst = ws.bst;
     int32_t* nstart = reinterpret_cast<int32_t*>(sm + Lo.oStart);
     int32_t* nsize = reinterpret_cast<int32_t*>(sm + Lo.oSize);
     for (int k = warp; k < ng; k += nw) {
@@ -1853,6 +1963,8 @@ struct FlatView {
     const int32_t* dS;
     const int32_t* dW;
     int C;
+    unsigned long long* bst = nullptr;   // bridge-search counters
+    int bmax = ISO_BRIDGE_MAX_PASSES;
 
     __device__ __forceinline__ Seg load(int k) const {
         const int4 s = seg[k];
@@ -1942,6 +2054,8 @@ ctl_bridge_kernel(int64_t m, int64_t half, int64_t nmerge, LongWs ws, CtlWs cw, 
     V.dS = ws.dS + c0;
     V.dW = ws.dW + c0;
     V.C = C;
+    V.bst = ws.bst;
+    V.bmax = ws.bmax;
     const int64_t j0 = 2 * k * half;
     merge_plan<WEIGHTED>(V, (int)j0, (int)(j0 + half));
 }
@@ -2061,6 +2175,8 @@ ctl_root_kernel(int64_t m, LongWs ws, CtlWs cw) {
     MView<WEIGHTED, false> V;
     V.c0 = c0;
     V.C = C;
+    V.bst = ws.bst;
+    V.bmax = ws.bmax;
     V.seg = ws.seg + c0;
     V.cnt = ws.cnt + c0;
     V.offS = ws.offS + c0;

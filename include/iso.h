@@ -306,6 +306,50 @@ iso_status iso_backward_noalloc(const float *grad, const uint8_t *blocks, const 
 int iso_profile_enable(int on);
 int iso_profile_read(float *ms, const char **names, int max_kernels);
 
+/*
+ * Depth of the long-row path's bridge searches (the paper's Section 5.2,
+ * Theorem 5.2: the merge depth is bounded by a capped walk followed by a
+ * nested bisection over the left hull's vertices, each tested against its
+ * tangent point on the right hull).
+ *
+ * A merge of two segment lists (hull vertices in global memory) moves the
+ * bridge's ends alternately to each other's tangent points; after
+ * ISO_BRIDGE_MAX_PASSES passes (a pass moves both ends) it finishes with the
+ * nested bisection, so no merge takes more than that many passes.  A merge of
+ * two flat hulls in shared memory uses the nested bisection from the start,
+ * 32 candidates per round, at most ISO_BRIDGE_MAX_ROUNDS rounds after the
+ * first window of 32 vertices next to the shared point.
+ *
+ * iso_bridge_stats_mode (a debugging aid, off by default) makes later long-row
+ * fits on the current device count their bridge searches:
+ *   mode 0: off;
+ *   mode 1: count;
+ *   mode 2: count, with every segment-list bridge search taking the nested
+ *           bisection from its first pass (to test that path on any input).
+ * Switching on allocates the device's eight counters once (cudaMalloc) and
+ * zeroes them.  Returns ISO_OK, ISO_ERR_INVALID_ARG for another mode, or
+ * ISO_ERR_CUDA.  Calls on several host threads must not change the mode
+ * concurrently.
+ *
+ * iso_bridge_stats_read synchronises the current device and copies its
+ * counters into out[0..7] (host memory):
+ *   [0] segment-list merges
+ *   [1] of those, bridge searches (the chain is not convex at the shared point)
+ *   [2] passes, summed over those searches
+ *   [3] the most passes of one search (at most ISO_BRIDGE_MAX_PASSES)
+ *   [4] searches that ended in the nested bisection
+ *   [5] flat merges with a bridge search
+ *   [6] the most narrowing rounds of one flat search (at most ISO_BRIDGE_MAX_ROUNDS)
+ *   [7] flat searches whose rounds ran out before the bridge was found (0 with
+ *       exactly convex hulls; nonzero would mean a wrong merge)
+ * It returns ISO_OK, ISO_ERR_INVALID_ARG for a NULL out or counting that was
+ * never switched on for the device, or ISO_ERR_CUDA.
+ */
+#define ISO_BRIDGE_MAX_PASSES 6
+#define ISO_BRIDGE_MAX_ROUNDS 8
+iso_status iso_bridge_stats_mode(int mode);
+iso_status iso_bridge_stats_read(uint64_t *out);
+
 #ifdef __cplusplus
 }
 #endif

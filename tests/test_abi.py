@@ -137,3 +137,19 @@ def test_empty_calls_do_nothing():
     assert lib.iso_fit(None, None, 0, -1, 1, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit(None, None, 0, 10, 2, None, None, None, 0, None, None) == chp.ISO_ERR_INVALID_ARG
     assert lib.iso_fit_ragged(None, None, None, 0, 0, 0, 1, None, None, None, 0, None, None) == chp.ISO_OK
+
+
+def test_bridge_bounds_match_header():
+    src = open(os.path.join(ROOT, "include", "iso.h")).read()
+    passes = int(re.search(r"#define ISO_BRIDGE_MAX_PASSES (\d+)", src).group(1))
+    rounds = int(re.search(r"#define ISO_BRIDGE_MAX_ROUNDS (\d+)", src).group(1))
+    assert (passes, rounds) == (chp.BRIDGE_MAX_PASSES, chp.BRIDGE_MAX_ROUNDS)
+    assert len(chp.BRIDGE_STATS) == 8
+
+
+def test_bridge_stats_mode_checks_host_only():
+    # an unknown mode is refused before any CUDA call; mode 0 makes none
+    with pytest.raises(chp.IsoError) as e:
+        chp.bridge_stats_mode(3)
+    assert e.value.status == chp.ISO_ERR_INVALID_ARG
+    chp.bridge_stats_mode(0)

@@ -85,7 +85,8 @@ def test_long_rows_families(cuda_ok, fam, weighting):
 @pytest.mark.parametrize("n", [20_000, 300_000])
 def test_long_rows_cliff_search(cuda_ok, n):
     """A cliff at the end pulls the top bridge across the whole row: the walks
-    give up and the nested bisection finds the bridge (paper Section 5.2)."""
+    give up and bisection over the lists finds the tangents (paper Section
+    5.2; test_gpu_bridge counts the searches)."""
     y = wl.family("cliff", 1, n, seed=1)
     parity(y, None, True, f"cliff n={n}")
     w = wl.weights("extreme", 1, n, seed=1)
