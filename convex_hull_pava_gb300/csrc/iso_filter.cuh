@@ -193,41 +193,32 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
     return keep & ~drop;
 }
 
-// Hull of a short list (n <= the CTA's threads) in one pass: entry t is a
-// strict vertex of the lower hull iff the steepest slope into it from an
-// earlier entry is below the shallowest slope out of it to a later one.  With
-// w = |P_j - P_t| and s = S_t - S_j for every other entry j, the steepest slope
-// in is the largest s / w over j < t and the shallowest slope out the smallest
-// -s / w over j > t, i.e. again the largest s / w: one running best per side,
-// compared exactly by cross products (w below 2^13, |s| below 2^63).  R
-// threads (R = the CTA's threads / n, a power of two up to 32, neighbours in
-// one warp) share an entry, each scanning a share of the other entries, and
-// their bests are combined by shuffles.  The test is then the exact turn from
-// the best entry before t, over t, to the best entry after it.  Entries 0 and
-// n - 1 are vertices.  The vertices' bits go to vm in warp_list_hull's layout
-// (lane l, bit k for entry l K + k, K = ceil((n - 1) / 32); the last entry
-// implied).  Every thread of the CTA calls it.
-template <int NT>
-__device__ __forceinline__ void cta_list_hull(const uint16_t* P, const int64_t* S, int n, uint32_t* vm) {
-    const int tid = threadIdx.x;
-    if (tid < 32) vm[tid] = 0u;
-    int R = 1;
-    while (R < 32 && 2 * R * n <= NT) R <<= 1;
-    const int t = tid / R, sub = tid % R;
-    __syncthreads();
+// Whether entry t of a sorted list (entries lo..hi, lo <= t <= hi) is a strict
+// corner of their lower hull: lo and hi are; an entry between them is when
+// the largest slope into it from the left (over entries lo..t-1) is below the
+// smallest slope out of it to the right (over t+1..hi), i.e. it lies strictly
+// below the segment between the two entries that attain them.  With w = |P_j -
+// P_t| and s = S_t - S_j for another entry j, the slope in is the largest s / w
+// over j < t and the slope out the smallest -s / w over j > t, i.e. again the
+// largest s / w: one running best per side, compared exactly by cross
+// products (w below 2^13, |s| below 2^63).  R threads per entry, neighbours in
+// a warp, each taking a share (sub) of the others, their bests combined by
+// shuffles; every thread of the warp calls it; the result is valid on sub 0.
+__device__ __forceinline__ bool list_corner(const uint16_t* P, const int64_t* S, int t, bool act, int lo,
+                                            int hi, int R, int sub) {
     // the running bests (entry, w, s) of this thread's share
-    int bl = 0, br = n - 1, wl = 1, wr = 1;
+    int bl = lo, br = hi, wl = 1, wr = 1;
     int64_t sl = 0, sr = 0;
-    const bool mine = t > 0 && t < n - 1;
+    const bool mine = act && t > lo && t < hi;
     int Pt = 0;
     int64_t St = 0;
     if (mine) {
         Pt = P[t];
         St = S[t];
-        wl = Pt - P[0]; sl = St - S[0];
-        wr = P[n - 1] - Pt; sr = St - S[n - 1];
-        const int span = (n - 2 + R - 1) / R;
-        const int j0 = 1 + sub * span, j1 = min(n - 1, j0 + span);
+        wl = Pt - P[lo]; sl = St - S[lo];
+        wr = P[hi] - Pt; sr = St - S[hi];
+        const int span = (hi - lo - 1 + R - 1) / R;
+        const int j0 = lo + 1 + sub * span, j1 = min(hi, j0 + span);
         for (int j = j0; j < j1; ++j) {
             const int w0 = P[j] - Pt;
             const int64_t sv = St - S[j];
@@ -250,13 +241,86 @@ __device__ __forceinline__ void cta_list_hull(const uint16_t* P, const int64_t* 
         if (left_turn_w32(wl, sl, owl, osl)) { bl = obl; wl = owl; sl = osl; }
         if (left_turn_w32(wr, sr, owr, osr)) { br = obr; wr = owr; sr = osr; }
     }
-    if (sub == 0 && t < n - 1) {
-        const bool vertex = t == 0 ||
-                            (mine && left_turn_w32(Pt - P[bl], St - S[bl], P[br] - P[bl], S[br] - S[bl]));
-        if (vertex) {
-            const int K = (n - 1 + 31) >> 5;
-            atomicOr(&vm[t / K], 1u << (t % K));
+    return act && (t == lo || t == hi ||
+                   (mine && left_turn_w32(Pt - P[bl], St - S[bl], P[br] - P[bl], S[br] - S[bl])));
+}
+
+// Threads per entry for a pass over n entries by NT threads (a power of two,
+// at most 32, R n <= NT).
+template <int NT>
+__device__ __forceinline__ int list_threads_per_entry(int n) {
+    int R = 1;
+    while (R < 32 && 2 * R * n <= NT) R <<= 1;
+    return R;
+}
+
+constexpr int kListBlock = 16;      // entries per block of the first pass
+constexpr int kListTwoPass = 32;    // longer lists take the first pass
+// bytes of cta_list_hull's scratch for NT threads
+__host__ __device__ constexpr int list_scratch_bytes(int nt) { return 13 * nt + 16; }
+
+// Lower hull of the n <= NT entries of a list by the CTA: entry i is the point
+// with index P[i] (increasing) and tile-relative sum S[i]; entries 0 and n - 1
+// are vertices.  An entry is a vertex when no other entry lies on or below the
+// line through it with a slope between its in and out slopes: the pairwise
+// test of list_corner over all entries.  A list of more than kListTwoPass
+// entries first keeps only the corners of its blocks of kListBlock entries (a
+// vertex of the whole list's hull is one of the hull of any block holding it),
+// then tests the survivors against each other: the same vertices, with far
+// fewer pairs.  On return bit t % K of vm[t / K] is set for each vertex t < n - 1,
+// K = ceil((n - 1) / 32).  scratch: list_scratch_bytes(NT) bytes of shared
+// memory, 8-byte aligned.  Every thread of the CTA calls it.
+template <int NT>
+__device__ __forceinline__ void cta_list_hull(const uint16_t* P, const int64_t* S, int n, uint32_t* vm,
+                                              unsigned char* scratch) {
+    const int tid = threadIdx.x;
+    if (tid < 32) vm[tid] = 0u;
+    const int K = (n - 1 + 31) >> 5;
+    const uint16_t* P2 = P;
+    const int64_t* S2 = S;
+    const uint16_t* Q = nullptr;       // survivor i is entry Q[i]
+    int m = n;
+    if (n > kListTwoPass) {
+        uint16_t* qP = reinterpret_cast<uint16_t*>(scratch);
+        uint16_t* qQ = qP + NT;
+        int64_t* qS = reinterpret_cast<int64_t*>(scratch + 4 * NT);
+        uint8_t* keep = scratch + 12 * NT;
+        int* s_m = reinterpret_cast<int*>(scratch + 13 * NT);
+        const int R = list_threads_per_entry<NT>(n);
+        const int t = tid / R, sub = tid % R;
+        const int lo = (t / kListBlock) * kListBlock;
+        const int hi = min(lo + kListBlock - 1, n - 1);
+        const bool c = list_corner(P, S, t, t < n, lo, hi, R, sub);
+        if (sub == 0 && t < n) keep[t] = c ? 1 : 0;
+        __syncthreads();
+        if (tid < 32) {
+            int base = 0;
+            for (int q = 0; q < n; q += 32) {
+                const int u = q + tid;
+                const bool k = u < n && keep[u];
+                const unsigned b = __ballot_sync(kFull, k);
+                if (k) {
+                    const int i = base + __popc(b & ((1u << tid) - 1u));
+                    qQ[i] = (uint16_t)u;
+                    qP[i] = P[u];
+                    qS[i] = S[u];
+                }
+                base += __popc(b);
+            }
+            if (tid == 0) *s_m = base;
         }
+        __syncthreads();
+        m = *s_m;
+        P2 = qP; S2 = qS; Q = qQ;
+    } else {
+        __syncthreads();
+    }
+    const int R = list_threads_per_entry<NT>(m);
+    const int t = tid / R, sub = tid % R;
+    const bool c = list_corner(P2, S2, t, t < m, 0, m - 1, R, sub);
+    if (sub == 0 && t < m - 1 && c) {
+        const int o = Q ? (int)Q[t] : t;
+        atomicOr(&vm[o / K], 1u << (o % K));
     }
     __syncthreads();
 }

@@ -86,7 +86,11 @@ struct LongWs {
     i128* offW;        // [M]
     int32_t* dS;       // [M] shift from chunk to row quantum
     int32_t* dW;       // [M]
-    ChunkEnds* ends;   // [M]
+    int4* eInfo;       // [M] chunk ends (ChunkEnds), as arrays: (lo, hi, pt0_vertex, bad)
+    i128* ePrevW;      // [M] previous root vertex
+    i128* ePrevS;
+    i128* eNextW;      // [M] next root vertex
+    i128* eNextS;
     int32_t* rowq;     // [rows][4]: qs_row, qw_row, bad
     i128* gfS;         // [G][kGroupFlatCap] each group's merged hull, row coordinates
     void* gfW;         // i128 (weighted) or int64 (unit weights: point index) per vertex
@@ -97,6 +101,26 @@ struct LongWs {
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// A chunk's ends, kept as arrays so that a warp's stores for consecutive
+// chunks are contiguous.
+__device__ __forceinline__ void store_ends(const LongWs& ws, int64_t c, const ChunkEnds& ce) {
+    ws.eInfo[c] = make_int4(ce.lo, ce.hi, ce.pt0_vertex, ce.bad);
+    ws.ePrevW[c] = ce.prevW;
+    ws.ePrevS[c] = ce.prevS;
+    ws.eNextW[c] = ce.nextW;
+    ws.eNextS[c] = ce.nextS;
+}
+__device__ __forceinline__ ChunkEnds load_ends(const LongWs& ws, int64_t c) {
+    ChunkEnds ce;
+    const int4 e = ws.eInfo[c];
+    ce.lo = e.x; ce.hi = e.y; ce.pt0_vertex = e.z; ce.bad = e.w;
+    ce.prevW = ws.ePrevW[c];
+    ce.prevS = ws.ePrevS[c];
+    ce.nextW = ws.eNextW[c];
+    ce.nextS = ws.eNextS[c];
+    return ce;
+}
 
 // Workspace of `rows` long rows holding M chunks in all.
 template <bool WEIGHTED>
@@ -124,7 +148,11 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t M, Lon
     w.offW = (i128*)take(sizeof(i128) * M);
     w.dS = (int32_t*)take(sizeof(int32_t) * M);
     w.dW = (int32_t*)take(sizeof(int32_t) * M);
-    w.ends = (ChunkEnds*)take(sizeof(ChunkEnds) * M);
+    w.eInfo = (int4*)take(sizeof(int4) * M);
+    w.ePrevW = (i128*)take(sizeof(i128) * M);
+    w.ePrevS = (i128*)take(sizeof(i128) * M);
+    w.eNextW = (i128*)take(sizeof(i128) * M);
+    w.eNextS = (i128*)take(sizeof(i128) * M);
     w.rowq = (int32_t*)take(sizeof(int32_t) * 4 * rows);
     const size_t G = (size_t)(M / kGroup + rows + 1);      // groups of all rows, at most
     w.gfS = (i128*)take(sizeof(i128) * kGroupFlatCap * G);
@@ -764,22 +792,31 @@ struct MergeLayout {
 // status bits, over the m chunks of the row (every thread of the CTA calls it).
 struct RowQ { int qs, qw, bad; };
 
-__device__ __forceinline__ RowQ row_quanta(int64_t m, const LongWs& ws, int64_t c0, int* red) {
+// cache: when not null, the row's chunk records are also copied there (m of
+// them), for the caller's next pass.
+__device__ __forceinline__ RowQ row_quanta(int64_t m, const LongWs& ws, int64_t c0, int* red,
+                                           ChunkMeta* cache = nullptr) {
     const int tid = threadIdx.x, nth = blockDim.x;
     if (tid == 0) { red[0] = -100000; red[1] = -100000; red[2] = 0; }
     __syncthreads();
     int qs = -100000, qw = -100000, bad = 0;
     // four chunks in flight per thread (the loads are independent)
     for (int64_t j0 = tid; j0 < m; j0 += 4 * (int64_t)nth) {
-        int4 q4[4];
+        int4 q4[4], t4[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int64_t j = j0 + (int64_t)u * nth;
             q4[u] = j < m ? *reinterpret_cast<const int4*>(&ws.meta[c0 + j]) : make_int4(0, 0, -100000, -100000);
+            if (cache && j < m) t4[u] = *(reinterpret_cast<const int4*>(&ws.meta[c0 + j]) + 1);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {   // (h, bad, qs, qw)
             bad |= q4[u].y; qs = max(qs, q4[u].z); qw = max(qw, q4[u].w);
+            const int64_t j = j0 + (int64_t)u * nth;
+            if (cache && j < m) {
+                reinterpret_cast<int4*>(&cache[j])[0] = q4[u];
+                reinterpret_cast<int4*>(&cache[j])[1] = t4[u];
+            }
         }
     }
 #pragma unroll
@@ -996,6 +1033,12 @@ struct FlatSm {
         get(o, Wo, So); get(a, Wa, Sa); get(b, Wb, Sb);
         return row_turn<WEIGHTED>(Wo, So, Wa, Sa, Wb, Sb);
     }
+    // the same with o's coordinates already at hand
+    __device__ __forceinline__ bool turn_from(i128 Wo, i128 So, int a, int b) const {
+        i128 Wa, Sa, Wb, Sb;
+        get(a, Wa, Sa); get(b, Wb, Sb);
+        return row_turn<WEIGHTED>(Wo, So, Wa, Sa, Wb, Sb);
+    }
 };
 
 constexpr int kFlatTagRank = 13;   // bits of the rank in a tag (C + 1 <= 2^13)
@@ -1013,7 +1056,9 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
         // galloping from R's first vertex (bridges lie near the shared point
         // as a rule)
         auto tangent = [&](int x) -> int {
-            auto h = [&](int j) { return j >= qR - 1 || F.turn(a0 + x, b0 + 1 + j, b0 + 2 + j); };
+            i128 Wx, Sx;
+            F.get(a0 + x, Wx, Sx);
+            auto h = [&](int j) { return j >= qR - 1 || F.turn_from(Wx, Sx, b0 + 1 + j, b0 + 2 + j); };
             int jl = 0, jh = qR - 1;
             if (qR > 32) {
                 if (h(0)) return 0;
@@ -1093,22 +1138,34 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
         }
     }
     // the right node's kept tail moves down behind the left node's kept head
+    // (dst < src): 32 U vertices per round, all read before any is written; a
+    // round's writes lie below the next round's reads, so one barrier a round
+    constexpr int U = WEIGHTED ? 2 : 4;
     const int len = nb - fromB, dst = a0 + keepA, src = b0 + fromB;
-    for (int q = 0; q < len; q += 32) {
-        const int k = q + lane;
-        i128 sv = 0, wv = 0;
-        int64_t wu = 0;
-        uint32_t tg = 0;
-        if (k < len) {
-            sv = F.S[src + k];
-            if constexpr (WEIGHTED) wv = F.Wi[src + k]; else wu = F.Wu[src + k];
-            tg = F.tag[src + k];
-        }
-        __syncwarp();
-        if (k < len) {
-            F.S[dst + k] = sv;
-            if constexpr (WEIGHTED) F.Wi[dst + k] = wv; else F.Wu[dst + k] = wu;
-            F.tag[dst + k] = tg;
+    if (dst != src) {
+        for (int q = 0; q < len; q += 32 * U) {
+            i128 sv[U], wv[U];
+            int64_t wu[U];
+            uint32_t tg[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = q + 32 * u + lane;
+                if (k < len) {
+                    sv[u] = F.S[src + k];
+                    if constexpr (WEIGHTED) wv[u] = F.Wi[src + k]; else wu[u] = F.Wu[src + k];
+                    tg[u] = F.tag[src + k];
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int k = q + 32 * u + lane;
+                if (k < len) {
+                    F.S[dst + k] = sv[u];
+                    if constexpr (WEIGHTED) F.Wi[dst + k] = wv[u]; else F.Wu[dst + k] = wu[u];
+                    F.tag[dst + k] = tg[u];
+                }
+            }
         }
         __syncwarp();
     }
@@ -1139,7 +1196,8 @@ constexpr int kMaxFlatGroups = 2 * kMergeThreads;   // groups of a row whose fla
 template <bool WEIGHTED>
 __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, int jb, int je,
                                                  const i128* gS, const i128* gW,
-                                                 const int32_t* gH, int64_t Hg, int64_t g) {
+                                                 const int32_t* gH, const int32_t* gDS,
+                                                 const int32_t* gDW, int64_t Hg, int64_t g) {
     constexpr int C = LongCfg<WEIGHTED>::C;
     const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
     const int mg = je - jb;
@@ -1158,19 +1216,37 @@ __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, i
         nsize[j] = (j + 1 < mg ? gH[j + 1] : (int32_t)Hg) - gH[j];
     }
     // every vertex in row coordinates: its chunk by bisection over the bases
-    for (int64_t i = tid; i < Hg; i += nth) {
-        int lo = 0, hi = mg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (gH[mid] <= i) lo = mid; else hi = mid - 1;
+    // (four vertices per thread in flight: their slot loads are independent)
+    for (int64_t i0 = tid; i0 < Hg; i0 += 4 * (int64_t)nth) {
+        int jl[4], rr[4];
+        int64_t sv[4], wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t i = i0 + (int64_t)u * nth;
+            jl[u] = -1; rr[u] = 0; sv[u] = 0; wv[u] = 0;
+            if (i < Hg) {
+                int lo = 0, hi = mg - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (gH[mid] <= i) lo = mid; else hi = mid - 1;
+                }
+                jl[u] = lo;
+                rr[u] = (int)(i - gH[lo]);
+                const size_t gi = (size_t)(c0 + jb + lo) * ((size_t)C + 1) + rr[u];
+                sv[u] = ws.slot_S[gi];
+                if constexpr (WEIGHTED) wv[u] = ws.slot_W[gi]; else wv[u] = ws.slot_p[gi];
+            }
         }
-        const int j = jb + lo;
-        const int r = (int)(i - gH[lo]);
-        const size_t g = (size_t)(c0 + j) * ((size_t)C + 1) + r;
-        F.S[i] = gS[lo] + conv(ws.slot_S[g], ws.dS[c0 + j]);
-        if constexpr (WEIGHTED) F.Wi[i] = gW[lo] + conv(ws.slot_W[g], ws.dW[c0 + j]);
-        else F.Wu[i] = (int64_t)j * C + ws.slot_p[g];
-        F.tag[i] = ((uint32_t)j << kFlatTagRank) | (uint32_t)r;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (jl[u] < 0) continue;
+            const int64_t i = i0 + (int64_t)u * nth;
+            const int lo = jl[u], j = jb + lo;
+            F.S[i] = gS[lo] + conv(sv[u], gDS[lo]);
+            if constexpr (WEIGHTED) F.Wi[i] = gW[lo] + conv(wv[u], gDW[lo]);
+            else F.Wu[i] = (int64_t)j * C + wv[u];
+            F.tag[i] = ((uint32_t)j << kFlatTagRank) | (uint32_t)rr[u];
+        }
     }
     __syncthreads();
     for (int half = 1; half < mg; half <<= 1) {
@@ -1239,6 +1315,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     __shared__ i128 s_part[2][kGroupThreads / 32];
     __shared__ i128 s_gS[kGroup], s_gW[kGroup];
     __shared__ int32_t s_gH[kGroup];
+    __shared__ int32_t s_gD[2][kGroup];
     __shared__ long long s_Hg;
     const int64_t row = geo.e0 ? (int64_t)geo.group_row[g] : g / ng;
     const RowRef R = geo_row<C>(geo, row);
@@ -1247,7 +1324,12 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     const int jb = (int)gi * kGroup;
     const int je = (int)imin64(jb + kGroup, m);
     const int tid = threadIdx.x, nth = blockDim.x;
-    const RowQ q = row_quanta(m, ws, c0, s_red);
+    // the row's chunk records, read once into the dynamic shared memory when they fit
+    // (the merges below use it only after the offsets are done)
+    constexpr int64_t kCacheBytes = MERGE ? kFlatSmem : kGroupSmem;
+    ChunkMeta* mc = m * (int64_t)sizeof(ChunkMeta) <= kCacheBytes ? reinterpret_cast<ChunkMeta*>(merge_smem)
+                                                                   : nullptr;
+    const RowQ q = row_quanta(m, ws, c0, s_red, mc);
     if (gi == 0 && tid == 0) {
         ws.rowq[row * 4 + 0] = q.qs; ws.rowq[row * 4 + 1] = q.qw; ws.rowq[row * 4 + 2] = q.bad;
         if (row_status) row_status[R.id] = (uint32_t)q.bad;
@@ -1256,7 +1338,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
         for (int j = jb + tid; j < je; j += nth) {
             ChunkEnds ce{};
             ce.lo = 1; ce.hi = 0; ce.bad = q.bad;
-            ws.ends[c0 + j] = ce;
+            store_ends(ws, c0 + j, ce);
         }
         return;
     }
@@ -1269,7 +1351,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int64_t j = j0 + (int64_t)u * nth;
-                if (j < jb) m4[u] = ws.meta[c0 + j];
+                if (j < jb) m4[u] = mc ? mc[j] : ws.meta[c0 + j];
                 else { m4[u].qs = q.qs; m4[u].qw = q.qw; m4[u].totS = 0; m4[u].totW = 0; }
             }
 #pragma unroll
@@ -1293,7 +1375,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
         const int j = jb + tid;
         const bool valid = tid < kGroup && j < je;
         ChunkMeta mt{};
-        if (valid) mt = ws.meta[c0 + j];
+        if (valid) mt = mc ? mc[j] : ws.meta[c0 + j];
         const int ds = valid ? q.qs - mt.qs : 0;
         const int dw = (valid && WEIGHTED) ? q.qw - mt.qw : 0;
         Acc3 v;
@@ -1310,6 +1392,8 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
             if (WEIGHTED) ws.offW[c0 + j] = bW + e.w;
             ws.dS[c0 + j] = ds;
             if (WEIGHTED) ws.dW[c0 + j] = dw;
+            s_gD[0][tid] = ds;
+            s_gD[1][tid] = dw;
         }
         if (tid == 0) s_Hg = tot.h;
         __syncthreads();
@@ -1317,7 +1401,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     if (!MERGE) return;
     const int64_t Hg = s_Hg;
     if (FlatLayout(je - jb, Hg, WEIGHTED).bytes <= (size_t)kFlatSmem) {
-        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, Hg, g);
+        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, s_gD[0], s_gD[1], Hg, g);
         return;
     }
     if (tid == 0) ws.gfN[g] = -1;
@@ -1395,7 +1479,7 @@ __device__ __forceinline__ void root_ends(const View& V, int64_t m, const LongWs
             const Seg gn = V.load(nextSeg[j]);
             V.at(gn, gn.lo, ce.nextW, ce.nextS);
         }
-        ws.ends[c0 + j] = ce;
+        store_ends(ws, c0 + j, ce);
     }
 }
 
@@ -1479,16 +1563,23 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
     F.bst = ws.bst;
     int32_t* nstart = reinterpret_cast<int32_t*>(sm + Lo.oStart);
     int32_t* nsize = reinterpret_cast<int32_t*>(sm + Lo.oSize);
-    for (int k = warp; k < ng; k += nw) {
-        const int n = ws.gfN[gb + k], b = gbase[k];
-        const size_t o = (size_t)(gb + k) * kGroupFlatCap;
-        if (lane == 0) { nstart[k] = b; nsize[k] = n; }
-        for (int i = lane; i < n; i += 32) {
-            F.S[b + i] = ws.gfS[o + i];
-            if constexpr (WEIGHTED) F.Wi[b + i] = reinterpret_cast<const i128*>(ws.gfW)[o + i];
-            else F.Wu[b + i] = reinterpret_cast<const int64_t*>(ws.gfW)[o + i];
-            F.tag[b + i] = ws.gfTag[o + i];
+    for (int k = tid; k < ng; k += nth) {
+        nstart[k] = gbase[k];
+        nsize[k] = (k + 1 < ng ? gbase[k + 1] : H) - gbase[k];
+    }
+    // every vertex at once: its group by bisection over the bases (the last
+    // group whose base is at or before it: empty groups are passed over)
+    for (int i = tid; i < H; i += nth) {
+        int lo = 0, hi = ng - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (gbase[mid] <= i) lo = mid; else hi = mid - 1;
         }
+        const size_t o = (size_t)(gb + lo) * kGroupFlatCap + (size_t)(i - gbase[lo]);
+        F.S[i] = ws.gfS[o];
+        if constexpr (WEIGHTED) F.Wi[i] = reinterpret_cast<const i128*>(ws.gfW)[o];
+        else F.Wu[i] = reinterpret_cast<const int64_t*>(ws.gfW)[o];
+        F.tag[i] = ws.gfTag[o];
     }
     __syncthreads();
     for (int half = 1; half < ng; half <<= 1) {
@@ -1535,7 +1626,7 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
             }
         }
         if (j + 1 < m) F.get(v0 + ub, ce.nextW, ce.nextS);
-        ws.ends[c0 + j] = ce;
+        store_ends(ws, c0 + j, ce);
     }
 }
 
@@ -1545,17 +1636,20 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
     const RowRef R = geo_row<C>(geo, row);
     const int64_t m = R.m, c0 = R.c0;
     const int tid = threadIdx.x, nth = blockDim.x;
+    // every group of the row kept a flat array and they fit: the flat top
+    const int64_t ng = (m + kGroup - 1) / kGroup;
+    const int64_t gb = geo.e0 ? geo.g0[row] : row * ng;
+    // the groups' sizes are read with the row's status (a bad row's are unused)
+    const int k0 = 2 * tid, k1 = 2 * tid + 1;
+    const bool flat_ok = ng <= kMaxFlatGroups;
+    const int c0n = flat_ok && k0 < ng ? ws.gfN[gb + k0] : 0;
+    const int c1n = flat_ok && k1 < ng ? ws.gfN[gb + k1] : 0;
     if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
     {
-        // every group of the row kept a flat array and they fit: the flat top
-        const int64_t ng = (m + kGroup - 1) / kGroup;
-        const int64_t gb = geo.e0 ? geo.g0[row] : row * ng;
         __shared__ int32_t s_gbase[kMaxFlatGroups];
         __shared__ int s_scan2[32];
-        if (ng <= kMaxFlatGroups) {
-            // the groups' sizes, bases by a block scan (ng <= blockDim.x * 2)
-            const int k0 = 2 * tid, k1 = 2 * tid + 1;
-            const int c0n = k0 < ng ? ws.gfN[gb + k0] : 0, c1n = k1 < ng ? ws.gfN[gb + k1] : 0;
+        if (flat_ok) {
+            // bases by a block scan (ng <= blockDim.x * 2)
             const bool ok = __syncthreads_and(c0n >= 0 && c1n >= 0);
             int tot;
             const int b = block_excl_scan_int(c0n + c1n, s_scan2, tot);
@@ -1652,7 +1746,7 @@ __device__ __forceinline__ void expand_one(const IO* __restrict__ y, const LongG
     const int64_t e0 = (c - R.c0) * C;
     const int nt = (int)imin64(C, R.n - e0);
     const int tid = threadIdx.x;
-    const ChunkEnds ce = ws.ends[c];
+    const ChunkEnds ce = load_ends(ws, c);
     IO* orow = out + R.e0 + e0;
     uint8_t* brow = blocks ? blocks + R.e0 + e0 : nullptr;
     const bool neg = !increasing;

@@ -423,7 +423,8 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     // list, whose hull one warp finds by farthest-point levels ----
     H.list = 0;
     if constexpr (!EMIT && !WEIGHTED && sizeof(IO) == 4) {
-        static_assert((3 * NT + 3 * (NT / 32)) * 4 <= SM::kPxB && kListCap * 10 <= SM::kPxB, "list area");
+        static_assert((3 * NT + 3 * (NT / 32)) * 4 <= SM::kPxB &&
+                      kListCap * 10 + list_scratch_bytes(NT) <= SM::kPxB, "list area");
         unsigned char* area = smem + SM::oPx;
         __syncthreads();                                     // lane starts written
         cand = chunk_filter<NT>(yv, e, lane, nt, H.qs, LSa, work ? cand : 0u,
@@ -449,8 +450,8 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
             if (lane == 0) { LP[0] = 0; LSv[0] = 0; LP[n_list - 1] = (uint16_t)nt; LSv[n_list - 1] = LSa[L]; }
             __syncthreads();
             if (n_list <= NT) {
-                // a short list: one pass, one thread per entry
-                cta_list_hull<NT>(LP, LSv, n_list, maska);
+                // a short list: the CTA's pairwise passes
+                cta_list_hull<NT>(LP, LSv, n_list, maska, area + 10 * kListCap);
                 H.list = n_list;
                 return;
             }
