@@ -169,26 +169,47 @@ __device__ uint32_t chunk_filter(const float (&yv)[32], int e, int lane, int nt,
     const FSeg mid = fseg(pa, fa, da, pb, fb, db, delta, fabsmax);          // the lowest point itself
     const FSeg gl = fseg(0, 0.0f, 0.0f, g, fg, dg, delta, fabsmax);         // chord from point 0 to g
     const FSeg gr = fseg(g, fg, dg, nt, fend, dend, delta, fabsmax);        // chord from g to the end
-    uint32_t drop = 0u;
+    // Every point's tests as bit masks (against the chord before the lane's
+    // lowest point, the chord after it, and the chunk chord on its side of g),
+    // combined once per lane: the same tests, on the same values, as choosing
+    // each point's chords one by one.
+    const int gk = g - (lane << 5);                        // g's position in this lane
+    const FSeg ga = gk > 0 ? gl : gr;                      // the chunk chord of most of the lane
+    uint32_t dL = 0u, dR = 0u, dG = 0u;
     f = G;
     float pf = (float)(lane << 5);
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
-        if (k < e && ((keep >> k) & 1u)) {
-            const int p = (lane << 5) + k;
-            const bool lt = p < pm, gt = p > pm, lg = p < g;
-            const float s1 = lt ? left.sigma : (gt ? right.sigma : mid.sigma);
-            const float b1 = lt ? left.beta : (gt ? right.beta : mid.beta);
-            const float m1 = lt ? left.M : (gt ? right.M : mid.M);
-            const float s2 = lg ? gl.sigma : gr.sigma;
-            const float b2 = lg ? gl.beta : gr.beta;
-            const float m2 = p == g ? __int_as_float(0x7f800000) : (lg ? gl.M : gr.M);
-            const float t1 = f - fmaf(s1, pf, b1);
-            const float t2 = f - fmaf(s2, pf, b2);
-            if (t1 > m1 || t2 > m2) drop |= 1u << k;
-        }
+        const float tl = f - fmaf(left.sigma, pf, left.beta);
+        const float tr = f - fmaf(right.sigma, pf, right.beta);
+        const float tg = f - fmaf(ga.sigma, pf, ga.beta);
+        if (tl > left.M) dL |= 1u << k;
+        if (tr > right.M) dR |= 1u << k;
+        if (tg > ga.M) dG |= 1u << k;
         if (k < e) f = f + (yv[k] - c);
         pf += 1.0f;
+    }
+    // before the lowest point the left chord, after it the right one
+    uint32_t drop = (dL & ((1u << kmin) - 1u)) | (dR & ~((2u << kmin) - 1u));
+    // the lowest point against the chord between the neighbours' lowest points
+    if (fmin - fmaf(mid.sigma, (float)pm, mid.beta) > mid.M) drop |= 1u << kmin;
+    // the chunk chord on each point's side of g (g itself takes neither)
+    const uint32_t sideA = gk > 0 ? (gk >= 32 ? 0xffffffffu : (1u << gk) - 1u)
+                                  : (gk < 0 ? 0xffffffffu : ~1u);
+    drop |= dG & sideA;
+    if (gk > 0 && gk < 31) {
+        // g's lane: its points after g against the chord from g to the end
+        uint32_t d2 = 0u;
+        f = G;
+        pf = (float)(lane << 5);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float t = f - fmaf(gr.sigma, pf, gr.beta);
+            if (t > gr.M) d2 |= 1u << k;
+            if (k < e) f = f + (yv[k] - c);
+            pf += 1.0f;
+        }
+        drop |= d2 & ~((2u << gk) - 1u);
     }
     return keep & ~drop;
 }

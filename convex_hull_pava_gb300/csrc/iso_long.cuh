@@ -311,8 +311,16 @@ __device__ __forceinline__ void chunk_hull_one(const IO* __restrict__ y,
 
 // One CTA per chunk; a ragged batch's grid is bounded and its CTAs take the
 // chunks in turn.
+// CTAs per SM that the chunk kernel's shared memory allows: its registers
+// are held to that many (228 KB per SM, 1 KB reserved per CTA).
+template <bool WEIGHTED, class IO>
+constexpr int chunk_min_blocks() {
+    constexpr int b = 233472 / (TileSmem<LongCfg<WEIGHTED>::NT, WEIGHTED, false, 1, IO>::kBytes + 1024);
+    return b < 1 ? 1 : (b > 8 ? 8 : b);
+}
+
 template <bool WEIGHTED, bool RAGGED, class IO>
-__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT)
+__global__ void __launch_bounds__(LongCfg<WEIGHTED>::NT, (chunk_min_blocks<WEIGHTED, IO>()))
 chunk_hull_kernel(const IO* __restrict__ y, const IO* __restrict__ w, LongGeo geo,
                   int increasing, LongWs ws) {
     if (!RAGGED) {
