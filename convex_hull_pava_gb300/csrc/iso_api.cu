@@ -36,6 +36,18 @@ int g_bridge_mode = 0;
 unsigned long long* g_bridge_stats[kStatDevices];
 }  // namespace
 
+int device_sms() {
+    static int sms[kStatDevices];
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStatDevices) return 1;
+    if (sms[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+        sms[dev] = n;
+    }
+    return sms[dev];
+}
+
 BridgeDebug bridge_debug() {
     BridgeDebug d{nullptr, ISO_BRIDGE_MAX_PASSES};
     if (g_bridge_mode == 0) return d;

@@ -21,6 +21,9 @@ struct BridgeDebug {
     int max_passes;
 };
 BridgeDebug bridge_debug();
+
+// The current device's SM count (queried once per device; 1 if unknown).
+int device_sms();
 iso_status bridge_stats_mode(int mode);
 iso_status bridge_stats_read(uint64_t* out);
 

@@ -772,7 +772,7 @@ __device__ __forceinline__ Acc3 block_excl_scan3(Acc3 v, Acc3* tmp, Acc3& total)
 // Each CTA reads its chunk hulls into shared memory when they fit (noisy rows
 // keep few vertices; the top kernel reads only the vertices still inside a
 // segment), else it reads them from the slots in global memory.
-constexpr int kGroupThreads = 256;
+constexpr int kGroupThreads = 512;   // the most threads of a group CTA (fewer when groups are many)
 constexpr int kGroupSmem = 48 * 1024;
 
 // Shared-memory layout for mc chunks and H vertices.
@@ -2327,7 +2327,10 @@ static cudaError_t long_launch(const IO* y, const IO* w, const LongGeo& geo,
     err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, RAGGED>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFlatSmem);
     if (err != cudaSuccess) return err;
-    err = launch_after(merge_groups_kernel<WEIGHTED, RAGGED>, (unsigned)gr.groups, kGroupThreads, kFlatSmem,
+    // one wave of groups: kGroupThreads threads each (shorter chains of merges
+    // per warp); more groups: half as many, two CTAs per SM
+    const int gthreads = gr.groups <= device_sms() ? kGroupThreads : kGroupThreads / 2;
+    err = launch_after(merge_groups_kernel<WEIGHTED, RAGGED>, (unsigned)gr.groups, gthreads, kFlatSmem,
                        stream, geo, gr.ng, ws, row_status);
     if (err != cudaSuccess) return err;
     prof_mark(stream, "merge_groups");
@@ -2474,7 +2477,7 @@ static cudaError_t long_control_t(const IO* y, const IO* w, int64_t rows, int64_
     err = cudaFuncSetAttribute(merge_groups_kernel<WEIGHTED, false, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kGroupSmem);
     if (err != cudaSuccess) return err;
-    merge_groups_kernel<WEIGHTED, false, false><<<(unsigned)(rows * ng), kGroupThreads, kGroupSmem,
+    merge_groups_kernel<WEIGHTED, false, false><<<(unsigned)(rows * ng), kGroupThreads / 2, kGroupSmem,
                                                   stream>>>(geo, ng, ws, row_status);
     ctl_base_kernel<WEIGHTED><<<(unsigned)rows, kMergeThreads, 0, stream>>>(m, ws, cw);
     ctl_flatten_kernel<WEIGHTED><<<(unsigned)M, 128, 0, stream>>>(m, ws, cw);
