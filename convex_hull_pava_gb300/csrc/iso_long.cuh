@@ -68,9 +68,9 @@ struct ChunkEnds {            // per chunk, from the root list
     int32_t lo, hi;           // rank range of the chunk's root segment, lo > hi if none
     int32_t pt0_vertex;       // 1 if the chunk's first point is a root vertex (closes the previous segment)
     int32_t bad;              // row status bits
-    i128 prevW, prevS;        // previous root vertex (row coordinates)
-    i128 nextW, nextS;        // next root vertex (row coordinates)
-};
+    double in_sl;             // slope of the root edge entering the chunk (chunk 0: 0)
+    double out_sl;            // slope of the root edge leaving its last root vertex (0 if none)
+};                            // (slopes in values: edge_slope, before the cast to the I/O type)
 
 struct LongWs {
     ChunkMeta* meta;   // [M]
@@ -87,10 +87,8 @@ struct LongWs {
     int32_t* dS;       // [M] shift from chunk to row quantum
     int32_t* dW;       // [M]
     int4* eInfo;       // [M] chunk ends (ChunkEnds), as arrays: (lo, hi, pt0_vertex, bad)
-    i128* ePrevW;      // [M] previous root vertex
-    i128* ePrevS;
-    i128* eNextW;      // [M] next root vertex
-    i128* eNextS;
+    double* eIn;       // [M] slope of the root edge entering the chunk
+    double* eOut;      // [M] slope of the root edge leaving its last root vertex
     int32_t* rowq;     // [rows][4]: qs_row, qw_row, bad
     i128* gfS;         // [G][kGroupFlatCap] each group's merged hull, row coordinates
     void* gfW;         // i128 (weighted) or int64 (unit weights: point index) per vertex
@@ -106,19 +104,15 @@ __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_
 // chunks are contiguous.
 __device__ __forceinline__ void store_ends(const LongWs& ws, int64_t c, const ChunkEnds& ce) {
     ws.eInfo[c] = make_int4(ce.lo, ce.hi, ce.pt0_vertex, ce.bad);
-    ws.ePrevW[c] = ce.prevW;
-    ws.ePrevS[c] = ce.prevS;
-    ws.eNextW[c] = ce.nextW;
-    ws.eNextS[c] = ce.nextS;
+    ws.eIn[c] = ce.in_sl;
+    ws.eOut[c] = ce.out_sl;
 }
 __device__ __forceinline__ ChunkEnds load_ends(const LongWs& ws, int64_t c) {
     ChunkEnds ce;
     const int4 e = ws.eInfo[c];
     ce.lo = e.x; ce.hi = e.y; ce.pt0_vertex = e.z; ce.bad = e.w;
-    ce.prevW = ws.ePrevW[c];
-    ce.prevS = ws.ePrevS[c];
-    ce.nextW = ws.eNextW[c];
-    ce.nextS = ws.eNextS[c];
+    ce.in_sl = ws.eIn[c];
+    ce.out_sl = ws.eOut[c];
     return ce;
 }
 
@@ -149,10 +143,8 @@ __host__ __device__ inline size_t carve(void* base, int64_t rows, int64_t M, Lon
     w.dS = (int32_t*)take(sizeof(int32_t) * M);
     w.dW = (int32_t*)take(sizeof(int32_t) * M);
     w.eInfo = (int4*)take(sizeof(int4) * M);
-    w.ePrevW = (i128*)take(sizeof(i128) * M);
-    w.ePrevS = (i128*)take(sizeof(i128) * M);
-    w.eNextW = (i128*)take(sizeof(i128) * M);
-    w.eNextS = (i128*)take(sizeof(i128) * M);
+    w.eIn = (double*)take(sizeof(double) * M);
+    w.eOut = (double*)take(sizeof(double) * M);
     w.rowq = (int32_t*)take(sizeof(int32_t) * 4 * rows);
     const size_t G = (size_t)(M / kGroup + rows + 1);      // groups of all rows, at most
     w.gfS = (i128*)take(sizeof(i128) * kGroupFlatCap * G);
@@ -220,11 +212,21 @@ __device__ __forceinline__ double i128_to_double(i128 x) {
     return neg ? -d : d;
 }
 
+// The slope of the root edge from (Wa, Sa) to (Wb, Sb) in row coordinates,
+// scaled by 2^k from the row's quanta to values (k = qs_row - qw_row): the
+// expansion casts it to the I/O type.
+__device__ __forceinline__ double edge_slope(i128 Wa, i128 Sa, i128 Wb, i128 Sb, int k);
+
 // Round x / 2^d to nearest (half up); d >= 0.
 __device__ __forceinline__ int64_t conv(int64_t x, int d) {
     if (d <= 0) return x;
     if (d >= 63) return 0;
     return (x + (1LL << (d - 1))) >> d;
+}
+
+__device__ __forceinline__ double edge_slope(i128 Wa, i128 Sa, i128 Wb, i128 Sb, int k) {
+    const double f = i128_to_double(Sb - Sa) / i128_to_double(Wb - Wa);
+    return ldexp(f, k);
 }
 
 // ---------------------------------------------------------------------------
@@ -1441,7 +1443,7 @@ merge_groups_kernel(LongGeo geo, int64_t ng, LongWs ws, uint32_t* __restrict__ r
 // scratch of m entries.
 template <bool WEIGHTED, class View>
 __device__ __forceinline__ void root_ends(const View& V, int64_t m, const LongWs& ws, int64_t c0,
-                                          int32_t* segOf, int32_t* nextSeg, int32_t* prevSeg) {
+                                          int32_t* segOf, int32_t* nextSeg, int32_t* prevSeg, int kq) {
     const int tid = threadIdx.x, nth = blockDim.x;
     // With c(j) the number of root segments of chunks <= j (a scan of "chunk j
     // holds one"), the first after chunk j is c(j) and the last before it is
@@ -1472,20 +1474,31 @@ __device__ __forceinline__ void root_ends(const View& V, int64_t m, const LongWs
         ChunkEnds ce;
         ce.bad = 0;
         const int sk = segOf[j];
-        if (sk >= 0) { const int4 s = seg[sk]; ce.lo = s.y; ce.hi = s.z; }
+        Seg gs{};
+        if (sk >= 0) { gs = V.load(sk); ce.lo = gs.lo; ce.hi = gs.hi; }
         else { ce.lo = 1; ce.hi = 0; }
-        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
+        ce.in_sl = ce.out_sl = 0.0;
         ce.pt0_vertex = 0;
+        i128 Wn = 0, Sn = 0;
+        if (j + 1 < m) {
+            const Seg gn = V.load(nextSeg[j]);
+            V.at(gn, gn.lo, Wn, Sn);
+        }
         if (j > 0) {
             const int pk = prevSeg[j];
             const Seg gp = V.load(pk);
-            V.at(gp, gp.hi, ce.prevW, ce.prevS);
+            i128 Wp, Sp, Wb = Wn, Sb = Sn;
+            V.at(gp, gp.hi, Wp, Sp);
             // the previous root vertex is this chunk's first point when it closes chunk j-1
             ce.pt0_vertex = (gp.jc == j - 1 && gp.hi == ws.meta[c0 + gp.jc].h - 1) ? 1 : 0;
+            // the entering edge ends at the chunk's first root vertex, else at the next one
+            if (sk >= 0) V.at(gs, gs.lo, Wb, Sb);
+            ce.in_sl = edge_slope(Wp, Sp, Wb, Sb, kq);
         }
-        if (j + 1 < m) {
-            const Seg gn = V.load(nextSeg[j]);
-            V.at(gn, gn.lo, ce.nextW, ce.nextS);
+        if (sk >= 0 && j + 1 < m) {
+            i128 Wa, Sa;
+            V.at(gs, gs.hi, Wa, Sa);
+            ce.out_sl = edge_slope(Wa, Sa, Wn, Sn, kq);
         }
         store_ends(ws, c0 + j, ce);
     }
@@ -1493,7 +1506,7 @@ __device__ __forceinline__ void root_ends(const View& V, int64_t m, const LongWs
 
 template <bool WEIGHTED, bool SMEM>
 __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c0, int64_t Hs,
-                                          int32_t* s_len, int32_t* s_lo) {
+                                          int32_t* s_len, int32_t* s_lo, int kq) {
     constexpr int C = LongCfg<WEIGHTED>::C;
     const int tid = threadIdx.x, nth = blockDim.x;
     MergeLayout L(m, SMEM ? Hs : 0, WEIGHTED, true);
@@ -1548,7 +1561,7 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
     }
     merge_levels<WEIGHTED, SMEM>(V, 0, m, kGroup);
 
-    root_ends<WEIGHTED>(V, m, ws, c0, segOf, nextSeg, prevSeg);
+    root_ends<WEIGHTED>(V, m, ws, c0, segOf, nextSeg, prevSeg, kq);
 }
 
 // The top of the tree over the groups' flat arrays (every group of the row
@@ -1559,7 +1572,7 @@ __device__ __forceinline__ void merge_top(int64_t m, const LongWs& ws, int64_t c
 // a chunk boundary is tagged with the chunk it ends, as in the segment lists.
 template <bool WEIGHTED>
 __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int64_t m, int64_t gb,
-                                               int ng, int H, const int32_t* gbase) {
+                                               int ng, int H, const int32_t* gbase, int kq) {
     const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
     const FlatLayout Lo(ng, H, WEIGHTED);
     unsigned char* sm = merge_smem;
@@ -1611,6 +1624,14 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
         const int64_t jhi = k == n ? m : (int64_t)(tg[k] >> kFlatTagRank);
         for (int64_t j = jlo; j <= jhi && j <= m; ++j) first[j] = k;
     }
+    // each root edge's slope once, after first[] (8-byte aligned)
+    double* esl = reinterpret_cast<double*>((reinterpret_cast<uintptr_t>(first + m + 1) + 7) & ~(uintptr_t)7);
+    for (int k = tid; k + 1 < n; k += nth) {
+        i128 Wa, Sa, Wb, Sb;
+        F.get(v0 + k, Wa, Sa);
+        F.get(v0 + k + 1, Wb, Sb);
+        esl[k] = edge_slope(Wa, Sa, Wb, Sb, kq);
+    }
     __syncthreads();
     constexpr int C = LongCfg<WEIGHTED>::C;
     for (int64_t j = tid; j < m; j += nth) {
@@ -1619,21 +1640,22 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
         ce.bad = 0;
         if (lb < ub) { ce.lo = (int)(tg[lb] & kRank); ce.hi = (int)(tg[ub - 1] & kRank); }
         else { ce.lo = 1; ce.hi = 0; }
-        ce.prevW = ce.prevS = ce.nextW = ce.nextS = 0;
         ce.pt0_vertex = 0;
+        // entering edge: from root vertex lb - 1 to lb (the chunk's first root
+        // vertex, else the next); leaving edge: from ub - 1 to ub
+        ce.in_sl = j > 0 ? esl[lb - 1] : 0.0;
+        ce.out_sl = (lb < ub && j + 1 < m) ? esl[ub - 1] : 0.0;
         if (j > 0) {
             const int k = v0 + lb - 1;
-            F.get(k, ce.prevW, ce.prevS);
             // the previous root vertex is this chunk's first point (it closes chunk j - 1)
             if constexpr (WEIGHTED) {
                 const uint32_t t = F.tag[k];
                 ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
                                  (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
             } else {
-                ce.pt0_vertex = ce.prevW == (i128)(j * C) ? 1 : 0;
+                ce.pt0_vertex = F.Wu[k] == (int64_t)(j * C) ? 1 : 0;
             }
         }
-        if (j + 1 < m) F.get(v0 + ub, ce.nextW, ce.nextS);
         store_ends(ws, c0 + j, ce);
     }
 }
@@ -1653,6 +1675,8 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
     const int c0n = flat_ok && k0 < ng ? ws.gfN[gb + k0] : 0;
     const int c1n = flat_ok && k1 < ng ? ws.gfN[gb + k1] : 0;
     if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
+    // root edge slopes: from the row's quanta to values
+    const int kq = ws.rowq[row * 4 + 0] - (WEIGHTED ? ws.rowq[row * 4 + 1] : 0);
     {
         __shared__ int32_t s_gbase[kMaxFlatGroups];
         __shared__ int s_scan2[32];
@@ -1664,8 +1688,9 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
             if (k0 < ng) s_gbase[k0] = b;
             if (k1 < ng) s_gbase[k1] = b + c0n;
             __syncthreads();
-            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes + 4 * (size_t)(m + 1) <= (size_t)kMergeSmem) {
-                merge_top_flat<WEIGHTED>(ws, c0, m, gb, (int)ng, tot, s_gbase);
+            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes + 4 * (size_t)(m + 1) + 8 * (size_t)tot + 8 <=
+                          (size_t)kMergeSmem) {
+                merge_top_flat<WEIGHTED>(ws, c0, m, gb, (int)ng, tot, s_gbase, kq);
                 return;
             }
         }
@@ -1701,9 +1726,9 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
     __syncthreads();
     const int64_t Hs = total;
     if (MergeLayout(m, Hs, WEIGHTED, true).bytes <= (size_t)kMergeSmem)
-        merge_top<WEIGHTED, true>(m, ws, c0, Hs, len, lo0);
+        merge_top<WEIGHTED, true>(m, ws, c0, Hs, len, lo0, kq);
     else
-        merge_top<WEIGHTED, false>(m, ws, c0, Hs, len, lo0);
+        merge_top<WEIGHTED, false>(m, ws, c0, Hs, len, lo0, kq);
 }
 
 template <bool WEIGHTED, bool RAGGED>
@@ -1802,25 +1827,11 @@ __device__ __forceinline__ void expand_one(const IO* __restrict__ y, const LongG
         }
         return;
     }
-    const int qs_row = ws.rowq[row * 4 + 0];
-    const int qw_row = WEIGHTED ? ws.rowq[row * 4 + 1] : 0;
     const ChunkMeta mt = ws.meta[c];
-    const i128 offS = ws.offS[c];
-    const i128 offW = WEIGHTED ? ws.offW[c] : (i128)0;
-    const int ds = ws.dS[c], dw = WEIGHTED ? ws.dW[c] : 0;
 
     const int cexp = mt.qs - (WEIGHTED ? mt.qw : 0);   // chunk quanta to values
     s_mask[tid] = 0u;
     __syncthreads();
-    auto row_slope = [&](i128 Wa, i128 Sa, i128 Wb, i128 Sb) -> IO {
-        const double f = i128_to_double(Sb - Sa) / i128_to_double(Wb - Wa);
-        return (IO)ldexp(f, qs_row - qw_row);
-    };
-    auto vrow = [&](int r, i128& Wv, i128& Sv) {
-        Sv = offS + conv(sS[r], ds);
-        if constexpr (WEIGHTED) Wv = offW + conv(sW[r], dw);
-        else Wv = (i128)(e0 + sp[r]);
-    };
     // root vertices of this chunk that start one of its elements (point < nt),
     // each with the slope of the root edge leaving it
     const bool has = ce.lo <= ce.hi;
@@ -1841,9 +1852,7 @@ __device__ __forceinline__ void expand_one(const IO* __restrict__ y, const LongG
                 const int64_t dW_ = WEIGHTED ? sW[r + 1] - sW[r] : (int64_t)(sp[r + 1] - p);
                 sl = ratio_t<IO>(dS_, dW_, cexp);
             } else {
-                i128 Wa, Sa;
-                vrow(r, Wa, Sa);
-                sl = row_slope(Wa, Sa, ce.nextW, ce.nextS);
+                sl = (IO)ce.out_sl;                       // the edge to the next root vertex
             }
             slope[spos_t<IO>(p >> 5, p & 31)] = sl;
         }
@@ -1851,13 +1860,7 @@ __device__ __forceinline__ void expand_one(const IO* __restrict__ y, const LongG
     if (tid == 0) {
         // the edge entering the chunk: from the previous root vertex to the first
         // root vertex of the chunk, or to the next root vertex if the chunk has none
-        IO in_sl = IO(0);
-        if (e0 > 0) {
-            i128 Wb, Sb;
-            if (has) vrow(ce.lo, Wb, Sb);
-            else { Wb = ce.nextW; Sb = ce.nextS; }
-            in_sl = row_slope(ce.prevW, ce.prevS, Wb, Sb);
-        }
+        const IO in_sl = e0 > 0 ? (IO)ce.in_sl : IO(0);
         if (ce.pt0_vertex) {
             atomicOr(&s_mask[0], 1u);
             slope[spos_t<IO>(0, 0)] = in_sl;
@@ -2286,7 +2289,8 @@ ctl_root_kernel(int64_t m, LongWs ws, CtlWs cw) {
     V.vb = nullptr;
     V.S = ws.slot_S; V.W = ws.slot_W; V.P = ws.slot_p;
     V.dS = ws.dS + c0; V.dW = ws.dW + c0;
-    root_ends<WEIGHTED>(V, m, ws, c0, ws.segOf + c0, ws.nextSeg + c0, ws.prevSeg + c0);
+    root_ends<WEIGHTED>(V, m, ws, c0, ws.segOf + c0, ws.nextSeg + c0, ws.prevSeg + c0,
+                        ws.rowq[row * 4 + 0] - (WEIGHTED ? ws.rowq[row * 4 + 1] : 0));
 }
 
 // Launch of a kernel that may start while the stream's previous kernel is
