@@ -1182,6 +1182,69 @@ __device__ int warp_merge(const FlatSm<WEIGHTED>& F, int a0, int na, int b0, int
     return keepA + len;
 }
 
+// The ends of chunks 0..m-1 of a row (the first is chunk c0 of the
+// workspace) from the row's root hull: n vertices at v0 of the flat arrays F,
+// tags in chunk order.  Scratch after the root's tags: first[] (m + 1 ints)
+// and the edge slopes (n doubles, 8-byte aligned), which the caller has
+// checked fit.  kq: from the row's quanta to values.  Every thread of the CTA
+// calls it, after the arrays before v0 + n are dead.
+template <bool WEIGHTED>
+__device__ __forceinline__ void flat_root_ends(const FlatSm<WEIGHTED>& F, int v0, int n, int64_t m,
+                                               const LongWs& ws, int64_t c0, int kq) {
+    // ends of every chunk from the root array R (tags in chunk order): first[j]
+    // = the first root vertex of a chunk >= j, filled by each root vertex for
+    // the chunks since its predecessor's (the nodes' arrays are dead now, so
+    // first[] lives in the vertex arrays' space after R)
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const uint32_t* tg = F.tag + v0;
+    int32_t* first = reinterpret_cast<int32_t*>(F.tag + v0 + n);
+    constexpr uint32_t kRank = (1u << kFlatTagRank) - 1u;
+    for (int k = tid; k <= n; k += nth) {
+        const int64_t jlo = k == 0 ? 0 : (int64_t)(tg[k - 1] >> kFlatTagRank) + 1;
+        const int64_t jhi = k == n ? m : (int64_t)(tg[k] >> kFlatTagRank);
+        for (int64_t j = jlo; j <= jhi && j <= m; ++j) first[j] = k;
+    }
+    // each root edge's slope once, after first[] (8-byte aligned)
+    double* esl = reinterpret_cast<double*>((reinterpret_cast<uintptr_t>(first + m + 1) + 7) & ~(uintptr_t)7);
+    for (int k = tid; k + 1 < n; k += nth) {
+        i128 Wa, Sa, Wb, Sb;
+        F.get(v0 + k, Wa, Sa);
+        F.get(v0 + k + 1, Wb, Sb);
+        esl[k] = edge_slope(Wa, Sa, Wb, Sb, kq);
+    }
+    __syncthreads();
+    constexpr int C = LongCfg<WEIGHTED>::C;
+    for (int64_t j = tid; j < m; j += nth) {
+        const int lb = first[j], ub = first[j + 1];
+        ChunkEnds ce;
+        ce.bad = 0;
+        if (lb < ub) { ce.lo = (int)(tg[lb] & kRank); ce.hi = (int)(tg[ub - 1] & kRank); }
+        else { ce.lo = 1; ce.hi = 0; }
+        ce.pt0_vertex = 0;
+        // entering edge: from root vertex lb - 1 to lb (the chunk's first root
+        // vertex, else the next); leaving edge: from ub - 1 to ub
+        ce.in_sl = j > 0 ? esl[lb - 1] : 0.0;
+        ce.out_sl = (lb < ub && j + 1 < m) ? esl[ub - 1] : 0.0;
+        if (j > 0) {
+            const int k = v0 + lb - 1;
+            // the previous root vertex is this chunk's first point (it closes chunk j - 1)
+            if constexpr (WEIGHTED) {
+                const uint32_t t = F.tag[k];
+                ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
+                                 (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
+            } else {
+                ce.pt0_vertex = F.Wu[k] == (int64_t)(j * C) ? 1 : 0;
+            }
+        }
+        store_ends(ws, c0 + j, ce);
+    }
+}
+
+// Shared-memory bytes of flat_root_ends' scratch past the root's tags.
+__host__ __device__ inline size_t flat_root_scratch(int64_t m, int64_t n) {
+    return 4 * (size_t)(m + 1) + 8 * (size_t)n + 8;
+}
+
 // Shared-memory layout of the flat group merge for mg chunks and H vertices.
 struct FlatLayout {
     size_t oS, oW, oTag, oStart, oSize, bytes;
@@ -1207,7 +1270,8 @@ template <bool WEIGHTED>
 __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, int jb, int je,
                                                  const i128* gS, const i128* gW,
                                                  const int32_t* gH, const int32_t* gDS,
-                                                 const int32_t* gDW, int64_t Hg, int64_t g) {
+                                                 const int32_t* gDW, int64_t Hg, int64_t g,
+                                                 int64_t whole_row, int kq) {
     constexpr int C = LongCfg<WEIGHTED>::C;
     const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nth >> 5;
     const int mg = je - jb;
@@ -1312,6 +1376,16 @@ __device__ __forceinline__ void merge_group_flat(const LongWs& ws, int64_t c0, i
             ws.gfTag[o + k] = F.tag[v0 + k];
         }
     }
+    // a row of this one group: this hull is the row's root hull, and its chunk
+    // ends are written here (the top kernel skips the row)
+    if (whole_row >= 0) {
+        const size_t used = (size_t)(reinterpret_cast<unsigned char*>(F.tag + v0 + n) - merge_smem);
+        if (used + flat_root_scratch(mg, n) <= (size_t)kFlatSmem) {
+            __syncthreads();              // the hull is written out and nsize, nstart read
+            flat_root_ends<WEIGHTED>(F, v0, n, mg, ws, c0, kq);
+            if (tid == 0) ws.rowq[whole_row * 4 + 3] = 1;
+        }
+    }
 }
 
 // One group of kGroup chunks: the row's quanta and status, the chunks' starts
@@ -1342,6 +1416,7 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     const RowQ q = row_quanta(m, ws, c0, s_red, mc);
     if (gi == 0 && tid == 0) {
         ws.rowq[row * 4 + 0] = q.qs; ws.rowq[row * 4 + 1] = q.qw; ws.rowq[row * 4 + 2] = q.bad;
+        ws.rowq[row * 4 + 3] = 0;       // set when this group also writes the row's ends
         if (row_status) row_status[R.id] = (uint32_t)q.bad;
     }
     if (q.bad) {
@@ -1411,7 +1486,8 @@ __device__ __forceinline__ void merge_group_one(const LongGeo& geo, int64_t ng, 
     if (!MERGE) return;
     const int64_t Hg = s_Hg;
     if (FlatLayout(je - jb, Hg, WEIGHTED).bytes <= (size_t)kFlatSmem) {
-        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, s_gD[0], s_gD[1], Hg, g);
+        merge_group_flat<WEIGHTED>(ws, c0, jb, je, s_gS, s_gW, s_gH, s_gD[0], s_gD[1], Hg, g,
+                                   m == je - jb ? row : -1, q.qs - (WEIGHTED ? q.qw : 0));
         return;
     }
     if (tid == 0) ws.gfN[g] = -1;
@@ -1610,54 +1686,9 @@ __device__ __forceinline__ void merge_top_flat(const LongWs& ws, int64_t c0, int
         }
         __syncthreads();
     }
-    // ends of every chunk from the root array R (tags in chunk order): first[j]
-    // = the first root vertex of a chunk >= j, filled by each root vertex for
-    // the chunks since its predecessor's (the nodes' arrays are dead now, so
-    // first[] lives in the vertex arrays' space after R)
     const int n = nsize[0], v0 = nstart[0];
-    const uint32_t* tg = F.tag + v0;
-    int32_t* first = reinterpret_cast<int32_t*>(F.tag + v0 + n);
     __syncthreads();                       // nsize and nstart are read: first[] may cover them
-    constexpr uint32_t kRank = (1u << kFlatTagRank) - 1u;
-    for (int k = tid; k <= n; k += nth) {
-        const int64_t jlo = k == 0 ? 0 : (int64_t)(tg[k - 1] >> kFlatTagRank) + 1;
-        const int64_t jhi = k == n ? m : (int64_t)(tg[k] >> kFlatTagRank);
-        for (int64_t j = jlo; j <= jhi && j <= m; ++j) first[j] = k;
-    }
-    // each root edge's slope once, after first[] (8-byte aligned)
-    double* esl = reinterpret_cast<double*>((reinterpret_cast<uintptr_t>(first + m + 1) + 7) & ~(uintptr_t)7);
-    for (int k = tid; k + 1 < n; k += nth) {
-        i128 Wa, Sa, Wb, Sb;
-        F.get(v0 + k, Wa, Sa);
-        F.get(v0 + k + 1, Wb, Sb);
-        esl[k] = edge_slope(Wa, Sa, Wb, Sb, kq);
-    }
-    __syncthreads();
-    constexpr int C = LongCfg<WEIGHTED>::C;
-    for (int64_t j = tid; j < m; j += nth) {
-        const int lb = first[j], ub = first[j + 1];
-        ChunkEnds ce;
-        ce.bad = 0;
-        if (lb < ub) { ce.lo = (int)(tg[lb] & kRank); ce.hi = (int)(tg[ub - 1] & kRank); }
-        else { ce.lo = 1; ce.hi = 0; }
-        ce.pt0_vertex = 0;
-        // entering edge: from root vertex lb - 1 to lb (the chunk's first root
-        // vertex, else the next); leaving edge: from ub - 1 to ub
-        ce.in_sl = j > 0 ? esl[lb - 1] : 0.0;
-        ce.out_sl = (lb < ub && j + 1 < m) ? esl[ub - 1] : 0.0;
-        if (j > 0) {
-            const int k = v0 + lb - 1;
-            // the previous root vertex is this chunk's first point (it closes chunk j - 1)
-            if constexpr (WEIGHTED) {
-                const uint32_t t = F.tag[k];
-                ce.pt0_vertex = ((int64_t)(t >> kFlatTagRank) == j - 1 &&
-                                 (int)(t & kRank) == ws.meta[c0 + j - 1].h - 1) ? 1 : 0;
-            } else {
-                ce.pt0_vertex = F.Wu[k] == (int64_t)(j * C) ? 1 : 0;
-            }
-        }
-        store_ends(ws, c0 + j, ce);
-    }
+    flat_root_ends<WEIGHTED>(F, v0, n, m, ws, c0, kq);
 }
 
 template <bool WEIGHTED>
@@ -1674,7 +1705,8 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
     const bool flat_ok = ng <= kMaxFlatGroups;
     const int c0n = flat_ok && k0 < ng ? ws.gfN[gb + k0] : 0;
     const int c1n = flat_ok && k1 < ng ? ws.gfN[gb + k1] : 0;
-    if (ws.rowq[row * 4 + 2]) return;    // a bad row: its ends are written
+    // a bad row, or a row of one group: its ends are written
+    if (ws.rowq[row * 4 + 2] || ws.rowq[row * 4 + 3]) return;
     // root edge slopes: from the row's quanta to values
     const int kq = ws.rowq[row * 4 + 0] - (WEIGHTED ? ws.rowq[row * 4 + 1] : 0);
     {
@@ -1688,8 +1720,7 @@ __device__ __forceinline__ void merge_top_row(const LongGeo& geo, const LongWs& 
             if (k0 < ng) s_gbase[k0] = b;
             if (k1 < ng) s_gbase[k1] = b + c0n;
             __syncthreads();
-            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes + 4 * (size_t)(m + 1) + 8 * (size_t)tot + 8 <=
-                          (size_t)kMergeSmem) {
+            if (ok && FlatLayout(ng, tot, WEIGHTED).bytes + flat_root_scratch(m, tot) <= (size_t)kMergeSmem) {
                 merge_top_flat<WEIGHTED>(ws, c0, m, gb, (int)ng, tot, s_gbase, kq);
                 return;
             }
