@@ -256,7 +256,18 @@ __device__ __forceinline__ void chunk_hull_one(const IO* __restrict__ y,
     int64_t* sS = ws.slot_S + c * cap;
     int64_t* sW = WEIGHTED ? ws.slot_W + c * cap : nullptr;
     int h;
-    if (H.list) {
+    if (H.all) {
+        // every point a vertex: point j = 32 lane + k at its lane's start plus
+        // the lane-relative sum (the end point: the tile's total)
+        h = nt + 1;
+        for (int j = threadIdx.x; j < h; j += NT) {
+            const int l = j >> 5, k = j & 31;
+            const bool endp = j == nt;
+            sp[j] = (uint16_t)j;
+            sS[j] = endp ? H.T.LS[NT] : H.T.LS[l] + Sx[l * kRow + k];
+            if constexpr (WEIGHTED) sW[j] = endp ? H.T.LW[NT] : H.T.LW[l] + Wx[l * kRow + k];
+        }
+    } else if (H.list) {
         // the hull of the candidates' list: its vertices (warp 0's bits, lane l
         // holding entries [l K, l K + K)) and the list's last entry, the end point
         __shared__ int s_h;

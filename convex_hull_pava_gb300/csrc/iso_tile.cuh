@@ -239,6 +239,7 @@ struct TileHull {
     bool live;       // the tile exists (row index in range)
     bool quick;      // the hull came from tile_quickhull (vertex masks only)
     int list;        // chunks: entries of the list whose hull was found (0: none)
+    bool all;        // chunks: every point is a hull vertex (the element means increase)
 };
 
 // Whole rows of kQuickMinLanes to 32 lanes (one warp) whose first half has a
@@ -362,6 +363,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     int64_t* myW = Wx + gl * kRow;
     int64_t s = 0, wsum = 0;
     uint32_t cand = 0;
+    int64_t u_first = 0, o_first = 1, u_last = 0, o_last = 1;   // the lane's first and last elements
     {
         const QuantT<IO> qy(emax), qw(ewmax);
         int64_t up = 0, op = 1;   // previous element's value and weight
@@ -381,6 +383,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
                 ok = in ? 1 : 0;
                 if (k > 0 && in && up < uk) cand |= 1u << k;
             }
+            if (k == 0) { u_first = uk; o_first = ok > 0 ? ok : 1; }
             up = uk;
             op = ok > 0 ? ok : 1;
             s += uk;
@@ -390,6 +393,8 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
                 myW[k + 1] = wsum;
             }
         }
+        u_last = up;
+        o_last = op;
     }
     // lane starts: exclusive scan of lane totals over the tile
     {
@@ -418,6 +423,34 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     T.L = L;
     T.nt = nt;
 
+    // ---- chunks of long rows (the tile is the CTA): when every point is
+    // locally convex (each element's mean below the next one's, across lane
+    // boundaries too) the polyline of cumulative sums turns strictly left at
+    // every point, so every point is a hull vertex and no hull needs building ----
+    H.all = false;
+    if constexpr (!EMIT && RMAX == 1) {
+        // first without the lanes' first points (one barrier, which also
+        // orders the lane starts' writes before their reads below)
+        const bool inner = !work || ((cand | 1u) & allp) == allp;
+        if (__syncthreads_and(inner) && live && H.bad == 0) {
+            // the previous lane's last element: a shuffle inside a warp, shared
+            // memory across warps (the bridge area is free until the rounds)
+            int64_t pu = __shfl_up_sync(kFull, u_last, 1), po = __shfl_up_sync(kFull, o_last, 1);
+            int64_t* xl = reinterpret_cast<int64_t*>(bridge);
+            if ((tid & 31) == 31 && tid + 1 < NT) { xl[2 * (tid >> 5)] = u_last; xl[2 * (tid >> 5) + 1] = o_last; }
+            __syncthreads();
+            if ((tid & 31) == 0 && tid > 0) { pu = xl[2 * ((tid >> 5) - 1)]; po = xl[2 * ((tid >> 5) - 1) + 1]; }
+            bool rise;
+            if constexpr (WEIGHTED) rise = (__int128)pu * o_first < (__int128)u_first * po;
+            else rise = pu < u_first;
+            const bool ok = !work || lane == 0 || rise;
+            if (__syncthreads_and(ok)) {
+                H.all = true;
+                return;
+            }
+        }
+    }
+
     // ---- chunks of long rows (unit weights, float32 input; the tile is the
     // CTA): the candidates filter (iso_filter.cuh); when few survive, their
     // list, whose hull one warp finds by farthest-point levels ----
@@ -426,7 +459,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
         static_assert((3 * NT + 3 * (NT / 32)) * 4 <= SM::kPxB &&
                       kListCap * 10 + list_scratch_bytes(NT) <= SM::kPxB, "list area");
         unsigned char* area = smem + SM::oPx;
-        __syncthreads();                                     // lane starts written
+        if constexpr (RMAX != 1) __syncthreads();            // lane starts written (RMAX 1: above)
         cand = chunk_filter<NT>(yv, e, lane, nt, H.qs, LSa, work ? cand : 0u,
                                 reinterpret_cast<float*>(area));
         const int cnt_l = __popc(cand);
