@@ -167,3 +167,28 @@ def test_stream_order_and_repeat(cuda_ok):
 def test_named_workloads_full_size(cuda_ok, name):
     W = wl.make(name)
     parity(W.y, W.w, W.increasing, name)
+
+
+# ---- chunks whose points are all locally convex but at lane boundaries: the
+# all-vertex test must look across lanes (a shuffle inside a warp, shared
+# memory across warps) ----
+@pytest.mark.parametrize("drop_at", [32, 31 * 32, 32 * 32, 64 * 32, 127 * 32, "every_lane"])
+@pytest.mark.parametrize("weighting", ["none", "uniform"])
+def test_long_rows_increasing_with_lane_boundary_drops(cuda_ok, drop_at, weighting):
+    C = 4096
+    n = 3 * C + 77
+    rng = np.random.default_rng(11)
+    base = np.sort(rng.random((2, n)), axis=1) + 1e-6 * np.arange(n)[None, :]
+    y = base.copy()
+    for c0 in range(0, n, C):
+        if drop_at == "every_lane":
+            for l in range(32, min(C, n - c0), 32):
+                y[:, c0 + l:] -= 0.25          # each lane starts below the last one's end
+        elif c0 + drop_at < n:
+            y[:, c0 + drop_at:] -= 0.5         # one drop at a lane (or warp) boundary
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    w = wl.weights(weighting, 2, n, seed=12)
+    for inc in (True, False):
+        parity(y if inc else -y, w, inc, f"drops at {drop_at} {weighting} inc={inc}")
+    # and the plain increasing rows (every chunk all vertices) beside them
+    parity(np.ascontiguousarray(base, dtype=np.float32), w, True, f"all vertices {weighting}")
