@@ -19,9 +19,11 @@
  *    (NVLink-C2C on GB300), with no separate copy.  The workspace is best
  *    kept in device memory.
  *  - Ownership: the caller owns every buffer, the workspace and the stream.
- *    The library allocates no memory, keeps no state between calls, and never
- *    synchronises the stream: every call only enqueues kernels on `stream`
- *    (a cudaStream_t; NULL = the legacy default stream) and returns.
+ *    The fit and backward calls allocate no memory, keep no state between
+ *    calls (beyond the device's SM count, read once), and never synchronise
+ *    the stream: every call only enqueues kernels on `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and returns.  Only the optional
+ *    benchmarking and debugging switches at the end of this file keep state.
  *  - Errors the host can see (NULL pointers, non-positive or oversized shapes,
  *    a workspace that is too small or misaligned) return a negative status and
  *    enqueue nothing.  A failed kernel launch returns ISO_ERR_CUDA.
