@@ -224,10 +224,33 @@ __device__ __forceinline__ int64_t conv(int64_t x, int d) {
     return (x + (1LL << (d - 1))) >> d;
 }
 
+#ifdef ISO_LONG_F64_IO
+// float64 I/O: in double.
 __device__ __forceinline__ double edge_slope(i128 Wa, i128 Sa, i128 Wb, i128 Sb, int k) {
     const double f = i128_to_double(Sb - Sa) / i128_to_double(Wb - Wa);
     return ldexp(f, k);
 }
+#else
+// A float32 within a few ulp of a 128-bit integer, from 32-bit conversions
+// (no 64-bit conversion: those run on the slow FP64 pipe of this part).
+__device__ __forceinline__ float i128_to_f32(i128 x) {
+    if (fits64(x)) return i64_to_f32((int64_t)x);
+    const bool neg = x < 0;
+    const unsigned __int128 u = neg ? (unsigned __int128)0 - (unsigned __int128)x : (unsigned __int128)x;
+    const uint64_t hi = (uint64_t)(u >> 64), lo = (uint64_t)u;
+    const float fh = __fmaf_rn(__uint2float_rn((unsigned)(hi >> 32)), 4294967296.0f, __uint2float_rn((unsigned)hi));
+    const float fl = __fmaf_rn(__uint2float_rn((unsigned)(lo >> 32)), 4294967296.0f, __uint2float_rn((unsigned)lo));
+    const float f = __fmaf_rn(fh, 0x1p64f, fl);
+    return neg ? -f : f;
+}
+// float32 I/O: in float32, as the slopes inside a chunk are (two rounded
+// conversions and one division, scaled exactly): the slope is cast to
+// float32 anyway, and the FP64 pipe of one SM would otherwise carry every
+// root edge's division.
+__device__ __forceinline__ double edge_slope(i128 Wa, i128 Sa, i128 Wb, i128 Sb, int k) {
+    return (double)Pow2(k)(i128_to_f32(Sb - Sa) / i128_to_f32(Wb - Wa));
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // 1. chunk hulls

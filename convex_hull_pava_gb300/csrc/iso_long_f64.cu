@@ -1,4 +1,6 @@
-// Long rows, float64 I/O (the templates are in iso_long.cuh).
+// Long rows, float64 I/O (the templates are in iso_long.cuh; root-edge slopes
+// in double).
+#define ISO_LONG_F64_IO
 #include "iso_long.cuh"
 
 namespace isodev {
