@@ -30,6 +30,44 @@ __device__ __forceinline__ void fit_row_tiles(const IO* __restrict__ yr,
     TileHull H;
     tile_hull_phase<NT, WEIGHTED, true, RMAX, IO>(yr, wr, n, live, neg, L, smem, H);
 
+    if constexpr (RMAX == 1) {
+        if (H.oneblock && live && H.bad == 0 && n > 1) {
+            // the row is one block: every element is fitted by its mean, the
+            // slope from the first point to the end (as the vertex's slope
+            // below), written with 16-byte stores; one block start, element 0
+            __shared__ IO s_mean;
+            if (threadIdx.x == 0)
+                s_mean = ratio_t<IO>(H.T.LS[L], WEIGHTED ? H.T.LW[L] : (int64_t)n, H.qs - H.qw);
+            __syncthreads();
+            const IO v = neg ? -s_mean : s_mean;
+            const int lane = H.lane;
+            if ((reinterpret_cast<uintptr_t>(orow) & 15u) == 0) {
+                using V = typename IoT<IO>::V;
+                constexpr int P = IoT<IO>::kPerV;
+                V vv;
+                IO* pv = reinterpret_cast<IO*>(&vv);
+#pragma unroll
+                for (int u = 0; u < P; ++u) pv[u] = v;
+                const int nv = n / P;
+                for (int i = lane; i < nv; i += L) reinterpret_cast<V*>(orow)[i] = vv;
+                for (int i = nv * P + lane; i < n; i += L) orow[i] = v;
+            } else {
+                for (int i = lane; i < n; i += L) orow[i] = v;
+            }
+            if (brow) {
+                if ((reinterpret_cast<uintptr_t>(brow) & 3u) == 0) {
+                    const int n4 = n >> 2;
+                    for (int i = lane; i < n4; i += L) reinterpret_cast<uint32_t*>(brow)[i] = i == 0 ? 1u : 0u;
+                    for (int i = (n4 << 2) + lane; i < n; i += L) brow[i] = i == 0 ? 1 : 0;
+                } else {
+                    for (int i = lane; i < n; i += L) brow[i] = i == 0 ? 1 : 0;
+                }
+            }
+            if (status && lane == 0) *status = 0;
+            return;
+        }
+    }
+
     const Tile& T = H.T;
     const int lane = H.lane, gl = H.gl, e = H.e;
     const bool work = live && H.bad == 0;

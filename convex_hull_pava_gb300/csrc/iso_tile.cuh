@@ -240,6 +240,7 @@ struct TileHull {
     bool quick;      // the hull came from tile_quickhull (vertex masks only)
     int list;        // chunks: entries of the list whose hull was found (0: none)
     bool all;        // chunks: every point is a hull vertex (the element means increase)
+    bool oneblock;   // whole rows of one tile per CTA: the row is one block
 };
 
 // Whole rows of kQuickMinLanes to 32 lanes (one warp) whose first half has a
@@ -503,6 +504,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
     bool rel = false;       // rows hold tile-relative sums
     bool oneblock = false;  // every tile of the CTA is one block
     H.quick = false;
+    H.oneblock = false;
     // ---- whole rows of more than one warp: a tile none of whose points (the
     // locally convex ones, and each lane's first) lies strictly below the
     // chord from its first point to its end is one block, its hull that chord;
@@ -529,6 +531,7 @@ __device__ __forceinline__ void tile_hull_phase(const IO* __restrict__ yr,
             }
         }
         oneblock = !__syncthreads_or(below);
+        H.oneblock = oneblock;
     }
     // ---- few vertices expected: the hull by levels of farthest-point splits,
     // on tile-relative rows ----
