@@ -332,10 +332,7 @@ rows_backward_kernel(const IO* __restrict__ grad, const uint8_t* __restrict__ bl
     const IO* stage = reinterpret_cast<const IO*>(smem + SM::oStage);
     const IO* ratio = reinterpret_cast<const IO*>(smem + (WEIGHTED ? SM::oStageW : SM::oStage));
     if (live) {
-        if (out) {
-            IO* orow = out + off;
-            for (int i = lane; i < n; i += L) orow[i] = stage[spos_t<IO>(tile * L + (i >> 5), i & 31)];
-        }
+        if (out) write_row<IO>(out + off, stage, tile * L, n, lane, L, true);   // 16-byte stores
         if (wg.dw) {
             const IO* yrow = wg.y + off;
             const IO* zrow = wg.fit + off;
