@@ -563,9 +563,12 @@ def run_gpu(args):
         h2d = t(lambda: yds[0].copy_(yhs[1], non_blocking=True))
         d2h = t(lambda: ohs[1].copy_(ods[0], non_blocking=True))
         bi = t(both)
+        # a step moves y (and w) in and the fit out: the floors at these rates
+        b_in, b_out = W.elements * (8 if W.weighted else 4), W.elements * 4
         return {"bytes": nb, "h2d_gbs": nb / h2d / 1e6, "d2h_gbs": nb / d2h / 1e6,
                 "both_directions_gbs": 2 * nb / bi / 1e6,
-                "one_call_floor_ms": h2d + d2h, "overlapped_floor_ms": bi}
+                "one_call_floor_ms": h2d * b_in / nb + d2h * b_out / nb,
+                "overlapped_floor_ms": bi * (b_in + b_out) / (2 * nb)}
 
     link = link_rates()
 
